@@ -1,0 +1,175 @@
+"""Pins of the oracle's block codecs (tq6_0, TBQ4, Q8_0, Q4_0) — CPU only."""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import codecs, tables
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "block_codecs.json")))
+RNG = np.random.default_rng(11)
+
+
+def _block(case):
+    x = np.zeros(case["n"], np.float32)
+    for i, v in case["x_nonzero"].items():
+        x[int(i)] = v
+    return x
+
+
+def _hex(a):
+    return [format(int(b), "02x") for b in np.asarray(a).reshape(-1)]
+
+
+# ------------------------------------------------------------------ hand-derived blocks
+def test_tq6_golden_block():
+    g = GOLD["tq6_0"]
+    d, code = codecs.tq6_encode(_block(g))
+    assert format(int(d.view(np.uint16)[0]), "04x") == g["d_bits"]
+    assert list(code[0, :8]) == g["codes_head"] and np.all(code[0, 8:] == g["code_rest"])
+    ql, qh = codecs.tq6_pack(code[0])
+    assert _hex(ql[:4]) == g["ql_head"] and set(_hex(ql[4:])) == {g["ql_rest"]}
+    assert _hex(qh[:2]) == g["qh_head"] and set(_hex(qh[2:])) == {g["qh_rest"]}
+    assert ql.size + qh.size + 2 == 98
+
+
+def test_q8_golden_block():
+    g = GOLD["q8_0"]
+    d, q = codecs.q8_encode(_block(g))
+    assert format(int(d.view(np.uint16)[0]), "04x") == g["d_bits"]
+    assert list(q[0, :5]) == g["q_head"] and np.all(q[0, 5:] == 0)
+    assert _hex(q[0, :5].view(np.uint8)) == g["bytes_head"]
+    assert q.size + 2 == 34
+
+
+def test_q4_golden_block():
+    g = GOLD["q4_0"]
+    d, c = codecs.q4_encode(_block(g))
+    assert format(int(d.view(np.uint16)[0]), "04x") == g["d_bits"]
+    assert list(c[0, :5]) == g["codes_head"] and np.all(c[0, 5:] == g["code_rest"])
+    b = codecs.pack_nibbles(c[0])
+    assert _hex(b[:3]) == g["bytes_head"] and set(_hex(b[3:])) == {g["byte_rest"]}
+    assert b.size + 2 == 18
+
+
+def test_tbq4_golden_blocks():
+    g = GOLD["tbq4"]
+    y = np.zeros(128, np.float32)
+    y[0] = 1.0
+    n16, idx = codecs.tbq4_encode(y)
+    assert format(int(n16.view(np.uint16)[0]), "04x") == g["one_hot"]["n_bits"]
+    assert idx[0, 0] == g["one_hot"]["idx_head"] and np.all(idx[0, 1:] == g["one_hot"]["idx_rest"])
+    b = codecs.pack_nibbles(idx[0])
+    assert _hex(b[:1]) == [g["one_hot"]["byte_head"]] and set(_hex(b[1:])) == {g["one_hot"]["byte_rest"]}
+    assert b.size + 2 == 66
+    y = np.full(128, 1 / 16, np.float32)
+    n16, idx = codecs.tbq4_encode(y)
+    assert format(int(n16.view(np.uint16)[0]), "04x") == g["const_1_16"]["n_bits"]
+    assert np.all(idx == g["const_1_16"]["idx"])
+    assert set(_hex(codecs.pack_nibbles(idx[0]))) == {g["const_1_16"]["byte"]}
+
+
+# ------------------------------------------------------------------ packing (bit-exact layout)
+def test_tq6_pack_exhaustive_positions_and_values():
+    # KV cache math reports a 3-bit packing bug that corrupted values 3-7 of each group:
+    # every code value at every position must round-trip, with the stated bit positions.
+    for v in range(64):
+        for pos in range(128):
+            code = np.full(128, 32, np.uint8)
+            code[pos] = v
+            ql, qh = codecs.tq6_pack(code)
+            assert (ql[pos // 2] >> (4 * (pos % 2))) & 0xF == v & 0xF
+            assert (qh[pos // 4] >> (2 * (pos % 4))) & 0x3 == v >> 4
+            assert np.array_equal(codecs.tq6_unpack(ql, qh), code)
+
+
+def test_nibble_and_bitplane_exhaustive():
+    for v in range(16):
+        for pos in range(32):
+            c = np.zeros(32, np.uint8)
+            c[pos] = v
+            b = codecs.pack_nibbles(c)
+            assert (b[pos // 2] >> (4 * (pos % 2))) & 0xF == v
+            assert np.array_equal(codecs.unpack_nibbles(b), c)
+    for pos in range(64):
+        bits = np.zeros(64, np.uint8)
+        bits[pos] = 1
+        b = codecs.pack_bitplane(bits)
+        assert b[pos // 8] == 1 << (pos % 8) and b.sum() == b[pos // 8]
+        assert np.array_equal(codecs.unpack_bitplane(b), bits)
+
+
+# ------------------------------------------------------------------ error bounds and invariants
+def _fp16_err(d):
+    return d.astype(np.float32) * np.float32(2 ** -11)
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 40.0])
+def test_tq6_error_bound_and_idempotence(scale):
+    x = (RNG.standard_normal((64, 256)) * scale).astype(np.float32)
+    d, code = codecs.tq6_encode(x)
+    xr = codecs.tq6_decode(d, code)
+    half = np.repeat(d.astype(np.float32) / 2, 128, axis=-1) * (1 + 1e-6)
+    # the stored scale may round below absmax/31, letting the extreme clip by < 31 * ulp(d)
+    slack = np.repeat(31 * _fp16_err(d), 128, axis=-1)
+    assert np.all(np.abs(x - xr) <= half + slack)
+    d2, code2 = codecs.tq6_encode(xr)
+    assert np.array_equal(code2, code)
+    assert np.all((code >= 1) & (code <= 63))
+
+
+def test_zero_blocks():
+    d, c = codecs.tq6_encode(np.zeros(128, np.float32))
+    assert d[0] == 0 and np.all(c == 32)
+    n, i = codecs.tbq4_encode(np.zeros(128, np.float32))
+    assert n[0] == 0 and np.all(codecs.tbq4_decode(n, i) == 0)
+    d, q = codecs.q8_encode(np.zeros(32, np.float32))
+    assert d[0] == 0 and np.all(q == 0)
+    d, c = codecs.q4_encode(np.zeros(32, np.float32))
+    assert d[0] == 0 and np.all(c == 8)
+
+
+@pytest.mark.parametrize("enc,dec,qmax", [(codecs.q8_encode, codecs.q8_decode, 127),
+                                          (codecs.q4_encode, codecs.q4_decode, 7)])
+def test_q_block_error_bound_and_idempotence(enc, dec, qmax):
+    x = (RNG.standard_normal((50, 128)) * 3).astype(np.float32)
+    d, c = enc(x)
+    xr = dec(d, c)
+    half = np.repeat(d.astype(np.float32) / 2, 32, axis=-1) * (1 + 1e-6)
+    slack = np.repeat(qmax * _fp16_err(d), 32, axis=-1)
+    assert np.all(np.abs(x - xr) <= half + slack)
+    d2, c2 = enc(xr)
+    assert np.array_equal(c2, c)
+
+
+def test_tbq4_index_is_nearest_centroid_and_mse():
+    cent, bnd = tables.tbq4_tables()
+    y = RNG.standard_normal((2000, 128)).astype(np.float32)
+    n16, idx = codecs.tbq4_encode(y)
+    u = y * (np.float32(1) / n16.astype(np.float32))
+    # brute force over the 16 levels in fp64 (boundaries are midpoints -> nearest level)
+    nearest = np.argmin(np.abs(u[..., None].astype(np.float64) - cent.astype(np.float64)), axis=-1)
+    agree = np.mean(nearest.reshape(idx.shape) == idx)
+    assert agree > 0.99999
+    # distortion of unit-variance-per-block data ~ Lloyd-Max 16-level MSE (~0.0095 sigma^2)
+    yr = codecs.tbq4_decode(n16, idx)
+    rel_mse = np.mean((y - yr) ** 2) / np.mean(y ** 2)
+    assert 0.0085 < rel_mse < 0.0110
+    assert np.allclose(n16.astype(np.float64), np.linalg.norm(y.reshape(-1, 128), axis=1).reshape(n16.shape),
+                       rtol=1e-3)
+
+
+def test_tbq4_ties_go_low():
+    # u exactly on boundary beta_9 (= bnd[8] = 0.0228) must take the lower cell, index 8.
+    cent, bnd = tables.tbq4_tables()
+    y = np.zeros(128, np.float32)
+    y[0] = 1.0
+    y[1] = bnd[8]
+    n16, idx = codecs.tbq4_encode(y)
+    assert n16[0] == 1.0            # sqrt(1 + 0.00052) rounds to fp16 1.0
+    assert idx[0, 1] == 8 and idx[0, 0] == 15
+    y[1] = np.nextafter(bnd[8], np.float32(1))
+    assert codecs.tbq4_encode(y)[1][0, 1] == 9

@@ -1,0 +1,100 @@
+"""Pins of the oracle's KVarN balancing and row rounding — CPU only.
+
+SJ-KVaRN §2.2 (balancing of a 128 x 256 tile by alternating row/column passes until
+spreads match; 16 passes; per-row b-bit rounding with its own scale and zero point; fp16
+scales) and §3 (2,304 B of scales per record per KV head = 0.28125 bits per value).
+The exact scales of a balanced tile are parity unpinned (no worked example on the pages);
+these tests pin the invariants.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import kvarn
+
+RNG = np.random.default_rng(5)
+
+
+def _tile(outliers=8, factor=16.0):
+    x = RNG.standard_normal((128, 256)).astype(np.float32)
+    ch = RNG.choice(256, outliers, replace=False)
+    x[:, ch] *= factor
+    return x
+
+
+def test_final_column_spread_is_one_and_factorisation():
+    X = _tile()
+    Y, r, c = kvarn.balance(X)
+    Y64 = Y.astype(np.float64)
+    col_std = Y64.std(axis=0)
+    assert np.max(np.abs(col_std - 1)) < 1e-5
+    # rows balanced too after 16 passes (spreads similar)
+    assert np.max(np.abs(Y64.std(axis=1) - 1)) < 0.05
+    recon = r.astype(np.float64)[:, None] * Y64 * c.astype(np.float64)[None, :]
+    assert np.max(np.abs(recon - X) / (np.abs(X) + 1e-3)) < 1e-4
+
+
+def test_fixed_point_of_sign_tile():
+    # X = alpha * a_t * b_j with balanced sign vectors: one row pass makes every row spread
+    # exactly alpha (power of two: all sums exact), after which Y is the sign pattern with
+    # unit spreads, so r = alpha, c = 1 exactly.
+    alpha = np.float32(0.5)
+    a = np.array([1, -1] * 64, np.float32)
+    b = np.array([1, 1, -1, -1] * 64, np.float32)
+    X = alpha * a[:, None] * b[None, :]
+    Y, r, c = kvarn.balance(X)
+    assert np.all(r == alpha) and np.all(c == 1) and np.array_equal(Y, a[:, None] * b[None, :])
+    code, S, Z, C = kvarn.encode(X, 4)
+    # lo = -1, hi = 1: S = fp16(0.5 * 2 / 15) = 0x2c44, Z = fp16(-0.5) = 0xb800, C = 1
+    assert np.all(S.view(np.uint16) == 0x2C44) and np.all(Z.view(np.uint16) == 0xB800)
+    assert np.all(C.view(np.uint16) == 0x3C00)
+    assert np.array_equal(code, np.where(X > 0, 15, 0))
+    assert np.allclose(kvarn.decode(code, S, Z, C), X, atol=0.5 * 15 * 2 ** -14 + 1e-3)
+
+
+@pytest.mark.parametrize("bits", [4, 5])
+def test_row_rounding_error_bound(bits):
+    X = _tile()
+    code, S, Z, C = kvarn.encode(X, bits)
+    assert code.max() <= 2 ** bits - 1
+    Xr = kvarn.decode(code, S, Z, C)
+    S32, C32 = S.astype(np.float32)[:, None], C.astype(np.float32)[None, :]
+    # half a step, plus the fp16 rounding of S, Z, C (relative 2^-11 each) over the row range
+    bound = 0.5 * S32 * np.abs(C32) + 3 * 2 ** -11 * (np.abs(X) + (2 ** bits) * S32 * np.abs(C32))
+    assert np.all(np.abs(Xr - X) <= bound + 1e-6)
+    # the row min / max are reconstructed within that bound too (codes 0 and Q are used)
+    assert np.all(code.min(axis=1) == 0) and np.all(code.max(axis=1) >= 2 ** bits - 2)
+
+
+def test_tile_bytes_and_bits_per_value():
+    X = _tile()
+    for bits in (4, 5):
+        code, S, Z, C = kvarn.encode(X, bits)
+        for role in "KV":
+            b = kvarn.pack_codes(code, bits, role)
+            assert b.size == 4096 * bits
+            assert np.array_equal(kvarn.unpack_codes(b, bits, role), code)
+        sb = kvarn.scale_block(S, Z, C)
+        assert sb.nbytes == 1152 and np.all(sb[512:] == 0)
+    # SJ-KVaRN §3: 2,304 B of scales per record per head (K + V) adds 0.28125 bits/value
+    assert 2 * 1152 * 8 / (2 * 128 * 256) == 0.28125
+    assert (4096 * 4 + 1152) * 8 / (128 * 256) == 4.28125
+
+
+def test_role_layouts():
+    code = (np.arange(128 * 256) % 32).astype(np.uint8).reshape(128, 256)
+    bK = kvarn.pack_codes(code, 5, "K")
+    bV = kvarn.pack_codes(code, 5, "V")
+    # K: token 1's first byte holds channels 0, 1 of token 1 (low nibbles of codes 0, 1)
+    assert bK[128] == (code[1, 0] & 15) | ((code[1, 1] & 15) << 4)
+    # V: channel 1's first byte holds tokens 0, 1 of channel 1
+    assert bV[64] == (code[0, 1] & 15) | ((code[1, 1] & 15) << 4)
+    # high planes: K row t occupies 32 B after the 16 KiB low plane; V row c 16 B
+    assert bK[16384 + 32 * 2] & 1 == code[2, 0] >> 4
+    assert (bV[16384 + 16 * 3] >> 2) & 1 == code[2, 3] >> 4
+
+
+def test_constant_rows_and_zero_tile():
+    X = np.zeros((128, 256), np.float32)
+    code, S, Z, C = kvarn.encode(X, 4)
+    assert np.all(S == 0) and np.all(code == 0) and np.all(kvarn.decode(code, S, Z, C) == 0)
