@@ -1,0 +1,532 @@
+#!/usr/bin/env python3
+"""Benchmark of the rotated low-bit KV cache hot path on GB300.
+
+One step = one decode step over every layer of the workload: append one position per
+sequence (rotate + tq6_0 staging or exact copy), seal when the seal policy asks, and
+decode attention over every region (split-K + log-sum-exp merge). The metric is the
+decode attention's effective KV bandwidth: the bytes the method must read (sink, body
+records, tq6_0 ring span, exact tail, q and out) divided by the time of the whole step.
+
+Default workload: hybrid27b_kvarn44 (16 layers, 4 KV heads x 256, 24 query heads, 32,768
+positions, KVarN 4/4 body, tq6_0 ring, 1,024-position exact tail, 256 decode steps with
+the seal at the journal's 8,192 mark). Prints one JSON line (rank 0).
+
+--impl reference times the CPU oracle (numpy, fp64 attention) on a bounded sample of the
+same workload: the reference this build is checked against.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn effective KV GB/s (% of GB300 HBM peak); seal groups/s; 32k-262k ctx"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "hybrid27b_kvarn44"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- byte model
+def layer_step_bytes(w, states):
+    """Algorithmic bytes one decode attention of one layer reads and writes.
+
+    states: list of (N, S) per sequence after the step's append and seal. Per KV head:
+    sink positions x 2 D x 2 B, body positions x (K + V record bytes) / 128, tq6_0 ring
+    span x 2 x (D/128) x 98 B, exact tail (or exact journal) positions x 2 D x 2 B; plus the
+    fp16 query and output of every sequence.
+    """
+    from quantized_kv_cache_gb300.configs import record_bytes
+    D, H = w.head_dim, w.n_kv_heads
+    rec = record_bytes(w.k_body, D) + record_bytes(w.v_body, D)
+    total = 0
+    for N, S in states:
+        sink = min(N, 128)
+        body = max(S - 128, 0)
+        if w.journal == "tq6_0":
+            E = max(S, N - w.tail)
+            ring, exact = E - S, N - max(E, 128)
+            per_head = sink * 4 * D + body * rec // 128 + ring * 2 * (D // 128) * 98 + exact * 4 * D
+        else:
+            exact = N - max(S, 128)
+            per_head = sink * 4 * D + body * rec // 128 + exact * 4 * D
+        total += H * per_head + 2 * w.n_q_heads * D * 2
+    return total
+
+
+def initial_states(w, contexts):
+    """(N, S) per sequence after prefill (the workload's starting state)."""
+    from quantized_kv_cache_gb300.configs import groups_to_seal
+    from quantized_kv_cache_gb300.runner import prefill_plan
+    cur = []
+    for n0 in contexts:
+        n, S = 0, 128
+        for c, seal in prefill_plan(w, n0):
+            n += c
+            if seal:
+                S += 128 * groups_to_seal(n, S, w.keep)
+        cur.append((n, S))
+    return cur
+
+
+def simulate_states(w, contexts, steps):
+    """(N, S) per sequence after each step's append and seal, following the seal policy."""
+    from quantized_kv_cache_gb300.configs import should_seal, groups_to_seal
+    cur = [list(s) for s in initial_states(w, contexts)]
+    out = []
+    for _ in range(steps):
+        for st in cur:
+            st[0] += 1
+            if should_seal(w, st[0], st[1]):
+                st[1] += 128 * groups_to_seal(st[0], st[1], w.keep)
+        out.append([tuple(s) for s in cur])
+    return out
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.samples = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), "--query-gpu=timestamp," + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.02 <= r[0] <= self.t1 + 0.02]
+        use = inside or rows[-5:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(p[1]) for _, p in use if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in use if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in use:
+            for n, v in zip(names, p[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(use), "in_timed_window": bool(inside)}
+
+
+# --------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_kv_cache_gb300 as pkg
+    from quantized_kv_cache_gb300 import configs, _lib
+    from quantized_kv_cache_gb300.runner import DeviceSynth, DecodeInputs, build_state
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = configs.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    n_steps = max(K, W)
+    seq_ids = list(range(len(w.contexts)))
+    cfg = w.config()
+    cfg.max_ctx = max(w.contexts) + n_steps + 512
+    cache = pkg.KVCache(cfg, local_rank)
+    ds = DeviceSynth(w, local_rank)
+    layers = list(range(w.n_layers))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    build_state(w, cache, ds, seq_ids, layers, stream=stream)
+    inp = DecodeInputs(w, ds, seq_ids, w.contexts, n_steps, layers)
+    out = torch.empty((w.n_layers, len(seq_ids), w.n_q_heads, w.head_dim), dtype=torch.float16, device=dev)
+    torch.cuda.synchronize()
+    snap = _lib.kv_snapshot(cache.h)
+    pool_backup = cache.pool.clone()
+
+    def restore():
+        torch.cuda.synchronize()
+        _lib.kv_restore(cache.h, snap)
+        cache.pool.copy_(pool_backup)
+        torch.cuda.synchronize()
+
+    def step(s, events=None):
+        return _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
+                                   inp.v[s].data_ptr(), out.data_ptr(), w.seal_trigger, w.keep,
+                                   cache.ws.data_ptr(), cache.ws_bytes, events, stream)
+
+    for s in range(W):
+        step(s)
+    restore()
+
+    # events around every attention launch of the timed region (recorded by the library)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * w.n_layers)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    handles = [[e.cuda_event for e in row] for row in evs]
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t_start.record()
+    sealed = 0
+    for s in range(K):
+        sealed += step(s, handles[s])
+    t_end.record()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    dist_barrier(world)
+    clocks.window(wall0, wall1)
+    time.sleep(0.1)
+    clocks.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed_max = dist_max(elapsed, world)
+
+    states = simulate_states(w, w.contexts, K)
+    step_bytes = [layer_step_bytes(w, st) for st in states]          # per layer-step, same for every layer
+    total_bytes = sum(step_bytes) * w.n_layers
+    attn_times = [evs[s][2 * l].elapsed_time(evs[s][2 * l + 1]) / 1e3 for s in range(K) for l in range(w.n_layers)]
+    attn_bytes = [step_bytes[s] for s in range(K) for _ in range(w.n_layers)]
+    hbm, peak_src = peaks()
+    achieved = sum(attn_bytes) / sum(attn_times) / 1e9
+    value = total_bytes * world / elapsed_max / 1e9
+
+    # seal throughput: time the seals of the policy's first seal point (or the bulk seal)
+    seal = measure_seal(w, cache, inp, seq_ids, out, restore, stream, K)
+
+    e2e = None
+    if not args.no_e2e:
+        restore()
+        e2e = measure_e2e(w, cache, inp, seq_ids, out, stream, K, total_bytes, world)
+
+    launches = K * w.n_layers * 3 + seal_launches(w, states)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(elapsed_max / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": config_block(w, K),
+        "pct_of_hbm_peak": round(100 * value / world / hbm, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "decode_split_kernel + decode_merge_kernel (one kv_decode_attn call)",
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "launches_timed": len(attn_times),
+                     "mean_launch_us": round(1e6 * sum(attn_times) / len(attn_times), 3),
+                     "algorithmic_bytes_per_launch": int(sum(attn_bytes) / len(attn_bytes))},
+        "seal": seal,
+        "groups_sealed_in_timed_region": sealed,
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+    }
+    if e2e:
+        result["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(args.workload, steps=6, heads=2)
+    cache.close()
+    return result
+
+
+def seal_launches(w, states):
+    n = 0
+    prev = None
+    for st in states:
+        if prev is not None:
+            for (a, s0), (b, s1) in zip(prev, st):
+                if s1 != s0:
+                    n += w.n_layers
+                    break
+        prev = st
+    return n
+
+
+def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K):
+    """Seal groups/s: time kv_seal calls alone with CUDA events."""
+    import torch
+    from quantized_kv_cache_gb300 import _lib
+    from quantized_kv_cache_gb300.configs import should_seal, groups_to_seal
+    restore()
+    states = [initial_states(w, w.contexts)] + simulate_states(w, w.contexts, max(K, w.steps, 1))
+    target = None
+    for s in range(1, len(states)):
+        if any(a[1] != b[1] for a, b in zip(states[s - 1], states[s])):
+            target = s - 1          # decode step index whose seal is timed
+            break
+    if w.bulk_seal_step >= 0:
+        target = ("bulk", w.bulk_seal_step)
+    if target is None:
+        return {"groups_per_s": None, "note": "no seal in the measured steps"}
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if isinstance(target, tuple):
+        for s in range(target[1]):
+            _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
+                                inp.v[s].data_ptr(), out.data_ptr(), -1, w.keep, cache.ws.data_ptr(),
+                                cache.ws_bytes, None, stream)
+        torch.cuda.synchronize()
+        ev0.record()
+        groups = _lib.kv_seal(cache.h, -1, seq_ids, w.keep, stream)
+        ev1.record()
+        torch.cuda.synchronize()
+        t = ev0.elapsed_time(ev1) / 1e3
+        kind = "bulk seal, all layers, one launch"
+    else:
+        for s in range(target):
+            _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
+                                inp.v[s].data_ptr(), out.data_ptr(), w.seal_trigger, w.keep, cache.ws.data_ptr(),
+                                cache.ws_bytes, None, stream)
+        t, groups = 0.0, 0
+        for l in range(w.n_layers):
+            _lib.kv_append(cache.h, l, seq_ids, 1, inp.k[target, l].data_ptr(), inp.v[target, l].data_ptr(), stream)
+            torch.cuda.synchronize()
+            ev0.record()
+            groups += _lib.kv_seal(cache.h, l, seq_ids, w.keep, stream)
+            ev1.record()
+            torch.cuda.synchronize()
+            t += ev0.elapsed_time(ev1) / 1e3
+        kind = "seal at the policy's trigger, one launch per layer"
+    from quantized_kv_cache_gb300.configs import record_bytes
+    D, H = w.head_dim, w.n_kv_heads
+    read = 128 * H * 2 * ((D // 128) * 98 if w.journal == "tq6_0" else D * 2)
+    write = H * (record_bytes(w.k_body, D) + record_bytes(w.v_body, D))
+    hbm, _ = peaks()
+    gps = groups / t if t > 0 else None
+    return {"groups_per_s": round(gps, 1) if gps else None, "groups": groups, "seconds": round(t, 6),
+            "bytes_per_group": read + write, "hbm_frac": round(gps * (read + write) / 1e9 / hbm, 4) if gps else None,
+            "kind": kind, "group": "128 positions x 1 layer x all KV heads x K and V"}
+
+
+def measure_e2e(w, cache, inp, seq_ids, out, stream, K, total_bytes, world):
+    """The same K steps through kv_decode_step with host buffers: each step copies its q, k,
+    v (all layers) from pinned host memory and copies the outputs back, inside the timing."""
+    import torch
+    from quantized_kv_cache_gb300 import _lib
+    hq = inp.q[:K].cpu().pin_memory()
+    hk = inp.k[:K].cpu().pin_memory()
+    hv = inp.v[:K].cpu().pin_memory()
+    hout = torch.empty((K,) + tuple(out.shape), dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(inp.q[0]), torch.empty_like(inp.k[0]), torch.empty_like(inp.v[0])
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in range(K):
+        dq.copy_(hq[s], non_blocking=True)
+        dk.copy_(hk[s], non_blocking=True)
+        dv.copy_(hv[s], non_blocking=True)
+        _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            out.data_ptr(), w.seal_trigger, w.keep, cache.ws.data_ptr(), cache.ws_bytes, None, stream)
+        hout[s].copy_(out, non_blocking=True)
+    t1.record()
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    el = dist_max(t0.elapsed_time(t1) / 1e3, world)
+    h2d = dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2
+    return {"value": round(total_bytes * world / el / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": round(el / K * 1e3, 4)}
+
+
+def config_block(w, K):
+    D = w.head_dim
+    per_step = layer_step_bytes(w, [(n + 1, 0) for n in w.contexts]) * w.n_layers
+    return {"workload": w.name, "layers": w.n_layers, "kv_heads": w.n_kv_heads, "head_dim": D,
+            "q_heads": w.n_q_heads, "batch": len(w.contexts), "contexts": w.contexts,
+            "body": f"{w.k_body}/{w.v_body}", "journal": w.journal, "tail": w.tail, "decode_steps": K,
+            "seal": f"keep {w.keep}, trigger {w.seal_trigger}",
+            "l2": f"inputs larger than L2: each step reads ~{per_step / 1e6:.0f} MB of cache (L2 129 MB)",
+            "inputs": "seeded synthetic fp16 K/V/q (splitmix64 counter streams over a normal quantile table)"}
+
+
+# --------------------------------------------------------------------------- oracle arm
+def cpu_baseline(workload, samples=1, steps=1, heads=1):
+    """Time the oracle in a fresh single-threaded process on a bounded sample."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", workload, str(steps), str(heads)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def oracle_sample(workload, steps, heads):
+    """Oracle decode attention of layer 0 of sequence 0, `heads` KV heads, `steps` steps, on a
+    cache built by the oracle from the same synthetic inputs (build time not counted)."""
+    import numpy as np
+    from quantized_kv_cache_gb300 import configs, synth
+    from quantized_kv_cache_gb300.runner import prefill_plan
+    from oracle import attention
+    from oracle.cache import HeadCache, HeadConfig
+    w = configs.WORKLOADS[workload]
+    n0 = w.contexts[0]
+    hcfg = HeadConfig(w.head_dim, w.k_body, w.v_body, w.journal, w.tail_fmt, w.tail, w.ring)
+    t_build = time.time()
+    caches = []
+    for h in range(heads):
+        hc = HeadCache(hcfg)
+        pos = 0
+        for c, seal in prefill_plan(w, n0):
+            k = synth.kv_values(w.seed, synth.T_K, 0, 0, h, pos, c, w.head_dim, w.n_out, w.out_factor)
+            v = synth.kv_values(w.seed, synth.T_V, 0, 0, h, pos, c, w.head_dim)
+            hc.append(k, v)
+            pos += c
+            if seal:
+                hc.seal(w.keep)
+        caches.append(hc)
+    t_build = time.time() - t_build
+    G, D = w.G, w.head_dim
+    t, nbytes = 0.0, 0
+    for s in range(steps):
+        q = synth.q_values(w.seed, 0, 0, s, w.n_q_heads, D)
+        for h, hc in enumerate(caches):
+            k = synth.kv_values(w.seed, synth.T_K, 0, 0, h, n0 + s, 1, D, w.n_out, w.out_factor)
+            v = synth.kv_values(w.seed, synth.T_V, 0, 0, h, n0 + s, 1, D)
+            t0 = time.perf_counter()
+            hc.append(k, v)
+            if configs.should_seal(w, hc.N, hc.S):
+                hc.seal(w.keep)
+            attention.attend(q[h * G:(h + 1) * G].astype(np.float64), hc.regions(), hc.cfg.rot, 1 / np.sqrt(D))
+            t += time.perf_counter() - t0
+            nbytes += (layer_step_bytes(w, [(hc.N, hc.S)]) - 2 * w.n_q_heads * D * 2) // w.n_kv_heads \
+                + 2 * G * D * 2
+    return {"value": round(nbytes / t / 1e9, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{workload}: layer 0, sequence 0, {heads} of {w.n_kv_heads} KV heads, {steps} decode "
+                      f"step(s) at {n0} positions (append, seal policy, dequantize every region, fp64 "
+                      f"attention); oracle cache build {t_build:.1f} s not counted",
+            "seconds": round(t, 3)}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle, timed on the host cores, per-step bounded samples."""
+    if rank != 0:
+        return None
+    from quantized_kv_cache_gb300 import configs
+    w = configs.WORKLOADS[args.workload]
+    steps = args.warmup + args.steps
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", args.workload, str(min(steps, 8)), "1"]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3000)
+    if r.returncode != 0:
+        return {"impl": "reference", "unavailable": "oracle run failed: " + r.stderr.strip().splitlines()[-1][:200]}
+    cb = json.loads(r.stdout.strip().splitlines()[-1])
+    v = cb["value"]
+    n = min(steps, 8)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(cb["seconds"] / n * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(w, args.steps),
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "note": f"oracle timed on {n} bounded sample step(s) of one layer / one KV head; see cpu_baseline.sample"}
+
+
+# --------------------------------------------------------------------------- distributed
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("KVQ_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-sample":
+        print(json.dumps(oracle_sample(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]))))
+        return 0
+    args = parse()
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,206 @@
+/*
+ * kvq.h — C ABI of the rotated low-bit KV cache and its decode attention (GB300, sm_103a).
+ *
+ * The calls mirror how the source pages state the problem: a KV cache written one token
+ * at a time into a staging journal (SJ-KVaRN §2.1 "The life of a token"), sealed in
+ * batches into compact body records (SJ-KVaRN §2.1 item 4, §4.3 "Adaptive tail"), read by
+ * one decode-attention pass that merges every region under one softmax (KV Cache
+ * Precision Tail §2; HAL #582 §5 P2, the two-region streaming combine), and sized in
+ * bytes per token (KV cache math, "Bytes per token").
+ *
+ * Conventions for every call:
+ *  - Return value: a kvq_status. No call throws or aborts across the ABI.
+ *  - Device pointers are plain CUDA device addresses, 16-byte aligned; host pointers are
+ *    plain host addresses. Nothing here takes or returns framework (torch) types.
+ *  - Ownership: the caller allocates the device pool, the decode workspace and every input
+ *    and output buffer. The library keeps only host-side metadata (an opaque kvq_cache)
+ *    plus pointers into the caller's pool, and never calls cudaMalloc.
+ *  - Ordering: device work is enqueued on the given stream (cudaStream_t passed as void*;
+ *    NULL is the legacy default stream). Lengths live on the host and are authoritative,
+ *    so refusals (KVQ_ENOSPC, KVQ_EINVAL) happen before anything is enqueued.
+ *  - Errors detected on the device (non-finite scales) set bits of a status word that
+ *    kv_get_status reads after the caller synchronises.
+ *
+ * Shapes: L layers, H KV heads, Hq query heads, G = Hq / H, D head_dim. Query head h reads
+ * KV head h / G. K/V/q inputs are IEEE fp16, row-major.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,        /* bad argument: null / misaligned pointer, index out of range, bad config */
+    KVQ_ENOSPC = 2,        /* journal ring or context capacity would overflow; nothing written */
+    KVQ_EUNSUPPORTED = 3,  /* valid config this build has no kernel for */
+    KVQ_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    KVQ_EDEVICE = 5        /* device status word reports a problem (see kv_get_status) */
+} kvq_status;
+
+/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, KVARN4, KVARN5. Journal: TQ6_0, F16, BF16.
+ * Exact tail: F16, BF16. */
+typedef enum {
+    KVQ_F16 = 0,
+    KVQ_BF16 = 1,
+    KVQ_TQ6_0 = 2,   /* SJ-KVaRN §2.1: rotated 6-bit, 98 B per 128 values */
+    KVQ_TBQ4 = 3,    /* KV cache math: sign flip, WHT, sign flip; 16 Lloyd-Max centroids; 66 B/128 */
+    KVQ_Q8_0 = 4,    /* 34 B per 32 values */
+    KVQ_Q4_0 = 5,    /* 18 B per 32 values */
+    KVQ_KVARN4 = 6,  /* SJ-KVaRN §2.2: 256-pt Hadamard, 16-pass balancing, 4-bit rows */
+    KVQ_KVARN5 = 7   /* same, 5-bit rows */
+} kvq_fmt;
+
+typedef struct {
+    int32_t n_layers;
+    int32_t n_kv_heads;
+    int32_t head_dim;        /* 128, 256 or 512; KVarN bodies need a multiple of 256 */
+    int32_t n_q_heads;       /* a multiple of n_kv_heads, with n_q_heads / n_kv_heads <= 16 */
+    int32_t max_seqs;        /* sequence slots */
+    int32_t reserved0;
+    int64_t max_ctx;         /* positions a slot can hold (sets the body capacity) */
+    int32_t k_body;          /* kvq_fmt of K body records */
+    int32_t v_body;          /* kvq_fmt of V body records; must share K's rotation */
+    int32_t journal;         /* KVQ_TQ6_0 (rotated ring + exact tail) or KVQ_F16 / KVQ_BF16 */
+    int32_t tail_fmt;        /* exact store format, KVQ_F16 or KVQ_BF16 (equals journal when exact) */
+    int32_t tail;            /* T: exact tail positions; also the smallest allowed seal keep */
+    int32_t ring_capacity;   /* R: journal positions, a multiple of 128 */
+    float softmax_scale;     /* 0 selects 1/sqrt(head_dim) */
+    int32_t reserved1;
+} kvq_config;
+
+/* Byte accounting (KV cache math, "Bytes per token"; SJ-KVaRN §3 and §7.2). All figures
+ * cover every layer and KV head, K and V together. */
+typedef struct {
+    int64_t body_bytes_per_token;    /* compact body records */
+    int64_t f16_bytes_per_token;     /* the same shape at 16 bits: 2 x L x H x D x 2 */
+    int64_t journal_bytes_per_slot;  /* one journal ring position */
+    int64_t tail_bytes_per_slot;     /* one exact-tail position (0 without a tq6_0 journal) */
+    int64_t sink_bytes;              /* the 128-position sink of one sequence */
+    int64_t fixed_bytes_per_seq;     /* sink + full journal ring + tail of one sequence */
+    int64_t pool_bytes;              /* device pool kv_create needs for this config */
+} kvq_bytes;
+
+typedef struct kvq_cache kvq_cache;  /* opaque host-side handle */
+
+/* kv_bytes_per_token — closed-form sizes of a config (KV cache math, "Bytes per token":
+ * 2 x layers x KV heads x head_dim x bytes per value; block formats by block bytes).
+ * Pure host arithmetic; out is a host pointer. KVQ_EINVAL on a bad config. */
+kvq_status kv_bytes_per_token(const kvq_config* cfg, kvq_bytes* out);
+
+/* kv_required_bytes — device pool bytes for kv_create and workspace bytes for
+ * kv_decode_attn with up to cfg->max_seqs sequences per call. Host pointers out. */
+kvq_status kv_required_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* workspace_bytes);
+
+/* kv_create — bind a config to a caller-owned device pool (>= pool_bytes from
+ * kv_required_bytes, 256-byte aligned) on CUDA device `device`. Every slot starts empty
+ * (N = 0, sealed end S = 128). Zeroes the pool's status word (synchronously). The handle
+ * is freed by kv_destroy; the pool stays the caller's. */
+kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes, int device,
+                     kvq_cache** out);
+kvq_status kv_destroy(kvq_cache* cache);
+
+/* kv_reset — empty one slot of one layer (layer -1: all layers). Host metadata only. */
+kvq_status kv_reset(kvq_cache* cache, int layer, int seq);
+
+/* kv_append — SJ-KVaRN §2.1: write positions N..N+n_tok-1 of each listed sequence of one
+ * layer. k, v: device fp16 [n_seq][n_tok][H][D]. Position p < 128 goes to the fp16 sink;
+ * p >= 128 goes to the journal slot (p - 128) mod R — tq6_0 of the rotated vector, or a
+ * verbatim F16 / round-to-nearest-even BF16 copy — and, with a tq6_0 journal, also to the
+ * exact tail slot p mod T. seq_ids: host int32 [n_seq], distinct. KVQ_ENOSPC (no write)
+ * if a journal would hold more than R unsealed positions or N would exceed max_ctx. */
+kvq_status kv_append(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq, int n_tok,
+                     const void* k, const void* v, void* stream);
+
+/* kv_seal — SJ-KVaRN §2.1 item 4 and §4.3: for each listed sequence of `layer` (-1: all
+ * layers) seal every full 128-position group g with S + 128 <= N - keep into body records,
+ * oldest first, and advance S. keep >= T. groups_sealed (host, may be NULL) receives the
+ * number of (layer, sequence) groups sealed. The count is decided on the host before launch. */
+kvq_status kv_seal(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq, int keep,
+                   int64_t* groups_sealed, void* stream);
+
+/* kv_decode_attn — one decode step of attention for each listed sequence of one layer over
+ * all N positions it holds: scores s_i = scale * <q, k_i> with the raw query on the exact
+ * regions (sink, exact tail, exact journal) and the rotated query R q on the rotated regions
+ * (body, tq6_0 ring span); one softmax over all positions; the rotated regions' weighted
+ * sum rotated back once (KV cache math, "rotate first"; KV Cache Precision Tail §2).
+ * q: device fp16 [n_seq][Hq][D]; out: device fp16 [n_seq][Hq][D].
+ * workspace: device, >= workspace_bytes of kv_required_bytes, zero-filled before its first
+ * use; each call leaves it ready for the next. Calls sharing a workspace must not overlap. */
+kvq_status kv_decode_attn(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq,
+                          const void* q, void* out, void* workspace, size_t ws_bytes, void* stream);
+
+/* kv_decode_step — one decode step over layers [0, n_layers) issued from C: for each layer
+ * l, kv_append of one position per sequence, then kv_seal(l, keep) of the sequences whose
+ * journal calls for it, then kv_decode_attn. Seal policy: seal_trigger > 0 seals a sequence
+ * when its journal holds seal_trigger positions (SJ-KVaRN §4.3 adaptive tail: grow to 8,192,
+ * seal back to the newest 4,096); seal_trigger == 0 seals whenever a full group older than
+ * keep exists; seal_trigger < 0 never seals. Layouts: q [n_layers][n_seq][Hq][D], k and v
+ * [n_layers][n_seq][1][H][D], out [n_layers][n_seq][Hq][D], all device fp16.
+ * events (may be NULL): 2 * n_layers caller-created cudaEvent_t handles; events[2l] and
+ * events[2l+1] are recorded on `stream` just before and after layer l's attention.
+ * groups_sealed (host, may be NULL) receives the groups sealed in this step. Stops at the
+ * first failing call and returns its status; earlier layers stay applied. */
+kvq_status kv_decode_step(kvq_cache* cache, int n_layers, const int32_t* seq_ids, int n_seq,
+                          const void* q, const void* k, const void* v, void* out,
+                          int seal_trigger, int keep, void* workspace, size_t ws_bytes,
+                          void* const* events, int64_t* groups_sealed, void* stream);
+
+/* kv_snapshot_size / kv_snapshot / kv_restore — copy the host-side lengths of every slot
+ * out of, or back into, a cache handle (host memory of kv_snapshot_size bytes). Restoring
+ * is valid only together with the device pool contents of the same moment; the caller owns
+ * both copies. Used to replay a benchmark from one starting state. */
+kvq_status kv_snapshot_size(const kvq_cache* cache, size_t* bytes);
+kvq_status kv_snapshot(const kvq_cache* cache, void* buf, size_t bytes);
+kvq_status kv_restore(kvq_cache* cache, const void* buf, size_t bytes);
+
+/* kv_state — host copies of one slot's lengths. */
+kvq_status kv_state(const kvq_cache* cache, int layer, int seq, int64_t* n_tokens, int64_t* sealed_end);
+
+/* kv_get_status — read (synchronously) and clear the device status word. Bit 0: a
+ * non-finite scale was produced by an encoder. Returns KVQ_EDEVICE if any bit was set. */
+kvq_status kv_get_status(kvq_cache* cache, uint32_t* word);
+
+/* ---------------------------------------------------------------------------------------
+ * Test and inspection calls (not on the decode path).
+ * ------------------------------------------------------------------------------------- */
+
+/* kv_dequant — decode positions [p0, p0+n) of (layer, seq, KV head, which: 0 = K, 1 = V)
+ * from whichever region holds them, into device fp32 out [n][D]: sink/exact values as
+ * stored, body and tq6_0 ring values in the rotated domain, with the format's dequant
+ * arithmetic (bit-exact definition). Positions must lie in [0, N). */
+kvq_status kv_dequant(kvq_cache* cache, int layer, int seq, int head, int which, int64_t p0,
+                      int64_t n, float* out, void* stream);
+
+/* Region ids for kv_region_ptr. */
+enum {
+    KVQ_REGION_SINK = 0,        /* fp16 [128][D] */
+    KVQ_REGION_JOURNAL = 1,     /* tq6_0: codes [R][D/128][96]; exact: [R][D] 16-bit */
+    KVQ_REGION_JOURNAL_SCALE = 2, /* tq6_0 only: fp16 [R][D/128] */
+    KVQ_REGION_TAIL = 3,        /* tq6_0 journal only: [T][D] 16-bit */
+    KVQ_REGION_BODY = 4         /* records [capacity groups][record bytes] */
+};
+
+/* kv_region_ptr — device address and byte size of one region's storage for
+ * (layer, seq, KV head, which). For inspection (byte-exact comparisons) only. */
+kvq_status kv_region_ptr(const kvq_cache* cache, int layer, int seq, int head, int which,
+                         int region, void** ptr, size_t* bytes);
+
+/* kv_format_tables — the constants this library derived on its own at load time: the TBQ4
+ * centroids and boundaries (fp32, Lloyd-Max for N(0, 1/128)) and the four splitmix64 sign
+ * words. Host pointers; any may be NULL. */
+kvq_status kv_format_tables(float centroids[16], float boundaries[15], uint64_t sign_words[4]);
+
+/* kv_status_string — static description of a status code. */
+const char* kv_status_string(kvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

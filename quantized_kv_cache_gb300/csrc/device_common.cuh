@@ -1,0 +1,57 @@
+// Device-side helpers shared by the CUDA translation units: pool addressing, 16-bit
+// conversions and the per-translation-unit copy of the format constants.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// Each translation unit holds its own copy (no relocatable device code); the host
+// uploads the same values to every copy once.
+static __constant__ FormatTables c_tab;
+
+__device__ __forceinline__ char* pool_at(const void* pool, int64_t off) {
+    return (char*)pool + off;
+}
+
+__device__ __forceinline__ uint16_t* sink_row(const Layout& L, const void* pool, int w, int64_t unit, int pos) {
+    return (uint16_t*)pool_at(pool, L.sink_off[w] + unit * L.sink_stride[w]) + (int64_t)pos * L.D;
+}
+// tq6_0 journal: code row (D/128 blocks of [ql 64 | qh 32]) and scale row (D/128 fp16).
+__device__ __forceinline__ uint8_t* jcode_row(const Layout& L, const void* pool, int w, int64_t unit, int slot) {
+    return (uint8_t*)pool_at(pool, L.jcode_off[w] + unit * L.jcode_stride[w]) + (int64_t)slot * L.jrow_bytes;
+}
+__device__ __forceinline__ uint16_t* jscale_row(const Layout& L, const void* pool, int w, int64_t unit, int slot) {
+    return (uint16_t*)pool_at(pool, L.jscale_off[w] + unit * L.jscale_stride[w]) + (int64_t)slot * (L.D / 128);
+}
+// Exact journal row (16-bit, D values) shares the jcode area.
+__device__ __forceinline__ uint16_t* jexact_row(const Layout& L, const void* pool, int w, int64_t unit, int slot) {
+    return (uint16_t*)pool_at(pool, L.jcode_off[w] + unit * L.jcode_stride[w]) + (int64_t)slot * L.D;
+}
+__device__ __forceinline__ uint16_t* tail_row(const Layout& L, const void* pool, int w, int64_t unit, int slot) {
+    return (uint16_t*)pool_at(pool, L.tail_off[w] + unit * L.tail_stride[w]) + (int64_t)slot * L.D;
+}
+__device__ __forceinline__ uint8_t* body_rec(const Layout& L, const void* pool, int w, int64_t unit, int g) {
+    return (uint8_t*)pool_at(pool, L.body_off[w] + unit * L.body_stride[w]) + (int64_t)g * L.rec_bytes[w];
+}
+__device__ __forceinline__ uint32_t* status_word(const Layout& L, const void* pool) {
+    return (uint32_t*)pool_at(pool, L.status_off);
+}
+
+__device__ __forceinline__ int journal_slot(const Layout& L, int pos) { return (pos - kSink) % L.R; }
+
+__device__ __forceinline__ float h2f(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+__device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+__device__ __forceinline__ float x16_to_f(uint16_t b, int fmt) { return fmt == KVQ_BF16 ? bf2f(b) : h2f(b); }
+__device__ __forceinline__ uint16_t f2h_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+__device__ __forceinline__ uint16_t f2bf_bits(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// -1 where bit i of the splitmix64 sign words is set (i < 128; set 0 = s1, 1 = s2).
+__device__ __forceinline__ bool sign_neg(int set, int i) {
+    return (c_tab.sign_words[2 * set + (i >> 6)] >> (i & 63)) & 1ULL;
+}
+
+}  // namespace kvq

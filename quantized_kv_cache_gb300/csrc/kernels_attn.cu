@@ -1,0 +1,545 @@
+// Split-K decode attention over every region of the cache, then a log-sum-exp merge.
+//
+// Work item = (sequence, KV head, span of positions inside one region). Each CTA of
+// decode_split_kernel streams its span in tiles: all threads decode the tile's K and V
+// records into shared memory as fp16 (scales applied), then warps run tensor-core
+// mma.sync m16n8k16 (fp16 in, fp32 accumulate): S^T = K Q^T with positions on M and the
+// GQA query group on N, an online softmax in the log2 domain, and O^T += V^T P^T with
+// channels on M. Rotated regions (body, tq6_0 ring span) are read with the rotated query
+// R q; at the end of the item the partial output is rotated back (R^T), so every partial
+// is in the original domain (KV cache math, "rotate first": the query is rotated once and
+// the output rotated back once; R^T distributes over the merge sum).
+// decode_merge_kernel combines the partials of one (sequence, KV head) under one softmax:
+// m* = max m_c, l* = sum 2^(m_c - m*) l_c, o = sum 2^(m_c - m*) o_c / l* (KV Cache
+// Precision Tail §2: results combined under one softmax; HAL #582 §5 P2: exact online-
+// softmax combine of typed regions).
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cfloat>
+#include "device_common.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTbqScale = 0.0883883461356163f;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                 : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ void store8(__half* dst, const float (&v)[8]) {
+    uint4 u;
+    u.x = pack_h2(v[0], v[1]);
+    u.y = pack_h2(v[2], v[3]);
+    u.z = pack_h2(v[4], v[5]);
+    u.w = pack_h2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dst) = u;
+}
+
+// Block-wide FWHT over rows of n values (shared fp32), ascending strides.
+__device__ void block_fwht_rows(float* xs, int total, int n) {
+    for (int s = 1; s < n; s <<= 1) {
+        for (int p = threadIdx.x; p < total / 2; p += blockDim.x) {
+            const int blk = p / (n / 2), q = p % (n / 2);
+            const int i = blk * n + (q / s) * 2 * s + (q % s);
+            const float a = xs[i], b = xs[i + s];
+            xs[i] = a + b;
+            xs[i + s] = a - b;
+        }
+        __syncthreads();
+    }
+}
+
+// Forward (inverse = false) or inverse rotation of `rows` vectors of D values in xs.
+__device__ void rotate_rows(float* xs, int rows, int D, int rot, bool inverse) {
+    const int total = rows * D;
+    if (rot == ROT_HAD256) {
+        block_fwht_rows(xs, total, 256);
+        for (int i = threadIdx.x; i < total; i += blockDim.x) xs[i] *= 0.0625f;
+        __syncthreads();
+    } else if (rot == ROT_TBQ128) {
+        const int first = inverse ? 1 : 0;
+        for (int i = threadIdx.x; i < total; i += blockDim.x)
+            if (sign_neg(first, i & 127)) xs[i] = -xs[i];
+        __syncthreads();
+        block_fwht_rows(xs, total, 128);
+        for (int i = threadIdx.x; i < total; i += blockDim.x) {
+            float y = xs[i];
+            if (sign_neg(1 - first, i & 127)) y = -y;
+            xs[i] = y * kTbqScale;
+        }
+        __syncthreads();
+    }
+}
+
+struct Item {
+    int b, h, kind, t0, t1, slot;
+};
+
+__device__ __forceinline__ Item decode_item(const AttnParams& p, int item) {
+    Item it;
+    int b = 0;
+    while (b + 1 < p.n_seq && p.seq[b + 1].first_item <= item) ++b;
+    const SeqSpan& s = p.seq[b];
+    const int local = item - s.first_item;
+    it.b = b;
+    it.h = local / s.items_per_head;
+    int c = local % s.items_per_head;
+    int r = 0;
+    while (r < 3 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
+    it.kind = s.kind[r];
+    it.t0 = s.lo[r] + c * p.chunk;
+    it.t1 = min(it.t0 + p.chunk, s.hi[r]);
+    it.slot = s.slot;
+    return it;
+}
+
+// --------------------------------------------------------------------------- tile fill
+// Token-major exact rows (sink, exact tail, exact journal) into dst[TILE][LD].
+template <int D, int TILE, int LD>
+__device__ void fill_exact(const Layout& L, const void* pool, int w, int64_t unit, int kind, int tstart,
+                           int nvalid, __half* dst) {
+    constexpr int U = D / 8;     // 16-byte units per row
+    const int fmt = (kind == RK_SINK) ? KVQ_F16 : (kind == RK_TAIL ? L.tail_fmt : L.journal);
+    for (int e = threadIdx.x; e < TILE * U; e += kThreads) {
+        const int i = e / U, u = e % U;
+        __half* o = dst + i * LD + 8 * u;
+        if (i >= nvalid) {
+            *reinterpret_cast<uint4*>(o) = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const int pos = tstart + i;
+        const uint16_t* row;
+        if (kind == RK_SINK) row = sink_row(L, pool, w, unit, pos);
+        else if (kind == RK_TAIL) row = tail_row(L, pool, w, unit, pos % L.T);
+        else row = jexact_row(L, pool, w, unit, journal_slot(L, pos));
+        const uint4 raw = *reinterpret_cast<const uint4*>(row + 8 * u);
+        if (fmt == KVQ_F16) {
+            *reinterpret_cast<uint4*>(o) = raw;
+        } else {
+            const uint16_t* r16 = reinterpret_cast<const uint16_t*>(&raw);
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = bf2f(r16[k]);
+            store8(o, v);
+        }
+    }
+}
+
+// tq6_0 ring rows (rotated domain), token-major.
+template <int D, int TILE, int LD>
+__device__ void fill_ring(const Layout& L, const void* pool, int w, int64_t unit, int tstart, int nvalid,
+                          __half* dst) {
+    constexpr int U = D / 8;
+    for (int e = threadIdx.x; e < TILE * U; e += kThreads) {
+        const int i = e / U, u = e % U;
+        __half* o = dst + i * LD + 8 * u;
+        if (i >= nvalid) {
+            *reinterpret_cast<uint4*>(o) = make_uint4(0, 0, 0, 0);
+            continue;
+        }
+        const int slot = journal_slot(L, tstart + i);
+        const int c0 = 8 * u, blk = c0 >> 7, j0 = c0 & 127;
+        const uint8_t* row = jcode_row(L, pool, w, unit, slot) + 96 * blk;
+        const float d = h2f(jscale_row(L, pool, w, unit, slot)[blk]);
+        const uint32_t ql = *reinterpret_cast<const uint32_t*>(row + (j0 >> 1));
+        const uint16_t qh = *reinterpret_cast<const uint16_t*>(row + 64 + (j0 >> 2));
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int code = ((ql >> (4 * k)) & 15) | (((qh >> (2 * k)) & 3) << 4);
+            v[k] = (float)(code - 32) * d;
+        }
+        store8(o, v);
+    }
+}
+
+// Body K records (token-major) of one tile: positions [tstart, tstart + TILE) of group g.
+template <int D, int TILE, int LD>
+__device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
+                            const float* cent) {
+    const int fmt = L.fmt[0];
+    const uint8_t* rec = body_rec(L, pool, 0, unit, g);
+    constexpr int U = D / 8;
+    for (int e = threadIdx.x; e < TILE * U; e += kThreads) {
+        const int i = e / U, u = e % U;
+        const int t = rel + i, c0 = 8 * u;
+        float v[8];
+        if (fmt == KVQ_TBQ4) {
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));
+            const float n = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 128) + (c0 >> 7)]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = cent[(w4 >> (4 * k)) & 15] * n;
+        } else if (fmt == KVQ_Q8_0) {
+            const uint2 w8 = *reinterpret_cast<const uint2*>(rec + t * D + c0);
+            const float d = h2f(reinterpret_cast<const uint16_t*>(rec + 128 * D)[t * (D / 32) + (c0 >> 5)]);
+            const int8_t* q = reinterpret_cast<const int8_t*>(&w8);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = (float)q[k] * d;
+        } else if (fmt == KVQ_Q4_0) {
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));
+            const float d = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 32) + (c0 >> 5)]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = (float)((int)((w4 >> (4 * k)) & 15) - 8) * d;
+        } else {   // KVarN
+            const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+            const int hh = c0 >> 8, j0 = c0 & 255;
+            const uint8_t* tr = rec + (int64_t)hh * (4096 * bits + 1152);
+            const uint32_t lo = *reinterpret_cast<const uint32_t*>(tr + t * 128 + (j0 >> 1));
+            const uint32_t hi = (bits == 5) ? tr[16384 + t * 32 + (j0 >> 3)] : 0u;
+            const uint16_t* sb = reinterpret_cast<const uint16_t*>(tr + 4096 * bits);
+            const float S = h2f(sb[t]), Z = h2f(sb[128 + t]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int code = ((lo >> (4 * k)) & 15) | (((hi >> k) & 1) << 4);
+                v[k] = ((float)code * S + Z) * h2f(sb[256 + j0 + k]);
+            }
+        }
+        store8(dst + i * LD + c0, v);
+    }
+}
+
+// Body V records (channel-major) of one tile into dst[D][LDV] (channel-major smem).
+template <int D, int TILE, int LDV>
+__device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
+                            const float* cent) {
+    const int fmt = L.fmt[1];
+    const uint8_t* rec = body_rec(L, pool, 1, unit, g);
+    constexpr int U = TILE / 8;   // 8-token units per channel
+    for (int e = threadIdx.x; e < D * U; e += kThreads) {
+        const int c = e / U, u = e % U;
+        const int t0 = rel + 8 * u;
+        float v[8];
+        if (fmt == KVQ_TBQ4) {
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + c * 64 + (t0 >> 1));
+            const uint16_t* nr = reinterpret_cast<const uint16_t*>(rec + 64 * D);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = cent[(w4 >> (4 * k)) & 15] * h2f(nr[(t0 + k) * (D / 128) + (c >> 7)]);
+        } else if (fmt == KVQ_Q4_0) {
+            const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + c * 64 + (t0 >> 1));
+            const uint16_t* dr = reinterpret_cast<const uint16_t*>(rec + 64 * D);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                v[k] = (float)((int)((w4 >> (4 * k)) & 15) - 8) * h2f(dr[(t0 + k) * (D / 32) + (c >> 5)]);
+        } else if (fmt == KVQ_Q8_0) {
+            const uint2 w8 = *reinterpret_cast<const uint2*>(rec + c * 128 + t0);
+            const int8_t* q = reinterpret_cast<const int8_t*>(&w8);
+            const uint16_t* dr = reinterpret_cast<const uint16_t*>(rec + 128 * D);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = (float)q[k] * h2f(dr[(t0 + k) * (D / 32) + (c >> 5)]);
+        } else {   // KVarN
+            const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+            const int hh = c >> 8, j = c & 255;
+            const uint8_t* tr = rec + (int64_t)hh * (4096 * bits + 1152);
+            const uint32_t lo = *reinterpret_cast<const uint32_t*>(tr + j * 64 + (t0 >> 1));
+            const uint32_t hi = (bits == 5) ? tr[16384 + j * 16 + (t0 >> 3)] : 0u;
+            const uint16_t* sb = reinterpret_cast<const uint16_t*>(tr + 4096 * bits);
+            const float C = h2f(sb[256 + j]);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int code = ((lo >> (4 * k)) & 15) | (((hi >> k) & 1) << 4);
+                v[k] = ((float)code * h2f(sb[t0 + k]) + h2f(sb[128 + t0 + k])) * C;
+            }
+        }
+        store8(dst + c * LDV + t0 - rel, v);
+    }
+}
+
+// --------------------------------------------------------------------------- split kernel
+template <int D, int NQ>
+struct Cfg {
+    static constexpr int TILE = (D == 512) ? 32 : 64;
+    static constexpr int LDK = D + 8;              // token-major row stride (halves)
+    static constexpr int LDV = TILE + 8;           // channel-major row stride (halves)
+    static constexpr int LDP = TILE + 8;
+    static constexpr int K_BYTES = TILE * LDK * 2;
+    static constexpr int V_BYTES = (TILE * LDK > D * LDV ? TILE * LDK : D * LDV) * 2;
+    static constexpr int Q_BYTES = NQ * LDK * 2;
+    static constexpr int S_BYTES = TILE * NQ * 4;
+    static constexpr int P_BYTES = NQ * LDP * 2;
+    static constexpr int QF_BYTES = NQ * D * 4;    // fp32 staging of q / the output rows
+    static constexpr int SMEM = K_BYTES + V_BYTES + Q_BYTES + S_BYTES + P_BYTES + QF_BYTES + 64 * 4 + 16 * 4;
+};
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnParams p) {
+    using C = Cfg<D, NQ>;
+    constexpr int TILE = C::TILE, LDK = C::LDK, LDV = C::LDV, LDP = C::LDP;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __half* Ks = reinterpret_cast<__half*>(smem);
+    __half* Vs = reinterpret_cast<__half*>(smem + C::K_BYTES);
+    __half* Qs = reinterpret_cast<__half*>(smem + C::K_BYTES + C::V_BYTES);
+    float* Ss = reinterpret_cast<float*>(smem + C::K_BYTES + C::V_BYTES + C::Q_BYTES);
+    __half* Ps = reinterpret_cast<__half*>(smem + C::K_BYTES + C::V_BYTES + C::Q_BYTES + C::S_BYTES);
+    float* QF = reinterpret_cast<float*>(smem + C::K_BYTES + C::V_BYTES + C::Q_BYTES + C::S_BYTES + C::P_BYTES);
+    float* stat = QF + NQ * D;          // m[16], l[16], alpha[16], cent[16]
+    float* m_run = stat;
+    float* l_run = stat + 16;
+    float* alpha = stat + 32;
+    float* cent = stat + 48;
+
+    const Item it = decode_item(p, blockIdx.x);
+    const int G = L.G;
+    const int64_t unit = L.unit(p.layer, it.slot, it.h);
+    const bool rotated = (it.kind == RK_BODY || it.kind == RK_RING) && L.rot != ROT_NONE;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+
+    if (threadIdx.x < 16) {
+        m_run[threadIdx.x] = -INFINITY;
+        l_run[threadIdx.x] = 0.f;
+        cent[threadIdx.x] = c_tab.cent[threadIdx.x];
+    }
+    // query rows of this KV head, rotated when the item reads a rotated region
+    const uint16_t* q = p.q + ((int64_t)it.b * L.Hq + (int64_t)it.h * G) * D;
+    for (int e = threadIdx.x; e < NQ * D; e += kThreads) {
+        const int r = e / D;
+        QF[e] = (r < G) ? h2f(q[e]) : 0.f;
+    }
+    __syncthreads();
+    if (rotated) rotate_rows(QF, NQ, D, L.rot, false);
+    for (int e = threadIdx.x; e < NQ * D; e += kThreads) {
+        const int r = e / D, c = e % D;
+        Qs[r * LDK + c] = __float2half_rn(QF[e]);
+    }
+    const float sc = L.scale * kLog2e;
+    const bool v_chmajor = (it.kind == RK_BODY);
+
+    constexpr int MT = D / 128;          // PV m-tiles of 16 channels per warp (warp: D/8 channels)
+    constexpr int NT = NQ / 8;
+    float acc[MT][NT][4];
+#pragma unroll
+    for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int bq = 0; bq < NT; ++bq)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[a][bq][k] = 0.f;
+    __syncthreads();
+
+    for (int tstart = it.t0; tstart < it.t1; tstart += TILE) {
+        const int nvalid = min(TILE, it.t1 - tstart);
+        // ---- decode the tile into shared memory
+        if (it.kind == RK_BODY) {
+            const int g = (tstart - kSink) / kGroup, rel = (tstart - kSink) % kGroup;
+            fill_body_k<D, TILE, LDK>(L, p.pool, unit, g, rel, Ks, cent);
+            fill_body_v<D, TILE, LDV>(L, p.pool, unit, g, rel, Vs, cent);
+        } else if (it.kind == RK_RING) {
+            fill_ring<D, TILE, LDK>(L, p.pool, 0, unit, tstart, nvalid, Ks);
+            fill_ring<D, TILE, LDK>(L, p.pool, 1, unit, tstart, nvalid, Vs);
+        } else {
+            fill_exact<D, TILE, LDK>(L, p.pool, 0, unit, it.kind, tstart, nvalid, Ks);
+            fill_exact<D, TILE, LDK>(L, p.pool, 1, unit, it.kind, tstart, nvalid, Vs);
+        }
+        __syncthreads();
+        // ---- scores: S^T[tok][q] = K Q^T, positions on M
+        if (warp < TILE / 16) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float c4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t a0, a1, a2, a3, b0, b1;
+                    ldsm_x4(smem_u32(Ks + (warp * 16 + (lane & 15)) * LDK + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+                    ldsm_x2(smem_u32(Qs + (nt * 8 + (lane & 7)) * LDK + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1);
+                    mma16816(c4, a0, a1, a2, a3, b0, b1);
+                }
+                const int r0 = warp * 16 + gq, qc = nt * 8 + 2 * tq;
+                Ss[r0 * NQ + qc] = (r0 < nvalid) ? c4[0] * sc : -INFINITY;
+                Ss[r0 * NQ + qc + 1] = (r0 < nvalid) ? c4[1] * sc : -INFINITY;
+                Ss[(r0 + 8) * NQ + qc] = (r0 + 8 < nvalid) ? c4[2] * sc : -INFINITY;
+                Ss[(r0 + 8) * NQ + qc + 1] = (r0 + 8 < nvalid) ? c4[3] * sc : -INFINITY;
+            }
+        }
+        __syncthreads();
+        // ---- online softmax (log2 domain), one warp per query
+        for (int qi = warp; qi < NQ; qi += kThreads / 32) {
+            float mt = -INFINITY;
+            for (int t = lane; t < TILE; t += 32) mt = fmaxf(mt, Ss[t * NQ + qi]);
+#pragma unroll
+            for (int s = 16; s >= 1; s >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, s));
+            const float mo = m_run[qi];
+            const float mn = fmaxf(mo, mt);
+            const float a = (mn == -INFINITY) ? 1.f : exp2f(mo - mn);
+            float sum = 0.f;
+            for (int t = lane; t < TILE; t += 32) {
+                const float s = Ss[t * NQ + qi];
+                const float pv = (mn == -INFINITY) ? 0.f : exp2f(s - mn);
+                const __half ph = __float2half_rn(pv);
+                Ps[qi * LDP + t] = ph;
+                sum += __half2float(ph);
+            }
+#pragma unroll
+            for (int s = 16; s >= 1; s >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, s);
+            __syncwarp();
+            if (lane == 0) {
+                m_run[qi] = mn;
+                l_run[qi] = l_run[qi] * a + sum;
+                alpha[qi] = a;
+            }
+        }
+        __syncthreads();
+        // ---- O^T[ch][q] += V^T P^T, channels on M; warp owns D/8 channels
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int ch0 = warp * (D / 8) + mt * 16;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float a0 = alpha[nt * 8 + 2 * tq], a1 = alpha[nt * 8 + 2 * tq + 1];
+                acc[mt][nt][0] *= a0;
+                acc[mt][nt][1] *= a1;
+                acc[mt][nt][2] *= a0;
+                acc[mt][nt][3] *= a1;
+            }
+#pragma unroll
+            for (int ks = 0; ks < TILE / 16; ++ks) {
+                uint32_t a0, a1, a2, a3;
+                const int mi = lane >> 3, ri = lane & 7;
+                if (v_chmajor) {
+                    ldsm_x4(smem_u32(Vs + (ch0 + (mi & 1) * 8 + ri) * LDV + ks * 16 + (mi >> 1) * 8), a0, a1, a2, a3);
+                } else {
+                    ldsm_x4_t(smem_u32(Vs + (ks * 16 + (mi >> 1) * 8 + ri) * LDK + ch0 + (mi & 1) * 8), a0, a1, a2, a3);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint32_t b0, b1;
+                    ldsm_x2(smem_u32(Ps + (nt * 8 + (lane & 7)) * LDP + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1);
+                    mma16816(acc[mt][nt], a0, a1, a2, a3, b0, b1);
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // ---- partial: o in the original domain (rotated items rotated back), m and l
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int ch0 = warp * (D / 8) + mt * 16;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int qc = nt * 8 + 2 * tq;
+            QF[qc * D + ch0 + gq] = acc[mt][nt][0];
+            QF[(qc + 1) * D + ch0 + gq] = acc[mt][nt][1];
+            QF[qc * D + ch0 + gq + 8] = acc[mt][nt][2];
+            QF[(qc + 1) * D + ch0 + gq + 8] = acc[mt][nt][3];
+        }
+    }
+    __syncthreads();
+    if (rotated) rotate_rows(QF, NQ, D, L.rot, true);
+    float* part = p.partials + (size_t)blockIdx.x * (2 * NQ + NQ * D);
+    if (threadIdx.x < NQ) {
+        part[threadIdx.x] = m_run[threadIdx.x];
+        part[NQ + threadIdx.x] = l_run[threadIdx.x];
+    }
+    float4* po = reinterpret_cast<float4*>(part + 2 * NQ);
+    const float4* qf4 = reinterpret_cast<const float4*>(QF);
+    for (int e = threadIdx.x; e < NQ * D / 4; e += kThreads) po[e] = qf4[e];
+}
+
+// --------------------------------------------------------------------------- merge kernel
+// grid (n_seq * H, D / 64); 256 threads; thread handles (q, channel) pairs of its chunk.
+template <int D, int NQ>
+__global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
+    const int bh = blockIdx.x;
+    const int b = bh / L.H, h = bh % L.H;
+    const SeqSpan& s = p.seq[b];
+    const int first = s.first_item + h * s.items_per_head, cnt = s.items_per_head;
+    const int G = L.G;
+    __shared__ float mstar[NQ], lstar[NQ];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t stride = 2 * NQ + NQ * D;
+    for (int qi = warp; qi < G; qi += 8) {
+        float m = -INFINITY;
+        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, p.partials[(first + c) * stride + qi]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int c = lane; c < cnt; c += 32) {
+            const float* pc = p.partials + (first + c) * stride;
+            if (pc[qi] != -INFINITY) l += exp2f(pc[qi] - m) * pc[NQ + qi];
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            mstar[qi] = m;
+            lstar[qi] = l;
+        }
+    }
+    __syncthreads();
+    const int c0 = blockIdx.y * 64;
+    for (int e = threadIdx.x; e < G * 64; e += blockDim.x) {
+        const int qi = e / 64, ch = c0 + e % 64;
+        const float m = mstar[qi];
+        float o = 0.f;
+        for (int c = 0; c < cnt; ++c) {
+            const float* pc = p.partials + (first + c) * stride;
+            const float mc = pc[qi];
+            if (mc != -INFINITY) o += exp2f(mc - m) * pc[2 * NQ + qi * D + ch];
+        }
+        const float l = lstar[qi];
+        p.out[((int64_t)b * L.Hq + (int64_t)h * G + qi) * D + ch] = f2h_bits(o / l);
+    }
+}
+
+template <int D, int NQ>
+int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
+    using C = Cfg<D, NQ>;
+    static bool attr = false;
+    if (!attr) {
+        cudaFuncSetAttribute(decode_split_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        attr = true;
+    }
+    decode_split_kernel<D, NQ><<<p.total_items, kThreads, C::SMEM, s>>>(L, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return (int)e;
+    dim3 mg(p.n_seq * L.H, D / 64);
+    decode_merge_kernel<D, NQ><<<mg, 256, 0, s>>>(L, p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int upload_tables_attn(const FormatTables& t) {
+    return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
+}
+
+int launch_decode(const Layout& L, const AttnParams& p, void* stream) {
+    if (p.total_items == 0) return 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L.NQ == 8) {
+        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s);
+        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s);
+        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s);
+    } else {
+        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s);
+        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s);
+        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s);
+    }
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

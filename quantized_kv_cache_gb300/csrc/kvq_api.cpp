@@ -1,0 +1,512 @@
+// Host side of the C ABI (include/kvq.h): configuration checks, the device-pool layout,
+// host-authoritative lengths, work decomposition and kernel launches. Lengths of every
+// (layer, sequence) live here, so refusals happen before anything is enqueued, and the
+// decode work list is derived from them without reading device memory.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <set>
+#include <vector>
+#include "kvq_internal.h"
+#include "../../include/kvq_synth.h"
+
+using namespace kvq;
+
+struct kvq_cache {
+    kvq_config cfg;
+    Layout lay;
+    void* pool;
+    size_t pool_bytes;
+    int device;
+    int sm_count;
+    std::vector<int64_t> n_tok;   // [L][max_seqs]
+    std::vector<int64_t> sealed;  // [L][max_seqs]
+};
+
+namespace kvq {
+
+static bool is_body(int f) {
+    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || f == KVQ_KVARN4 || f == KVQ_KVARN5;
+}
+
+bool make_layout(const kvq_config& c, Layout* out) {
+    Layout L{};
+    if (c.n_layers <= 0 || c.n_kv_heads <= 0 || c.max_seqs <= 0) return false;
+    if (c.head_dim != 128 && c.head_dim != 256 && c.head_dim != 512) return false;
+    if (c.n_q_heads <= 0 || c.n_q_heads % c.n_kv_heads) return false;
+    const int G = c.n_q_heads / c.n_kv_heads;
+    if (G > kMaxG) return false;
+    if (!is_body(c.k_body) || !is_body(c.v_body)) return false;
+    if (rotation_of(c.k_body) != rotation_of(c.v_body)) return false;
+    if (rotation_of(c.k_body) == ROT_HAD256 && c.head_dim % 256) return false;
+    if (c.journal != KVQ_TQ6_0 && c.journal != KVQ_F16 && c.journal != KVQ_BF16) return false;
+    if (c.tail_fmt != KVQ_F16 && c.tail_fmt != KVQ_BF16) return false;
+    if (c.journal != KVQ_TQ6_0 && c.tail_fmt != c.journal) return false;
+    if (c.tail <= 0 || c.ring_capacity <= 0 || c.ring_capacity % kGroup) return false;
+    if (c.ring_capacity < c.tail + kGroup) return false;   // a full group must fit beyond the tail
+    if (c.max_ctx < kSink + kGroup || c.max_ctx > (int64_t)1 << 30) return false;
+    if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return false;
+    L.L = c.n_layers; L.H = c.n_kv_heads; L.D = c.head_dim; L.Hq = c.n_q_heads; L.G = G;
+    L.NQ = G <= 8 ? 8 : 16;
+    L.max_seqs = c.max_seqs; L.T = c.tail; L.R = c.ring_capacity;
+    L.gcap = (int32_t)((c.max_ctx - kSink + kGroup - 1) / kGroup);
+    L.max_ctx = c.max_ctx;
+    L.fmt[0] = c.k_body; L.fmt[1] = c.v_body;
+    L.journal = c.journal; L.tail_fmt = c.tail_fmt; L.rot = rotation_of(c.k_body);
+    L.jrow_bytes = (c.journal == KVQ_TQ6_0) ? (c.head_dim / 128) * 96 : c.head_dim * 2;
+    L.scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / std::sqrt((float)c.head_dim);
+    const int64_t units = (int64_t)L.L * L.max_seqs * L.H;
+    int64_t off = 256;   // status word area
+    L.status_off = 0;
+    auto region = [&](int64_t per_unit, int64_t* o, int64_t* st, int w) {
+        st[w] = align256(per_unit);
+        o[w] = off;
+        off += st[w] * units;
+    };
+    for (int w = 0; w < 2; ++w) {
+        region((int64_t)kSink * L.D * 2, L.sink_off, L.sink_stride, w);
+        region((int64_t)L.R * L.jrow_bytes, L.jcode_off, L.jcode_stride, w);
+        if (c.journal == KVQ_TQ6_0) {
+            region((int64_t)L.R * (L.D / 128) * 2, L.jscale_off, L.jscale_stride, w);
+            region((int64_t)L.T * L.D * 2, L.tail_off, L.tail_stride, w);
+        }
+        L.rec_bytes[w] = record_bytes(L.fmt[w], L.D);
+        region((int64_t)L.gcap * L.rec_bytes[w], L.body_off, L.body_stride, w);
+    }
+    L.total = off;
+    *out = L;
+    return true;
+}
+
+}  // namespace kvq
+
+namespace {
+
+std::mutex g_tab_mu;
+std::set<int> g_tab_devices;
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+kvq_status ensure_tables(int device) {
+    std::lock_guard<std::mutex> lk(g_tab_mu);
+    if (g_tab_devices.count(device)) return KVQ_OK;
+    const FormatTables& t = host_tables();
+    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0) return KVQ_ECUDA;
+    g_tab_devices.insert(device);
+    return KVQ_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+kvq_status check_cache(const kvq_cache* c) {
+    if (!c) return KVQ_EINVAL;
+    if (current_device() != c->device) return KVQ_EINVAL;
+    return KVQ_OK;
+}
+
+kvq_status check_seqs(const kvq_cache* c, const int32_t* seq_ids, int n_seq) {
+    if (!seq_ids || n_seq <= 0 || n_seq > kMaxSeqPerCall) return n_seq > kMaxSeqPerCall ? KVQ_EUNSUPPORTED : KVQ_EINVAL;
+    for (int i = 0; i < n_seq; ++i) {
+        if (seq_ids[i] < 0 || seq_ids[i] >= c->cfg.max_seqs) return KVQ_EINVAL;
+        for (int j = 0; j < i; ++j)
+            if (seq_ids[j] == seq_ids[i]) return KVQ_EINVAL;
+    }
+    return KVQ_OK;
+}
+
+int64_t& NT(kvq_cache* c, int l, int s) { return c->n_tok[(size_t)l * c->cfg.max_seqs + s]; }
+int64_t& ST(kvq_cache* c, int l, int s) { return c->sealed[(size_t)l * c->cfg.max_seqs + s]; }
+
+kvq_status cuda_status(int e) { return e == 0 ? KVQ_OK : KVQ_ECUDA; }
+
+size_t workspace_items(const kvq_config& c) {
+    const int n = std::min(c.max_seqs, kMaxSeqPerCall);
+    return 2048 + (size_t)4 * c.n_kv_heads * n;
+}
+
+// Region spans of one sequence in read order (sink, body, ring or exact journal, tail).
+int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[4], int32_t hi[4], int32_t kind[4]) {
+    int n = 0;
+    auto add = [&](int64_t a, int64_t b, int k) {
+        if (b > a) { lo[n] = (int32_t)a; hi[n] = (int32_t)b; kind[n] = k; ++n; }
+    };
+    add(0, std::min<int64_t>(N, kSink), RK_SINK);
+    add(kSink, S, RK_BODY);
+    if (L.journal == KVQ_TQ6_0) {
+        const int64_t E = std::max<int64_t>(S, N - L.T);
+        add(S, E, RK_RING);
+        add(std::max<int64_t>(E, kSink), N, RK_TAIL);
+    } else {
+        add(std::max<int64_t>(S, kSink), N, RK_JEXACT);
+    }
+    for (int i = n; i < 4; ++i) { lo[i] = hi[i] = 0; kind[i] = 0; }
+    return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kv_status_string(kvq_status s) {
+    switch (s) {
+        case KVQ_OK: return "ok";
+        case KVQ_EINVAL: return "invalid argument";
+        case KVQ_ENOSPC: return "journal or context capacity exceeded";
+        case KVQ_EUNSUPPORTED: return "unsupported configuration";
+        case KVQ_ECUDA: return "CUDA error";
+        case KVQ_EDEVICE: return "device status word set";
+    }
+    return "unknown status";
+}
+
+kvq_status kv_bytes_per_token(const kvq_config* cfg, kvq_bytes* out) {
+    if (!cfg || !out) return KVQ_EINVAL;
+    Layout L;
+    if (!make_layout(*cfg, &L)) return KVQ_EINVAL;
+    const int64_t LH = (int64_t)L.L * L.H;
+    kvq_bytes b{};
+    b.body_bytes_per_token = LH * (L.rec_bytes[0] + L.rec_bytes[1]) / kGroup;
+    b.f16_bytes_per_token = 2 * LH * L.D * 2;
+    b.journal_bytes_per_slot = 2 * LH * (cfg->journal == KVQ_TQ6_0 ? (int64_t)(L.D / 128) * 98 : (int64_t)L.D * 2);
+    b.tail_bytes_per_slot = cfg->journal == KVQ_TQ6_0 ? 2 * LH * L.D * 2 : 0;
+    b.sink_bytes = 2 * LH * kSink * L.D * 2;
+    b.fixed_bytes_per_seq = b.sink_bytes + b.journal_bytes_per_slot * L.R + b.tail_bytes_per_slot * L.T;
+    b.pool_bytes = L.total;
+    *out = b;
+    return KVQ_OK;
+}
+
+kvq_status kv_required_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* workspace_bytes) {
+    if (!cfg) return KVQ_EINVAL;
+    Layout L;
+    if (!make_layout(*cfg, &L)) return KVQ_EINVAL;
+    if (pool_bytes) *pool_bytes = (size_t)L.total;
+    if (workspace_bytes) *workspace_bytes = workspace_items(*cfg) * (2 * L.NQ + (size_t)L.NQ * L.D) * sizeof(float);
+    return KVQ_OK;
+}
+
+kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes, int device, kvq_cache** out) {
+    if (!cfg || !out || !device_pool) return KVQ_EINVAL;
+    Layout L;
+    if (!make_layout(*cfg, &L)) return KVQ_EINVAL;
+    if (pool_bytes < (size_t)L.total || ((uintptr_t)device_pool & 255)) return KVQ_EINVAL;
+    if (current_device() != device) return KVQ_EINVAL;
+    kvq_status st = ensure_tables(device);
+    if (st != KVQ_OK) return st;
+    if (cudaMemset(device_pool, 0, 256) != cudaSuccess) return KVQ_ECUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KVQ_ECUDA;
+    kvq_cache* c = new kvq_cache;
+    c->cfg = *cfg;
+    c->lay = L;
+    c->pool = device_pool;
+    c->pool_bytes = pool_bytes;
+    c->device = device;
+    c->sm_count = sms;
+    c->n_tok.assign((size_t)L.L * cfg->max_seqs, 0);
+    c->sealed.assign((size_t)L.L * cfg->max_seqs, kSink);
+    *out = c;
+    return KVQ_OK;
+}
+
+kvq_status kv_destroy(kvq_cache* c) {
+    if (!c) return KVQ_EINVAL;
+    delete c;
+    return KVQ_OK;
+}
+
+kvq_status kv_reset(kvq_cache* c, int layer, int seq) {
+    if (!c || seq < 0 || seq >= c->cfg.max_seqs || layer < -1 || layer >= c->cfg.n_layers) return KVQ_EINVAL;
+    for (int l = 0; l < c->cfg.n_layers; ++l) {
+        if (layer >= 0 && l != layer) continue;
+        NT(c, l, seq) = 0;
+        ST(c, l, seq) = kSink;
+    }
+    return KVQ_OK;
+}
+
+kvq_status kv_append(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, int n_tok,
+                     const void* k, const void* v, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (layer < 0 || layer >= c->cfg.n_layers || n_tok <= 0 || !k || !v || !aligned16(k) || !aligned16(v))
+        return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    if ((int64_t)n_seq * n_tok > (int64_t)1 << 31) return KVQ_EINVAL;
+    AppendParams p{};
+    p.pool = c->pool;
+    p.k = (const uint16_t*)k;
+    p.v = (const uint16_t*)v;
+    p.layer = layer;
+    p.n_seq = n_seq;
+    p.n_tok = n_tok;
+    for (int i = 0; i < n_seq; ++i) {
+        const int s = seq_ids[i];
+        const int64_t N = NT(c, layer, s), S = ST(c, layer, s);
+        if (N + n_tok > c->cfg.max_ctx) return KVQ_ENOSPC;
+        if (std::max<int64_t>(N + n_tok, kSink) - S > c->cfg.ring_capacity) return KVQ_ENOSPC;
+        p.slot[i] = s;
+        p.n0[i] = (int32_t)N;
+    }
+    const int e = launch_append(c->lay, p, stream);
+    if (e != 0) return KVQ_ECUDA;
+    for (int i = 0; i < n_seq; ++i) NT(c, layer, seq_ids[i]) += n_tok;
+    return KVQ_OK;
+}
+
+kvq_status kv_seal(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, int keep,
+                   int64_t* groups_sealed, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (layer < -1 || layer >= c->cfg.n_layers || keep < c->cfg.tail) return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    const int l0 = layer < 0 ? 0 : layer, l1 = layer < 0 ? c->cfg.n_layers : layer + 1;
+    // groups per (layer, seq): every full group with S + 128 <= N - keep
+    auto groups_of = [&](int l, int s) -> int64_t {
+        const int64_t lim = NT(c, l, s) - keep - ST(c, l, s);
+        return lim >= kGroup ? lim / kGroup : 0;
+    };
+    int64_t total = 0;
+    int l = l0;
+    while (l < l1) {
+        // extend the launch over layers whose per-sequence state matches layer l
+        int le = l + 1;
+        auto same = [&](int a, int b) {
+            for (int i = 0; i < n_seq; ++i) {
+                const int s = seq_ids[i];
+                if (NT(c, a, s) != NT(c, b, s) || ST(c, a, s) != ST(c, b, s)) return false;
+            }
+            return true;
+        };
+        while (le < l1 && same(l, le)) ++le;
+        SealParams p{};
+        p.pool = c->pool;
+        p.layer0 = l;
+        p.n_layers = le - l;
+        p.n_seq = 0;
+        int32_t acc = 0;
+        for (int i = 0; i < n_seq; ++i) {
+            const int s = seq_ids[i];
+            const int64_t g = groups_of(l, s);
+            if (g <= 0) continue;
+            SealSeq& q = p.seq[p.n_seq++];
+            q.slot = s;
+            q.first_pos = (int32_t)ST(c, l, s);
+            q.first_group = (int32_t)((ST(c, l, s) - kSink) / kGroup);
+            q.n_groups = (int32_t)g;
+            q.prefix = acc;
+            acc += (int32_t)g;
+        }
+        p.groups_per_layer = acc;
+        if (acc > 0) {
+            if ((int64_t)acc * p.n_layers > 0x7fffffff) return KVQ_EINVAL;
+            const int e = launch_seal(c->lay, p, stream);
+            if (e != 0) return KVQ_ECUDA;
+            for (int ll = l; ll < le; ++ll)
+                for (int i = 0; i < p.n_seq; ++i)
+                    ST(c, ll, p.seq[i].slot) += (int64_t)kGroup * p.seq[i].n_groups;
+            total += (int64_t)acc * p.n_layers;
+        }
+        l = le;
+    }
+    if (groups_sealed) *groups_sealed = total;
+    return KVQ_OK;
+}
+
+kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (layer < 0 || layer >= c->cfg.n_layers || !q || !out || !workspace) return KVQ_EINVAL;
+    if (!aligned16(q) || !aligned16(out) || !aligned16(workspace)) return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    const Layout& L = c->lay;
+    size_t need = 0;
+    kv_required_bytes(&c->cfg, nullptr, &need);
+    if (ws_bytes < need) return KVQ_EINVAL;
+    const size_t cap = workspace_items(c->cfg);
+    AttnParams p{};
+    p.pool = c->pool;
+    p.q = (const uint16_t*)q;
+    p.out = (uint16_t*)out;
+    p.partials = (float*)workspace;
+    p.layer = layer;
+    p.n_seq = n_seq;
+    int64_t total_tok = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        const int64_t N = NT(c, layer, seq_ids[i]);
+        if (N <= 0) return KVQ_EINVAL;
+        total_tok += N;
+    }
+    // chunk: a multiple of 128 giving about two waves of resident CTAs
+    const int per_sm = (L.D == 512) ? 1 : (L.D == 256 ? 2 : 4);
+    const int64_t target = (int64_t)2 * c->sm_count * per_sm;
+    int64_t chunk = (total_tok * L.H + target - 1) / target;
+    chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
+    for (;;) {
+        int64_t items = 0;
+        for (int i = 0; i < n_seq; ++i) {
+            SeqSpan& s = p.seq[i];
+            s.slot = seq_ids[i];
+            s.n_tok = (int32_t)NT(c, layer, s.slot);
+            spans(L, s.n_tok, ST(c, layer, s.slot), s.lo, s.hi, s.kind);
+            s.items_per_head = 0;
+            for (int r = 0; r < 4; ++r) {
+                s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + chunk - 1) / chunk);
+                s.items_per_head += s.nchunk[r];
+            }
+            s.first_item = (int32_t)items;
+            items += (int64_t)s.items_per_head * L.H;
+        }
+        if ((size_t)items <= cap) {
+            p.total_items = (int32_t)items;
+            break;
+        }
+        chunk *= 2;
+    }
+    p.chunk = (int32_t)chunk;
+    const int e = launch_decode(L, p, stream);
+    return e == 0 ? KVQ_OK : KVQ_ECUDA;
+}
+
+kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
+                          const void* k, const void* v, void* out, int seal_trigger, int keep, void* workspace,
+                          size_t ws_bytes, void* const* events, int64_t* groups_sealed, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (n_layers <= 0 || n_layers > c->cfg.n_layers || !q || !k || !v || !out) return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    const Layout& L = c->lay;
+    const size_t qb = (size_t)n_seq * L.Hq * L.D * 2, kb = (size_t)n_seq * L.H * L.D * 2;
+    int64_t total = 0;
+    int32_t need[kMaxSeqPerCall];
+    for (int l = 0; l < n_layers; ++l) {
+        st = kv_append(c, l, seq_ids, n_seq, 1, (const char*)k + l * kb, (const char*)v + l * kb, stream);
+        if (st != KVQ_OK) return st;
+        int nn = 0;
+        for (int i = 0; i < n_seq; ++i) {
+            const int s = seq_ids[i];
+            const int64_t N = NT(c, l, s), S = ST(c, l, s);
+            bool seal = false;
+            if (seal_trigger > 0) seal = std::max<int64_t>(N, kSink) - S >= seal_trigger;
+            else if (seal_trigger == 0) seal = N - keep - S >= kGroup;
+            if (seal) need[nn++] = s;
+        }
+        if (nn) {
+            int64_t g = 0;
+            st = kv_seal(c, l, need, nn, keep, &g, stream);
+            if (st != KVQ_OK) return st;
+            total += g;
+        }
+        if (events && cudaEventRecord((cudaEvent_t)events[2 * l], (cudaStream_t)stream) != cudaSuccess)
+            return KVQ_ECUDA;
+        st = kv_decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace,
+                            ws_bytes, stream);
+        if (st != KVQ_OK) return st;
+        if (events && cudaEventRecord((cudaEvent_t)events[2 * l + 1], (cudaStream_t)stream) != cudaSuccess)
+            return KVQ_ECUDA;
+    }
+    if (groups_sealed) *groups_sealed = total;
+    return KVQ_OK;
+}
+
+kvq_status kv_snapshot_size(const kvq_cache* c, size_t* bytes) {
+    if (!c || !bytes) return KVQ_EINVAL;
+    *bytes = 2 * c->n_tok.size() * sizeof(int64_t);
+    return KVQ_OK;
+}
+
+kvq_status kv_snapshot(const kvq_cache* c, void* buf, size_t bytes) {
+    if (!c || !buf || bytes < 2 * c->n_tok.size() * sizeof(int64_t)) return KVQ_EINVAL;
+    std::memcpy(buf, c->n_tok.data(), c->n_tok.size() * sizeof(int64_t));
+    std::memcpy((char*)buf + c->n_tok.size() * sizeof(int64_t), c->sealed.data(), c->sealed.size() * sizeof(int64_t));
+    return KVQ_OK;
+}
+
+kvq_status kv_restore(kvq_cache* c, const void* buf, size_t bytes) {
+    if (!c || !buf || bytes < 2 * c->n_tok.size() * sizeof(int64_t)) return KVQ_EINVAL;
+    std::memcpy(c->n_tok.data(), buf, c->n_tok.size() * sizeof(int64_t));
+    std::memcpy(c->sealed.data(), (const char*)buf + c->n_tok.size() * sizeof(int64_t), c->sealed.size() * sizeof(int64_t));
+    return KVQ_OK;
+}
+
+kvq_status kv_state(const kvq_cache* c, int layer, int seq, int64_t* n_tokens, int64_t* sealed_end) {
+    if (!c || layer < 0 || layer >= c->cfg.n_layers || seq < 0 || seq >= c->cfg.max_seqs) return KVQ_EINVAL;
+    const size_t i = (size_t)layer * c->cfg.max_seqs + seq;
+    if (n_tokens) *n_tokens = c->n_tok[i];
+    if (sealed_end) *sealed_end = c->sealed[i];
+    return KVQ_OK;
+}
+
+kvq_status kv_get_status(kvq_cache* c, uint32_t* word) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    uint32_t w = 0;
+    if (cudaMemcpy(&w, (char*)c->pool + c->lay.status_off, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return KVQ_ECUDA;
+    if (w && cudaMemset((char*)c->pool + c->lay.status_off, 0, 4) != cudaSuccess) return KVQ_ECUDA;
+    if (word) *word = w;
+    return w ? KVQ_EDEVICE : KVQ_OK;
+}
+
+kvq_status kv_dequant(kvq_cache* c, int layer, int seq, int head, int which, int64_t p0, int64_t n, float* out,
+                      void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (layer < 0 || layer >= c->cfg.n_layers || seq < 0 || seq >= c->cfg.max_seqs || head < 0 ||
+        head >= c->cfg.n_kv_heads || (which != 0 && which != 1) || !out || p0 < 0 || n <= 0)
+        return KVQ_EINVAL;
+    const int64_t N = NT(c, layer, seq), S = ST(c, layer, seq);
+    if (p0 + n > N) return KVQ_EINVAL;
+    int32_t lo[4], hi[4], kind[4];
+    const int ns = spans(c->lay, N, S, lo, hi, kind);
+    for (int r = 0; r < ns; ++r) {
+        const int64_t a = std::max<int64_t>(lo[r], p0), b = std::min<int64_t>(hi[r], p0 + n);
+        if (b <= a) continue;
+        const int e = launch_dequant(c->lay, c->pool, layer, seq, head, which, kind[r], a, b - a,
+                                     out + (a - p0) * c->lay.D, stream);
+        if (e != 0) return KVQ_ECUDA;
+    }
+    return KVQ_OK;
+}
+
+kvq_status kv_region_ptr(const kvq_cache* c, int layer, int seq, int head, int which, int region, void** ptr,
+                         size_t* bytes) {
+    if (!c || !ptr || layer < 0 || layer >= c->cfg.n_layers || seq < 0 || seq >= c->cfg.max_seqs || head < 0 ||
+        head >= c->cfg.n_kv_heads || (which != 0 && which != 1))
+        return KVQ_EINVAL;
+    const Layout& L = c->lay;
+    const int64_t u = L.unit(layer, seq, head);
+    int64_t off = 0, sz = 0;
+    const bool tq = L.journal == KVQ_TQ6_0;
+    switch (region) {
+        case KVQ_REGION_SINK: off = L.sink_off[which] + u * L.sink_stride[which]; sz = (int64_t)kSink * L.D * 2; break;
+        case KVQ_REGION_JOURNAL: off = L.jcode_off[which] + u * L.jcode_stride[which]; sz = (int64_t)L.R * L.jrow_bytes; break;
+        case KVQ_REGION_JOURNAL_SCALE:
+            if (!tq) return KVQ_EINVAL;
+            off = L.jscale_off[which] + u * L.jscale_stride[which]; sz = (int64_t)L.R * (L.D / 128) * 2; break;
+        case KVQ_REGION_TAIL:
+            if (!tq) return KVQ_EINVAL;
+            off = L.tail_off[which] + u * L.tail_stride[which]; sz = (int64_t)L.T * L.D * 2; break;
+        case KVQ_REGION_BODY: off = L.body_off[which] + u * L.body_stride[which]; sz = (int64_t)L.gcap * L.rec_bytes[which]; break;
+        default: return KVQ_EINVAL;
+    }
+    *ptr = (char*)c->pool + off;
+    if (bytes) *bytes = (size_t)sz;
+    return KVQ_OK;
+}
+
+kvq_status kv_format_tables(float centroids[16], float boundaries[15], uint64_t sign_words[4]) {
+    const FormatTables& t = host_tables();
+    if (centroids) std::memcpy(centroids, t.cent, sizeof(t.cent));
+    if (boundaries) std::memcpy(boundaries, t.bnd, sizeof(t.bnd));
+    if (sign_words) std::memcpy(sign_words, t.sign_words, sizeof(t.sign_words));
+    return KVQ_OK;
+}
+
+}  // extern "C"

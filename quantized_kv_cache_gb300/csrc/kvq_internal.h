@@ -1,0 +1,147 @@
+// Internal definitions shared by the host library and the CUDA kernels of the rotated
+// low-bit KV cache: the device-pool layout, per-format record geometry and the launch
+// parameter blocks. Not part of the public C ABI (include/kvq.h).
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include "../../include/kvq.h"
+
+#ifdef __CUDACC__
+#define KVQ_HD __host__ __device__ __forceinline__
+#else
+#define KVQ_HD inline
+#endif
+
+namespace kvq {
+
+constexpr int kSink = 128;      // SJ-KVaRN §2.1: first 128 positions kept at 16 bits
+constexpr int kGroup = 128;     // SJ-KVaRN §2.1: 128-token groups
+constexpr int kMaxSeqPerCall = 32;   // keeps every launch parameter block under 4 KB
+constexpr int kMaxG = 16;       // query heads per KV head handled by the decode kernel
+
+enum Rot : int32_t { ROT_NONE = 0, ROT_HAD256 = 1, ROT_TBQ128 = 2 };
+
+// Record bytes of one 128-position group of one KV head (K or V), per format.
+KVQ_HD int64_t record_bytes(int fmt, int D) {
+    switch (fmt) {
+        case KVQ_TBQ4: return 66LL * D;                       // 64 B idx + 2 B norm per 128
+        case KVQ_Q8_0: return 136LL * D;                      // 34 B per 32, 128 tokens
+        case KVQ_Q4_0: return 72LL * D;                       // 18 B per 32
+        case KVQ_KVARN4: return (int64_t)(D / 256) * (4096 * 4 + 1152);
+        case KVQ_KVARN5: return (int64_t)(D / 256) * (4096 * 5 + 1152);
+        default: return -1;
+    }
+}
+
+// Code bytes (before the scale area) of a non-KVarN record.
+KVQ_HD int64_t record_code_bytes(int fmt, int D) {
+    switch (fmt) {
+        case KVQ_TBQ4: return 64LL * D;
+        case KVQ_Q8_0: return 128LL * D;
+        case KVQ_Q4_0: return 64LL * D;
+        default: return -1;
+    }
+}
+
+KVQ_HD int rotation_of(int fmt) {
+    if (fmt == KVQ_TBQ4) return ROT_TBQ128;
+    if (fmt == KVQ_KVARN4 || fmt == KVQ_KVARN5) return ROT_HAD256;
+    return ROT_NONE;
+}
+
+KVQ_HD int64_t align256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+// Geometry of the device pool. Every per-(layer, seq, head) region of kind X for
+// which w (0 = K, 1 = V) lives at  base + off_X[w] + unit * stride_X[w]  with
+// unit = (layer * max_seqs + seq) * H + head.
+struct Layout {
+    int32_t L, H, D, Hq, G, NQ;
+    int32_t max_seqs, T, R, gcap;
+    int64_t max_ctx;
+    int32_t fmt[2];          // body format of K, V
+    int32_t journal, tail_fmt, rot, jrow_bytes;   // jrow_bytes: bytes of one journal code row
+    float scale;             // softmax scale
+    int32_t pad;
+    int64_t status_off;
+    int64_t sink_off[2], sink_stride[2];
+    int64_t jcode_off[2], jcode_stride[2];
+    int64_t jscale_off[2], jscale_stride[2];
+    int64_t tail_off[2], tail_stride[2];
+    int64_t body_off[2], body_stride[2], rec_bytes[2];
+    int64_t total;
+
+    KVQ_HD int64_t unit(int l, int s, int h) const { return ((int64_t)l * max_seqs + s) * H + h; }
+};
+
+// Builds the layout; returns false on an invalid config (host side).
+bool make_layout(const kvq_config& c, Layout* out);
+
+// ---------------------------------------------------------------------------- launches
+// One contiguous span of positions of one sequence that the decode kernel reads with a
+// single region reader.
+enum RegionKind : int32_t { RK_SINK = 0, RK_BODY = 1, RK_RING = 2, RK_TAIL = 3, RK_JEXACT = 4 };
+
+struct SeqSpan {
+    int32_t slot;            // sequence slot in the pool
+    int32_t n_tok;           // N
+    int32_t lo[4], hi[4];    // spans of the (up to) four regions in read order
+    int32_t kind[4];         // RegionKind of each span
+    int32_t nchunk[4];       // chunks of each span
+    int32_t items_per_head;  // sum of nchunk
+    int32_t first_item;      // index of this sequence's first work item
+};
+
+struct AttnParams {
+    const void* pool;
+    const uint16_t* q;       // [n_seq][Hq][D] fp16
+    uint16_t* out;           // [n_seq][Hq][D] fp16
+    float* partials;         // workspace: per item [2 * NQ + NQ * D] floats
+    int32_t layer, n_seq, chunk, total_items;
+    SeqSpan seq[kMaxSeqPerCall];
+};
+
+struct AppendParams {
+    const void* pool;
+    const uint16_t* k;       // [n_seq][n_tok][H][D]
+    const uint16_t* v;
+    int32_t layer, n_seq, n_tok, pad;
+    int32_t slot[kMaxSeqPerCall];
+    int32_t n0[kMaxSeqPerCall];       // N before this append
+};
+
+struct SealSeq {             // one sequence's batch of consecutive groups (same in every sealed layer)
+    int32_t slot;
+    int32_t first_pos;       // position of the first group to seal
+    int32_t first_group;     // its body group index
+    int32_t n_groups;
+    int32_t prefix;          // groups of the earlier sequences of this launch
+};
+
+struct SealParams {
+    const void* pool;
+    int32_t layer0, n_layers, n_seq, groups_per_layer;
+    SealSeq seq[kMaxSeqPerCall];
+};
+
+// Device constants: TBQ4 centroids / boundaries and sign vectors (host-derived).
+struct FormatTables {
+    float cent[16];
+    float bnd[15];
+    float pad;
+    uint64_t sign_words[4];
+};
+
+const FormatTables& host_tables();   // derived once per process (tables.cpp)
+
+// Kernel launchers (kernels_*.cu). Each returns cudaError_t as int.
+int launch_append(const Layout& lay, const AppendParams& p, void* stream);
+int launch_seal(const Layout& lay, const SealParams& p, void* stream);
+int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
+int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
+                   int kind, int64_t p0, int64_t n, float* out, void* stream);
+int upload_tables_codec(const FormatTables& t);
+int upload_tables_attn(const FormatTables& t);
+int query_sm_count(int device);
+
+}  // namespace kvq
