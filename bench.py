@@ -228,11 +228,13 @@ def run_ours(args, rank, world, local_rank):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
+    torch.cuda.nvtx.range_push("timed")
     t_start.record()
     sealed = 0
     for s in range(K):
         sealed += step(s, handles[s])
     t_end.record()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     wall1 = time.time()
     dist_barrier(world)
@@ -387,7 +389,7 @@ def measure_e2e(w, cache, inp, seq_ids, out, stream, K, total_bytes, world):
 
 def config_block(w, K):
     D = w.head_dim
-    per_step = layer_step_bytes(w, [(n + 1, 0) for n in w.contexts]) * w.n_layers
+    per_step = layer_step_bytes(w, [(n + 1, S) for n, S in initial_states(w, w.contexts)]) * w.n_layers
     return {"workload": w.name, "layers": w.n_layers, "kv_heads": w.n_kv_heads, "head_dim": D,
             "q_heads": w.n_q_heads, "batch": len(w.contexts), "contexts": w.contexts,
             "body": f"{w.k_body}/{w.v_body}", "journal": w.journal, "tail": w.tail, "decode_steps": K,

@@ -461,7 +461,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
 }
 
 // --------------------------------------------------------------------------- merge kernel
-// grid (n_seq * H, D / 64); 256 threads; thread handles (q, channel) pairs of its chunk.
+// grid (n_seq * H, D / 64); 8 warps. Warps take the partials of one (sequence, KV head)
+// round-robin; a lane owns channels c0 + lane and c0 + lane + 32 of every query of the
+// group, so each partial is read with coalesced 128-byte rows; warp sums meet in shared
+// memory at the end.
 template <int D, int NQ>
 __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
     const int bh = blockIdx.x;
@@ -470,6 +473,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     const int first = s.first_item + h * s.items_per_head, cnt = s.items_per_head;
     const int G = L.G;
     __shared__ float mstar[NQ], lstar[NQ];
+    __shared__ float red[8][NQ][64];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t stride = 2 * NQ + NQ * D;
     for (int qi = warp; qi < G; qi += 8) {
@@ -491,17 +495,35 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     }
     __syncthreads();
     const int c0 = blockIdx.y * 64;
-    for (int e = threadIdx.x; e < G * 64; e += blockDim.x) {
-        const int qi = e / 64, ch = c0 + e % 64;
-        const float m = mstar[qi];
-        float o = 0.f;
-        for (int c = 0; c < cnt; ++c) {
-            const float* pc = p.partials + (first + c) * stride;
-            const float mc = pc[qi];
-            if (mc != -INFINITY) o += exp2f(mc - m) * pc[2 * NQ + qi * D + ch];
+    float acc[NQ][2];
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) acc[qi][0] = acc[qi][1] = 0.f;
+#pragma unroll 2
+    for (int c = warp; c < cnt; c += 8) {
+        const float* pc = p.partials + (first + c) * stride;
+#pragma unroll
+        for (int qi = 0; qi < NQ; ++qi) {
+            if (qi < G) {
+                const float mc = pc[qi];
+                const float wgt = (mc == -INFINITY) ? 0.f : exp2f(mc - mstar[qi]);
+                const float* row = pc + 2 * NQ + qi * D + c0;
+                acc[qi][0] += wgt * row[lane];
+                acc[qi][1] += wgt * row[lane + 32];
+            }
         }
-        const float l = lstar[qi];
-        p.out[((int64_t)b * L.Hq + (int64_t)h * G + qi) * D + ch] = f2h_bits(o / l);
+    }
+#pragma unroll
+    for (int qi = 0; qi < NQ; ++qi) {
+        red[warp][qi][lane] = acc[qi][0];
+        red[warp][qi][lane + 32] = acc[qi][1];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * 64; e += blockDim.x) {
+        const int qi = e / 64, ch = e % 64;
+        float o = 0.f;
+#pragma unroll
+        for (int wv = 0; wv < 8; ++wv) o += red[wv][qi][ch];
+        p.out[((int64_t)b * L.Hq + (int64_t)h * G + qi) * D + c0 + ch] = f2h_bits(o / lstar[qi]);
     }
 }
 

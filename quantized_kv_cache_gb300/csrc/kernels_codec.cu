@@ -178,9 +178,13 @@ __global__ void append_kernel(Layout L, AppendParams p) {
             dst[i] = (L.journal == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
         return;
     }
-    uint16_t* tl = tail_row(L, p.pool, w, unit, pos % L.T);
-    for (int i = threadIdx.x; i < D; i += blockDim.x)
-        tl[i] = (L.tail_fmt == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
+    // Exact tail copy. Positions of one append that share a tail slot (pos mod T) would
+    // race; only the newest T positions of the append write it.
+    if (pos + L.T >= p.n0[b] + p.n_tok) {
+        uint16_t* tl = tail_row(L, p.pool, w, unit, pos % L.T);
+        for (int i = threadIdx.x; i < D; i += blockDim.x)
+            tl[i] = (L.tail_fmt == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
+    }
 
     extern __shared__ float xs[];
     uint8_t* cs = (uint8_t*)(xs + D);
