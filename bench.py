@@ -182,7 +182,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     w = configs.WORKLOADS[args.workload]
     K, W = args.steps, args.warmup
-    n_steps = max(K, W)
+    n_steps = max(K, W, w.steps)
     seq_ids = list(range(len(w.contexts)))
     cfg = w.config()
     cfg.max_ctx = max(w.contexts) + n_steps + 512
@@ -283,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
     if e2e:
         result["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(args.workload, steps=6, heads=2)
+        result["cpu_baseline"] = cpu_baseline(args.workload, steps=64, heads=4)
     cache.close()
     return result
 
@@ -464,20 +464,21 @@ def run_reference(args, rank, world):
     w = configs.WORKLOADS[args.workload]
     steps = args.warmup + args.steps
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", args.workload, str(min(steps, 8)), "1"]
+    n = min(steps, 256)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-sample", args.workload, str(n),
+           str(w.n_kv_heads)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=3000)
     if r.returncode != 0:
         return {"impl": "reference", "unavailable": "oracle run failed: " + r.stderr.strip().splitlines()[-1][:200]}
     cb = json.loads(r.stdout.strip().splitlines()[-1])
     v = cb["value"]
-    n = min(steps, 8)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(cb["seconds"] / n * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_block(w, args.steps),
             "cpu_baseline": cb,
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-            "note": f"oracle timed on {n} bounded sample step(s) of one layer / one KV head; see cpu_baseline.sample"}
+            "note": f"oracle timed on {n} decode step(s) of one layer (all KV heads); see cpu_baseline.sample"}
 
 
 # --------------------------------------------------------------------------- distributed
