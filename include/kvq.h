@@ -159,6 +159,19 @@ kvq_status kv_snapshot_size(const kvq_cache* cache, size_t* bytes);
 kvq_status kv_snapshot(const kvq_cache* cache, void* buf, size_t bytes);
 kvq_status kv_restore(kvq_cache* cache, const void* buf, size_t bytes);
 
+/* kv_decode_attn_noalloc — kv_decode_attn for callers that cannot allocate device memory
+ * (for example a host program that only links this ABI inside a runtime whose memory manager
+ * already owns the device, or a loop that cannot afford cudaMalloc's implicit
+ * synchronisation). The source pages have no counterpart: this is a library convenience.
+ * Same arguments and results as kv_decode_attn, minus the workspace: the library uses a
+ * fixed 32 MiB device array that every GPU loading the library holds until exit. Configs whose
+ * kv_required_bytes workspace exceeds 32 MiB are refused with KVQ_EUNSUPPORTED. All calls
+ * share the array (nothing in it needs to start at zero); calls that overlap on the GPU race
+ * and must be avoided. The first call on each device looks up the array's address with that
+ * device current; make that first call before any stream capture begins. Allocates nothing. */
+kvq_status kv_decode_attn_noalloc(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq,
+                                  const void* q, void* out, void* stream);
+
 /* kv_state — host copies of one slot's lengths. */
 kvq_status kv_state(const kvq_cache* cache, int layer, int seq, int64_t* n_tokens, int64_t* sealed_end);
 

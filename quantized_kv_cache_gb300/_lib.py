@@ -66,6 +66,7 @@ _SIGS = {
                          ctypes.POINTER(ctypes.c_uint64)],
     "kv_decode_step": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
                        P, SZ, ctypes.POINTER(P), ctypes.POINTER(I64), P],
+    "kv_decode_attn_noalloc": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P],
     "kv_snapshot_size": [P, ctypes.POINTER(SZ)],
     "kv_snapshot": [P, P, SZ],
     "kv_restore": [P, P, SZ],
@@ -161,6 +162,13 @@ def kv_decode_step(h, n_layers, seq_ids, q_ptr, k_ptr, v_ptr, out_ptr, seal_trig
                                                    seal_trigger, keep, P(ws_ptr), ws_bytes, ev, ctypes.byref(g),
                                                    P(stream)))
     return g.value
+
+
+def kv_decode_attn_noalloc(h, layer, seq_ids, q_ptr, out_ptr, stream=0):
+    """kv_decode_attn without a caller workspace (the library's fixed device array)."""
+    ids, n = _ids(seq_ids)
+    _check("kv_decode_attn_noalloc", load().kv_decode_attn_noalloc(h, layer, ids, n, P(q_ptr), P(out_ptr),
+                                                                   P(stream)))
 
 
 def kv_snapshot(h):

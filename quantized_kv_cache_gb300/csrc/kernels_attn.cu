@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cfloat>
+#include <mutex>
 #include "device_common.cuh"
 
 namespace kvq {
@@ -565,3 +566,50 @@ int launch_decode(const Layout& L, const AttnParams& p, void* stream) {
 }
 
 }  // namespace kvq
+
+// ---------------------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers of this library have no way to call cudaMalloc: a host program that links
+// only this C ABI inside a runtime whose memory manager has already reserved the device
+// (an inference server's fixed pool), or a latency-critical loop where cudaMalloc's implicit
+// synchronisation is not acceptable. kv_decode_attn needs a caller-provided workspace for
+// its per-work-item partial results; kv_decode_attn_noalloc uses the fixed array below
+// instead, so the caller passes only inputs and outputs.
+//
+// The array is a file-scope device variable: every GPU that loads this library holds its
+// 32 MiB until the process exits. All calls share it and it keeps the last call's contents;
+// nothing in it has to start at zero (each call writes every partial it later reads), and
+// calls that overlap on the GPU (concurrent streams, or host threads racing) corrupt each
+// other's partials. Its device address is looked up once per device, on the first call made
+// with that device current; make that first call before any stream capture begins.
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;
+}  // namespace
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+extern "C" kvq_status kv_decode_attn_noalloc(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq,
+                                             const void* q, void* out, void* stream) {
+    using namespace kvq;
+    const kvq_config* cfg = cache_config(cache);
+    if (!cfg) return KVQ_EINVAL;
+    size_t need = 0;
+    kvq_status st = kv_required_bytes(cfg, nullptr, &need);
+    if (st != KVQ_OK) return st;
+    if (need > kNoAllocScratchBytes) return KVQ_EUNSUPPORTED;   // workspace would exceed the fixed 32 MiB
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KVQ_ECUDA;
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    void* ptr = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (!addr[dev]) {
+            void* a = nullptr;
+            if (cudaGetSymbolAddress(&a, g_noalloc_scratch) != cudaSuccess || !a) return KVQ_ECUDA;
+            addr[dev] = a;
+        }
+        ptr = addr[dev];
+    }
+    return kv_decode_attn(cache, layer, seq_ids, n_seq, q, out, ptr, kNoAllocScratchBytes, stream);
+}

@@ -80,6 +80,8 @@ bool make_layout(const kvq_config& c, Layout* out) {
     return true;
 }
 
+const kvq_config* cache_config(const kvq_cache* c) { return c ? &c->cfg : nullptr; }
+
 }  // namespace kvq
 
 namespace {

@@ -7,6 +7,8 @@
 #include <cstddef>
 #include "../../include/kvq.h"
 
+struct kvq_cache;
+
 #ifdef __CUDACC__
 #define KVQ_HD __host__ __device__ __forceinline__
 #else
@@ -141,6 +143,7 @@ int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
 int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
                    int kind, int64_t p0, int64_t n, float* out, void* stream);
 int upload_tables_codec(const FormatTables& t);
+const kvq_config* cache_config(const kvq_cache* c);   // the config a handle was created with
 int upload_tables_attn(const FormatTables& t);
 int query_sm_count(int device);
 
