@@ -26,6 +26,7 @@ UNITS = {
     "tables.cpp": [],
     "kernels_codec.cu": ["-fmad=false"],
     "kernels_attn.cu": [],
+    "kernels_body.cu": [],
     "synth.cu": [],
 }
 

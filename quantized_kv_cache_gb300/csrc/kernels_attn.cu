@@ -112,7 +112,7 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int item) {
     it.h = local / s.items_per_head;
     int c = local % s.items_per_head;
     int r = 0;
-    while (r < 3 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
+    while (r < 2 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
     it.kind = s.kind[r];
     it.t0 = s.lo[r] + c * p.chunk;
     it.t1 = min(it.t0 + p.chunk, s.hi[r]);
@@ -471,20 +471,23 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     const int bh = blockIdx.x;
     const int b = bh / L.H, h = bh % L.H;
     const SeqSpan& s = p.seq[b];
-    const int first = s.first_item + h * s.items_per_head, cnt = s.items_per_head;
+    const int first = s.first_item + h * s.items_per_head, cnt_r = s.items_per_head;
+    const int bfirst = s.body_first + h * s.body_per_head;
+    const int cnt = cnt_r + s.body_per_head;
     const int G = L.G;
     __shared__ float mstar[NQ], lstar[NQ];
     __shared__ float red[8][NQ][64];
+    auto item_of = [&](int c) { return c < cnt_r ? first + c : bfirst + (c - cnt_r); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t stride = 2 * NQ + NQ * D;
     for (int qi = warp; qi < G; qi += 8) {
         float m = -INFINITY;
-        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, p.partials[(first + c) * stride + qi]);
+        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, p.partials[item_of(c) * stride + qi]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
         for (int c = lane; c < cnt; c += 32) {
-            const float* pc = p.partials + (first + c) * stride;
+            const float* pc = p.partials + item_of(c) * stride;
             if (pc[qi] != -INFINITY) l += exp2f(pc[qi] - m) * pc[NQ + qi];
         }
 #pragma unroll
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     for (int qi = 0; qi < NQ; ++qi) acc[qi][0] = acc[qi][1] = 0.f;
 #pragma unroll 2
     for (int c = warp; c < cnt; c += 8) {
-        const float* pc = p.partials + (first + c) * stride;
+        const float* pc = p.partials + item_of(c) * stride;
 #pragma unroll
         for (int qi = 0; qi < NQ; ++qi) {
             if (qi < G) {
@@ -536,9 +539,16 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
         cudaFuncSetAttribute(decode_split_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         attr = true;
     }
-    decode_split_kernel<D, NQ><<<p.total_items, kThreads, C::SMEM, s>>>(L, p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return (int)e;
+    if (p.n_region_items > 0) {
+        decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return (int)e;
+    }
+    const int n_body = p.total_items - p.n_region_items;
+    if (n_body > 0) {
+        const int e = launch_decode_body(L, p, n_body, s);
+        if (e != 0) return e;
+    }
     dim3 mg(p.n_seq * L.H, D / 64);
     decode_merge_kernel<D, NQ><<<mg, 256, 0, s>>>(L, p);
     return (int)cudaGetLastError();

@@ -99,7 +99,7 @@ kvq_status ensure_tables(int device) {
     std::lock_guard<std::mutex> lk(g_tab_mu);
     if (g_tab_devices.count(device)) return KVQ_OK;
     const FormatTables& t = host_tables();
-    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0) return KVQ_ECUDA;
+    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0) return KVQ_ECUDA;
     g_tab_devices.insert(device);
     return KVQ_OK;
 }
@@ -132,14 +132,14 @@ size_t workspace_items(const kvq_config& c) {
     return 2048 + (size_t)4 * c.n_kv_heads * n;
 }
 
-// Region spans of one sequence in read order (sink, body, ring or exact journal, tail).
-int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[4], int32_t hi[4], int32_t kind[4]) {
+// Non-body region spans of one sequence in read order (sink, ring span or exact journal,
+// exact tail); the body [128, S) is listed separately.
+int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[3], int32_t hi[3], int32_t kind[3]) {
     int n = 0;
     auto add = [&](int64_t a, int64_t b, int k) {
         if (b > a) { lo[n] = (int32_t)a; hi[n] = (int32_t)b; kind[n] = k; ++n; }
     };
     add(0, std::min<int64_t>(N, kSink), RK_SINK);
-    add(kSink, S, RK_BODY);
     if (L.journal == KVQ_TQ6_0) {
         const int64_t E = std::max<int64_t>(S, N - L.T);
         add(S, E, RK_RING);
@@ -147,7 +147,7 @@ int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[4], int32_t hi[4], i
     } else {
         add(std::max<int64_t>(S, kSink), N, RK_JEXACT);
     }
-    for (int i = n; i < 4; ++i) { lo[i] = hi[i] = 0; kind[i] = 0; }
+    for (int i = n; i < 3; ++i) { lo[i] = hi[i] = 0; kind[i] = 0; }
     return n;
 }
 
@@ -340,38 +340,55 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     p.partials = (float*)workspace;
     p.layer = layer;
     p.n_seq = n_seq;
-    int64_t total_tok = 0;
+    int64_t region_tok = 0, body_groups = 0;
     for (int i = 0; i < n_seq; ++i) {
         const int64_t N = NT(c, layer, seq_ids[i]);
         if (N <= 0) return KVQ_EINVAL;
-        total_tok += N;
+        const int64_t S = ST(c, layer, seq_ids[i]);
+        region_tok += N - (S - kSink);
+        body_groups += (S - kSink) / kGroup;
     }
-    // chunk: a multiple of 128 giving about two waves of resident CTAs
+    // region items: chunks (multiples of 128) giving about two waves of the region kernel;
+    // body items: runs of groups giving about one wave of resident body-kernel CTAs
     const int per_sm = (L.D == 512) ? 1 : (L.D == 256 ? 2 : 4);
     const int64_t target = (int64_t)2 * c->sm_count * per_sm;
-    int64_t chunk = (total_tok * L.H + target - 1) / target;
+    int64_t chunk = (region_tok * L.H + target - 1) / target;
     chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
+    const int body_slots = std::max(1, body_ctas_per_sm(L)) * c->sm_count;
+    int64_t bchunk = std::max<int64_t>(1, (body_groups * L.H + body_slots - 1) / body_slots);
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
             s.slot = seq_ids[i];
             s.n_tok = (int32_t)NT(c, layer, s.slot);
-            spans(L, s.n_tok, ST(c, layer, s.slot), s.lo, s.hi, s.kind);
+            const int64_t S = ST(c, layer, s.slot);
+            spans(L, s.n_tok, S, s.lo, s.hi, s.kind);
             s.items_per_head = 0;
-            for (int r = 0; r < 4; ++r) {
+            for (int r = 0; r < 3; ++r) {
                 s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + chunk - 1) / chunk);
                 s.items_per_head += s.nchunk[r];
             }
             s.first_item = (int32_t)items;
             items += (int64_t)s.items_per_head * L.H;
         }
+        const int64_t n_region = items;
+        for (int i = 0; i < n_seq; ++i) {
+            SeqSpan& s = p.seq[i];
+            s.body_groups = (int32_t)((ST(c, layer, s.slot) - kSink) / kGroup);
+            s.body_per_head = (int32_t)((s.body_groups + bchunk - 1) / bchunk);
+            s.body_first = (int32_t)items;
+            items += (int64_t)s.body_per_head * L.H;
+        }
         if ((size_t)items <= cap) {
             p.total_items = (int32_t)items;
+            p.n_region_items = (int32_t)n_region;
             break;
         }
         chunk *= 2;
+        bchunk *= 2;
     }
+    p.body_chunk = (int32_t)bchunk;
     p.chunk = (int32_t)chunk;
     const int e = launch_decode(L, p, stream);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;
@@ -466,7 +483,8 @@ kvq_status kv_dequant(kvq_cache* c, int layer, int seq, int head, int which, int
     const int64_t N = NT(c, layer, seq), S = ST(c, layer, seq);
     if (p0 + n > N) return KVQ_EINVAL;
     int32_t lo[4], hi[4], kind[4];
-    const int ns = spans(c->lay, N, S, lo, hi, kind);
+    int ns = spans(c->lay, N, S, lo, hi, kind);
+    if (S > kSink) { lo[ns] = kSink; hi[ns] = (int32_t)S; kind[ns] = RK_BODY; ++ns; }
     for (int r = 0; r < ns; ++r) {
         const int64_t a = std::max<int64_t>(lo[r], p0), b = std::min<int64_t>(hi[r], p0 + n);
         if (b <= a) continue;

@@ -87,11 +87,14 @@ enum RegionKind : int32_t { RK_SINK = 0, RK_BODY = 1, RK_RING = 2, RK_TAIL = 3, 
 struct SeqSpan {
     int32_t slot;            // sequence slot in the pool
     int32_t n_tok;           // N
-    int32_t lo[4], hi[4];    // spans of the (up to) four regions in read order
-    int32_t kind[4];         // RegionKind of each span
-    int32_t nchunk[4];       // chunks of each span
-    int32_t items_per_head;  // sum of nchunk
-    int32_t first_item;      // index of this sequence's first work item
+    int32_t lo[3], hi[3];    // non-body regions in read order (sink, ring span or exact journal, tail)
+    int32_t kind[3];         // RegionKind of each span
+    int32_t nchunk[3];       // chunks of each span
+    int32_t items_per_head;  // region work items per KV head (sum of nchunk)
+    int32_t first_item;      // index of this sequence's first region work item
+    int32_t body_groups;     // sealed groups [128, S)
+    int32_t body_per_head;   // body work items per KV head
+    int32_t body_first;      // index of this sequence's first body work item
 };
 
 struct AttnParams {
@@ -100,6 +103,8 @@ struct AttnParams {
     uint16_t* out;           // [n_seq][Hq][D] fp16
     float* partials;         // workspace: per item [2 * NQ + NQ * D] floats
     int32_t layer, n_seq, chunk, total_items;
+    int32_t n_region_items;  // region items come first, body items after them
+    int32_t body_chunk;      // groups per body work item
     SeqSpan seq[kMaxSeqPerCall];
 };
 
@@ -140,6 +145,9 @@ const FormatTables& host_tables();   // derived once per process (tables.cpp)
 int launch_append(const Layout& lay, const AppendParams& p, void* stream);
 int launch_seal(const Layout& lay, const SealParams& p, void* stream);
 int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
+int launch_decode_body(const Layout& lay, const AttnParams& p, int n_body, void* stream);
+int upload_tables_body(const FormatTables& t);
+int body_ctas_per_sm(const Layout& lay);   // resident body-kernel CTAs per SM (0 if unsupported)
 int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
                    int kind, int64_t p0, int64_t n, float* out, void* stream);
 int upload_tables_codec(const FormatTables& t);
