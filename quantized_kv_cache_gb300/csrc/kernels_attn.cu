@@ -121,32 +121,43 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int item) {
 }
 
 // --------------------------------------------------------------------------- tile fill
+// Each fill first issues every global load of its share of the tile into registers, then
+// decodes and stores to shared memory, so a thread has all its loads in flight at once.
 // Token-major exact rows (sink, exact tail, exact journal) into dst[TILE][LD].
 template <int D, int TILE, int LD>
 __device__ void fill_exact(const Layout& L, const void* pool, int w, int64_t unit, int kind, int tstart,
                            int nvalid, __half* dst) {
     constexpr int U = D / 8;     // 16-byte units per row
+    constexpr int IT = (TILE * U + kThreads - 1) / kThreads;
     const int fmt = (kind == RK_SINK) ? KVQ_F16 : (kind == RK_TAIL ? L.tail_fmt : L.journal);
-    for (int e = threadIdx.x; e < TILE * U; e += kThreads) {
+    uint4 raw[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        const int i = e / U, u = e % U;
+        raw[k] = make_uint4(0, 0, 0, 0);
+        if (e < TILE * U && i < nvalid) {
+            const int pos = tstart + i;
+            const uint16_t* row;
+            if (kind == RK_SINK) row = sink_row(L, pool, w, unit, pos);
+            else if (kind == RK_TAIL) row = tail_row(L, pool, w, unit, pos % L.T);
+            else row = jexact_row(L, pool, w, unit, journal_slot(L, pos));
+            raw[k] = __ldg(reinterpret_cast<const uint4*>(row + 8 * u));
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        if (e >= TILE * U) break;
         const int i = e / U, u = e % U;
         __half* o = dst + i * LD + 8 * u;
-        if (i >= nvalid) {
-            *reinterpret_cast<uint4*>(o) = make_uint4(0, 0, 0, 0);
-            continue;
-        }
-        const int pos = tstart + i;
-        const uint16_t* row;
-        if (kind == RK_SINK) row = sink_row(L, pool, w, unit, pos);
-        else if (kind == RK_TAIL) row = tail_row(L, pool, w, unit, pos % L.T);
-        else row = jexact_row(L, pool, w, unit, journal_slot(L, pos));
-        const uint4 raw = *reinterpret_cast<const uint4*>(row + 8 * u);
-        if (fmt == KVQ_F16) {
-            *reinterpret_cast<uint4*>(o) = raw;
+        if (fmt == KVQ_F16 || i >= nvalid) {
+            *reinterpret_cast<uint4*>(o) = raw[k];
         } else {
-            const uint16_t* r16 = reinterpret_cast<const uint16_t*>(&raw);
+            const uint16_t* r16 = reinterpret_cast<const uint16_t*>(&raw[k]);
             float v[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = bf2f(r16[k]);
+            for (int j = 0; j < 8; ++j) v[j] = bf2f(r16[j]);
             store8(o, v);
         }
     }
@@ -157,24 +168,35 @@ template <int D, int TILE, int LD>
 __device__ void fill_ring(const Layout& L, const void* pool, int w, int64_t unit, int tstart, int nvalid,
                           __half* dst) {
     constexpr int U = D / 8;
-    for (int e = threadIdx.x; e < TILE * U; e += kThreads) {
+    constexpr int IT = (TILE * U + kThreads - 1) / kThreads;
+    uint32_t ql[IT];
+    uint16_t qh[IT], ds[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        const int i = e / U, u = e % U;
+        ql[k] = 0; qh[k] = 0; ds[k] = 0;
+        if (e < TILE * U && i < nvalid) {
+            const int slot = journal_slot(L, tstart + i);
+            const int c0 = 8 * u, blk = c0 >> 7, j0 = c0 & 127;
+            const uint8_t* row = jcode_row(L, pool, w, unit, slot) + 96 * blk;
+            ql[k] = __ldg(reinterpret_cast<const uint32_t*>(row + (j0 >> 1)));
+            qh[k] = __ldg(reinterpret_cast<const uint16_t*>(row + 64 + (j0 >> 2)));
+            ds[k] = __ldg(jscale_row(L, pool, w, unit, slot) + blk);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+        const int e = threadIdx.x + k * kThreads;
+        if (e >= TILE * U) break;
         const int i = e / U, u = e % U;
         __half* o = dst + i * LD + 8 * u;
-        if (i >= nvalid) {
-            *reinterpret_cast<uint4*>(o) = make_uint4(0, 0, 0, 0);
-            continue;
-        }
-        const int slot = journal_slot(L, tstart + i);
-        const int c0 = 8 * u, blk = c0 >> 7, j0 = c0 & 127;
-        const uint8_t* row = jcode_row(L, pool, w, unit, slot) + 96 * blk;
-        const float d = h2f(jscale_row(L, pool, w, unit, slot)[blk]);
-        const uint32_t ql = *reinterpret_cast<const uint32_t*>(row + (j0 >> 1));
-        const uint16_t qh = *reinterpret_cast<const uint16_t*>(row + 64 + (j0 >> 2));
+        const float d = h2f(ds[k]);
         float v[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int code = ((ql >> (4 * k)) & 15) | (((qh >> (2 * k)) & 3) << 4);
-            v[k] = (float)(code - 32) * d;
+        for (int j = 0; j < 8; ++j) {
+            const int code = ((ql[k] >> (4 * j)) & 15) | (((qh[k] >> (2 * j)) & 3) << 4);
+            v[j] = (i < nvalid) ? (float)(code - 32) * d : 0.f;
         }
         store8(o, v);
     }
@@ -462,10 +484,12 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
 }
 
 // --------------------------------------------------------------------------- merge kernel
-// grid (n_seq * H, D / 64); 8 warps. Warps take the partials of one (sequence, KV head)
-// round-robin; a lane owns channels c0 + lane and c0 + lane + 32 of every query of the
-// group, so each partial is read with coalesced 128-byte rows; warp sums meet in shared
-// memory at the end.
+// grid (n_seq * H, D / 32); 256 threads. Phase 1: per query, the global max m* and
+// l* = sum 2^(m_c - m*) l_c, and every partial's weight 2^(m_c - m*) into shared memory.
+// Phase 2: thread (item slice, query, channel) sums w_c o_c over its slice of the partials
+// with eight independent loads in flight; slices meet in shared memory.
+constexpr int kMergeMaxItems = 1024;
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
     const int bh = blockIdx.x;
@@ -475,8 +499,10 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     const int bfirst = s.body_first + h * s.body_per_head;
     const int cnt = cnt_r + s.body_per_head;
     const int G = L.G;
+    extern __shared__ float msm[];
+    float* wgt = msm;                                   // [cnt][NQ]
     __shared__ float mstar[NQ], lstar[NQ];
-    __shared__ float red[8][NQ][64];
+    __shared__ float red[8][NQ][32];
     auto item_of = [&](int c) { return c < cnt_r ? first + c : bfirst + (c - cnt_r); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t stride = 2 * NQ + NQ * D;
@@ -488,7 +514,10 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
         float l = 0.f;
         for (int c = lane; c < cnt; c += 32) {
             const float* pc = p.partials + item_of(c) * stride;
-            if (pc[qi] != -INFINITY) l += exp2f(pc[qi] - m) * pc[NQ + qi];
+            const float mc = pc[qi];
+            const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - m);
+            wgt[c * NQ + qi] = w;
+            l += w * pc[NQ + qi];
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -498,32 +527,36 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
         }
     }
     __syncthreads();
-    const int c0 = blockIdx.y * 64;
-    float acc[NQ][2];
+    const int c0 = blockIdx.y * 32;
+    // thread = (slice = warp, channel = lane); it sums its slice of the partials for all queries
+    float acc[NQ];
 #pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) acc[qi][0] = acc[qi][1] = 0.f;
-#pragma unroll 2
-    for (int c = warp; c < cnt; c += 8) {
-        const float* pc = p.partials + item_of(c) * stride;
+    for (int qi = 0; qi < NQ; ++qi) acc[qi] = 0.f;
+    for (int cb = warp * 8; cb < cnt; cb += 64) {
+        float v[8][NQ];
 #pragma unroll
-        for (int qi = 0; qi < NQ; ++qi) {
-            if (qi < G) {
-                const float mc = pc[qi];
-                const float wgt = (mc == -INFINITY) ? 0.f : exp2f(mc - mstar[qi]);
-                const float* row = pc + 2 * NQ + qi * D + c0;
-                acc[qi][0] += wgt * row[lane];
-                acc[qi][1] += wgt * row[lane + 32];
+        for (int u = 0; u < 8; ++u) {
+            const int c = cb + u;
+            if (c < cnt) {
+                const float* row = p.partials + item_of(c) * stride + 2 * NQ + c0 + lane;
+#pragma unroll
+                for (int qi = 0; qi < NQ; ++qi) v[u][qi] = (qi < G) ? row[qi * D] : 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = cb + u;
+            if (c < cnt) {
+#pragma unroll
+                for (int qi = 0; qi < NQ; ++qi) acc[qi] += wgt[c * NQ + qi] * v[u][qi];
             }
         }
     }
 #pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) {
-        red[warp][qi][lane] = acc[qi][0];
-        red[warp][qi][lane + 32] = acc[qi][1];
-    }
+    for (int qi = 0; qi < NQ; ++qi) red[warp][qi][lane] = acc[qi];
     __syncthreads();
-    for (int e = threadIdx.x; e < G * 64; e += blockDim.x) {
-        const int qi = e / 64, ch = e % 64;
+    for (int e = threadIdx.x; e < G * 32; e += blockDim.x) {
+        const int qi = e / 32, ch = e % 32;
         float o = 0.f;
 #pragma unroll
         for (int wv = 0; wv < 8; ++wv) o += red[wv][qi][ch];
@@ -549,8 +582,12 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
         const int e = launch_decode_body(L, p, n_body, s);
         if (e != 0) return e;
     }
-    dim3 mg(p.n_seq * L.H, D / 64);
-    decode_merge_kernel<D, NQ><<<mg, 256, 0, s>>>(L, p);
+    int max_cnt = 0;
+    for (int i = 0; i < p.n_seq; ++i)
+        max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
+    if (max_cnt > kMergeMaxItems) return (int)cudaErrorInvalidConfiguration;
+    dim3 mg(p.n_seq * L.H, D / 32);
+    decode_merge_kernel<D, NQ><<<mg, 256, (size_t)max_cnt * NQ * sizeof(float), s>>>(L, p);
     return (int)cudaGetLastError();
 }
 

@@ -351,7 +351,7 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     // region items: chunks (multiples of 128) giving about two waves of the region kernel;
     // body items: runs of groups giving about one wave of resident body-kernel CTAs
     const int per_sm = (L.D == 512) ? 1 : (L.D == 256 ? 2 : 4);
-    const int64_t target = (int64_t)2 * c->sm_count * per_sm;
+    const int64_t target = (int64_t)c->sm_count * per_sm;
     int64_t chunk = (region_tok * L.H + target - 1) / target;
     chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
     const int body_slots = std::max(1, body_ctas_per_sm(L)) * c->sm_count;
