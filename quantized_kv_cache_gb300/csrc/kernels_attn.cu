@@ -112,7 +112,7 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int item) {
     it.h = local / s.items_per_head;
     int c = local % s.items_per_head;
     int r = 0;
-    while (r < 2 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
+    while (r < 3 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
     it.kind = s.kind[r];
     it.t0 = s.lo[r] + c * p.chunk;
     it.t1 = min(it.t0 + p.chunk, s.hi[r]);

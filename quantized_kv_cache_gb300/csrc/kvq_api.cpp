@@ -132,14 +132,16 @@ size_t workspace_items(const kvq_config& c) {
     return 2048 + (size_t)4 * c.n_kv_heads * n;
 }
 
-// Non-body region spans of one sequence in read order (sink, ring span or exact journal,
-// exact tail); the body [128, S) is listed separately.
-int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[3], int32_t hi[3], int32_t kind[3]) {
+// Region-kernel spans of one sequence in read order: the sink, the body [128, S) when
+// with_body (layouts the body kernel has no instance for), the ring span or exact journal,
+// and the exact tail.
+int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[4], int32_t hi[4], int32_t kind[4], bool with_body) {
     int n = 0;
     auto add = [&](int64_t a, int64_t b, int k) {
         if (b > a) { lo[n] = (int32_t)a; hi[n] = (int32_t)b; kind[n] = k; ++n; }
     };
     add(0, std::min<int64_t>(N, kSink), RK_SINK);
+    if (with_body) add(kSink, S, RK_BODY);
     if (L.journal == KVQ_TQ6_0) {
         const int64_t E = std::max<int64_t>(S, N - L.T);
         add(S, E, RK_RING);
@@ -147,7 +149,7 @@ int spans(const Layout& L, int64_t N, int64_t S, int32_t lo[3], int32_t hi[3], i
     } else {
         add(std::max<int64_t>(S, kSink), N, RK_JEXACT);
     }
-    for (int i = n; i < 3; ++i) { lo[i] = hi[i] = 0; kind[i] = 0; }
+    for (int i = n; i < 4; ++i) { lo[i] = hi[i] = 0; kind[i] = 0; }
     return n;
 }
 
@@ -340,13 +342,14 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     p.partials = (float*)workspace;
     p.layer = layer;
     p.n_seq = n_seq;
+    const bool body_kernel = body_ctas_per_sm(L) > 0;
     int64_t region_tok = 0, body_groups = 0;
     for (int i = 0; i < n_seq; ++i) {
         const int64_t N = NT(c, layer, seq_ids[i]);
         if (N <= 0) return KVQ_EINVAL;
         const int64_t S = ST(c, layer, seq_ids[i]);
-        region_tok += N - (S - kSink);
-        body_groups += (S - kSink) / kGroup;
+        region_tok += body_kernel ? N - (S - kSink) : N;
+        body_groups += body_kernel ? (S - kSink) / kGroup : 0;
     }
     // region items: chunks (multiples of 128) giving about two waves of the region kernel;
     // body items: runs of groups giving about one wave of resident body-kernel CTAs
@@ -363,9 +366,9 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
             s.slot = seq_ids[i];
             s.n_tok = (int32_t)NT(c, layer, s.slot);
             const int64_t S = ST(c, layer, s.slot);
-            spans(L, s.n_tok, S, s.lo, s.hi, s.kind);
+            spans(L, s.n_tok, S, s.lo, s.hi, s.kind, !body_kernel);
             s.items_per_head = 0;
-            for (int r = 0; r < 3; ++r) {
+            for (int r = 0; r < 4; ++r) {
                 s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + chunk - 1) / chunk);
                 s.items_per_head += s.nchunk[r];
             }
@@ -375,7 +378,7 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
         const int64_t n_region = items;
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
-            s.body_groups = (int32_t)((ST(c, layer, s.slot) - kSink) / kGroup);
+            s.body_groups = body_kernel ? (int32_t)((ST(c, layer, s.slot) - kSink) / kGroup) : 0;
             s.body_per_head = (int32_t)((s.body_groups + bchunk - 1) / bchunk);
             s.body_first = (int32_t)items;
             items += (int64_t)s.body_per_head * L.H;
@@ -483,8 +486,7 @@ kvq_status kv_dequant(kvq_cache* c, int layer, int seq, int head, int which, int
     const int64_t N = NT(c, layer, seq), S = ST(c, layer, seq);
     if (p0 + n > N) return KVQ_EINVAL;
     int32_t lo[4], hi[4], kind[4];
-    int ns = spans(c->lay, N, S, lo, hi, kind);
-    if (S > kSink) { lo[ns] = kSink; hi[ns] = (int32_t)S; kind[ns] = RK_BODY; ++ns; }
+    const int ns = spans(c->lay, N, S, lo, hi, kind, true);
     for (int r = 0; r < ns; ++r) {
         const int64_t a = std::max<int64_t>(lo[r], p0), b = std::min<int64_t>(hi[r], p0 + n);
         if (b <= a) continue;

@@ -87,9 +87,9 @@ enum RegionKind : int32_t { RK_SINK = 0, RK_BODY = 1, RK_RING = 2, RK_TAIL = 3, 
 struct SeqSpan {
     int32_t slot;            // sequence slot in the pool
     int32_t n_tok;           // N
-    int32_t lo[3], hi[3];    // non-body regions in read order (sink, ring span or exact journal, tail)
-    int32_t kind[3];         // RegionKind of each span
-    int32_t nchunk[3];       // chunks of each span
+    int32_t lo[4], hi[4];    // region-kernel spans in read order (sink, [body], ring span or exact journal, tail)
+    int32_t kind[4];         // RegionKind of each span
+    int32_t nchunk[4];       // chunks of each span
     int32_t items_per_head;  // region work items per KV head (sum of nchunk)
     int32_t first_item;      // index of this sequence's first region work item
     int32_t body_groups;     // sealed groups [128, S)
