@@ -1,24 +1,26 @@
 // Decode attention over sealed body records: the bandwidth-critical part of the path.
 //
-// One CTA per work item (sequence, KV head, run of 128-position groups). Warp 8 is a
-// producer: it streams each group's K record and V record (contiguous, 16-byte multiples)
-// into a ring of shared-memory stages with cp.async.bulk, completion tracked by mbarriers.
-// Warps 0-7 consume each group in three phases separated by consumer-only barriers:
-//   1. scores: warp w takes positions [16w, 16w+16) and all D channels, decoding its K rows
-//      from shared memory straight into mma.sync m16n8k16 fragments (positions on M, the GQA
-//      query group on N) against query fragments prepared once per group (KVarN: the column
-//      scales folded in, q' = q C) or once per item;
-//   2. softmax: warp per query over the group's 128 positions (log2 domain, running max and
-//      sum); it writes P' = p x (value scale of the position) in fp16, laid out in mma
-//      fragment order, one copy per value-scale block;
-//   3. values: warp w takes channels [wD/8, (w+1)D/8) for all 128 positions, decoding V rows
-//      (channel-major records: one 16-byte read covers 32 positions of a channel) into
-//      fragments, O^T[ch][q] += V^T P'^T.
-// Q8_0 / Q4_0 codes keep the fp16 exponent-trick offset (1024 + code is exact in fp16), removed
-// once per group with the sum of the matching operand (sum q' for scores, sum P' for values);
-// KVarN codes enter centred (code - 2^(b-1)), their zero point absorbing the centre. Scales: KVarN K row scale / zero point and TBQ4 / Q8_0 / Q4_0 K block
-// scales in the score epilogue; V row / block scales in P'; KVarN V column scale and zero
-// point once per group (O += C acc + C sum_t p_t (Z_t + 2^(b-1) S_t)).
+// One CTA per work item (sequence, KV head, run of 128-position groups), two CTAs per SM
+// where shared memory allows. Warp 8 is a producer: it streams each group's K record and V
+// record (contiguous, 16-byte multiples) into a ring of shared-memory stages with
+// cp.async.bulk, completion tracked by mbarriers. Warps 0-7 consume each group:
+//   0. (KVarN) the query fragments times the group's column scales, q' = q C in fp16, one
+//      8-channel chunk per thread from the fp16 rotated query held in registers; barrier.
+//   1. scores: warp w takes the 16 positions that value k-step w of step 3 covers and all D
+//      channels, decoding K rows from shared memory straight into mma.sync m16n8k16 A
+//      fragments (positions on M, the GQA query group on N); an mma with an all-ones A gives
+//      sum_c q'_c per query for the offset / zero-point term. Epilogue: log2-domain scores,
+//      the warp's maximum per query to shared memory; barrier; every thread forms the group
+//      maximum, the rescale factor alpha, p = 2^(s - m) and its running sum (registers), and
+//      P' = p x (value scale of the position) in fp16; movmatrix transposes the 16 x 8 P'
+//      tile into the B-fragment order of step 3 (one 8-byte store per lane); barrier.
+//   3. values: warp w takes channels [wD/8, (w+1)D/8) and all 128 positions, decoding V
+//      rows (channel-major records: 16 bytes cover 32 positions of a channel) into A
+//      fragments: O^T[ch][q] = alpha O^T + F (V^T P'^T + zero-point term).
+// Codes enter the mma through the fp16 exponent trick: a 4-bit code n placed in mantissa bits
+// 4-7 under exponent 6 reads exactly 64 + n (the fifth KVarN bit is mantissa bit 8, +16), a
+// signed byte b reads 1152 + b. The offsets cancel against sum q' (scores) or sum P' (values):
+// per group for KVarN values, through running sums for Q8_0 / Q4_0 values.
 // The partial (m, l, o) is rotated back to the original domain and merged with the region
 // partials by decode_merge_kernel (kernels_attn.cu).
 #include <cuda_runtime.h>
@@ -91,21 +93,33 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
                  : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// ------------------------------------------------------------------------------ half2 decode
+// ------------------------------------------------------------------------------ code decode
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ uint32_t pack_f2(float a, float b) { return as_u(__floats2half2_rn(a, b)); }
-// Nibbles x and x+4 of w (x = sh / 4) as half2 (1024 + code_x, 1024 + code_x+4), exact.
-__device__ __forceinline__ uint32_t nibraw(uint32_t w, int sh) { return ((w >> sh) & 0x000F000Fu) | 0x64006400u; }
-// Bits x and x+4 of w as half2 (0 or 1), exact.
-__device__ __forceinline__ __half2 bit2(uint32_t w, int x) {
-    const uint32_t t = w >> x;
-    return __hsub2(as_h2((t & 1u) | ((t << 12) & 0x10000u) | 0x64006400u), as_h2(0x64006400u));
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return as_u(__hmul2(as_h2(a), as_h2(b))); }
+// Nibbles x and x+4 of w (x = 0..3) as half2 (64 + n_x, 64 + n_x+4), exact: each nibble moved
+// to mantissa bits 4-7 of a half with exponent 6.
+__device__ __forceinline__ uint32_t nib64(uint32_t w, int x) {
+    const uint32_t t = (x == 0) ? (w << 4) : (w >> (4 * x - 4));
+    return (t & 0x00F000F0u) | 0x54005400u;
+}
+// Adds 16 x bit x (low half) and 16 x bit x+4 (high half) of h to a nib64 pair: mantissa bit 8.
+__device__ __forceinline__ uint32_t add_bit5(uint32_t raw, uint32_t h, int x) {
+    const uint32_t t = ((h >> x) & 0x11u) * 0x00100100u;
+    return (t & 0x01000100u) | raw;
 }
 // Signed bytes of w (sel 0x5140: bytes 0,1; 0x7362: bytes 2,3) as half2 (1152 + b), exact.
 __device__ __forceinline__ uint32_t i8raw(uint32_t w, uint32_t sel) {
     return __byte_perm(w ^ 0x80808080u, 0x64646464u, sel);
 }
+__device__ __forceinline__ uint32_t movtrans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+    return d;
+}
+__device__ __forceinline__ float lo_f(uint32_t u) { return __low2float(as_h2(u)); }
+__device__ __forceinline__ float hi_f(uint32_t u) { return __high2float(as_h2(u)); }
 
 // ------------------------------------------------------------------------------ geometry
 template <int D, int NQ, int KF, int VF, int KB, int VB>
@@ -120,53 +134,29 @@ struct Geo {
     static constexpr int MT = D / 128;                                  // value m-tiles per warp
     static constexpr bool KNIB = (KF == KF_KVARN || KF == KF_Q4);       // K pairs (x, x+4)
     static constexpr bool VNIB = (VF == KF_KVARN || VF == KF_Q4);
-    static constexpr float KOFF = (KF == KF_Q8) ? 1152.f : (KF == KF_Q4 ? 1032.f : 0.f);
-    static constexpr float VOFF = (VF == KF_Q8) ? 1152.f : (VF == KF_Q4 ? 1032.f : 0.f);
-    // KVarN codes enter the mma centred (code - 2^(b-1), small exact integers): the row's zero
-    // point then absorbs the centre, Z + 2^(b-1) S, and no large offset cancels in the sums
-    static constexpr float KCEN = (KF == KF_KVARN) ? (float)(1 << (KB - 1)) : 0.f;
-    static constexpr float VCEN = (VF == KF_KVARN) ? (float)(1 << (VB - 1)) : 0.f;
+    // value the raw fp16 operand reads for code 0 (the code's own centre included)
+    static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : (KF == KF_Q8 ? 1152.f : 0.f));
+    static constexpr float VOFF = (VF == KF_KVARN) ? 64.f : (VF == KF_Q4 ? 72.f : (VF == KF_Q8 ? 1152.f : 0.f));
+    static constexpr bool ZV = (VF == KF_KVARN);                        // per-group value zero-point sums
+    static constexpr bool PSV = (VF == KF_Q8 || VF == KF_Q4);           // running sums of P' (offset)
     static constexpr bool LUT = (KF == KF_TBQ4) || (VF == KF_TBQ4);
-    // shared memory beyond the stages (bytes)
-    static constexpr bool QHALF = NQ * D > 4096;                        // rotated query kept in fp16
-    static constexpr int QR_BYTES = NQ * D * (QHALF ? 2 : 4);
-    static constexpr int QB_BYTES = NT * KS * 32 * 8;                   // query fragments
-    static constexpr int S_BYTES = 128 * NQ * 4;                        // scores of one group
-    static constexpr int P_BYTES = NVB * NQ * 128 * 2;                  // P' copies
-    static constexpr int ST_FLOATS = NQ * (4 + 2 * NVB + 2 * NBK);     // m, l, alpha, pad, psum, zsum, sumq, zq
-    static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QR_BYTES + QB_BYTES + S_BYTES + P_BYTES + ST_FLOATS * 4;
+    static constexpr int rec(int f, int b) {
+        return f == KF_KVARN ? (D / 256) * (4096 * b + 1152) : (f == KF_TBQ4 ? 66 * D : (f == KF_Q8 ? 136 * D : 72 * D));
+    }
+    static constexpr int REC_K = rec(KF, KB), REC_V = rec(VF, VB);
+    static constexpr int V_OFF = (REC_K + 127) & ~127;
+    static constexpr int STAGE = (V_OFF + REC_V + 127) & ~127;
+    static constexpr int QB_BYTES = NT * KS * 256;                      // query fragments (= NQ D fp16)
+    static constexpr int P_BYTES = NVB * 8 * NT * 256;                  // P' fragments
+    static constexpr int RED_FLOATS = (NVB + 2) * NQ * 8;               // [q][warp] exchange rows
+    static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    static constexpr int TWO_CTA_BYTES = 112 * 1024;
+    static constexpr bool TWO = FIXED + 2 * STAGE <= TWO_CTA_BYTES;
+    static constexpr int MINB = TWO ? 2 : 1;
+    static constexpr int BUDGET = TWO ? TWO_CTA_BYTES : 227 * 1024;
+    static constexpr int NTASK = NQ * D / 8;                            // 8-channel query chunks
+    static constexpr int TPT = (NTASK + kCT - 1) / kCT;                 // chunks per consumer thread
 };
-
-// Index of position t inside one query's [kk][tq][4] P' row: the value k-step kk and slot e
-// that thread quad tq feeds to the mma for that position (the V decoder's pairing).
-template <bool VNIB>
-__device__ __forceinline__ int pidx(int t) {
-    const int tq = t >> 5, r = t & 31;
-    int kk, e;
-    if (VNIB) {    // nibble words of 8 positions, pairs (x, x+4), (x+1, x+5)
-        const int m = r >> 3, rr = r & 7;
-        kk = 2 * m + ((rr >> 1) & 1);
-        e = ((rr & 1) << 1) | (rr >> 2);
-    } else {       // natural pairs (2i, 2i+1)
-        kk = r >> 2;
-        e = r & 3;
-    }
-    return (kk * 4 + tq) * 4 + e;
-}
-
-// Channel of column e (0..3) of score k-step j for thread quad tq.
-template <int KSPB, int WK, bool KNIB>
-__device__ __forceinline__ int kchan(int j, int tq, int e) {
-    const int b = j / KSPB, jj = j % KSPB;
-    int c;
-    if (KNIB) {
-        const int cx = 8 * (jj >> 1) + 2 * (jj & 1);
-        c = cx + ((e & 1) ? 4 : 0) + (e >> 1);
-    } else {
-        c = 4 * jj + e;
-    }
-    return b * WK + (WK / 4) * tq + c;
-}
 
 // Forward rotation of one block (n = 32 NK values, value i = lane + 32 k in v[k]) of a query
 // row with warp shuffles: FWHT butterflies, strides ascending, then scale and signs.
@@ -238,10 +228,11 @@ __device__ void inverse_rotate_c(float* xs, int rows, int D, int rot) {
 
 // ------------------------------------------------------------------------------ the kernel
 template <int D, int NQ, int KF, int VF, int KB, int VB>
-__global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, AttnParams p, int nst) {
+__global__ void __launch_bounds__(kBodyThreads, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
+decode_body_kernel(Layout L, AttnParams p, int nst) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     constexpr int NT = Gm::NT, KS = Gm::KS, NBK = Gm::NBK, KSPB = Gm::KSPB, WK = Gm::WK;
-    constexpr int NVB = Gm::NVB, WV = Gm::WV, MT = Gm::MT;
+    constexpr int NVB = Gm::NVB, WV = Gm::WV, MT = Gm::MT, TPT = Gm::TPT;
     extern __shared__ __align__(128) uint8_t smem[];
 
     // ---- work item: body items follow the region items
@@ -256,9 +247,8 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
     const int64_t unit = L.unit(p.layer, sp.slot, h);
     uint32_t* status = status_word(L, p.pool);
 
-    const uint32_t recK = (uint32_t)L.rec_bytes[0], recV = (uint32_t)L.rec_bytes[1];
-    const uint32_t v_off = (recK + 127u) & ~127u;
-    const uint32_t stage_bytes = (v_off + recV + 127u) & ~127u;
+    constexpr uint32_t recK = Gm::REC_K, recV = Gm::REC_V;
+    constexpr uint32_t v_off = Gm::V_OFF, stage_bytes = Gm::STAGE;
     uint8_t* stages = smem;
     uint8_t* tailp = smem + (size_t)nst * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(tailp);
@@ -266,19 +256,10 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
     uint8_t* cur = tailp + 128;
     uint32_t* lut = reinterpret_cast<uint32_t*>(cur);
     cur += Gm::LUT ? kLutBytes : 0;
-    float* qr = reinterpret_cast<float*>(cur);            // fp32 rows, or fp16 rows when Gm::QHALF
-    __half* qrh = reinterpret_cast<__half*>(cur);         cur += Gm::QR_BYTES;
     uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += Gm::QB_BYTES;
-    float* sbuf = reinterpret_cast<float*>(cur);          cur += Gm::S_BYTES;
-    __half* pbuf = reinterpret_cast<__half*>(cur);        cur += Gm::P_BYTES;
-    float* stt = reinterpret_cast<float*>(cur);
-    float* m_run = stt;                // [NQ]
-    float* l_run = stt + NQ;           // [NQ]
-    float* alpha = stt + 2 * NQ;       // [NQ]
-    float* psum = stt + 4 * NQ;        // [NVB][NQ] offset x sum of P'
-    float* zsum = psum + NVB * NQ;     // [NVB][NQ] sum of p Z (KVarN V)
-    float* sumq = zsum + NVB * NQ;     // [NBK][NQ] offset x sum of the query fragments
-    float* zq = sumq + NBK * NQ;       // [NBK][NQ] sum of the query fragments (KVarN zero point)
+    uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
+    float* red = reinterpret_cast<float*>(cur);
+    float* zsm = red + NQ * 8;                            // [NVB][NQ][warp] value zero-point sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_abort;
@@ -328,7 +309,8 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
             lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
         }
     }
-    {   // rotated query rows (one warp per rotation block of a row)
+    __half* qr = reinterpret_cast<__half*>(qb);           // rotated query rows, fp16 [NQ][D]
+    {
         const uint16_t* q = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
         const int rot = L.rot;
         if (rot == ROT_HAD256) {
@@ -340,10 +322,7 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
                     for (int k = 0; k < 8; ++k) v[k] = (rr < G) ? h2f(q[rr * D + c0 + lane + 32 * k]) : 0.f;
                     warp_rotate<8>(v, lane, rot);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if constexpr (Gm::QHALF) qrh[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
-                        else qr[rr * D + c0 + lane + 32 * k] = v[k];
-                    }
+                    for (int k = 0; k < 8; ++k) qr[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
                 }
             }
         } else {
@@ -354,94 +333,145 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
                 for (int k = 0; k < 4; ++k) v[k] = (rr < G) ? h2f(q[rr * D + c0 + lane + 32 * k]) : 0.f;
                 warp_rotate<4>(v, lane, rot);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    if constexpr (Gm::QHALF) qrh[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
-                    else qr[rr * D + c0 + lane + 32 * k] = v[k];
-                }
+                for (int k = 0; k < 4; ++k) qr[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
             }
-        }
-        if (threadIdx.x < NQ) {
-            m_run[threadIdx.x] = -INFINITY;
-            l_run[threadIdx.x] = 0.f;
         }
     }
     csync();
 
-    // query fragments: entry (nt, j, g, tq) holds, for query nt*8+g, the 4 channels of the
-    // column slots of thread (g, tq) in score k-step j (KVarN: times the group's column scale)
-    auto build_qb = [&](const uint8_t* krec) {
-        for (int e = threadIdx.x; e < NT * KS * 32; e += kCT) {
-            const int tq_ = e & 3, g_ = (e >> 2) & 7, j = (e >> 5) % KS, nt = (e >> 5) / KS;
-            const int qi = nt * 8 + g_;
-            float v[4];
+    // This thread's query chunks (8 consecutive channels of one query) in the order of the two
+    // fragment entries they feed (k-steps j0, j0 + 1): KNIB pairs (0,4) (1,5) | (2,6) (3,7),
+    // otherwise (0,1) (2,3) | (4,5) (6,7).
+    uint32_t qv[TPT][4];
+    int qe[TPT], qcoff[TPT];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int c = kchan<KSPB, WK, Gm::KNIB>(j, tq_, k);
-                float x;
-                if constexpr (Gm::QHALF) x = __half2float(qrh[qi * D + c]);
-                else x = qr[qi * D + c];
-                if (KF == KF_KVARN) {
-                    const uint16_t* sb =
-                        reinterpret_cast<const uint16_t*>(krec + (c >> 8) * (4096 * KB + 1152) + 4096 * KB);
-                    x *= h2f(sb[256 + (c & 255)]);
-                }
-                v[k] = x;
-            }
-            uint2 u;
-            u.x = pack_f2(v[0], v[1]);
-            u.y = pack_f2(v[2], v[3]);
-            reinterpret_cast<uint2*>(qb)[e] = u;
-        }
-        csync();
-        // per query and K block: the sum of the rounded fragments, times the decode offset
-        // (and plain, for the KVarN zero point); one warp per (block, query)
-        for (int u = warp; u < NBK * NQ; u += kConsumers) {
-            const int bk = u / NQ, qi = u % NQ;
-            const int nt = qi / 8, g_ = qi % 8;
-            float s = 0.f;
-            for (int e = lane; e < KSPB * 4; e += 32) {
-                const int j = bk * KSPB + e / 4, tq_ = e & 3;
-                const uint2 uu = reinterpret_cast<const uint2*>(qb)[((nt * KS + j) * 8 + g_) * 4 + tq_];
-                const float2 a = __half22float2(as_h2(uu.x)), c2 = __half22float2(as_h2(uu.y));
-                s += (a.x + a.y) + (c2.x + c2.y);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0) {
-                sumq[bk * NQ + qi] = s * Gm::KOFF;
-                zq[bk * NQ + qi] = s;
+    for (int k = 0; k < TPT; ++k) {
+        const int t = threadIdx.x + kCT * k;
+        qe[k] = -1;
+        qcoff[k] = 0;
+        qv[k][0] = qv[k][1] = qv[k][2] = qv[k][3] = 0u;
+        if (t < Gm::NTASK) {
+            const int qi = t / (D / 8), u = t % (D / 8);
+            const int bb = u / (WK / 8), ub = u % (WK / 8);
+            const int tq_ = ub / (WK / 32), m = ub % (WK / 32);
+            const int j0 = bb * KSPB + 2 * m;
+            qe[k] = (((qi >> 3) * KS + j0) * 8 + (qi & 7)) * 4 + tq_;
+            qcoff[k] = bb * (4096 * KB + 1152) + 4096 * KB + 512 + 16 * ub;   // KVarN column scales
+            const uint4 x = *reinterpret_cast<const uint4*>(qr + qi * D + 8 * u);
+            if (Gm::KNIB) {
+                qv[k][0] = __byte_perm(x.x, x.z, 0x5410);
+                qv[k][1] = __byte_perm(x.x, x.z, 0x7632);
+                qv[k][2] = __byte_perm(x.y, x.w, 0x5410);
+                qv[k][3] = __byte_perm(x.y, x.w, 0x7632);
+            } else {
+                qv[k][0] = x.x; qv[k][1] = x.y; qv[k][2] = x.z; qv[k][3] = x.w;
             }
         }
-        csync();
+    }
+    csync();   // every chunk is read before the fragment area is rewritten
+    // query fragments; KVarN: times the column scales of the group whose K record is at kr
+    auto write_qb = [&](const uint8_t* kr) {
+#pragma unroll
+        for (int k = 0; k < TPT; ++k) {
+            if (qe[k] < 0) continue;
+            uint32_t v0 = qv[k][0], v1 = qv[k][1], v2 = qv[k][2], v3 = qv[k][3];
+            if (KF == KF_KVARN) {
+                const uint4 c = *reinterpret_cast<const uint4*>(kr + qcoff[k]);
+                v0 = hmul2u(v0, __byte_perm(c.x, c.z, 0x5410));
+                v1 = hmul2u(v1, __byte_perm(c.x, c.z, 0x7632));
+                v2 = hmul2u(v2, __byte_perm(c.y, c.w, 0x5410));
+                v3 = hmul2u(v3, __byte_perm(c.y, c.w, 0x7632));
+            }
+            uint2* e = reinterpret_cast<uint2*>(qb) + qe[k];
+            e[0] = make_uint2(v0, v1);
+            e[32] = make_uint2(v2, v3);
+        }
     };
-    if (KF != KF_KVARN) build_qb(nullptr);
-
-    float O[MT][NT][4];
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) O[mt][nt][i] = 0.f;
-    const float sc = L.scale * kLog2e;
     const uint2* qb2 = reinterpret_cast<const uint2*>(qb);
     const uint2* pb2 = reinterpret_cast<const uint2*>(pbuf);
+    constexpr uint32_t ONE2 = 0x3C003C00u;
+    // sum of q' per K block for this thread's queries (columns 2tq, 2tq+1 of each n-tile)
+    float zk[NBK][NT][2];
+#pragma unroll
+    for (int bk = 0; bk < NBK; ++bk)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) zk[bk][nt][0] = zk[bk][nt][1] = 0.f;
+    if (KF != KF_KVARN) {
+        write_qb(nullptr);
+        csync();
+        if (Gm::KOFF != 0.f) {
+#pragma unroll
+            for (int bk = 0; bk < NBK; ++bk)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int jj = 0; jj < KSPB; ++jj) {
+                        const uint2 bq = qb2[((nt * KS + bk * KSPB + jj) * 8 + g) * 4 + tq];
+                        mma16816(a1, ONE2, ONE2, ONE2, ONE2, bq.x, bq.y);
+                    }
+                    zk[bk][nt][0] = a1[0];
+                    zk[bk][nt][1] = a1[1];
+                }
+        }
+    }
+
+    // score rows g and g+8 of this warp: the positions value k-step `warp` feeds (see step 3)
+    const int t0 = Gm::VNIB ? 32 * (g >> 1) + 8 * (warp >> 1) + 2 * (warp & 1) + 4 * (g & 1)
+                            : 32 * (g >> 1) + 4 * warp + (g & 1);
+    const int t1 = t0 + (Gm::VNIB ? 1 : 2);
+    const int vw = (warp * (D / 8)) / WV;                 // value scale block of this warp's channels
+    const float sc = L.scale * kLog2e;
+
+    float m_run[NT][2], l_part[NT][2], ps_run[NVB][NT][2];
+    float O[MT][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_part[nt][0] = l_part[nt][1] = 0.f;
+#pragma unroll
+        for (int v = 0; v < NVB; ++v) ps_run[v][nt][0] = ps_run[v][nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
+    }
 
     for (int gi = 0; gi < ngroups; ++gi) {
         const int sl = gi % nst;
         mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
         const uint8_t* kr = stages + (size_t)sl * stage_bytes;
         const uint8_t* vr = kr + v_off;
-        if (KF == KF_KVARN) build_qb(kr);
+        if (KF == KF_KVARN) {
+            write_qb(kr);
+            csync();
+        }
 
-        // ---------------- phase 1: scores of positions [16 warp, 16 warp + 16), all channels
+        // ---------------- step 1: scores of positions t0, t1 (rows g, g+8), all channels
+        float s4[NT][4];
         {
-            const int t0 = 16 * warp + g, t1 = t0 + 8;
             float acc[NBK][NT][4];
+            float a1[NBK][NT][4];
 #pragma unroll
             for (int bk = 0; bk < NBK; ++bk)
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) acc[bk][nt][0] = acc[bk][nt][1] = acc[bk][nt][2] = acc[bk][nt][3] = 0.f;
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[bk][nt][i] = a1[bk][nt][i] = 0.f;
+            // TBQ4: blocks of 128 channels, 16 bytes of this row and block per thread; with two
+            // blocks, odd rows read them in the other order so a quarter warp hits 32 banks
+            uint4 tY0[NBK], tY1[NBK];
+            if (KF == KF_TBQ4) {
+                const bool sw = (NBK == 2) && (g & 1);
+#pragma unroll
+                for (int bk = 0; bk < NBK; ++bk) {
+                    const int bka = sw ? (NBK - 1 - bk) : bk;
+                    tY0[bk] = *reinterpret_cast<const uint4*>(kr + t0 * (D / 2) + 64 * bka + 16 * tq);
+                    tY1[bk] = *reinterpret_cast<const uint4*>(kr + t1 * (D / 2) + 64 * bka + 16 * tq);
+                }
+                if (NBK == 2 && sw) {
+                    const uint4 a = tY0[0]; tY0[0] = tY0[NBK - 1]; tY0[NBK - 1] = a;
+                    const uint4 c = tY1[0]; tY1[0] = tY1[NBK - 1]; tY1[NBK - 1] = c;
+                }
+            }
 #pragma unroll
             for (int bk = 0; bk < NBK; ++bk) {
                 if (KF == KF_KVARN) {
@@ -466,46 +496,37 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
                     }
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
-                        const int m = jj >> 1, sh = 8 * (jj & 1);
-                        uint32_t a0 = nibraw(W0[m], sh), a2 = nibraw(W0[m], sh + 4);
-                        uint32_t a1 = nibraw(W1[m], sh), a3 = nibraw(W1[m], sh + 4);
+                        const int m = jj >> 1, x = 2 * (jj & 1);
+                        uint32_t a0 = nib64(W0[m], x), a2 = nib64(W0[m], x + 1);
+                        uint32_t a1r = nib64(W1[m], x), a3 = nib64(W1[m], x + 1);
                         if (KB == 5) {
-                            const int x = 8 * m + 2 * (jj & 1);
-                            const uint32_t h0 = (x < 32) ? H0.x : H0.y, h1 = (x < 32) ? H1.x : H1.y;
-                            const __half2 s16 = __float2half2_rn(16.f);
-                            a0 = as_u(__hfma2(bit2(h0, x & 31), s16, as_h2(a0)));
-                            a2 = as_u(__hfma2(bit2(h0, (x & 31) + 1), s16, as_h2(a2)));
-                            a1 = as_u(__hfma2(bit2(h1, x & 31), s16, as_h2(a1)));
-                            a3 = as_u(__hfma2(bit2(h1, (x & 31) + 1), s16, as_h2(a3)));
-                        }
-                        {   // 1024 + code  ->  code - 2^(b-1)
-                            const __half2 off = __float2half2_rn(1024.f + Gm::KCEN);
-                            a0 = as_u(__hsub2(as_h2(a0), off)); a1 = as_u(__hsub2(as_h2(a1), off));
-                            a2 = as_u(__hsub2(as_h2(a2), off)); a3 = as_u(__hsub2(as_h2(a3), off));
+                            const int bx = 8 * (m & 3) + x;
+                            const uint32_t h0 = (m < 4) ? H0.x : H0.y, h1 = (m < 4) ? H1.x : H1.y;
+                            a0 = add_bit5(a0, h0, bx); a2 = add_bit5(a2, h0, bx + 1);
+                            a1r = add_bit5(a1r, h1, bx); a3 = add_bit5(a3, h1, bx + 1);
                         }
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1, a2, a3, bq.x, bq.y);
+                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
+                            mma16816(a1[bk][nt], ONE2, ONE2, ONE2, ONE2, bq.x, bq.y);
                         }
                     }
                 } else if (KF == KF_TBQ4) {
-                    // blocks of 128 channels: 16 bytes of this row and block per thread
-                    const uint4 y0 = *reinterpret_cast<const uint4*>(kr + t0 * (D / 2) + 64 * bk + 16 * tq);
-                    const uint4 y1 = *reinterpret_cast<const uint4*>(kr + t1 * (D / 2) + 64 * bk + 16 * tq);
-                    const uint32_t W0[4] = {y0.x, y0.y, y0.z, y0.w}, W1[4] = {y1.x, y1.y, y1.z, y1.w};
+                    const uint4 y0 = tY0[bk], y1 = tY1[bk];
+                    const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
                     const uint32_t* lt = lut + lane;
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
                         const int m = jj >> 1, sh = 16 * (jj & 1);
-                        const uint32_t a0 = lt[((W0[m] >> sh) & 0xFF) * 32], a2 = lt[((W0[m] >> (sh + 8)) & 0xFF) * 32];
-                        const uint32_t a1 = lt[((W1[m] >> sh) & 0xFF) * 32], a3 = lt[((W1[m] >> (sh + 8)) & 0xFF) * 32];
+                        const uint32_t a0 = lt[((Y0[m] >> sh) & 0xFF) * 32], a2 = lt[((Y0[m] >> (sh + 8)) & 0xFF) * 32];
+                        const uint32_t a1r = lt[((Y1[m] >> sh) & 0xFF) * 32], a3 = lt[((Y1[m] >> (sh + 8)) & 0xFF) * 32];
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1, a2, a3, bq.x, bq.y);
+                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
                 } else if (KF == KF_Q8) {
@@ -515,33 +536,32 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
                         const uint32_t a0 = i8raw(W0[jj], 0x5140), a2 = i8raw(W0[jj], 0x7362);
-                        const uint32_t a1 = i8raw(W1[jj], 0x5140), a3 = i8raw(W1[jj], 0x7362);
+                        const uint32_t a1r = i8raw(W1[jj], 0x5140), a3 = i8raw(W1[jj], 0x7362);
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1, a2, a3, bq.x, bq.y);
+                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
-                } else {   // Q4_0 K
+                } else {   // Q4_0 K: one word of 8 nibbles per row and block
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr + t0 * (D / 2) + 16 * bk + 4 * tq);
                     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr + t1 * (D / 2) + 16 * bk + 4 * tq);
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
-                        const int sh = 8 * (jj & 1);
-                        const uint32_t a0 = nibraw(w0, sh), a2 = nibraw(w0, sh + 4);
-                        const uint32_t a1 = nibraw(w1, sh), a3 = nibraw(w1, sh + 4);
+                        const int x = 2 * jj;
+                        const uint32_t a0 = nib64(w0, x), a2 = nib64(w0, x + 1);
+                        const uint32_t a1r = nib64(w1, x), a3 = nib64(w1, x + 1);
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1, a2, a3, bq.x, bq.y);
+                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
                 }
             }
-            // epilogue: s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q'
-            float s4[NT][4];
+            // s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q', log2 domain
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) s4[nt][0] = s4[nt][1] = s4[nt][2] = s4[nt][3] = 0.f;
 #pragma unroll
@@ -551,8 +571,12 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
                     const uint16_t* sb =
                         reinterpret_cast<const uint16_t*>(kr + (size_t)bk * (4096 * KB + 1152) + 4096 * KB);
                     e0 = h2f(sb[t0]); e1 = h2f(sb[t1]);
-                    z0 = h2f(sb[128 + t0]) + Gm::KCEN * e0;
-                    z1 = h2f(sb[128 + t1]) + Gm::KCEN * e1;
+                    z0 = h2f(sb[128 + t0]); z1 = h2f(sb[128 + t1]);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        zk[bk][nt][0] = a1[bk][nt][0];
+                        zk[bk][nt][1] = a1[bk][nt][1];
+                    }
                 } else if (KF == KF_TBQ4) {
                     const uint16_t* nr = reinterpret_cast<const uint16_t*>(kr + 64 * D);
                     e0 = h2f(nr[t0 * (D / 128) + bk]); e1 = h2f(nr[t1 * (D / 128) + bk]);
@@ -562,97 +586,120 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int qc = nt * 8 + 2 * tq;
-                    const float o0 = sumq[bk * NQ + qc], o1 = sumq[bk * NQ + qc + 1];
-                    const float y0 = zq[bk * NQ + qc], y1 = zq[bk * NQ + qc + 1];
-                    s4[nt][0] += e0 * (acc[bk][nt][0] - o0) + z0 * y0;
-                    s4[nt][1] += e0 * (acc[bk][nt][1] - o1) + z0 * y1;
-                    s4[nt][2] += e1 * (acc[bk][nt][2] - o0) + z1 * y0;
-                    s4[nt][3] += e1 * (acc[bk][nt][3] - o1) + z1 * y1;
+                    const float y0 = zk[bk][nt][0], y1 = zk[bk][nt][1];
+                    if (Gm::KOFF != 0.f) {
+                        const float o0 = Gm::KOFF * y0, o1 = Gm::KOFF * y1;
+                        s4[nt][0] += e0 * (acc[bk][nt][0] - o0) + z0 * y0;
+                        s4[nt][1] += e0 * (acc[bk][nt][1] - o1) + z0 * y1;
+                        s4[nt][2] += e1 * (acc[bk][nt][2] - o0) + z1 * y0;
+                        s4[nt][3] += e1 * (acc[bk][nt][3] - o1) + z1 * y1;
+                    } else {
+                        s4[nt][0] += e0 * acc[bk][nt][0];
+                        s4[nt][1] += e0 * acc[bk][nt][1];
+                        s4[nt][2] += e1 * acc[bk][nt][2];
+                        s4[nt][3] += e1 * acc[bk][nt][3];
+                    }
                 }
+            }
+        }
+        // the warp's maximum per query
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float mx0, mx1;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s4[nt][i] *= sc;
+            mx0 = fmaxf(s4[nt][0], s4[nt][2]);
+            mx1 = fmaxf(s4[nt][1], s4[nt][3]);
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            if (g == 0) {
+                red[(nt * 8 + 2 * tq) * 8 + warp] = mx0;
+                red[(nt * 8 + 2 * tq + 1) * 8 + warp] = mx1;
+            }
+        }
+        csync();
+
+        // ---------------- step 2: group maximum, p, running sums, P' fragments
+        float al[NT][2];
+        float pr[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float4* r4 = reinterpret_cast<const float4*>(red + (nt * 8 + 2 * tq + c) * 8);
+                const float4 x = r4[0], y = r4[1];
+                const float gm = fmaxf(fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)), fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+                const float mn = fmaxf(m_run[nt][c], gm);
+                al[nt][c] = exp2f(m_run[nt][c] - mn);
+                m_run[nt][c] = mn;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pr[nt][i] = exp2f(s4[nt][i] - m_run[nt][i & 1]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) l_part[nt][c] = al[nt][c] * l_part[nt][c] + pr[nt][c] + pr[nt][c + 2];
+        }
+#pragma unroll
+        for (int v = 0; v < NVB; ++v) {
+            float f0, f1, z0 = 0.f, z1 = 0.f;
+            if (VF == KF_KVARN) {
+                const uint16_t* sb =
+                    reinterpret_cast<const uint16_t*>(vr + (size_t)v * (4096 * VB + 1152) + 4096 * VB);
+                f0 = h2f(sb[t0]); f1 = h2f(sb[t1]);
+                z0 = h2f(sb[128 + t0]); z1 = h2f(sb[128 + t1]);
+            } else if (VF == KF_TBQ4) {
+                const uint16_t* nr = reinterpret_cast<const uint16_t*>(vr + 64 * D);
+                f0 = h2f(nr[t0 * (D / 128) + v]); f1 = h2f(nr[t1 * (D / 128) + v]);
+            } else {
+                const uint16_t* dr = reinterpret_cast<const uint16_t*>(vr + (VF == KF_Q8 ? 128 : 64) * D);
+                f0 = h2f(dr[t0 * (D / 32) + v]); f1 = h2f(dr[t1 * (D / 32) + v]);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int qc = nt * 8 + 2 * tq;
-                sbuf[t0 * NQ + qc] = s4[nt][0] * sc;
-                sbuf[t0 * NQ + qc + 1] = s4[nt][1] * sc;
-                sbuf[t1 * NQ + qc] = s4[nt][2] * sc;
-                sbuf[t1 * NQ + qc + 1] = s4[nt][3] * sc;
-            }
-        }
-        csync();
-
-        // ---------------- phase 2: softmax over the group, P' copies in fragment order
-        for (int qi = warp; qi < NQ; qi += kConsumers) {
-            float sv[4];
-            float mx = -INFINITY;
+                const uint32_t P0 = pack_f2(pr[nt][0] * f0, pr[nt][1] * f0);   // position t0, queries 2tq, 2tq+1
+                const uint32_t P1 = pack_f2(pr[nt][2] * f1, pr[nt][3] * f1);   // position t1
+                if (Gm::ZV) {
+                    float zc0 = pr[nt][0] * z0 + pr[nt][2] * z1 - Gm::VOFF * (lo_f(P0) + lo_f(P1));
+                    float zc1 = pr[nt][1] * z0 + pr[nt][3] * z1 - Gm::VOFF * (hi_f(P0) + hi_f(P1));
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                sv[i] = sbuf[(lane + 32 * i) * NQ + qi];
-                mx = fmaxf(mx, sv[i]);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float mo = m_run[qi];
-            const float mn = fmaxf(mo, mx);
-            const float a = exp2f(mo - mn);
-            float ls = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                sv[i] = exp2f(sv[i] - mn);
-                ls += sv[i];
-            }
-            float ps[NVB], zs[NVB];
-#pragma unroll
-            for (int v = 0; v < NVB; ++v) {
-                ps[v] = 0.f;
-                zs[v] = 0.f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int t = lane + 32 * i;
-                    float f;
-                    if (VF == KF_KVARN) {
-                        const uint16_t* sb =
-                            reinterpret_cast<const uint16_t*>(vr + (size_t)v * (4096 * VB + 1152) + 4096 * VB);
-                        f = h2f(sb[t]);
-                        zs[v] += sv[i] * (h2f(sb[128 + t]) + Gm::VCEN * f);
-                    } else if (VF == KF_TBQ4) {
-                        f = h2f(reinterpret_cast<const uint16_t*>(vr + 64 * D)[t * (D / 128) + v]);
-                    } else {
-                        f = h2f(reinterpret_cast<const uint16_t*>(vr + (VF == KF_Q8 ? 128 : 64) * D)[t * (D / 32) + v]);
+                    for (int o = 4; o <= 16; o <<= 1) {
+                        zc0 += __shfl_xor_sync(0xffffffffu, zc0, o);
+                        zc1 += __shfl_xor_sync(0xffffffffu, zc1, o);
                     }
-                    const __half ph = __float2half_rn(sv[i] * f);
-                    pbuf[((size_t)v * NQ + qi) * 128 + pidx<Gm::VNIB>(t)] = ph;
-                    ps[v] += __half2float(ph);
+                    if (g == 0) {
+                        zsm[(v * NQ + nt * 8 + 2 * tq) * 8 + warp] = zc0;
+                        zsm[(v * NQ + nt * 8 + 2 * tq + 1) * 8 + warp] = zc1;
+                    }
                 }
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                ls += __shfl_xor_sync(0xffffffffu, ls, o);
-#pragma unroll
-                for (int v = 0; v < NVB; ++v) {
-                    ps[v] += __shfl_xor_sync(0xffffffffu, ps[v], o);
-                    zs[v] += __shfl_xor_sync(0xffffffffu, zs[v], o);
+                if (Gm::PSV) {
+                    ps_run[v][nt][0] = al[nt][0] * ps_run[v][nt][0] + lo_f(P0) + lo_f(P1);
+                    ps_run[v][nt][1] = al[nt][1] * ps_run[v][nt][1] + hi_f(P0) + hi_f(P1);
                 }
-            }
-            if (lane == 0) {
-                m_run[qi] = mn;
-                l_run[qi] = l_run[qi] * a + ls;
-                alpha[qi] = a;
-#pragma unroll
-                for (int v = 0; v < NVB; ++v) {
-                    psum[v * NQ + qi] = ps[v] * Gm::VOFF;
-                    zsum[v * NQ + qi] = zs[v];
-                }
+                reinterpret_cast<uint2*>(pbuf)[((v * 8 + warp) * NT + nt) * 32 + lane] =
+                    make_uint2(movtrans(P0), movtrans(P1));
             }
         }
         csync();
 
-        // ---------------- phase 3: O^T[ch][q] += V^T P'^T for channels [w D/8, (w+1) D/8)
+        // ---------------- step 3: O^T[ch][q] = alpha O^T + F (V^T P'^T + z) for this warp's channels
+        float zv[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            zv[nt][0] = zv[nt][1] = 0.f;
+            if (Gm::ZV) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const float4* r4 = reinterpret_cast<const float4*>(zsm + (vw * NQ + nt * 8 + 2 * tq + c) * 8);
+                    const float4 x = r4[0], y = r4[1];
+                    zv[nt][c] = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
+                }
+            }
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const int c0 = warp * (D / 8) + 16 * mt + g, c1 = c0 + 8;
-            const int v = (warp * (D / 8) + 16 * mt) / WV;
             float acc[NT][4];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -692,39 +739,30 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
             const uint32_t* lt = lut + lane;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a0, a1, a2, a3;
+                uint32_t a0, a1r, a2, a3;
                 if (Gm::VNIB) {
-                    const int m = kk >> 1, sh = 8 * (kk & 1);
-                    a0 = nibraw(X0[m], sh); a2 = nibraw(X0[m], sh + 4);
-                    a1 = nibraw(X1[m], sh); a3 = nibraw(X1[m], sh + 4);
+                    const int m = kk >> 1, x = 2 * (kk & 1);
+                    a0 = nib64(X0[m], x); a2 = nib64(X0[m], x + 1);
+                    a1r = nib64(X1[m], x); a3 = nib64(X1[m], x + 1);
                     if (VF == KF_KVARN && VB == 5) {
-                        const int x = 8 * m + 2 * (kk & 1);
-                        const __half2 s16 = __float2half2_rn(16.f);
-                        a0 = as_u(__hfma2(bit2(H0, x), s16, as_h2(a0)));
-                        a2 = as_u(__hfma2(bit2(H0, x + 1), s16, as_h2(a2)));
-                        a1 = as_u(__hfma2(bit2(H1, x), s16, as_h2(a1)));
-                        a3 = as_u(__hfma2(bit2(H1, x + 1), s16, as_h2(a3)));
-                    }
-                    if (VF == KF_KVARN) {   // 1024 + code  ->  code - 2^(b-1)
-                        const __half2 off = __float2half2_rn(1024.f + Gm::VCEN);
-                        a0 = as_u(__hsub2(as_h2(a0), off)); a1 = as_u(__hsub2(as_h2(a1), off));
-                        a2 = as_u(__hsub2(as_h2(a2), off)); a3 = as_u(__hsub2(as_h2(a3), off));
+                        const int bx = 8 * m + x;
+                        a0 = add_bit5(a0, H0, bx); a2 = add_bit5(a2, H0, bx + 1);
+                        a1r = add_bit5(a1r, H1, bx); a3 = add_bit5(a3, H1, bx + 1);
                     }
                 } else if (VF == KF_TBQ4) {
                     const int m = kk >> 1, sh = 16 * (kk & 1);
                     a0 = lt[((X0[m] >> sh) & 0xFF) * 32]; a2 = lt[((X0[m] >> (sh + 8)) & 0xFF) * 32];
-                    a1 = lt[((X1[m] >> sh) & 0xFF) * 32]; a3 = lt[((X1[m] >> (sh + 8)) & 0xFF) * 32];
+                    a1r = lt[((X1[m] >> sh) & 0xFF) * 32]; a3 = lt[((X1[m] >> (sh + 8)) & 0xFF) * 32];
                 } else {
                     a0 = i8raw(X0[kk], 0x5140); a2 = i8raw(X0[kk], 0x7362);
-                    a1 = i8raw(X1[kk], 0x5140); a3 = i8raw(X1[kk], 0x7362);
+                    a1r = i8raw(X1[kk], 0x5140); a3 = i8raw(X1[kk], 0x7362);
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bp = pb2[(((size_t)v * NQ + nt * 8 + g) * 8 + kk) * 4 + tq];
-                    mma16816(acc[nt], a0, a1, a2, a3, bp.x, bp.y);
+                    const uint2 bp = pb2[((vw * 8 + kk) * NT + nt) * 32 + lane];
+                    mma16816(acc[nt], a0, a1r, a2, a3, bp.x, bp.y);
                 }
             }
-            // O = alpha O + F (acc - off sum P' + sum p Z)
             float F0 = 1.f, F1 = 1.f;
             if (VF == KF_KVARN) {
                 const uint16_t* sb = reinterpret_cast<const uint16_t*>(vt + 4096 * VB);
@@ -733,45 +771,69 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const int qc = nt * 8 + 2 * tq;
-                const float al0 = alpha[qc], al1 = alpha[qc + 1];
-                const float ps0 = psum[v * NQ + qc], ps1 = psum[v * NQ + qc + 1];
-                float z0 = 0.f, z1 = 0.f;
-                if (VF == KF_KVARN) {
-                    z0 = zsum[v * NQ + qc];
-                    z1 = zsum[v * NQ + qc + 1];
-                }
-                O[mt][nt][0] = al0 * O[mt][nt][0] + F0 * (acc[nt][0] - ps0 + z0);
-                O[mt][nt][1] = al1 * O[mt][nt][1] + F0 * (acc[nt][1] - ps1 + z1);
-                O[mt][nt][2] = al0 * O[mt][nt][2] + F1 * (acc[nt][2] - ps0 + z0);
-                O[mt][nt][3] = al1 * O[mt][nt][3] + F1 * (acc[nt][3] - ps1 + z1);
+                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + F0 * (acc[nt][0] + zv[nt][0]);
+                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + F0 * (acc[nt][1] + zv[nt][1]);
+                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + F1 * (acc[nt][2] + zv[nt][0]);
+                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + F1 * (acc[nt][3] + zv[nt][1]);
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&empty[sl]));
     }
 
-    // ---- partial: o rotated back to the original domain, m and l
+    // ---- partial: running sums over rows and warps, o rotated back to the original domain
+    csync();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float l = l_part[nt][c];
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (g == 0) red[(nt * 8 + 2 * tq + c) * 8 + warp] = l;
+            if (Gm::PSV) {
+#pragma unroll
+                for (int v = 0; v < NVB; ++v) {
+                    float s = ps_run[v][nt][c];
+#pragma unroll
+                    for (int o = 4; o <= 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                    if (g == 0) zsm[(v * NQ + nt * 8 + 2 * tq + c) * 8 + warp] = s;
+                }
+            }
+            if (warp == 0 && g == 0) red[(NVB + 1) * NQ * 8 + nt * 8 + 2 * tq + c] = m_run[nt][c];
+        }
     csync();
     float* ofin = reinterpret_cast<float*>(stages);                     // [NQ][D], stages drained
 #pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-        const int c0 = warp * (D / 8) + 16 * mt + g;
+    for (int nt = 0; nt < NT; ++nt) {
+        float off0 = 0.f, off1 = 0.f;
+        if (Gm::PSV) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int qc = nt * 8 + 2 * tq;
-            ofin[qc * D + c0] = O[mt][nt][0];
-            ofin[(qc + 1) * D + c0] = O[mt][nt][1];
-            ofin[qc * D + c0 + 8] = O[mt][nt][2];
-            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3];
+            for (int c = 0; c < 2; ++c) {
+                const float4* r4 = reinterpret_cast<const float4*>(zsm + (vw * NQ + nt * 8 + 2 * tq + c) * 8);
+                const float4 x = r4[0], y = r4[1];
+                const float s = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
+                (c == 0 ? off0 : off1) = Gm::VOFF * s;
+            }
+        }
+        const int qc = nt * 8 + 2 * tq;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int c0 = warp * (D / 8) + 16 * mt + g;
+            ofin[qc * D + c0] = O[mt][nt][0] - off0;
+            ofin[(qc + 1) * D + c0] = O[mt][nt][1] - off1;
+            ofin[qc * D + c0 + 8] = O[mt][nt][2] - off0;
+            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3] - off1;
         }
     }
     csync();
     inverse_rotate_c(ofin, NQ, D, L.rot);
     float* part = p.partials + (size_t)item * (2 * NQ + NQ * D);
     if (threadIdx.x < NQ) {
-        part[threadIdx.x] = m_run[threadIdx.x];
-        part[NQ + threadIdx.x] = l_run[threadIdx.x];
+        const float4* r4 = reinterpret_cast<const float4*>(red + threadIdx.x * 8);
+        const float4 x = r4[0], y = r4[1];
+        part[threadIdx.x] = red[(NVB + 1) * NQ * 8 + threadIdx.x];
+        part[NQ + threadIdx.x] = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
     }
     float4* po = reinterpret_cast<float4*>(part + 2 * NQ);
     const float4* o4 = reinterpret_cast<const float4*>(ofin);
@@ -782,9 +844,9 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_body_kernel(Layout L, 
 template <int D, int NQ, int KF, int VF, int KB, int VB>
 int nstages(const Layout& L) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
-    const uint32_t recK = (uint32_t)L.rec_bytes[0], recV = (uint32_t)L.rec_bytes[1];
-    const size_t stage = ((((recK + 127u) & ~127u) + recV + 127u) & ~127u);
-    const size_t budget = 227 * 1024;
+    if (L.rec_bytes[0] != Gm::REC_K || L.rec_bytes[1] != Gm::REC_V) return 0;
+    const size_t stage = Gm::STAGE;
+    const size_t budget = Gm::BUDGET;
     if ((size_t)Gm::FIXED >= budget) return 0;
     int nst = (int)((budget - Gm::FIXED) / stage);
     if (nst > 4) nst = 4;
@@ -797,12 +859,11 @@ int launch_t(const Layout& L, const AttnParams& p, int n_body, cudaStream_t st) 
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
     if (nst == 0) return (int)cudaErrorInvalidConfiguration;
-    const uint32_t recK = (uint32_t)L.rec_bytes[0], recV = (uint32_t)L.rec_bytes[1];
-    const size_t stage = ((((recK + 127u) & ~127u) + recV + 127u) & ~127u);
-    const size_t smem = (size_t)nst * stage + Gm::FIXED;
-    cudaFuncSetAttribute(decode_body_kernel<D, NQ, KF, VF, KB, VB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)smem);
-    decode_body_kernel<D, NQ, KF, VF, KB, VB><<<n_body, kBodyThreads, smem, st>>>(L, p, nst);
+    const size_t smem = (size_t)nst * Gm::STAGE + Gm::FIXED;
+    auto kern = decode_body_kernel<D, NQ, KF, VF, KB, VB>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+    kern<<<n_body, kBodyThreads, smem, st>>>(L, p, nst);
     return (int)cudaGetLastError();
 }
 
@@ -826,10 +887,10 @@ int dispatch(const Layout& L, F&& f) {
     return -1;
 }
 
-struct NstFn {
+struct CtasFn {
     const Layout& L;
     template <int D, int NQ, int KF, int VF, int KB, int VB>
-    int run() { return nstages<D, NQ, KF, VF, KB, VB>(L); }
+    int run() { return nstages<D, NQ, KF, VF, KB, VB>(L) > 0 ? Geo<D, NQ, KF, VF, KB, VB>::MINB : 0; }
 };
 struct LaunchFn {
     const Layout& L;
@@ -846,11 +907,11 @@ int upload_tables_body(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-// 1 when the body kernel has an instance for this layout (and its stages fit), else 0.
+// Resident body-kernel CTAs per SM for this layout (1 or 2), 0 when no instance fits it.
 int body_ctas_per_sm(const Layout& L) {
-    NstFn f{L};
+    CtasFn f{L};
     const int r = dispatch(L, f);
-    return r > 0 ? 1 : 0;
+    return r > 0 ? r : 0;
 }
 
 // Launches the body kernel over the body items (those after the region items of p).
