@@ -16,6 +16,7 @@ same workload: the reference this build is checked against.
 """
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -41,6 +42,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (a smaller case for profiling; the line names it)")
     return ap.parse_args()
 
 
@@ -181,6 +184,8 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = configs.WORKLOADS[args.workload]
+    if args.layers:
+        w = dataclasses.replace(w, n_layers=min(args.layers, w.n_layers))
     K, W = args.steps, args.warmup
     n_steps = max(K, W, w.steps)
     seq_ids = list(range(len(w.contexts)))

@@ -490,6 +490,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
 // with eight independent loads in flight; slices meet in shared memory.
 constexpr int kMergeMaxItems = 1024;
 
+// grid (n_seq * H, D / 8), 256 threads: block (bh, y) combines the partials of sequence
+// bh / H, KV head bh % H for channels [8y, 8y + 8). Every partial's m and l are loaded at once
+// (one thread per partial) into shared memory; a warp per query forms m*, the weights
+// 2^(m_c - m*) and l*; then each thread issues the loads of all its partials' slices before
+// accumulating them.
 template <int D, int NQ>
 __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
     const int bh = blockIdx.x;
@@ -500,84 +505,125 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     const int cnt = cnt_r + s.body_per_head;
     const int G = L.G;
     extern __shared__ float msm[];
-    float* wgt = msm;                                   // [cnt][NQ]
-    __shared__ float mstar[NQ], lstar[NQ];
-    __shared__ float red[8][NQ][32];
+    float* wgt = msm;                                   // [cnt][NQ]: m_c, then the weights
+    float* lsm = msm + (size_t)cnt * NQ;                // [cnt][NQ]: l_c
+    __shared__ float lstar[NQ];
+    constexpr int FPI = 2 * NQ;                         // float4 slices per partial (8 channels x NQ)
+    constexpr int IL = 256 / FPI;                       // partials in flight per pass
+    __shared__ float4 red4[IL][FPI];
     auto item_of = [&](int c) { return c < cnt_r ? first + c : bfirst + (c - cnt_r); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t stride = 2 * NQ + NQ * D;
+    for (int c = threadIdx.x; c < cnt; c += blockDim.x) {
+        const float4* pc = reinterpret_cast<const float4*>(p.partials + item_of(c) * stride);
+        float4 mv[NQ / 4], lv[NQ / 4];
+#pragma unroll
+        for (int k = 0; k < NQ / 4; ++k) {
+            mv[k] = pc[k];
+            lv[k] = pc[NQ / 4 + k];
+        }
+#pragma unroll
+        for (int k = 0; k < NQ / 4; ++k) {
+            reinterpret_cast<float4*>(wgt + c * NQ)[k] = mv[k];
+            reinterpret_cast<float4*>(lsm + c * NQ)[k] = lv[k];
+        }
+    }
+    __syncthreads();
     for (int qi = warp; qi < G; qi += 8) {
         float m = -INFINITY;
-        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, p.partials[item_of(c) * stride + qi]);
+        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, wgt[c * NQ + qi]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
         for (int c = lane; c < cnt; c += 32) {
-            const float* pc = p.partials + item_of(c) * stride;
-            const float mc = pc[qi];
+            const float mc = wgt[c * NQ + qi];
             const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - m);
             wgt[c * NQ + qi] = w;
-            l += w * pc[NQ + qi];
+            l += w * lsm[c * NQ + qi];
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            mstar[qi] = m;
-            lstar[qi] = l;
-        }
+        if (lane == 0) lstar[qi] = l;
     }
     __syncthreads();
-    const int c0 = blockIdx.y * 32;
-    // thread = (slice = warp, channel = lane); it sums its slice of the partials for all queries
-    float acc[NQ];
+    const int c0 = blockIdx.y * 8;
+    const int il = threadIdx.x / FPI, f = threadIdx.x % FPI;
+    const int qi = f >> 1, half = f & 1;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qi < G) {
+        constexpr int U = 8;
+        for (int cb = il; cb < cnt; cb += IL * U) {
+            float4 v[U];
 #pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) acc[qi] = 0.f;
-    for (int cb = warp * 8; cb < cnt; cb += 64) {
-        float v[8][NQ];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = cb + u;
-            if (c < cnt) {
-                const float* row = p.partials + item_of(c) * stride + 2 * NQ + c0 + lane;
-#pragma unroll
-                for (int qi = 0; qi < NQ; ++qi) v[u][qi] = (qi < G) ? row[qi * D] : 0.f;
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + IL * u;
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c < cnt)
+                    v[u] = *reinterpret_cast<const float4*>(p.partials + item_of(c) * stride + 2 * NQ + qi * D + c0 +
+                                                            4 * half);
             }
-        }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = cb + u;
-            if (c < cnt) {
-#pragma unroll
-                for (int qi = 0; qi < NQ; ++qi) acc[qi] += wgt[c * NQ + qi] * v[u][qi];
+            for (int u = 0; u < U; ++u) {
+                const int c = cb + IL * u;
+                if (c < cnt) {
+                    const float w = wgt[c * NQ + qi];
+                    acc.x += w * v[u].x;
+                    acc.y += w * v[u].y;
+                    acc.z += w * v[u].z;
+                    acc.w += w * v[u].w;
+                }
             }
         }
     }
-#pragma unroll
-    for (int qi = 0; qi < NQ; ++qi) red[warp][qi][lane] = acc[qi];
+    red4[il][f] = acc;
     __syncthreads();
-    for (int e = threadIdx.x; e < G * 32; e += blockDim.x) {
-        const int qi = e / 32, ch = e % 32;
-        float o = 0.f;
+    if (threadIdx.x < FPI && qi < G) {
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int wv = 0; wv < 8; ++wv) o += red[wv][qi][ch];
-        p.out[((int64_t)b * L.Hq + (int64_t)h * G + qi) * D + c0 + ch] = f2h_bits(o / lstar[qi]);
+        for (int k = 0; k < IL; ++k) {
+            const float4 x = red4[k][f];
+            o.x += x.x; o.y += x.y; o.z += x.z; o.w += x.w;
+        }
+        const float inv = 1.f / lstar[qi];
+        uint2 hv;
+        hv.x = pack_h2(o.x * inv, o.y * inv);
+        hv.y = pack_h2(o.z * inv, o.w * inv);
+        *reinterpret_cast<uint2*>(p.out + ((int64_t)b * L.Hq + (int64_t)h * G + qi) * D + c0 + 4 * half) = hv;
     }
 }
 
 template <int D, int NQ>
-int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
+int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaStream_t aux, cudaEvent_t evf,
+                    cudaEvent_t evj) {
     using C = Cfg<D, NQ>;
     static bool attr = false;
     if (!attr) {
         cudaFuncSetAttribute(decode_split_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         attr = true;
     }
-    if (p.n_region_items > 0) {
-        decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return (int)e;
-    }
     const int n_body = p.total_items - p.n_region_items;
+    if (p.n_region_items > 0) {
+        // the streaming region kernel takes the region items when the body kernel takes the
+        // body (so no body positions are among them) and the layout is one it covers; with
+        // body work too it runs on the auxiliary stream, beside the body kernel
+        if (region_kernel_ok(L) && body_ctas_per_sm(L) > 0) {
+            const bool fork = aux && evf && evj && n_body > 0;
+            if (fork) {
+                if (cudaEventRecord(evf, s) != cudaSuccess || cudaStreamWaitEvent(aux, evf, 0) != cudaSuccess)
+                    return (int)cudaGetLastError();
+            }
+            const int e = launch_decode_region(L, p, fork ? aux : s);
+            if (fork) {
+                cudaEventRecord(evj, aux);
+                cudaStreamWaitEvent(s, evj, 0);
+            }
+            if (e != 0) return e;
+        } else {
+            decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return (int)e;
+        }
+    }
     if (n_body > 0) {
         const int e = launch_decode_body(L, p, n_body, s);
         if (e != 0) return e;
@@ -586,8 +632,11 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
     for (int i = 0; i < p.n_seq; ++i)
         max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
     if (max_cnt > kMergeMaxItems) return (int)cudaErrorInvalidConfiguration;
-    dim3 mg(p.n_seq * L.H, D / 32);
-    decode_merge_kernel<D, NQ><<<mg, 256, (size_t)max_cnt * NQ * sizeof(float), s>>>(L, p);
+    dim3 mg(p.n_seq * L.H, D / 8);
+    const size_t msmem = (size_t)max_cnt * NQ * 2 * sizeof(float);
+    if (msmem > 48 * 1024)
+        cudaFuncSetAttribute(decode_merge_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
+    decode_merge_kernel<D, NQ><<<mg, 256, msmem, s>>>(L, p);
     return (int)cudaGetLastError();
 }
 
@@ -597,17 +646,18 @@ int upload_tables_attn(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-int launch_decode(const Layout& L, const AttnParams& p, void* stream) {
+int launch_decode(const Layout& L, const AttnParams& p, void* stream, void* aux, void* ev_fork, void* ev_join) {
     if (p.total_items == 0) return 0;
-    cudaStream_t s = (cudaStream_t)stream;
+    cudaStream_t s = (cudaStream_t)stream, a = (cudaStream_t)aux;
+    cudaEvent_t f = (cudaEvent_t)ev_fork, j = (cudaEvent_t)ev_join;
     if (L.NQ == 8) {
-        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s);
-        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s);
-        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s);
+        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s, a, f, j);
+        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s, a, f, j);
+        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s, a, f, j);
     } else {
-        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s);
-        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s);
-        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s);
+        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s, a, f, j);
+        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s, a, f, j);
+        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s, a, f, j);
     }
     return (int)cudaErrorInvalidValue;
 }

@@ -158,8 +158,39 @@ __device__ __forceinline__ void load_journal_row(const Layout& L, const void* po
     }
 }
 
+// One tq6_0 block (values lane + 32 m, m = 0..3, taken from v[k0 + m]) of a journal slot:
+// scale, codes through shared memory, then the ql / qh planes.
+template <int NK>
+__device__ __forceinline__ void tq6_block(const float (&v)[NK], int k0, int blk, int lane, uint8_t* cs, uint8_t* row,
+                                          uint16_t* sc) {
+    float a = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a = fmaxf(a, fabsf(v[k0 + m]));
+    a = warp_max(a);
+    const uint16_t d16 = f2h_bits(fdiv(a, 31.0f));
+    const float d = h2f(d16);
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        float q = (d == 0.f) ? 0.f : rintf(fmul(v[k0 + m], inv));
+        q = fminf(fmaxf(q, -31.f), 31.f);
+        cs[128 * blk + lane + 32 * m] = (uint8_t)((int)q + 32);
+    }
+    __syncwarp();
+    const uint8_t* c = cs + 128 * blk;
+    uint8_t* out = row + 96 * blk;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int j = lane + 32 * r;
+        out[j] = (uint8_t)((c[2 * j] & 15) | ((c[2 * j + 1] & 15) << 4));
+    }
+    out[64 + lane] = (uint8_t)((c[4 * lane] >> 4) | ((c[4 * lane + 1] >> 4) << 2) | ((c[4 * lane + 2] >> 4) << 4) |
+                               ((c[4 * lane + 3] >> 4) << 6));
+    if (lane == 0) sc[blk] = d16;
+}
+
 // ---------------------------------------------------------------------------- append
-// grid (n_seq * n_tok, H, 2), block max(32, D / 4) threads; dynamic smem D floats + D bytes.
+// grid (n_seq * n_tok, H, 2), block D / 4 threads (one warp per 128 values); dynamic smem D bytes.
 __global__ void append_kernel(Layout L, AppendParams p) {
     const int b = blockIdx.x / p.n_tok, t = blockIdx.x % p.n_tok;
     const int h = blockIdx.y, w = blockIdx.z, D = L.D;
@@ -186,44 +217,43 @@ __global__ void append_kernel(Layout L, AppendParams p) {
             tl[i] = (L.tail_fmt == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
     }
 
-    extern __shared__ float xs[];
-    uint8_t* cs = (uint8_t*)(xs + D);
-    for (int i = threadIdx.x; i < D; i += blockDim.x) xs[i] = h2f(src[i]);
-    __syncthreads();
-    block_rotate(xs, D, L.rot);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // rotation: one warp per rotation block (256 values for HAD256, else 128), value
+    // i = lane + 32 k of the block in v[k]; the butterflies, signs and scale are those of the
+    // block-wide rotation, in the same order
+    extern __shared__ uint8_t cs[];                   // D codes
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     uint8_t* row = jcode_row(L, p.pool, w, unit, slot);
     uint16_t* sc = jscale_row(L, p.pool, w, unit, slot);
-    for (int blk = warp; blk < D / 128; blk += blockDim.x >> 5) {
-        float v[4];
-        float a = 0.f;
+    if (L.rot == ROT_HAD256) {
+        for (int u = warp; u < D / 256; u += nw) {
+            float v[8];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            v[m] = xs[128 * blk + lane + 32 * m];
-            a = fmaxf(a, fabsf(v[m]));
-        }
-        a = warp_max(a);
-        const uint16_t d16 = f2h_bits(fdiv(a, 31.0f));
-        const float d = h2f(d16);
-        const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+            for (int k = 0; k < 8; ++k) v[k] = h2f(src[256 * u + lane + 32 * k]);
+            warp_fwht<8>(v, lane);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            float q = (d == 0.f) ? 0.f : rintf(fmul(v[m], inv));
-            q = fminf(fmaxf(q, -31.f), 31.f);
-            cs[128 * blk + lane + 32 * m] = (uint8_t)((int)q + 32);
+            for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
+            tq6_block(v, 0, 2 * u, lane, cs, row, sc);
+            tq6_block(v, 4, 2 * u + 1, lane, cs, row, sc);
         }
-        __syncwarp();
-        const uint8_t* c = cs + 128 * blk;
-        uint8_t* out = row + 96 * blk;
+    } else {
+        for (int u = warp; u < D / 128; u += nw) {
+            float v[4];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int j = lane + 32 * r;
-            out[j] = (uint8_t)((c[2 * j] & 15) | ((c[2 * j + 1] & 15) << 4));
+            for (int k = 0; k < 4; ++k) v[k] = h2f(src[128 * u + lane + 32 * k]);
+            if (L.rot == ROT_TBQ128) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (sign_neg(0, lane + 32 * k)) v[k] = -v[k];
+                warp_fwht<4>(v, lane);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float y = v[k];
+                    if (sign_neg(1, lane + 32 * k)) y = -y;
+                    v[k] = fmul(y, kTbqScale);
+                }
+            }
+            tq6_block(v, 0, u, lane, cs, row, sc);
         }
-        out[64 + lane] = (uint8_t)((c[4 * lane] >> 4) | ((c[4 * lane + 1] >> 4) << 2) |
-                                   ((c[4 * lane + 2] >> 4) << 4) | ((c[4 * lane + 3] >> 4) << 6));
-        if (lane == 0) sc[blk] = d16;
     }
 }
 
@@ -579,8 +609,8 @@ int upload_tables_codec(const FormatTables& t) {
 
 int launch_append(const Layout& L, const AppendParams& p, void* stream) {
     dim3 grid(p.n_seq * p.n_tok, L.H, 2);
-    const int threads = L.D / 4 < 32 ? 32 : L.D / 4;
-    const size_t smem = (size_t)L.D * (sizeof(float) + 1);
+    const int threads = L.D / 4;
+    const size_t smem = (size_t)L.D;
     append_kernel<<<grid, threads, smem, (cudaStream_t)stream>>>(L, p);
     return (int)cudaGetLastError();
 }

@@ -1,0 +1,553 @@
+// Decode attention over the unsealed regions: the tq6_0 ring span (rotated domain) and the
+// fp16 rows of the sink, the exact tail and an F16 exact journal (original domain).
+//
+// One CTA per region work item (sequence, KV head, run of positions inside one region), in
+// runs of up to 128 positions. Warp 8 streams each run into shared memory with cp.async.bulk:
+// one copy per contiguous slot range of the K rows, V rows and tq6_0 scale rows (many small
+// copies per run cost far more TMA time than a few large ones). Warps 0-7 consume each run
+// like the body kernel:
+//   1. scores: warp w takes positions [16w, 16w + 16) and all D channels. tq6_0 K rows are
+//      decoded straight into mma.sync m16n8k16 A fragments (6-bit code c: nibble in mantissa
+//      bits 4-7 and the two high bits in bits 8-9 of a half with exponent 6, i.e. 64 + c);
+//      fp16 K rows are the A fragments as they stand. Positions past the run's end score -inf.
+//   2. group maximum, p = 2^(s - m), running sums, P' = p x (tq6_0 value scale of the block);
+//      movmatrix gives the B fragments of step 3 (one 8-byte store per lane).
+//   3. values: warp w takes channels [wD/8, (w+1)D/8). The rows are token-major, so the A
+//      fragments of V^T come from transposes: ldmatrix.trans for fp16 rows, movmatrix of the
+//      decoded tq6_0 tile for the ring (whose fragment rows then hold channels in the order
+//      0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
+//      removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
+// The partial (m, l, o) of a ring item is rotated back to the original domain; the merge
+// kernel (kernels_attn.cu) combines all partials of a (sequence, KV head) under one softmax.
+#include "stream_common.cuh"
+
+namespace kvq {
+namespace {
+
+template <int D, int NQ>
+struct RGeo {
+    static constexpr int NT = NQ / 8;
+    static constexpr int KS = D / 16;
+    static constexpr int MT = D / 128;
+    static constexpr int NB = D / 128;                                  // tq6_0 blocks per row
+    static constexpr int CODE_ROW = NB * 96;                            // tq6_0 code row bytes
+    static constexpr int CLD = CODE_ROW;                                // smem row stride (dense)
+    static constexpr int SC_BYTES = (128 * NB * 2 + 15) & ~15;         // scale rows of a run
+    static constexpr int TQ_HALF = 128 * CLD + SC_BYTES;                // K (or V) part of a ring stage
+    static constexpr int TQ_STAGE = 2 * TQ_HALF;
+    static constexpr int FLD = 2 * D;                                   // fp16 row stride (dense)
+    static constexpr int F_HALF = 128 * FLD;
+    static constexpr int F_STAGE = 2 * F_HALF;
+    static constexpr int AREA = (2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE;
+    static constexpr int QB_BYTES = NT * KS * 256;
+    static constexpr int P_BYTES = NB * 8 * NT * 256;
+    static constexpr int RED_FLOATS = 2 * NQ * 8 + 2 * NQ;
+    static constexpr int SMEM = AREA + 128 + QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    static constexpr int NTASK = NQ * D / 8;
+    static constexpr int TPT = (NTASK + kCT - 1) / kCT;
+};
+
+// Adds the two high bits of tq6_0 codes y and y+4 (fields 2y and 2y+8 of h) as 16 x value:
+// mantissa bits 8-9 of each half of a nib64 pair.
+__device__ __forceinline__ uint32_t add_hi2(uint32_t raw, uint32_t h, int y) {
+    const uint32_t t = ((h >> (2 * y)) & 0x303u) * 0x00010100u;
+    return (t & 0x03000300u) | raw;
+}
+// nib64 with a run-time pair index x (0..3): a funnel shift brings nibbles x, x+4 to bits 4-7, 20-23.
+__device__ __forceinline__ uint32_t nib64_rt(uint32_t w, int x) {
+    const uint32_t t = __funnelshift_r(w << 4, w >> 28, 4 * x);
+    return (t & 0x00F000F0u) | 0x54005400u;
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+template <int D, int NQ>
+__global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L, AttnParams p) {
+    using Gm = RGeo<D, NQ>;
+    constexpr int NT = Gm::NT, KS = Gm::KS, MT = Gm::MT, NB = Gm::NB, TPT = Gm::TPT;
+    constexpr int CLD = Gm::CLD, FLD = Gm::FLD;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    // ---- work item (same enumeration as the generic region kernel)
+    const int item = (int)blockIdx.x;
+    int b = 0;
+    while (b + 1 < p.n_seq && p.seq[b + 1].first_item <= item) ++b;
+    const SeqSpan& sp = p.seq[b];
+    const int local = item - sp.first_item;
+    const int h = local / sp.items_per_head;
+    int cidx = local % sp.items_per_head, r = 0;
+    while (r < 3 && cidx >= sp.nchunk[r]) { cidx -= sp.nchunk[r]; ++r; }
+    const int kind = sp.kind[r];
+    const int t0 = sp.lo[r] + cidx * p.chunk;
+    const int t1 = min(t0 + p.chunk, sp.hi[r]);
+    const int nrun = (t1 - t0 + 127) / 128;
+    const bool ring = (kind == RK_RING);
+    const int64_t unit = L.unit(p.layer, sp.slot, h);
+    uint32_t* status = status_word(L, p.pool);
+
+    const uint32_t stage_bytes = ring ? Gm::TQ_STAGE : Gm::F_STAGE;
+    const uint32_t half_bytes = ring ? Gm::TQ_HALF : Gm::F_HALF;
+    const int nst = min(4, Gm::AREA / (int)stage_bytes);
+    uint8_t* stages = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
+    uint64_t* empty = full + 4;
+    uint8_t* cur = smem + Gm::AREA + 128;
+    uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += Gm::QB_BYTES;
+    uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
+    float* red = reinterpret_cast<float*>(cur);           // [NQ][warp] maxima, then sums; m at 2 NQ 8
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int s_abort;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(su32(&full[i]), 1);
+            mbar_init(su32(&empty[i]), kConsumers);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+
+    // ================================================================== producer warp
+    if (warp == kConsumers) {
+        int issued = 0;
+        bool ok = true;
+        for (int i = 0; i < nrun; ++i) {
+            const int sl = i % nst;
+            if (i >= nst) {
+                int good = 1;
+                if (lane == 0) good = mbar_wait(su32(&empty[sl]), ((i / nst) - 1) & 1, status, &s_abort) ? 1 : 0;
+                good = __shfl_sync(0xffffffffu, good, 0);
+                if (!good) { ok = false; break; }
+            }
+            const int pc = t0 + 128 * i, n = min(128, t1 - pc);
+            uint8_t* st = stages + (size_t)sl * stage_bytes;
+            const uint32_t fb = su32(&full[sl]);
+            // contiguous slot runs: one copy each (a run of the ring never wraps; the tail and an
+            // exact journal wrap at most once)
+            if (lane == 0) {
+                if (ring) {
+                    mbar_expect_tx(fb, 2u * (n * Gm::CODE_ROW + Gm::SC_BYTES));
+                    for (int w = 0; w < 2; ++w) {
+                        uint8_t* dst = st + w * half_bytes;
+                        const int s0 = journal_slot(L, pc);
+                        bulk_g2s(su32(dst), jcode_row(L, p.pool, w, unit, s0), n * Gm::CODE_ROW, fb);
+                        bulk_g2s(su32(dst + 128 * CLD), jscale_row(L, p.pool, w, unit, s0), Gm::SC_BYTES, fb);
+                    }
+                } else {
+                    mbar_expect_tx(fb, 2u * n * 2 * D);
+                    for (int w = 0; w < 2; ++w) {
+                        uint8_t* dst = st + w * half_bytes;
+                        int done = 0;
+                        while (done < n) {
+                            const int pos = pc + done;
+                            const uint16_t* src;
+                            int cnt;
+                            if (kind == RK_SINK) {
+                                src = sink_row(L, p.pool, w, unit, pos);
+                                cnt = n - done;
+                            } else if (kind == RK_TAIL) {
+                                const int sl0 = pos % L.T;
+                                src = tail_row(L, p.pool, w, unit, sl0);
+                                cnt = min(n - done, L.T - sl0);
+                            } else {
+                                const int sl0 = journal_slot(L, pos);
+                                src = jexact_row(L, p.pool, w, unit, sl0);
+                                cnt = min(n - done, L.R - sl0);
+                            }
+                            bulk_g2s(su32(dst + done * FLD), src, cnt * 2 * D, fb);
+                            done += cnt;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            ++issued;
+        }
+        if (!ok && lane == 0) {   // a wait timed out: wait (bounded, fresh limit) for copies in flight
+            s_abort = 0;
+            for (int i = max(0, issued - nst); i < issued; ++i)
+                mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
+        }
+        return;
+    }
+
+    // ================================================================== consumers: set-up
+    const int g = lane >> 2, tq = lane & 3;
+    const int G = L.G;
+    __half* qr = reinterpret_cast<__half*>(qb);           // query rows, fp16 [NQ][D]
+    {
+        const uint16_t* q = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
+        const int rot = ring ? L.rot : (int)ROT_NONE;
+        if (rot == ROT_HAD256) {
+            if constexpr (D >= 256) {
+                for (int u = warp; u < NQ * (D / 256); u += kConsumers) {
+                    const int rr = u / (D / 256), c0 = (u % (D / 256)) * 256;
+                    float v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] = (rr < G) ? h2f(q[rr * D + c0 + lane + 32 * k]) : 0.f;
+                    warp_rotate<8>(v, lane, rot);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) qr[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
+                }
+            }
+        } else {
+            for (int u = warp; u < NQ * (D / 128); u += kConsumers) {
+                const int rr = u / (D / 128), c0 = (u % (D / 128)) * 128;
+                float v[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[k] = (rr < G) ? h2f(q[rr * D + c0 + lane + 32 * k]) : 0.f;
+                warp_rotate<4>(v, lane, rot);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) qr[rr * D + c0 + lane + 32 * k] = __float2half_rn(v[k]);
+            }
+        }
+    }
+    csync();
+    // Query fragments. tq6_0 K: thread quad tq holds channels [32 tq, 32 tq + 32) of every
+    // 128-channel block, k-step pairs (x, x+4) of 8-channel words. fp16 K: thread quad tq holds
+    // the 16-byte chunks 4i + tq of the row, k-steps 2i and 2i + 1 in natural pairs.
+    uint2 qe0[TPT], qe1[TPT];
+    int qidx[TPT];
+#pragma unroll
+    for (int k = 0; k < TPT; ++k) {
+        const int t = threadIdx.x + kCT * k;
+        qidx[k] = -1;
+        if (t < Gm::NTASK) {
+            const int qi = t / (D / 8), u = t % (D / 8);
+            int tq_, j0;
+            if (ring) {
+                const int bb = u / 16, ub = u % 16;
+                tq_ = ub / 4;
+                j0 = bb * 8 + 2 * (ub % 4);
+            } else {
+                tq_ = u & 3;
+                j0 = 2 * (u >> 2);
+            }
+            qidx[k] = (((qi >> 3) * KS + j0) * 8 + (qi & 7)) * 4 + tq_;
+            const uint4 x = *reinterpret_cast<const uint4*>(qr + qi * D + 8 * u);
+            if (ring) {
+                qe0[k] = make_uint2(__byte_perm(x.x, x.z, 0x5410), __byte_perm(x.x, x.z, 0x7632));
+                qe1[k] = make_uint2(__byte_perm(x.y, x.w, 0x5410), __byte_perm(x.y, x.w, 0x7632));
+            } else {
+                qe0[k] = make_uint2(x.x, x.y);
+                qe1[k] = make_uint2(x.z, x.w);
+            }
+        }
+    }
+    csync();
+#pragma unroll
+    for (int k = 0; k < TPT; ++k) {
+        if (qidx[k] < 0) continue;
+        uint2* e = reinterpret_cast<uint2*>(qb) + qidx[k];
+        e[0] = qe0[k];
+        e[32] = qe1[k];
+    }
+    csync();
+    const uint2* qb2 = reinterpret_cast<const uint2*>(qb);
+    const uint2* pb2 = reinterpret_cast<const uint2*>(pbuf);
+    constexpr uint32_t ONE2 = 0x3C003C00u;
+    // ring: sum of the query fragments per 128-channel block (offset 96 of the raw codes)
+    float zk[NB][NT][2];
+#pragma unroll
+    for (int bk = 0; bk < NB; ++bk)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            zk[bk][nt][0] = zk[bk][nt][1] = 0.f;
+            if (ring) {
+                float a1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint2 bq = qb2[((nt * KS + bk * 8 + jj) * 8 + g) * 4 + tq];
+                    mma16816(a1, ONE2, ONE2, ONE2, ONE2, bq.x, bq.y);
+                }
+                zk[bk][nt][0] = a1[0];
+                zk[bk][nt][1] = a1[1];
+            }
+        }
+
+    const int r0 = 16 * warp + g, r1 = r0 + 8;            // this thread's score rows (positions in the run)
+    const int vw = (warp * (D / 8)) >> 7;                 // tq6_0 block of this warp's value channels
+    const float sc = L.scale * kLog2e;
+    float m_run[NT][2], l_part[NT][2];
+    float O[MT][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_part[nt][0] = l_part[nt][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
+    }
+
+    for (int gi = 0; gi < nrun; ++gi) {
+        const int sl = gi % nst;
+        mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
+        const int n = min(128, t1 - (t0 + 128 * gi));
+        uint8_t* kr = stages + (size_t)sl * stage_bytes;
+        uint8_t* vr = kr + half_bytes;
+        if (!ring && n < 128) {   // rows past the run's end: zeros, so 0 x row stays 0 in P.V
+            for (int e = threadIdx.x; e < (128 - n) * (2 * D / 16); e += kCT) {
+                const int rr = n + e / (2 * D / 16), u = e % (2 * D / 16);
+                *reinterpret_cast<uint4*>(vr + rr * FLD + 16 * u) = make_uint4(0, 0, 0, 0);
+            }
+        }
+
+        // ---------------- step 1: scores of rows r0, r1
+        float s4[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s4[nt][0] = s4[nt][1] = s4[nt][2] = s4[nt][3] = 0.f;
+        if (ring) {
+            const uint16_t* ksc = reinterpret_cast<const uint16_t*>(kr + 128 * CLD);
+#pragma unroll
+            for (int bk = 0; bk < NB; ++bk) {
+                float acc[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+                const uint8_t* row0 = kr + r0 * CLD + 96 * bk;
+                const uint8_t* row1 = kr + r1 * CLD + 96 * bk;
+                const uint4 w0 = *reinterpret_cast<const uint4*>(row0 + 16 * tq);
+                const uint4 w1 = *reinterpret_cast<const uint4*>(row1 + 16 * tq);
+                const uint2 h0 = *reinterpret_cast<const uint2*>(row0 + 64 + 8 * tq);
+                const uint2 h1 = *reinterpret_cast<const uint2*>(row1 + 64 + 8 * tq);
+                const uint32_t W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
+                const uint32_t H0[2] = {h0.x, h0.y}, H1[2] = {h1.x, h1.y};
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int m = jj >> 1, x = 2 * (jj & 1), y = 8 * (m & 1) + x;
+                    const uint32_t a0 = add_hi2(nib64(W0[m], x), H0[m >> 1], y);
+                    const uint32_t a2 = add_hi2(nib64(W0[m], x + 1), H0[m >> 1], y + 1);
+                    const uint32_t a1 = add_hi2(nib64(W1[m], x), H1[m >> 1], y);
+                    const uint32_t a3 = add_hi2(nib64(W1[m], x + 1), H1[m >> 1], y + 1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint2 bq = qb2[((nt * KS + bk * 8 + jj) * 8 + g) * 4 + tq];
+                        mma16816(acc[nt], a0, a1, a2, a3, bq.x, bq.y);
+                    }
+                }
+                const float e0 = h2f(ksc[r0 * NB + bk]), e1 = h2f(ksc[r1 * NB + bk]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float o0 = 96.f * zk[bk][nt][0], o1 = 96.f * zk[bk][nt][1];
+                    s4[nt][0] += e0 * (acc[nt][0] - o0);
+                    s4[nt][1] += e0 * (acc[nt][1] - o1);
+                    s4[nt][2] += e1 * (acc[nt][2] - o0);
+                    s4[nt][3] += e1 * (acc[nt][3] - o1);
+                }
+            }
+        } else {
+            // 16-byte chunk 4i + tq of rows r0, r1; odd rows load chunk pairs in the other order
+            const int odd = g & 1;
+#pragma unroll
+            for (int i2 = 0; i2 < D / 64; ++i2) {
+                uint4 c0a = *reinterpret_cast<const uint4*>(kr + r0 * FLD + 16 * (4 * (2 * i2 + odd) + tq));
+                uint4 c0b = *reinterpret_cast<const uint4*>(kr + r0 * FLD + 16 * (4 * (2 * i2 + 1 - odd) + tq));
+                uint4 c1a = *reinterpret_cast<const uint4*>(kr + r1 * FLD + 16 * (4 * (2 * i2 + odd) + tq));
+                uint4 c1b = *reinterpret_cast<const uint4*>(kr + r1 * FLD + 16 * (4 * (2 * i2 + 1 - odd) + tq));
+                if (odd) {
+                    const uint4 t = c0a; c0a = c0b; c0b = t;
+                    const uint4 u = c1a; c1a = c1b; c1b = u;
+                }
+                const uint32_t A0[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+                const uint32_t A1[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = 4 * i2 + jj;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                        mma16816(s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1], bq.x, bq.y);
+                    }
+                }
+            }
+        }
+        const bool v0 = r0 < n, v1 = r1 < n;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            s4[nt][0] = v0 ? s4[nt][0] * sc : -INFINITY;
+            s4[nt][1] = v0 ? s4[nt][1] * sc : -INFINITY;
+            s4[nt][2] = v1 ? s4[nt][2] * sc : -INFINITY;
+            s4[nt][3] = v1 ? s4[nt][3] * sc : -INFINITY;
+            float mx0 = fmaxf(s4[nt][0], s4[nt][2]), mx1 = fmaxf(s4[nt][1], s4[nt][3]);
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            if (g == 0) {
+                red[(nt * 8 + 2 * tq) * 8 + warp] = mx0;
+                red[(nt * 8 + 2 * tq + 1) * 8 + warp] = mx1;
+            }
+        }
+        csync();
+
+        // ---------------- step 2: group maximum, p, running sums, P' fragments
+        float al[NT][2], pr[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const float4* r4 = reinterpret_cast<const float4*>(red + (nt * 8 + 2 * tq + c) * 8);
+                const float4 x = r4[0], y = r4[1];
+                const float gm = fmaxf(fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)), fmaxf(fmaxf(y.x, y.y), fmaxf(y.z, y.w)));
+                const float mn = fmaxf(m_run[nt][c], gm);
+                al[nt][c] = exp2f(m_run[nt][c] - mn);
+                m_run[nt][c] = mn;
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pr[nt][i] = exp2f(s4[nt][i] - m_run[nt][i & 1]);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) l_part[nt][c] = al[nt][c] * l_part[nt][c] + pr[nt][c] + pr[nt][c + 2];
+        }
+        const uint16_t* vsc = reinterpret_cast<const uint16_t*>(vr + 128 * CLD);
+#pragma unroll
+        for (int v = 0; v < NB; ++v) {
+            if (!ring && v > 0) break;
+            const float f0 = ring ? h2f(vsc[r0 * NB + v]) : 1.f, f1 = ring ? h2f(vsc[r1 * NB + v]) : 1.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t P0 = v0 ? pack_f2(pr[nt][0] * f0, pr[nt][1] * f0) : 0u;
+                const uint32_t P1 = v1 ? pack_f2(pr[nt][2] * f1, pr[nt][3] * f1) : 0u;
+                reinterpret_cast<uint2*>(pbuf)[((v * 8 + warp) * NT + nt) * 32 + lane] =
+                    make_uint2(movtrans(P0), movtrans(P1));
+            }
+        }
+        csync();
+
+        // ---------------- step 3: O^T = alpha O^T + V^T P'^T for this warp's channels
+        const int pv = ring ? vw : 0;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int c0 = warp * (D / 8) + 16 * mt;
+            float acc[NT][4], a1s[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[nt][i] = a1s[nt][i] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                if (ring) {
+                    // 8 x 8 tiles (positions x channels) decoded in A-fragment order, then transposed
+                    const int pa = 16 * kk + g, pb = pa + 8;
+                    // channels c0..c0+15 (c0 a multiple of 16): one 8-byte ql load and one qh word per row
+                    const uint8_t* ra = vr + pa * CLD + 96 * (c0 >> 7);
+                    const uint8_t* rb = vr + pb * CLD + 96 * (c0 >> 7);
+                    const int qa = (c0 & 127) >> 1, ha = 64 + ((c0 & 127) >> 4) * 4;
+                    const int ya = tq, ya1 = 8 + tq;
+                    const uint2 wa = *reinterpret_cast<const uint2*>(ra + qa);
+                    const uint2 wb = *reinterpret_cast<const uint2*>(rb + qa);
+                    const uint32_t xa0 = *reinterpret_cast<const uint32_t*>(ra + ha), xa1 = xa0;
+                    const uint32_t xb0 = *reinterpret_cast<const uint32_t*>(rb + ha), xb1 = xb0;
+                    const uint32_t wa0 = wa.x, wa1 = wa.y, wb0 = wb.x, wb1 = wb.y;
+                    a0 = movtrans(add_hi2(nib64_rt(wa0, tq), xa0, ya));
+                    a1 = movtrans(add_hi2(nib64_rt(wa1, tq), xa1, ya1));
+                    a2 = movtrans(add_hi2(nib64_rt(wb0, tq), xb0, ya));
+                    a3 = movtrans(add_hi2(nib64_rt(wb1, tq), xb1, ya1));
+                } else {
+                    const int mi = lane >> 3, rr = lane & 7;
+                    const int pos = 16 * kk + 8 * (mi >> 1) + rr, ch = c0 + 8 * (mi & 1);
+                    ldsm_x4_t(su32(vr + pos * FLD + 2 * ch), a0, a1, a2, a3);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 bp = pb2[((pv * 8 + kk) * NT + nt) * 32 + lane];
+                    mma16816(acc[nt], a0, a1, a2, a3, bp.x, bp.y);
+                    if (ring) mma16816(a1s[nt], ONE2, ONE2, ONE2, ONE2, bp.x, bp.y);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float z0 = ring ? 96.f * a1s[nt][0] : 0.f, z1 = ring ? 96.f * a1s[nt][1] : 0.f;
+                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + (acc[nt][0] - z0);
+                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + (acc[nt][1] - z1);
+                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + (acc[nt][2] - z0);
+                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + (acc[nt][3] - z1);
+            }
+        }
+        if (!ring) fence_async_smem();    // the zero fill above precedes the next bulk copy into this stage
+        __syncwarp();
+        if (lane == 0) mbar_arrive(su32(&empty[sl]));
+    }
+
+    // ---- partial: sums over rows and warps, o (ring: rotated back), m and l
+    csync();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            float l = l_part[nt][c];
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+            if (g == 0) red[(nt * 8 + 2 * tq + c) * 8 + warp] = l;
+            if (warp == 0 && g == 0) red[2 * NQ * 8 + nt * 8 + 2 * tq + c] = m_run[nt][c];
+        }
+    csync();
+    float* ofin = reinterpret_cast<float*>(stages);                     // [NQ][D], stages drained
+    // ring fragment rows hold channels 0,4,1,5,2,6,3,7 of each 8-channel group
+    const int cg = ring ? ((g >> 1) + 4 * (g & 1)) : g;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int qc = nt * 8 + 2 * tq;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int c0 = warp * (D / 8) + 16 * mt + cg;
+            ofin[qc * D + c0] = O[mt][nt][0];
+            ofin[(qc + 1) * D + c0] = O[mt][nt][1];
+            ofin[qc * D + c0 + 8] = O[mt][nt][2];
+            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3];
+        }
+    }
+    if (threadIdx.x < NQ) {
+        const float4* r4 = reinterpret_cast<const float4*>(red + threadIdx.x * 8);
+        const float4 x = r4[0], y = r4[1];
+        red[2 * NQ * 8 + NQ + threadIdx.x] = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
+    }
+    csync();
+    write_partial<D, NQ>(ofin, red + 2 * NQ * 8, red + 2 * NQ * 8 + NQ, p.partials + (size_t)item * (2 * NQ + NQ * D),
+                         ring ? L.rot : (int)ROT_NONE);
+}
+
+template <int D, int NQ>
+int launch_region_t(const Layout& L, const AttnParams& p, cudaStream_t st) {
+    using Gm = RGeo<D, NQ>;
+    auto kern = decode_region_kernel<D, NQ>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
+    kern<<<p.n_region_items, kBodyThreads, Gm::SMEM, st>>>(L, p);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+int upload_tables_region(const FormatTables& t) {
+    return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
+}
+
+// 1 when the streaming region kernel takes this layout's region items: head_dim 128 or 256,
+// the ring (when present) in runs of whole 128-slot chunks, fp16 exact rows.
+int region_kernel_ok(const Layout& L) {
+    if (L.D != 128 && L.D != 256) return 0;
+    if (L.journal == KVQ_TQ6_0) {
+        if (L.R % 128 != 0 || L.tail_fmt != KVQ_F16) return 0;
+    } else if (L.journal != KVQ_F16) {
+        return 0;
+    }
+    return 1;
+}
+
+int launch_decode_region(const Layout& L, const AttnParams& p, void* stream) {
+    if (p.n_region_items <= 0) return 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (L.NQ == 8) {
+        if (L.D == 128) return launch_region_t<128, 8>(L, p, s);
+        if (L.D == 256) return launch_region_t<256, 8>(L, p, s);
+    } else {
+        if (L.D == 128) return launch_region_t<128, 16>(L, p, s);
+        if (L.D == 256) return launch_region_t<256, 16>(L, p, s);
+    }
+    return (int)cudaErrorInvalidValue;
+}
+
+}  // namespace kvq

@@ -23,6 +23,10 @@ struct kvq_cache {
     int sm_count;
     std::vector<int64_t> n_tok;   // [L][max_seqs]
     std::vector<int64_t> sealed;  // [L][max_seqs]
+    // decode attention runs its region kernel on `aux`, forked from and joined back into the
+    // caller's stream through the two events (so it overlaps the body kernel)
+    cudaStream_t aux = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace kvq {
@@ -99,7 +103,9 @@ kvq_status ensure_tables(int device) {
     std::lock_guard<std::mutex> lk(g_tab_mu);
     if (g_tab_devices.count(device)) return KVQ_OK;
     const FormatTables& t = host_tables();
-    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0) return KVQ_ECUDA;
+    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0 ||
+        upload_tables_region(t) != 0)
+        return KVQ_ECUDA;
     g_tab_devices.insert(device);
     return KVQ_OK;
 }
@@ -206,7 +212,19 @@ kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes
     if (cudaMemset(device_pool, 0, 256) != cudaSuccess) return KVQ_ECUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KVQ_ECUDA;
+    cudaStream_t aux = nullptr;
+    cudaEvent_t evf = nullptr, evj = nullptr;
+    if (cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) != cudaSuccess) return KVQ_ECUDA;
+    if (cudaEventCreateWithFlags(&evf, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&evj, cudaEventDisableTiming) != cudaSuccess) {
+        if (evf) cudaEventDestroy(evf);
+        cudaStreamDestroy(aux);
+        return KVQ_ECUDA;
+    }
     kvq_cache* c = new kvq_cache;
+    c->aux = aux;
+    c->ev_fork = evf;
+    c->ev_join = evj;
     c->cfg = *cfg;
     c->lay = L;
     c->pool = device_pool;
@@ -221,6 +239,10 @@ kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes
 
 kvq_status kv_destroy(kvq_cache* c) {
     if (!c) return KVQ_EINVAL;
+    if (c->aux) cudaStreamSynchronize(c->aux);
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->aux) cudaStreamDestroy(c->aux);
     delete c;
     return KVQ_OK;
 }
@@ -393,7 +415,7 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     }
     p.body_chunk = (int32_t)bchunk;
     p.chunk = (int32_t)chunk;
-    const int e = launch_decode(L, p, stream);
+    const int e = launch_decode(L, p, stream, c->aux, c->ev_fork, c->ev_join);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;
 }
 

@@ -144,10 +144,15 @@ const FormatTables& host_tables();   // derived once per process (tables.cpp)
 // Kernel launchers (kernels_*.cu). Each returns cudaError_t as int.
 int launch_append(const Layout& lay, const AppendParams& p, void* stream);
 int launch_seal(const Layout& lay, const SealParams& p, void* stream);
-int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
+// Region kernel on `aux` (forked from / joined into `stream` by the two events) when all three
+// are given, else everything on `stream`.
+int launch_decode(const Layout& lay, const AttnParams& p, void* stream, void* aux, void* ev_fork, void* ev_join);
 int launch_decode_body(const Layout& lay, const AttnParams& p, int n_body, void* stream);
 int upload_tables_body(const FormatTables& t);
-int body_ctas_per_sm(const Layout& lay);   // resident body-kernel CTAs per SM (0 if unsupported)
+int upload_tables_region(const FormatTables& t);
+int body_ctas_per_sm(const Layout& lay);
+int region_kernel_ok(const Layout& lay);   // 1 if the streaming region kernel takes the region items
+int launch_decode_region(const Layout& lay, const AttnParams& p, void* stream);   // resident body-kernel CTAs per SM (0 if unsupported)
 int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
                    int kind, int64_t p0, int64_t n, float* out, void* stream);
 int upload_tables_codec(const FormatTables& t);
