@@ -1,9 +1,10 @@
 // Decode attention over sealed body records: the bandwidth-critical part of the path.
 //
-// One CTA per work item (sequence, KV head, run of 128-position groups), two CTAs per SM
-// where shared memory allows. Warp 8 is a producer: it streams each group's K record and V
-// record (contiguous, 16-byte multiples) into a ring of shared-memory stages with
-// cp.async.bulk, completion tracked by mbarriers. Warps 0-7 consume each group:
+// One CTA of 8 warps per work item (sequence, KV head, run of 128-position groups), two CTAs
+// per SM where shared memory allows. Thread 0 streams each group's K record and V record
+// (contiguous, 16-byte multiples) into a ring of shared-memory stages with cp.async.bulk,
+// completion tracked by mbarriers; a stage is refilled after the first barrier of the group
+// that follows its last reader. All 8 warps consume each group:
 //   0. (KVarN) the query fragments times the group's column scales, q' = q C in fp16, one
 //      8-channel chunk per thread from the fp16 rotated query held in registers; barrier.
 //   1. scores: warp w takes the 16 positions that value k-step w of step 3 covers and all D
@@ -20,7 +21,7 @@
 // Codes enter the mma through the fp16 exponent trick: a 4-bit code n placed in mantissa bits
 // 4-7 under exponent 6 reads exactly 64 + n (the fifth KVarN bit is mantissa bit 8, +16), a
 // signed byte b reads 1152 + b. The offsets cancel against sum q' (scores) or sum P' (values):
-// per group for KVarN values, through running sums for Q8_0 / Q4_0 values.
+// per group (values: an all-ones mma over the warp's P' copy gives sum P').
 // The partial (m, l, o) is rotated back to the original domain and merged with the region
 // partials by decode_merge_kernel (kernels_attn.cu).
 #include "stream_common.cuh"
@@ -45,7 +46,7 @@ struct Geo {
     static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : (KF == KF_Q8 ? 1152.f : 0.f));
     static constexpr float VOFF = (VF == KF_KVARN) ? 64.f : (VF == KF_Q4 ? 72.f : (VF == KF_Q8 ? 1152.f : 0.f));
     static constexpr bool ZV = (VF == KF_KVARN);                        // per-group value zero-point sums
-    static constexpr bool PSV = (VF == KF_Q8 || VF == KF_Q4);           // running sums of P' (offset)
+    static constexpr bool PSV = (VF == KF_Q8 || VF == KF_Q4);           // sum of P' per group (offset)
     static constexpr bool LUT = (KF == KF_TBQ4) || (VF == KF_TBQ4);
     static constexpr int rec(int f, int b) {
         return f == KF_KVARN ? (D / 256) * (4096 * b + 1152) : (f == KF_TBQ4 ? 66 * D : (f == KF_Q8 ? 136 * D : 72 * D));
@@ -65,9 +66,36 @@ struct Geo {
     static constexpr int TPT = (NTASK + kCT - 1) / kCT;                 // chunks per consumer thread
 };
 
+// The N fp16 values of one position's scale row (16-byte aligned rows of N values), as floats.
+template <int N>
+__device__ __forceinline__ void load_row_f(const uint16_t* row, float (&f)[N]) {
+    if constexpr (N == 1) {
+        f[0] = h2f(row[0]);
+    } else if constexpr (N == 2) {
+        const float2 v = __half22float2(as_h2(*reinterpret_cast<const uint32_t*>(row)));
+        f[0] = v.x; f[1] = v.y;
+    } else if constexpr (N == 4) {
+        const uint2 u = *reinterpret_cast<const uint2*>(row);
+        const float2 a = __half22float2(as_h2(u.x)), b = __half22float2(as_h2(u.y));
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+#pragma unroll
+        for (int k = 0; k < N / 8; ++k) {
+            const uint4 u = reinterpret_cast<const uint4*>(row)[k];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 a = __half22float2(as_h2(w[i]));
+                f[8 * k + 2 * i] = a.x;
+                f[8 * k + 2 * i + 1] = a.y;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------ the kernel
 template <int D, int NQ, int KF, int VF, int KB, int VB>
-__global__ void __launch_bounds__(kBodyThreads, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
+__global__ void __launch_bounds__(kCT, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
 decode_body_kernel(Layout L, AttnParams p, int nst) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     constexpr int NT = Gm::NT, KS = Gm::KS, NBK = Gm::NBK, KSPB = Gm::KSPB, WK = Gm::WK;
@@ -91,7 +119,6 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
     uint8_t* stages = smem;
     uint8_t* tailp = smem + (size_t)nst * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(tailp);
-    uint64_t* empty = full + nst;
     uint8_t* cur = tailp + 128;
     uint32_t* lut = reinterpret_cast<uint32_t*>(cur);
     cur += Gm::LUT ? kLutBytes : 0;
@@ -102,42 +129,26 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_abort;
+    // thread 0 streams the records: group i into stage i % nst, issued once stage i % nst is
+    // free (the first barrier of group i - nst + 1 follows every read of group i - nst)
+    const uint8_t* kb = body_rec(L, p.pool, 0, unit, g0);
+    const uint8_t* vb = body_rec(L, p.pool, 1, unit, g0);
+    auto issue = [&](int i) {
+        const int sl = i % nst;
+        const uint32_t dst = su32(stages + (size_t)sl * stage_bytes);
+        const uint32_t fb = su32(&full[sl]);
+        mbar_expect_tx(fb, recK + recV);
+        bulk_g2s(dst, kb + (size_t)i * recK, recK, fb);
+        bulk_g2s(dst + v_off, vb + (size_t)i * recV, recV, fb);
+    };
+    int issued = 0;
     if (threadIdx.x == 0) {
         s_abort = 0;
-        for (int i = 0; i < nst; ++i) {
-            mbar_init(su32(&full[i]), 1);
-            mbar_init(su32(&empty[i]), kConsumers);
-        }
+        for (int i = 0; i < nst; ++i) mbar_init(su32(&full[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        for (; issued < min(nst, ngroups); ++issued) issue(issued);
     }
     __syncthreads();
-
-    // ================================================================== producer warp
-    if (warp == kConsumers) {
-        if (lane == 0) {
-            const uint8_t* kb = body_rec(L, p.pool, 0, unit, g0);
-            const uint8_t* vb = body_rec(L, p.pool, 1, unit, g0);
-            int issued = 0;
-            bool ok = true;
-            for (int i = 0; i < ngroups; ++i) {
-                const int sl = i % nst;
-                if (i >= nst) ok = mbar_wait(su32(&empty[sl]), ((i / nst) - 1) & 1, status, &s_abort);
-                if (!ok) break;
-                const uint32_t dst = su32(stages + (size_t)sl * stage_bytes);
-                const uint32_t fb = su32(&full[sl]);
-                mbar_expect_tx(fb, recK + recV);
-                bulk_g2s(dst, kb + (size_t)i * recK, recK, fb);
-                bulk_g2s(dst + v_off, vb + (size_t)i * recV, recV, fb);
-                ++issued;
-            }
-            if (!ok) {   // a wait timed out: wait (bounded, fresh limit) for copies still in flight
-                s_abort = 0;
-                for (int i = max(0, issued - nst); i < issued; ++i)
-                    mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
-            }
-        }
-        return;
-    }
 
     // ================================================================== consumers: set-up
     const int g = lane >> 2, tq = lane & 3;
@@ -190,9 +201,13 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
         qcoff[k] = 0;
         qv[k][0] = qv[k][1] = qv[k][2] = qv[k][3] = 0u;
         if (t < Gm::NTASK) {
-            const int qi = t / (D / 8), u = t % (D / 8);
-            const int bb = u / (WK / 8), ub = u % (WK / 8);
-            const int tq_ = ub / (WK / 32), m = ub % (WK / 32);
+            // lanes of a warp take the 32 entries (query, quad) of one k-step pair: the stores
+            // below are consecutive 8-byte words
+            const int ln = t & 31, rest = t >> 5;
+            const int tq_ = ln & 3, nt_ = rest % NT, jb = rest / NT;
+            const int qi = nt_ * 8 + (ln >> 2);
+            const int bb = jb / (WK / 32), m = jb % (WK / 32);
+            const int ub = tq_ * (WK / 32) + m, u = bb * (WK / 8) + ub;
             const int j0 = bb * KSPB + 2 * m;
             qe[k] = (((qi >> 3) * KS + j0) * 8 + (qi & 7)) * 4 + tq_;
             qcoff[k] = bb * (4096 * KB + 1152) + 4096 * KB + 512 + 16 * ub;   // KVarN column scales
@@ -235,9 +250,16 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
     for (int bk = 0; bk < NBK; ++bk)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) zk[bk][nt][0] = zk[bk][nt][1] = 0.f;
+    // formats whose fragments are fixed per item keep them in registers (one n-tile)
+    constexpr bool QREG = (KF != KF_KVARN) && (NT == 1);
+    uint2 qf[QREG ? KS : 1];
     if (KF != KF_KVARN) {
         write_qb(nullptr);
         csync();
+        if constexpr (QREG) {
+#pragma unroll
+            for (int j = 0; j < KS; ++j) qf[j] = qb2[(j * 8 + g) * 4 + tq];
+        }
         if (Gm::KOFF != 0.f) {
 #pragma unroll
             for (int bk = 0; bk < NBK; ++bk)
@@ -262,14 +284,12 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
     const int vw = (warp * (D / 8)) / WV;                 // value scale block of this warp's channels
     const float sc = L.scale * kLog2e;
 
-    float m_run[NT][2], l_part[NT][2], ps_run[NVB][NT][2];
+    float m_run[NT][2], l_part[NT][2];
     float O[MT][NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         m_run[nt][0] = m_run[nt][1] = -INFINITY;
         l_part[nt][0] = l_part[nt][1] = 0.f;
-#pragma unroll
-        for (int v = 0; v < NVB; ++v) ps_run[v][nt][0] = ps_run[v][nt][1] = 0.f;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
     }
@@ -282,19 +302,23 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
         if (KF == KF_KVARN) {
             write_qb(kr);
             csync();
+            if (threadIdx.x == 0 && gi >= 1 && issued < ngroups) issue(issued++);
         }
 
         // ---------------- step 1: scores of positions t0, t1 (rows g, g+8), all channels
         float s4[NT][4];
         {
-            float acc[NBK][NT][4];
-            float a1[NBK][NT][4];
+            // two accumulation chains per (block, n-tile), by k-step parity, so consecutive mma
+            // do not wait on each other
+            float acc[NBK][NT][2][4];
+            float a1[NBK][NT][2][4];
 #pragma unroll
             for (int bk = 0; bk < NBK; ++bk)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc[bk][nt][i] = a1[bk][nt][i] = 0.f;
+                    for (int i = 0; i < 4; ++i)
+                        acc[bk][nt][0][i] = acc[bk][nt][1][i] = a1[bk][nt][0][i] = a1[bk][nt][1][i] = 0.f;
             // TBQ4: blocks of 128 channels, 16 bytes of this row and block per thread; with two
             // blocks, odd rows read them in the other order so a quarter warp hits 32 banks
             uint4 tY0[NBK], tY1[NBK];
@@ -347,9 +371,9 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
-                            mma16816(a1[bk][nt], ONE2, ONE2, ONE2, ONE2, bq.x, bq.y);
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
+                            mma16816(a1[bk][nt][jj & 1], ONE2, ONE2, ONE2, ONE2, bq.x, bq.y);
                         }
                     }
                 } else if (KF == KF_TBQ4) {
@@ -364,8 +388,8 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
                 } else if (KF == KF_Q8) {
@@ -379,8 +403,8 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
                 } else {   // Q4_0 K: one word of 8 nibbles per row and block
@@ -394,13 +418,30 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                            mma16816(acc[bk][nt], a0, a1r, a2, a3, bq.x, bq.y);
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
                 }
             }
-            // s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q', log2 domain
+#pragma unroll
+            for (int bk = 0; bk < NBK; ++bk)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[bk][nt][0][i] += acc[bk][nt][1][i];
+                        a1[bk][nt][0][i] += a1[bk][nt][1][i];
+                    }
+            // s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q', log2 domain; the
+            // per-position block scales of TBQ4 / Q8_0 / Q4_0 come in one vector load per row
+            float ek0[NBK], ek1[NBK];
+            if (KF != KF_KVARN) {
+                const uint16_t* er = reinterpret_cast<const uint16_t*>(
+                    kr + (KF == KF_TBQ4 ? 64 : (KF == KF_Q8 ? 128 : 64)) * D);
+                load_row_f<NBK>(er + t0 * NBK, ek0);
+                load_row_f<NBK>(er + t1 * NBK, ek1);
+            }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) s4[nt][0] = s4[nt][1] = s4[nt][2] = s4[nt][3] = 0.f;
 #pragma unroll
@@ -413,30 +454,27 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                     z0 = h2f(sb[128 + t0]); z1 = h2f(sb[128 + t1]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        zk[bk][nt][0] = a1[bk][nt][0];
-                        zk[bk][nt][1] = a1[bk][nt][1];
+                        zk[bk][nt][0] = a1[bk][nt][0][0];
+                        zk[bk][nt][1] = a1[bk][nt][0][1];
                     }
-                } else if (KF == KF_TBQ4) {
-                    const uint16_t* nr = reinterpret_cast<const uint16_t*>(kr + 64 * D);
-                    e0 = h2f(nr[t0 * (D / 128) + bk]); e1 = h2f(nr[t1 * (D / 128) + bk]);
                 } else {
-                    const uint16_t* dr = reinterpret_cast<const uint16_t*>(kr + (KF == KF_Q8 ? 128 : 64) * D);
-                    e0 = h2f(dr[t0 * (D / 32) + bk]); e1 = h2f(dr[t1 * (D / 32) + bk]);
+                    e0 = ek0[bk];
+                    e1 = ek1[bk];
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float y0 = zk[bk][nt][0], y1 = zk[bk][nt][1];
                     if (Gm::KOFF != 0.f) {
                         const float o0 = Gm::KOFF * y0, o1 = Gm::KOFF * y1;
-                        s4[nt][0] += e0 * (acc[bk][nt][0] - o0) + z0 * y0;
-                        s4[nt][1] += e0 * (acc[bk][nt][1] - o1) + z0 * y1;
-                        s4[nt][2] += e1 * (acc[bk][nt][2] - o0) + z1 * y0;
-                        s4[nt][3] += e1 * (acc[bk][nt][3] - o1) + z1 * y1;
+                        s4[nt][0] += e0 * (acc[bk][nt][0][0] - o0) + z0 * y0;
+                        s4[nt][1] += e0 * (acc[bk][nt][0][1] - o1) + z0 * y1;
+                        s4[nt][2] += e1 * (acc[bk][nt][0][2] - o0) + z1 * y0;
+                        s4[nt][3] += e1 * (acc[bk][nt][0][3] - o1) + z1 * y1;
                     } else {
-                        s4[nt][0] += e0 * acc[bk][nt][0];
-                        s4[nt][1] += e0 * acc[bk][nt][1];
-                        s4[nt][2] += e1 * acc[bk][nt][2];
-                        s4[nt][3] += e1 * acc[bk][nt][3];
+                        s4[nt][0] += e0 * acc[bk][nt][0][0];
+                        s4[nt][1] += e0 * acc[bk][nt][0][1];
+                        s4[nt][2] += e1 * acc[bk][nt][0][2];
+                        s4[nt][3] += e1 * acc[bk][nt][0][3];
                     }
                 }
             }
@@ -460,6 +498,7 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
             }
         }
         csync();
+        if (KF != KF_KVARN && threadIdx.x == 0 && gi >= 1 && issued < ngroups) issue(issued++);
 
         // ---------------- step 2: group maximum, p, running sums, P' fragments
         float al[NT][2];
@@ -480,6 +519,12 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
 #pragma unroll
             for (int c = 0; c < 2; ++c) l_part[nt][c] = al[nt][c] * l_part[nt][c] + pr[nt][c] + pr[nt][c + 2];
         }
+        float fv0[NVB], fv1[NVB];
+        if (VF != KF_KVARN) {
+            const uint16_t* fr = reinterpret_cast<const uint16_t*>(vr + (VF == KF_Q8 ? 128 : 64) * D);
+            load_row_f<NVB>(fr + t0 * NVB, fv0);
+            load_row_f<NVB>(fr + t1 * NVB, fv1);
+        }
 #pragma unroll
         for (int v = 0; v < NVB; ++v) {
             float f0, f1, z0 = 0.f, z1 = 0.f;
@@ -488,12 +533,9 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                     reinterpret_cast<const uint16_t*>(vr + (size_t)v * (4096 * VB + 1152) + 4096 * VB);
                 f0 = h2f(sb[t0]); f1 = h2f(sb[t1]);
                 z0 = h2f(sb[128 + t0]); z1 = h2f(sb[128 + t1]);
-            } else if (VF == KF_TBQ4) {
-                const uint16_t* nr = reinterpret_cast<const uint16_t*>(vr + 64 * D);
-                f0 = h2f(nr[t0 * (D / 128) + v]); f1 = h2f(nr[t1 * (D / 128) + v]);
             } else {
-                const uint16_t* dr = reinterpret_cast<const uint16_t*>(vr + (VF == KF_Q8 ? 128 : 64) * D);
-                f0 = h2f(dr[t0 * (D / 32) + v]); f1 = h2f(dr[t1 * (D / 32) + v]);
+                f0 = fv0[v];
+                f1 = fv1[v];
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -511,10 +553,6 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         zsm[(v * NQ + nt * 8 + 2 * tq) * 8 + warp] = zc0;
                         zsm[(v * NQ + nt * 8 + 2 * tq + 1) * 8 + warp] = zc1;
                     }
-                }
-                if (Gm::PSV) {
-                    ps_run[v][nt][0] = al[nt][0] * ps_run[v][nt][0] + lo_f(P0) + lo_f(P1);
-                    ps_run[v][nt][1] = al[nt][1] * ps_run[v][nt][1] + hi_f(P0) + hi_f(P1);
                 }
                 reinterpret_cast<uint2*>(pbuf)[((v * 8 + warp) * NT + nt) * 32 + lane] =
                     make_uint2(movtrans(P0), movtrans(P1));
@@ -536,30 +574,37 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                 }
             }
         }
+        // rows of every m-tile first, then k-steps outer / m-tiles inner: the m-tiles' mma chains
+        // interleave (a single m-tile splits its chain by k-step parity)
+        constexpr int C3 = (MT == 1) ? 2 : 1;
+        float acc[MT][C3][NT][4];
+        uint32_t X0[MT][8], X1[MT][8];
+        uint32_t H0[MT], H1[MT];
+        const uint8_t* vt[MT];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const int c0 = warp * (D / 8) + 16 * mt + g, c1 = c0 + 8;
-            float acc[NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-            uint32_t X0[8], X1[8];
-            uint32_t H0 = 0, H1 = 0;
-            const uint8_t* vt = vr;
+            for (int ch = 0; ch < C3; ++ch)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[mt][ch][nt][0] = acc[mt][ch][nt][1] = acc[mt][ch][nt][2] = acc[mt][ch][nt][3] = 0.f;
+            H0[mt] = H1[mt] = 0;
+            vt[mt] = vr;
             if (VF == KF_KVARN) {
-                vt = vr + (size_t)(c0 >> 8) * (4096 * VB + 1152);
-                const uint4 y0 = *reinterpret_cast<const uint4*>(vt + (c0 & 255) * 64 + 16 * tq);
-                const uint4 y1 = *reinterpret_cast<const uint4*>(vt + (c1 & 255) * 64 + 16 * tq);
-                X0[0] = y0.x; X0[1] = y0.y; X0[2] = y0.z; X0[3] = y0.w;
-                X1[0] = y1.x; X1[1] = y1.y; X1[2] = y1.z; X1[3] = y1.w;
+                vt[mt] = vr + (size_t)(c0 >> 8) * (4096 * VB + 1152);
+                const uint4 y0 = *reinterpret_cast<const uint4*>(vt[mt] + (c0 & 255) * 64 + 16 * tq);
+                const uint4 y1 = *reinterpret_cast<const uint4*>(vt[mt] + (c1 & 255) * 64 + 16 * tq);
+                X0[mt][0] = y0.x; X0[mt][1] = y0.y; X0[mt][2] = y0.z; X0[mt][3] = y0.w;
+                X1[mt][0] = y1.x; X1[mt][1] = y1.y; X1[mt][2] = y1.z; X1[mt][3] = y1.w;
                 if (VB == 5) {
-                    H0 = *reinterpret_cast<const uint32_t*>(vt + 16384 + (c0 & 255) * 16 + 4 * tq);
-                    H1 = *reinterpret_cast<const uint32_t*>(vt + 16384 + (c1 & 255) * 16 + 4 * tq);
+                    H0[mt] = *reinterpret_cast<const uint32_t*>(vt[mt] + 16384 + (c0 & 255) * 16 + 4 * tq);
+                    H1[mt] = *reinterpret_cast<const uint32_t*>(vt[mt] + 16384 + (c1 & 255) * 16 + 4 * tq);
                 }
             } else if (VF == KF_TBQ4 || VF == KF_Q4) {
                 const uint4 y0 = *reinterpret_cast<const uint4*>(vr + c0 * 64 + 16 * tq);
                 const uint4 y1 = *reinterpret_cast<const uint4*>(vr + c1 * 64 + 16 * tq);
-                X0[0] = y0.x; X0[1] = y0.y; X0[2] = y0.z; X0[3] = y0.w;
-                X1[0] = y1.x; X1[1] = y1.y; X1[2] = y1.z; X1[3] = y1.w;
+                X0[mt][0] = y0.x; X0[mt][1] = y0.y; X0[mt][2] = y0.z; X0[mt][3] = y0.w;
+                X1[mt][0] = y1.x; X1[mt][1] = y1.y; X1[mt][2] = y1.z; X1[mt][3] = y1.w;
             } else {   // Q8_0: 32 positions = 32 bytes of the channel row; odd rows swap halves (banks)
                 const int odd = g & 1;
                 uint4 y0a = *reinterpret_cast<const uint4*>(vr + c0 * 128 + 32 * tq + 16 * odd);
@@ -570,58 +615,83 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                     const uint4 t = y0a; y0a = y0b; y0b = t;
                     const uint4 u = y1a; y1a = y1b; y1b = u;
                 }
-                X0[0] = y0a.x; X0[1] = y0a.y; X0[2] = y0a.z; X0[3] = y0a.w;
-                X0[4] = y0b.x; X0[5] = y0b.y; X0[6] = y0b.z; X0[7] = y0b.w;
-                X1[0] = y1a.x; X1[1] = y1a.y; X1[2] = y1a.z; X1[3] = y1a.w;
-                X1[4] = y1b.x; X1[5] = y1b.y; X1[6] = y1b.z; X1[7] = y1b.w;
+                X0[mt][0] = y0a.x; X0[mt][1] = y0a.y; X0[mt][2] = y0a.z; X0[mt][3] = y0a.w;
+                X0[mt][4] = y0b.x; X0[mt][5] = y0b.y; X0[mt][6] = y0b.z; X0[mt][7] = y0b.w;
+                X1[mt][0] = y1a.x; X1[mt][1] = y1a.y; X1[mt][2] = y1a.z; X1[mt][3] = y1a.w;
+                X1[mt][4] = y1b.x; X1[mt][5] = y1b.y; X1[mt][6] = y1b.z; X1[mt][7] = y1b.w;
             }
-            const uint32_t* lt = lut + lane;
+        }
+        const uint32_t* lt = lut + lane;
+        // Q8_0 / Q4_0 values: an all-ones mma sums this warp's P' copy (the code offset term)
+        float a1v[NT][4];
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+        for (int nt = 0; nt < NT; ++nt) a1v[nt][0] = a1v[nt][1] = a1v[nt][2] = a1v[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint2 bp[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                bp[nt] = pb2[((vw * 8 + kk) * NT + nt) * 32 + lane];
+                if (Gm::PSV) mma16816(a1v[nt], ONE2, ONE2, ONE2, ONE2, bp[nt].x, bp[nt].y);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a0, a1r, a2, a3;
                 if (Gm::VNIB) {
                     const int m = kk >> 1, x = 2 * (kk & 1);
-                    a0 = nib64(X0[m], x); a2 = nib64(X0[m], x + 1);
-                    a1r = nib64(X1[m], x); a3 = nib64(X1[m], x + 1);
+                    a0 = nib64(X0[mt][m], x); a2 = nib64(X0[mt][m], x + 1);
+                    a1r = nib64(X1[mt][m], x); a3 = nib64(X1[mt][m], x + 1);
                     if (VF == KF_KVARN && VB == 5) {
                         const int bx = 8 * m + x;
-                        a0 = add_bit5(a0, H0, bx); a2 = add_bit5(a2, H0, bx + 1);
-                        a1r = add_bit5(a1r, H1, bx); a3 = add_bit5(a3, H1, bx + 1);
+                        a0 = add_bit5(a0, H0[mt], bx); a2 = add_bit5(a2, H0[mt], bx + 1);
+                        a1r = add_bit5(a1r, H1[mt], bx); a3 = add_bit5(a3, H1[mt], bx + 1);
                     }
                 } else if (VF == KF_TBQ4) {
                     const int m = kk >> 1, sh = 16 * (kk & 1);
-                    a0 = lt[((X0[m] >> sh) & 0xFF) * 32]; a2 = lt[((X0[m] >> (sh + 8)) & 0xFF) * 32];
-                    a1r = lt[((X1[m] >> sh) & 0xFF) * 32]; a3 = lt[((X1[m] >> (sh + 8)) & 0xFF) * 32];
+                    a0 = lt[((X0[mt][m] >> sh) & 0xFF) * 32]; a2 = lt[((X0[mt][m] >> (sh + 8)) & 0xFF) * 32];
+                    a1r = lt[((X1[mt][m] >> sh) & 0xFF) * 32]; a3 = lt[((X1[mt][m] >> (sh + 8)) & 0xFF) * 32];
                 } else {
-                    a0 = i8raw(X0[kk], 0x5140); a2 = i8raw(X0[kk], 0x7362);
-                    a1r = i8raw(X1[kk], 0x5140); a3 = i8raw(X1[kk], 0x7362);
+                    a0 = i8raw(X0[mt][kk], 0x5140); a2 = i8raw(X0[mt][kk], 0x7362);
+                    a1r = i8raw(X1[mt][kk], 0x5140); a3 = i8raw(X1[mt][kk], 0x7362);
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bp = pb2[((vw * 8 + kk) * NT + nt) * 32 + lane];
-                    mma16816(acc[nt], a0, a1r, a2, a3, bp.x, bp.y);
-                }
+                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][kk % C3][nt], a0, a1r, a2, a3, bp[nt].x, bp[nt].y);
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const int c0 = warp * (D / 8) + 16 * mt + g, c1 = c0 + 8;
+            if (C3 == 2) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[mt][0][nt][i] += acc[mt][C3 - 1][nt][i];
             }
             float F0 = 1.f, F1 = 1.f;
             if (VF == KF_KVARN) {
-                const uint16_t* sb = reinterpret_cast<const uint16_t*>(vt + 4096 * VB);
+                const uint16_t* sb = reinterpret_cast<const uint16_t*>(vt[mt] + 4096 * VB);
                 F0 = h2f(sb[256 + (c0 & 255)]);
                 F1 = h2f(sb[256 + (c1 & 255)]);
             }
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + F0 * (acc[nt][0] + zv[nt][0]);
-                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + F0 * (acc[nt][1] + zv[nt][1]);
-                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + F1 * (acc[nt][2] + zv[nt][0]);
-                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + F1 * (acc[nt][3] + zv[nt][1]);
+                const float u0 = Gm::PSV ? zv[nt][0] - Gm::VOFF * a1v[nt][0] : zv[nt][0];
+                const float u1 = Gm::PSV ? zv[nt][1] - Gm::VOFF * a1v[nt][1] : zv[nt][1];
+                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + F0 * (acc[mt][0][nt][0] + u0);
+                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + F0 * (acc[mt][0][nt][1] + u1);
+                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + F1 * (acc[mt][0][nt][2] + u0);
+                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + F1 * (acc[mt][0][nt][3] + u1);
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(su32(&empty[sl]));
     }
 
     // ---- partial: running sums over rows and warps, o rotated back to the original domain
     csync();
+    if (threadIdx.x == 0 && s_abort) {   // a wait timed out: wait (bounded, fresh limit) for copies in flight
+        s_abort = 0;
+        for (int i = max(0, issued - nst); i < issued; ++i)
+            mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -630,39 +700,20 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
 #pragma unroll
             for (int o = 4; o <= 16; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
             if (g == 0) red[(nt * 8 + 2 * tq + c) * 8 + warp] = l;
-            if (Gm::PSV) {
-#pragma unroll
-                for (int v = 0; v < NVB; ++v) {
-                    float s = ps_run[v][nt][c];
-#pragma unroll
-                    for (int o = 4; o <= 16; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                    if (g == 0) zsm[(v * NQ + nt * 8 + 2 * tq + c) * 8 + warp] = s;
-                }
-            }
             if (warp == 0 && g == 0) red[(NVB + 1) * NQ * 8 + nt * 8 + 2 * tq + c] = m_run[nt][c];
         }
     csync();
     float* ofin = reinterpret_cast<float*>(stages);                     // [NQ][D], stages drained
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        float off0 = 0.f, off1 = 0.f;
-        if (Gm::PSV) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const float4* r4 = reinterpret_cast<const float4*>(zsm + (vw * NQ + nt * 8 + 2 * tq + c) * 8);
-                const float4 x = r4[0], y = r4[1];
-                const float s = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
-                (c == 0 ? off0 : off1) = Gm::VOFF * s;
-            }
-        }
         const int qc = nt * 8 + 2 * tq;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const int c0 = warp * (D / 8) + 16 * mt + g;
-            ofin[qc * D + c0] = O[mt][nt][0] - off0;
-            ofin[(qc + 1) * D + c0] = O[mt][nt][1] - off1;
-            ofin[qc * D + c0 + 8] = O[mt][nt][2] - off0;
-            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3] - off1;
+            ofin[qc * D + c0] = O[mt][nt][0];
+            ofin[(qc + 1) * D + c0] = O[mt][nt][1];
+            ofin[qc * D + c0 + 8] = O[mt][nt][2];
+            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3];
         }
     }
     if (threadIdx.x < NQ) {
@@ -698,7 +749,7 @@ int launch_t(const Layout& L, const AttnParams& p, int n_body, cudaStream_t st) 
     auto kern = decode_body_kernel<D, NQ, KF, VF, KB, VB>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    kern<<<n_body, kBodyThreads, smem, st>>>(L, p, nst);
+    kern<<<n_body, kCT, smem, st>>>(L, p, nst);
     return (int)cudaGetLastError();
 }
 

@@ -217,15 +217,18 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
         const int t = threadIdx.x + kCT * k;
         qidx[k] = -1;
         if (t < Gm::NTASK) {
-            const int qi = t / (D / 8), u = t % (D / 8);
-            int tq_, j0;
-            if (ring) {
-                const int bb = u / 16, ub = u % 16;
-                tq_ = ub / 4;
-                j0 = bb * 8 + 2 * (ub % 4);
-            } else {
-                tq_ = u & 3;
-                j0 = 2 * (u >> 2);
+            // lanes of a warp take the 32 entries (query, quad) of one k-step pair
+            const int ln = t & 31, rest = t >> 5;
+            const int tq_ = ln & 3, nt_ = rest % NT, jb = rest / NT;
+            const int qi = nt_ * 8 + (ln >> 2);
+            int u, j0;
+            if (ring) {   // 128-channel blocks, quad tq holds channels [32 tq, 32 tq + 32) of each
+                const int bb = jb / 4, m = jb % 4;
+                u = bb * 16 + tq_ * 4 + m;
+                j0 = bb * 8 + 2 * m;
+            } else {      // chunk 4 jb + tq
+                u = 4 * jb + tq_;
+                j0 = 2 * jb;
             }
             qidx[k] = (((qi >> 3) * KS + j0) * 8 + (qi & 7)) * 4 + tq_;
             const uint4 x = *reinterpret_cast<const uint4*>(qr + qi * D + 8 * u);
@@ -303,9 +306,11 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
             const uint16_t* ksc = reinterpret_cast<const uint16_t*>(kr + 128 * CLD);
 #pragma unroll
             for (int bk = 0; bk < NB; ++bk) {
-                float acc[NT][4];
+                float acc[2][NT][4];   // two mma chains, by k-step parity
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+                for (int ch = 0; ch < 2; ++ch)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) acc[ch][nt][0] = acc[ch][nt][1] = acc[ch][nt][2] = acc[ch][nt][3] = 0.f;
                 const uint8_t* row0 = kr + r0 * CLD + 96 * bk;
                 const uint8_t* row1 = kr + r1 * CLD + 96 * bk;
                 const uint4 w0 = *reinterpret_cast<const uint4*>(row0 + 16 * tq);
@@ -324,21 +329,29 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint2 bq = qb2[((nt * KS + bk * 8 + jj) * 8 + g) * 4 + tq];
-                        mma16816(acc[nt], a0, a1, a2, a3, bq.x, bq.y);
+                        mma16816(acc[jj & 1][nt], a0, a1, a2, a3, bq.x, bq.y);
                     }
                 }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[0][nt][i] += acc[1][nt][i];
                 const float e0 = h2f(ksc[r0 * NB + bk]), e1 = h2f(ksc[r1 * NB + bk]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const float o0 = 96.f * zk[bk][nt][0], o1 = 96.f * zk[bk][nt][1];
-                    s4[nt][0] += e0 * (acc[nt][0] - o0);
-                    s4[nt][1] += e0 * (acc[nt][1] - o1);
-                    s4[nt][2] += e1 * (acc[nt][2] - o0);
-                    s4[nt][3] += e1 * (acc[nt][3] - o1);
+                    s4[nt][0] += e0 * (acc[0][nt][0] - o0);
+                    s4[nt][1] += e0 * (acc[0][nt][1] - o1);
+                    s4[nt][2] += e1 * (acc[0][nt][2] - o0);
+                    s4[nt][3] += e1 * (acc[0][nt][3] - o1);
                 }
             }
         } else {
-            // 16-byte chunk 4i + tq of rows r0, r1; odd rows load chunk pairs in the other order
+            // 16-byte chunk 4i + tq of rows r0, r1; odd rows load chunk pairs in the other order;
+            // a second mma chain (sb) takes the odd k-steps
+            float sb[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) sb[nt][0] = sb[nt][1] = sb[nt][2] = sb[nt][3] = 0.f;
             const int odd = g & 1;
 #pragma unroll
             for (int i2 = 0; i2 < D / 64; ++i2) {
@@ -358,10 +371,15 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                        mma16816(s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1], bq.x, bq.y);
+                        mma16816((jj & 1) ? sb[nt] : s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1],
+                                 bq.x, bq.y);
                     }
                 }
             }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s4[nt][i] += sb[nt][i];
         }
         const bool v0 = r0 < n, v1 = r1 < n;
 #pragma unroll
@@ -418,16 +436,32 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
 
         // ---------------- step 3: O^T = alpha O^T + V^T P'^T for this warp's channels
         const int pv = ring ? vw : 0;
+        // k-steps outer, m-tiles inner: the m-tiles' mma chains interleave (one m-tile splits its
+        // chain by k-step parity); the all-ones mma is shared by the m-tiles
+        constexpr int C3 = (MT == 1) ? 2 : 1;
+        float acc[MT][C3][NT][4], a1s[NT][4];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int c0 = warp * (D / 8) + 16 * mt;
-            float acc[NT][4], a1s[NT][4];
+        for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+            for (int i = 0; i < 4; ++i) a1s[nt][i] = 0.f;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[nt][i] = a1s[nt][i] = 0.f;
+            for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+                for (int ch = 0; ch < C3; ++ch)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc[mt][ch][nt][i] = 0.f;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint2 bp[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                bp[nt] = pb2[((pv * 8 + kk) * NT + nt) * 32 + lane];
+                if (ring) mma16816(a1s[nt], ONE2, ONE2, ONE2, ONE2, bp[nt].x, bp[nt].y);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int c0 = warp * (D / 8) + 16 * mt;
                 uint32_t a0, a1, a2, a3;
                 if (ring) {
                     // 8 x 8 tiles (positions x channels) decoded in A-fragment order, then transposed
@@ -452,21 +486,22 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
                     ldsm_x4_t(su32(vr + pos * FLD + 2 * ch), a0, a1, a2, a3);
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bp = pb2[((pv * 8 + kk) * NT + nt) * 32 + lane];
-                    mma16816(acc[nt], a0, a1, a2, a3, bp.x, bp.y);
-                    if (ring) mma16816(a1s[nt], ONE2, ONE2, ONE2, ONE2, bp.x, bp.y);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float z0 = ring ? 96.f * a1s[nt][0] : 0.f, z1 = ring ? 96.f * a1s[nt][1] : 0.f;
-                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + (acc[nt][0] - z0);
-                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + (acc[nt][1] - z1);
-                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + (acc[nt][2] - z0);
-                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + (acc[nt][3] - z1);
+                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][kk % C3][nt], a0, a1, a2, a3, bp[nt].x, bp[nt].y);
             }
         }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float r[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) r[i] = acc[mt][0][nt][i] + (C3 == 2 ? acc[mt][C3 - 1][nt][i] : 0.f);
+                const float z0 = ring ? 96.f * a1s[nt][0] : 0.f, z1 = ring ? 96.f * a1s[nt][1] : 0.f;
+                O[mt][nt][0] = al[nt][0] * O[mt][nt][0] + (r[0] - z0);
+                O[mt][nt][1] = al[nt][1] * O[mt][nt][1] + (r[1] - z1);
+                O[mt][nt][2] = al[nt][0] * O[mt][nt][2] + (r[2] - z0);
+                O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + (r[3] - z1);
+            }
         if (!ring) fence_async_smem();    // the zero fill above precedes the next bulk copy into this stage
         __syncwarp();
         if (lane == 0) mbar_arrive(su32(&empty[sl]));
