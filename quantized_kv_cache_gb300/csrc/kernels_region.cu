@@ -12,7 +12,8 @@
 //      fp16 K rows are the A fragments as they stand. Positions past the run's end score -inf.
 //   2. group maximum, p = 2^(s - m), running sums, P' = p x (tq6_0 value scale of the block);
 //      movmatrix gives the B fragments of step 3 (one 8-byte store per lane).
-//   3. values: warp w takes channels [wD/8, (w+1)D/8). The rows are token-major, so the A
+//   3. values: warp w takes channels [wD/8, (w+1)D/8) (fp16 rows come in runs of 16384 / D
+//      positions at most, so a stage stays at 64 KB; warps past the run skip step 1). The rows are token-major, so the A
 //      fragments of V^T come from transposes: ldmatrix.trans for fp16 rows, movmatrix of the
 //      decoded tq6_0 tile for the ring (whose fragment rows then hold channels in the order
 //      0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
@@ -36,7 +37,8 @@ struct RGeo {
     static constexpr int TQ_HALF = 128 * CLD + SC_BYTES;                // K (or V) part of a ring stage
     static constexpr int TQ_STAGE = 2 * TQ_HALF;
     static constexpr int FLD = 2 * D;                                   // fp16 row stride (dense)
-    static constexpr int F_HALF = 128 * FLD;
+    static constexpr int RUNF = (16384 / D < 128) ? 16384 / D : 128;    // fp16 rows per run (64 KB stage)
+    static constexpr int F_HALF = RUNF * FLD;
     static constexpr int F_STAGE = 2 * F_HALF;
     static constexpr int AREA = (2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE;
     static constexpr int QB_BYTES = NT * KS * 256;
@@ -65,7 +67,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 template <int D, int NQ>
-__global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L, AttnParams p) {
+__global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L, AttnParams p) {
     using Gm = RGeo<D, NQ>;
     constexpr int NT = Gm::NT, KS = Gm::KS, MT = Gm::MT, NB = Gm::NB, TPT = Gm::TPT;
     constexpr int CLD = Gm::CLD, FLD = Gm::FLD;
@@ -83,8 +85,9 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
     const int kind = sp.kind[r];
     const int t0 = sp.lo[r] + cidx * p.chunk;
     const int t1 = min(t0 + p.chunk, sp.hi[r]);
-    const int nrun = (t1 - t0 + 127) / 128;
     const bool ring = (kind == RK_RING);
+    const int RUN = ring ? 128 : Gm::RUNF;                // positions per run
+    const int nrun = (t1 - t0 + RUN - 1) / RUN;
     const int64_t unit = L.unit(p.layer, sp.slot, h);
     uint32_t* status = status_word(L, p.pool);
 
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) { ok = false; break; }
             }
-            const int pc = t0 + 128 * i, n = min(128, t1 - pc);
+            const int pc = t0 + RUN * i, n = min(RUN, t1 - pc);
             uint8_t* st = stages + (size_t)sl * stage_bytes;
             const uint32_t fb = su32(&full[sl]);
             // contiguous slot runs: one copy each (a run of the ring never wraps; the tail and an
@@ -288,11 +291,11 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
     for (int gi = 0; gi < nrun; ++gi) {
         const int sl = gi % nst;
         mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
-        const int n = min(128, t1 - (t0 + 128 * gi));
+        const int n = min(RUN, t1 - (t0 + RUN * gi));
         uint8_t* kr = stages + (size_t)sl * stage_bytes;
         uint8_t* vr = kr + half_bytes;
-        if (!ring && n < 128) {   // rows past the run's end: zeros, so 0 x row stays 0 in P.V
-            for (int e = threadIdx.x; e < (128 - n) * (2 * D / 16); e += kCT) {
+        if (!ring && n < RUN) {   // rows past the run's end: zeros, so 0 x row stays 0 in P.V
+            for (int e = threadIdx.x; e < (RUN - n) * (2 * D / 16); e += kCT) {
                 const int rr = n + e / (2 * D / 16), u = e % (2 * D / 16);
                 *reinterpret_cast<uint4*>(vr + rr * FLD + 16 * u) = make_uint4(0, 0, 0, 0);
             }
@@ -346,7 +349,7 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
                     s4[nt][3] += e1 * (acc[0][nt][3] - o1);
                 }
             }
-        } else {
+        } else if (16 * warp < RUN) {
             // 16-byte chunk 4i + tq of rows r0, r1; odd rows load chunk pairs in the other order;
             // a second mma chain (sb) takes the odd k-steps
             float sb[NT][4];
@@ -453,6 +456,7 @@ __global__ void __launch_bounds__(kBodyThreads, 1) decode_region_kernel(Layout L
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
+            if (16 * kk >= RUN) break;
             uint2 bp[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
