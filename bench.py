@@ -56,6 +56,16 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# DRAM bytes (read + write) of one kv_decode_attn call (region, body and merge kernels), one ncu
+# capture per workload of the current kernels at the same per-layer shape; profiles/
+# decode_attn_launches.md gives the command and the per-kernel split.
+MEASURED_TRAFFIC = {
+    "hybrid27b_kvarn44": 46.09e6,
+    "fa14b_q8q4": 222.33e6,
+    "longctx_tbq4": 751.06e6,
+}
+
+
 # --------------------------------------------------------------------------- byte model
 def layer_step_bytes(w, states):
     """Algorithmic bytes one decode attention of one layer reads and writes.
@@ -256,7 +266,7 @@ def run_ours(args, rank, world, local_rank):
     attn_bytes = [step_bytes[s] for s in range(K) for _ in range(w.n_layers)]
     hbm, peak_src = peaks()
     achieved = sum(attn_bytes) / sum(attn_times) / 1e9
-    value = total_bytes * world / elapsed_max / 1e9
+    value = weak_value(total_bytes, elapsed_max, world)
 
     # seal throughput: time the seals of the policy's first seal point (or the bulk seal)
     seal = measure_seal(w, cache, inp, seq_ids, out, restore, stream, K)
@@ -274,8 +284,10 @@ def run_ours(args, rank, world, local_rank):
         "config": config_block(w, K),
         "pct_of_hbm_peak": round(100 * value / world / hbm, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "decode_split_kernel + decode_merge_kernel (one kv_decode_attn call)",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": MEASURED_TRAFFIC.get(w.name),
+                     "kernel": "one kv_decode_attn call: decode_region_kernel beside decode_body_kernel, then "
+                               "decode_merge_kernel (timed by events on the calling stream)",
                      "peak_source": f"{peak_src} hbm_gbs",
                      "launches_timed": len(attn_times),
                      "mean_launch_us": round(1e6 * sum(attn_times) / len(attn_times), 3),
@@ -505,6 +517,12 @@ def dist_barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def weak_value(bytes_per_rank, elapsed_max, world):
+    """Whole-job GB/s under weak scaling: every rank reads bytes_per_rank; the job's time is the
+    slowest rank's."""
+    return bytes_per_rank * world / elapsed_max / 1e9
 
 
 def dist_max(x, world):
