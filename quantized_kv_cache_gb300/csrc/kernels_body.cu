@@ -34,7 +34,10 @@ template <int D, int NQ, int KF, int VF, int KB, int VB>
 struct Geo {
     static constexpr int NT = NQ / 8;
     static constexpr int KS = D / 16;                                   // score k-steps
-    static constexpr int WK = (KF == KF_KVARN) ? 256 : (KF == KF_TBQ4 ? 128 : 32);   // K scale block
+    // K fragment block: the channels one set of score accumulators covers. Q8_0 K is dequantised
+    // in registers (code x block scale), so one block spans all D channels and each thread quad
+    // owns a contiguous quarter of the row
+    static constexpr int WK = (KF == KF_KVARN) ? 256 : (KF == KF_TBQ4 ? 128 : (KF == KF_Q8 ? D : 32));
     static constexpr int NBK = D / WK;
     static constexpr int KSPB = WK / 16;                                // k-steps per K block
     static constexpr int WV = (VF == KF_KVARN) ? 256 : (VF == KF_TBQ4 ? 128 : 32);   // V scale block
@@ -43,7 +46,7 @@ struct Geo {
     static constexpr bool KNIB = (KF == KF_KVARN || KF == KF_Q4);       // K pairs (x, x+4)
     static constexpr bool VNIB = (VF == KF_KVARN || VF == KF_Q4);
     // value the raw fp16 operand reads for code 0 (the code's own centre included)
-    static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : (KF == KF_Q8 ? 1152.f : 0.f));
+    static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : 0.f);
     static constexpr float VOFF = (VF == KF_KVARN) ? 64.f : (VF == KF_Q4 ? 72.f : (VF == KF_Q8 ? 1152.f : 0.f));
     static constexpr bool ZV = (VF == KF_KVARN);                        // per-group value zero-point sums
     static constexpr bool PSV = (VF == KF_Q8 || VF == KF_Q4);           // sum of P' per group (offset)
@@ -393,13 +396,43 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         }
                     }
                 } else if (KF == KF_Q8) {
-                    const uint2 x0 = *reinterpret_cast<const uint2*>(kr + t0 * D + 32 * bk + 8 * tq);
-                    const uint2 x1 = *reinterpret_cast<const uint2*>(kr + t1 * D + 32 * bk + 8 * tq);
-                    const uint32_t W0[2] = {x0.x, x0.y}, W1[2] = {x1.x, x1.y};
+                    // channels [tq D/4, (tq+1) D/4) of rows t0, t1 (k-step j: 4 bytes at 4j), in 16-byte
+                    // loads, odd rows taking each pair of loads in the other order (banks); each code
+                    // byte b becomes (1152 + b) - 1152 = b, times its 32-channel block scale
+                    constexpr int CPT = D / 4, NL = CPT / 16, NSB = CPT / 32;
+                    const int odd = g & 1;
+                    uint32_t W0[CPT / 4], W1[CPT / 4];
+#pragma unroll
+                    for (int i = 0; i < NL; i += 2) {
+                        uint4 y0a = *reinterpret_cast<const uint4*>(kr + t0 * D + CPT * tq + 16 * (i + odd));
+                        uint4 y0b = *reinterpret_cast<const uint4*>(kr + t0 * D + CPT * tq + 16 * (i + 1 - odd));
+                        uint4 y1a = *reinterpret_cast<const uint4*>(kr + t1 * D + CPT * tq + 16 * (i + odd));
+                        uint4 y1b = *reinterpret_cast<const uint4*>(kr + t1 * D + CPT * tq + 16 * (i + 1 - odd));
+                        if (odd) {
+                            const uint4 t = y0a; y0a = y0b; y0b = t;
+                            const uint4 u = y1a; y1a = y1b; y1b = u;
+                        }
+                        W0[4 * i] = y0a.x; W0[4 * i + 1] = y0a.y; W0[4 * i + 2] = y0a.z; W0[4 * i + 3] = y0a.w;
+                        W0[4 * i + 4] = y0b.x; W0[4 * i + 5] = y0b.y; W0[4 * i + 6] = y0b.z; W0[4 * i + 7] = y0b.w;
+                        W1[4 * i] = y1a.x; W1[4 * i + 1] = y1a.y; W1[4 * i + 2] = y1a.z; W1[4 * i + 3] = y1a.w;
+                        W1[4 * i + 4] = y1b.x; W1[4 * i + 5] = y1b.y; W1[4 * i + 6] = y1b.z; W1[4 * i + 7] = y1b.w;
+                    }
+                    const uint16_t* dr = reinterpret_cast<const uint16_t*>(kr + 128 * D);
+                    uint32_t s0[NSB], s1[NSB];
+#pragma unroll
+                    for (int b2 = 0; b2 < NSB; ++b2) {
+                        const uint32_t h0 = dr[t0 * (D / 32) + NSB * tq + b2], h1 = dr[t1 * (D / 32) + NSB * tq + b2];
+                        s0[b2] = h0 | (h0 << 16);
+                        s1[b2] = h1 | (h1 << 16);
+                    }
+                    const __half2 c1152 = __float2half2_rn(1152.f);
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
-                        const uint32_t a0 = i8raw(W0[jj], 0x5140), a2 = i8raw(W0[jj], 0x7362);
-                        const uint32_t a1r = i8raw(W1[jj], 0x5140), a3 = i8raw(W1[jj], 0x7362);
+                        const int b2 = jj / 8;
+                        const uint32_t a0 = hmul2u(as_u(__hsub2(as_h2(i8raw(W0[jj], 0x5140)), c1152)), s0[b2]);
+                        const uint32_t a2 = hmul2u(as_u(__hsub2(as_h2(i8raw(W0[jj], 0x7362)), c1152)), s0[b2]);
+                        const uint32_t a1r = hmul2u(as_u(__hsub2(as_h2(i8raw(W1[jj], 0x5140)), c1152)), s1[b2]);
+                        const uint32_t a3 = hmul2u(as_u(__hsub2(as_h2(i8raw(W1[jj], 0x7362)), c1152)), s1[b2]);
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -436,7 +469,7 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
             // s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q', log2 domain; the
             // per-position block scales of TBQ4 / Q8_0 / Q4_0 come in one vector load per row
             float ek0[NBK], ek1[NBK];
-            if (KF != KF_KVARN) {
+            if (KF != KF_KVARN && KF != KF_Q8) {
                 const uint16_t* er = reinterpret_cast<const uint16_t*>(
                     kr + (KF == KF_TBQ4 ? 64 : (KF == KF_Q8 ? 128 : 64)) * D);
                 load_row_f<NBK>(er + t0 * NBK, ek0);
@@ -457,6 +490,8 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                         zk[bk][nt][0] = a1[bk][nt][0][0];
                         zk[bk][nt][1] = a1[bk][nt][0][1];
                     }
+                } else if (KF == KF_Q8) {
+                    e0 = e1 = 1.f;                  // dequantised in the fragments
                 } else {
                     e0 = ek0[bk];
                     e1 = ek1[bk];
