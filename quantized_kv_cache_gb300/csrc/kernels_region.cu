@@ -1,5 +1,6 @@
 // Decode attention over the unsealed regions: the tq6_0 ring span (rotated domain) and the
-// fp16 rows of the sink, the exact tail and an F16 exact journal (original domain).
+// 16-bit rows of the sink, the exact tail and an exact journal (original domain). bf16 rows use
+// the bf16 mma with the query and P' each split into bf16 high and low parts (16 significant bits).
 //
 // One CTA per region work item (sequence, KV head, run of positions inside one region), in
 // runs of up to 128 positions. Warp 8 streams each run into shared memory with cp.async.bulk:
@@ -20,6 +21,7 @@
 //      removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
 // The partial (m, l, o) of a ring item is rotated back to the original domain; the merge
 // kernel (kernels_attn.cu) combines all partials of a (sequence, KV head) under one softmax.
+#include <cuda_bf16.h>
 #include "stream_common.cuh"
 
 namespace kvq {
@@ -41,10 +43,11 @@ struct RGeo {
     static constexpr int F_HALF = RUNF * FLD;
     static constexpr int F_STAGE = 2 * F_HALF;
     static constexpr int AREA = (2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE;
-    static constexpr int QB_BYTES = NT * KS * 256;
-    static constexpr int P_BYTES = NB * 8 * NT * 256;
+    static constexpr int QB_BYTES = NT * KS * 256;                      // one fragment set
+    static constexpr int PC = NB > 2 ? NB : 2;                          // P' copies (bf16 rows: hi, lo)
+    static constexpr int P_BYTES = PC * 8 * NT * 256;
     static constexpr int RED_FLOATS = 2 * NQ * 8 + 2 * NQ;
-    static constexpr int SMEM = AREA + 128 + QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    static constexpr int SMEM = AREA + 128 + 2 * QB_BYTES + P_BYTES + RED_FLOATS * 4;
     static constexpr int NTASK = NQ * D / 8;
     static constexpr int TPT = (NTASK + kCT - 1) / kCT;
 };
@@ -63,6 +66,22 @@ __device__ __forceinline__ uint32_t nib64_rt(uint32_t w, int x) {
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// A pair of floats as bf16 (round to nearest even): the high part and the remainder, so that
+// hi + lo carries 16 significant bits.
+__device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
@@ -86,6 +105,8 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     const int t0 = sp.lo[r] + cidx * p.chunk;
     const int t1 = min(t0 + p.chunk, sp.hi[r]);
     const bool ring = (kind == RK_RING);
+    // bf16 exact rows: bf16 mma, the query and P' each split into bf16 high and low parts
+    const bool bf = !ring && kind != RK_SINK && ((kind == RK_TAIL ? L.tail_fmt : L.journal) == KVQ_BF16);
     const int RUN = ring ? 128 : Gm::RUNF;                // positions per run
     const int nrun = (t1 - t0 + RUN - 1) / RUN;
     const int64_t unit = L.unit(p.layer, sp.slot, h);
@@ -98,7 +119,7 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
     uint64_t* empty = full + 4;
     uint8_t* cur = smem + Gm::AREA + 128;
-    uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += Gm::QB_BYTES;
+    uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += 2 * Gm::QB_BYTES;   // bf16 rows: hi, lo
     uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
     float* red = reinterpret_cast<float*>(cur);           // [NQ][warp] maxima, then sums; m at 2 NQ 8
 
@@ -213,7 +234,7 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     // Query fragments. tq6_0 K: thread quad tq holds channels [32 tq, 32 tq + 32) of every
     // 128-channel block, k-step pairs (x, x+4) of 8-channel words. fp16 K: thread quad tq holds
     // the 16-byte chunks 4i + tq of the row, k-steps 2i and 2i + 1 in natural pairs.
-    uint2 qe0[TPT], qe1[TPT];
+    uint2 qe0[TPT], qe1[TPT], ql0[TPT], ql1[TPT];
     int qidx[TPT];
 #pragma unroll
     for (int k = 0; k < TPT; ++k) {
@@ -238,6 +259,18 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
             if (ring) {
                 qe0[k] = make_uint2(__byte_perm(x.x, x.z, 0x5410), __byte_perm(x.x, x.z, 0x7632));
                 qe1[k] = make_uint2(__byte_perm(x.y, x.w, 0x5410), __byte_perm(x.y, x.w, 0x7632));
+            } else if (bf) {
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __half22float2(as_h2(xs[i]));
+                    split_bf2(f.x, f.y, hi[i], lo[i]);
+                }
+                qe0[k] = make_uint2(hi[0], hi[1]);
+                qe1[k] = make_uint2(hi[2], hi[3]);
+                ql0[k] = make_uint2(lo[0], lo[1]);
+                ql1[k] = make_uint2(lo[2], lo[3]);
             } else {
                 qe0[k] = make_uint2(x.x, x.y);
                 qe1[k] = make_uint2(x.z, x.w);
@@ -251,6 +284,10 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
         uint2* e = reinterpret_cast<uint2*>(qb) + qidx[k];
         e[0] = qe0[k];
         e[32] = qe1[k];
+        if (bf) {
+            e[Gm::QB_BYTES / 8] = ql0[k];
+            e[Gm::QB_BYTES / 8 + 32] = ql1[k];
+        }
     }
     csync();
     const uint2* qb2 = reinterpret_cast<const uint2*>(qb);
@@ -373,9 +410,16 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                     const int j = 4 * i2 + jj;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const uint2 bq = qb2[((nt * KS + j) * 8 + g) * 4 + tq];
-                        mma16816((jj & 1) ? sb[nt] : s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1],
-                                 bq.x, bq.y);
+                        const int qix = ((nt * KS + j) * 8 + g) * 4 + tq;
+                        const uint2 bq = qb2[qix];
+                        if (bf) {   // high part in s4, low part in sb
+                            const uint2 bl = qb2[Gm::QB_BYTES / 8 + qix];
+                            mma_bf16(s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1], bq.x, bq.y);
+                            mma_bf16(sb[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1], A1[2 * jj + 1], bl.x, bl.y);
+                        } else {
+                            mma16816((jj & 1) ? sb[nt] : s4[nt], A0[2 * jj], A1[2 * jj], A0[2 * jj + 1],
+                                     A1[2 * jj + 1], bq.x, bq.y);
+                        }
                     }
                 }
             }
@@ -423,9 +467,19 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
             for (int c = 0; c < 2; ++c) l_part[nt][c] = al[nt][c] * l_part[nt][c] + pr[nt][c] + pr[nt][c + 2];
         }
         const uint16_t* vsc = reinterpret_cast<const uint16_t*>(vr + 128 * CLD);
+        if (bf) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                uint32_t h0, l0, h1, l1;
+                split_bf2(v0 ? pr[nt][0] : 0.f, v0 ? pr[nt][1] : 0.f, h0, l0);
+                split_bf2(v1 ? pr[nt][2] : 0.f, v1 ? pr[nt][3] : 0.f, h1, l1);
+                reinterpret_cast<uint2*>(pbuf)[((0 * 8 + warp) * NT + nt) * 32 + lane] = make_uint2(movtrans(h0), movtrans(h1));
+                reinterpret_cast<uint2*>(pbuf)[((1 * 8 + warp) * NT + nt) * 32 + lane] = make_uint2(movtrans(l0), movtrans(l1));
+            }
+        }
 #pragma unroll
         for (int v = 0; v < NB; ++v) {
-            if (!ring && v > 0) break;
+            if (!ring && (bf || v > 0)) break;
             const float f0 = ring ? h2f(vsc[r0 * NB + v]) : 1.f, f1 = ring ? h2f(vsc[r1 * NB + v]) : 1.f;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -490,7 +544,15 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                     ldsm_x4_t(su32(vr + pos * FLD + 2 * ch), a0, a1, a2, a3);
                 }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma16816(acc[mt][kk % C3][nt], a0, a1, a2, a3, bp[nt].x, bp[nt].y);
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (bf) {
+                        const uint2 bl = pb2[((8 + kk) * NT + nt) * 32 + lane];
+                        mma_bf16(acc[mt][kk % C3][nt], a0, a1, a2, a3, bp[nt].x, bp[nt].y);
+                        mma_bf16(acc[mt][kk % C3][nt], a0, a1, a2, a3, bl.x, bl.y);
+                    } else {
+                        mma16816(acc[mt][kk % C3][nt], a0, a1, a2, a3, bp[nt].x, bp[nt].y);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -565,14 +627,10 @@ int upload_tables_region(const FormatTables& t) {
 }
 
 // 1 when the streaming region kernel takes this layout's region items: head_dim 128 or 256,
-// the ring (when present) in runs of whole 128-slot chunks, fp16 exact rows.
+// the ring (when present) in runs of whole 128-slot chunks.
 int region_kernel_ok(const Layout& L) {
     if (L.D != 128 && L.D != 256) return 0;
-    if (L.journal == KVQ_TQ6_0) {
-        if (L.R % 128 != 0 || L.tail_fmt != KVQ_F16) return 0;
-    } else if (L.journal != KVQ_F16) {
-        return 0;
-    }
+    if (L.journal == KVQ_TQ6_0 && L.R % 128 != 0) return 0;
     return 1;
 }
 
