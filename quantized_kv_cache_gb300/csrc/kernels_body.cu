@@ -61,10 +61,14 @@ struct Geo {
     static constexpr int P_BYTES = NVB * 8 * NT * 256;                  // P' fragments
     static constexpr int RED_FLOATS = (NVB + 2) * NQ * 8 + NQ;          // [q][warp] exchange rows, m, l
     static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    // resident CTAs per SM: three when two stages fit in a third of shared memory, else two,
+    // else one (the per-CTA budgets leave the 1 KB per CTA the SM reserves)
+    static constexpr int THREE_CTA_BYTES = 74 * 1024;
     static constexpr int TWO_CTA_BYTES = 112 * 1024;
+    static constexpr bool THREE = FIXED + 2 * STAGE <= THREE_CTA_BYTES;
     static constexpr bool TWO = FIXED + 2 * STAGE <= TWO_CTA_BYTES;
-    static constexpr int MINB = TWO ? 2 : 1;
-    static constexpr int BUDGET = TWO ? TWO_CTA_BYTES : 227 * 1024;
+    static constexpr int MINB = THREE ? 3 : (TWO ? 2 : 1);
+    static constexpr int BUDGET = THREE ? THREE_CTA_BYTES : (TWO ? TWO_CTA_BYTES : 227 * 1024);
     static constexpr int NTASK = NQ * D / 8;                            // 8-channel query chunks
     static constexpr int TPT = (NTASK + kCT - 1) / kCT;                 // chunks per consumer thread
 };
