@@ -602,22 +602,25 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaSt
         attr = true;
     }
     const int n_body = p.total_items - p.n_region_items;
+    bool joined = true;
     if (p.n_region_items > 0) {
         // the streaming region kernel takes the region items when the body kernel takes the
         // body (so no body positions are among them) and the layout is one it covers; with
-        // body work too it runs on the auxiliary stream, beside the body kernel
+        // body work too it runs on the auxiliary stream, beside the body kernel, and joins the
+        // caller's stream before the merge
         if (region_kernel_ok(L) && body_ctas_per_sm(L) > 0) {
             const bool fork = aux && evf && evj && n_body > 0;
             if (fork) {
                 if (cudaEventRecord(evf, s) != cudaSuccess || cudaStreamWaitEvent(aux, evf, 0) != cudaSuccess)
                     return (int)cudaGetLastError();
+                joined = false;
             }
             const int e = launch_decode_region(L, p, fork ? aux : s);
-            if (fork) {
-                cudaEventRecord(evj, aux);
-                cudaStreamWaitEvent(s, evj, 0);
+            if (fork) cudaEventRecord(evj, aux);
+            if (e != 0) {
+                if (!joined) cudaStreamWaitEvent(s, evj, 0);
+                return e;
             }
-            if (e != 0) return e;
         } else {
             decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
             cudaError_t e = cudaGetLastError();
@@ -626,7 +629,10 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaSt
     }
     if (n_body > 0) {
         const int e = launch_decode_body(L, p, n_body, s);
+        if (!joined) cudaStreamWaitEvent(s, evj, 0);
         if (e != 0) return e;
+    } else if (!joined) {
+        cudaStreamWaitEvent(s, evj, 0);
     }
     int max_cnt = 0;
     for (int i = 0; i < p.n_seq; ++i)

@@ -116,8 +116,9 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
     const SeqSpan& sp = p.seq[b];
     const int local = item - sp.body_first;
     const int h = local / sp.body_per_head;
-    const int g0 = (local % sp.body_per_head) * p.body_chunk;
-    const int ngroups = min(g0 + p.body_chunk, sp.body_groups) - g0;
+    const int kb_ = local % sp.body_per_head;             // the head's groups split evenly over its items
+    const int g0 = (int)((int64_t)kb_ * sp.body_groups / sp.body_per_head);
+    const int ngroups = (int)((int64_t)(kb_ + 1) * sp.body_groups / sp.body_per_head) - g0;
     const int64_t unit = L.unit(p.layer, sp.slot, h);
     uint32_t* status = status_word(L, p.pool);
 

@@ -379,8 +379,10 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     const int64_t target = (int64_t)c->sm_count * per_sm;
     int64_t chunk = (region_tok * L.H + target - 1) / target;
     chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
+    // body items: per (sequence, head), a number of items proportional to its groups, in all
+    // at most the resident body-kernel CTAs (one wave, no tail); groups split evenly
     const int body_slots = std::max(1, body_ctas_per_sm(L)) * c->sm_count;
-    int64_t bchunk = std::max<int64_t>(1, (body_groups * L.H + body_slots - 1) / body_slots);
+    int64_t slots_per_head = std::max<int64_t>(1, body_slots / L.H);
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {
@@ -401,7 +403,9 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
             s.body_groups = body_kernel ? (int32_t)((ST(c, layer, s.slot) - kSink) / kGroup) : 0;
-            s.body_per_head = (int32_t)((s.body_groups + bchunk - 1) / bchunk);
+            int64_t nb = s.body_groups > 0 ? slots_per_head * s.body_groups / std::max<int64_t>(1, body_groups) : 0;
+            if (s.body_groups > 0) nb = std::min<int64_t>(std::max<int64_t>(nb, 1), s.body_groups);
+            s.body_per_head = (int32_t)nb;
             s.body_first = (int32_t)items;
             items += (int64_t)s.body_per_head * L.H;
         }
@@ -411,9 +415,9 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
             break;
         }
         chunk *= 2;
-        bchunk *= 2;
+        slots_per_head = std::max<int64_t>(1, slots_per_head / 2);
     }
-    p.body_chunk = (int32_t)bchunk;
+    p.body_chunk = 0;
     p.chunk = (int32_t)chunk;
     const int e = launch_decode(L, p, stream, c->aux, c->ev_fork, c->ev_join);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;

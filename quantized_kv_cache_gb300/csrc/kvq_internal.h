@@ -104,7 +104,7 @@ struct AttnParams {
     float* partials;         // workspace: per item [2 * NQ + NQ * D] floats
     int32_t layer, n_seq, chunk, total_items;
     int32_t n_region_items;  // region items come first, body items after them
-    int32_t body_chunk;      // groups per body work item
+    int32_t body_chunk;      // unused (body items split each head's groups evenly)
     SeqSpan seq[kMaxSeqPerCall];
 };
 
