@@ -602,38 +602,32 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaSt
         attr = true;
     }
     const int n_body = p.total_items - p.n_region_items;
-    bool joined = true;
+    // the streaming region kernel takes the region items when the body kernel takes the body
+    // (so no body positions are among them) and the layout is one it covers. With body work too,
+    // the body kernel is launched first (its items are the long ones) and the region kernel runs
+    // beside it on the auxiliary stream, which joins the caller's stream before the merge.
+    const bool streaming = p.n_region_items > 0 && region_kernel_ok(L) && body_ctas_per_sm(L) > 0;
+    const bool fork = streaming && aux && evf && evj && n_body > 0;
+    if (fork) {
+        if (cudaEventRecord(evf, s) != cudaSuccess || cudaStreamWaitEvent(aux, evf, 0) != cudaSuccess)
+            return (int)cudaGetLastError();
+    }
+    int eb = 0, er = 0;
+    if (n_body > 0) eb = launch_decode_body(L, p, n_body, s);
     if (p.n_region_items > 0) {
-        // the streaming region kernel takes the region items when the body kernel takes the
-        // body (so no body positions are among them) and the layout is one it covers; with
-        // body work too it runs on the auxiliary stream, beside the body kernel, and joins the
-        // caller's stream before the merge
-        if (region_kernel_ok(L) && body_ctas_per_sm(L) > 0) {
-            const bool fork = aux && evf && evj && n_body > 0;
-            if (fork) {
-                if (cudaEventRecord(evf, s) != cudaSuccess || cudaStreamWaitEvent(aux, evf, 0) != cudaSuccess)
-                    return (int)cudaGetLastError();
-                joined = false;
-            }
-            const int e = launch_decode_region(L, p, fork ? aux : s);
-            if (fork) cudaEventRecord(evj, aux);
-            if (e != 0) {
-                if (!joined) cudaStreamWaitEvent(s, evj, 0);
-                return e;
-            }
+        if (streaming) {
+            er = launch_decode_region(L, p, fork ? aux : s);
         } else {
             decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
-            cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return (int)e;
+            er = (int)cudaGetLastError();
         }
     }
-    if (n_body > 0) {
-        const int e = launch_decode_body(L, p, n_body, s);
-        if (!joined) cudaStreamWaitEvent(s, evj, 0);
-        if (e != 0) return e;
-    } else if (!joined) {
+    if (fork) {
+        cudaEventRecord(evj, aux);
         cudaStreamWaitEvent(s, evj, 0);
     }
+    if (eb != 0) return eb;
+    if (er != 0) return er;
     int max_cnt = 0;
     for (int i = 0; i < p.n_seq; ++i)
         max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
