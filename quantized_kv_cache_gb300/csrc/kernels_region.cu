@@ -15,9 +15,9 @@
 //      movmatrix gives the B fragments of step 3 (one 8-byte store per lane).
 //   3. values: warp w takes channels [wD/8, (w+1)D/8) (fp16 rows come in runs of 16384 / D
 //      positions at most, so a stage stays at 64 KB; warps past the run skip step 1). The rows are token-major, so the A
-//      fragments of V^T come from transposes: ldmatrix.trans for fp16 rows, movmatrix of the
-//      decoded tq6_0 tile for the ring (whose fragment rows then hold channels in the order
-//      0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
+//      fragments of V^T come from transposes: ldmatrix.trans of the fp16 rows, or of a small
+//      per-warp buffer of decoded tq6_0 rows for the ring (whose fragment rows then hold channels
+//      in the order 0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
 //      removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
 // The partial (m, l, o) of a ring item is rotated back to the original domain; the merge
 // kernel (kernels_attn.cu) combines all partials of a (sequence, KV head) under one softmax.
@@ -47,22 +47,24 @@ struct RGeo {
     static constexpr int PC = NB > 2 ? NB : 2;                          // P' copies (bf16 rows: hi, lo)
     static constexpr int P_BYTES = PC * 8 * NT * 256;
     static constexpr int RED_FLOATS = 2 * NQ * 8 + 2 * NQ;
-    static constexpr int SMEM = AREA + 128 + 2 * QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    // tq6_0 values: per-warp buffer of decoded rows (ROWS positions x the warp's D/8 channels,
+    // fp16, padded rows) read back transposed by ldmatrix
+    static constexpr int CPW = D / 8, WPP = CPW / 8, VROWS = 32 / WPP, VRS = CPW * 2 + 16;
+    static constexpr int VB_BYTES = VROWS * VRS;
+    // shared memory: one query-fragment set, a second one for layouts with bf16 rows
+    static constexpr int smem(bool bf16_rows) {
+        return AREA + 128 + (bf16_rows ? 2 : 1) * QB_BYTES + P_BYTES + RED_FLOATS * 4 + kConsumers * VB_BYTES;
+    }
     static constexpr int NTASK = NQ * D / 8;
     static constexpr int TPT = (NTASK + kCT - 1) / kCT;
 };
 
-// Adds the two high bits of tq6_0 codes y and y+4 (fields 2y and 2y+8 of h) as 16 x value:
-// mantissa bits 8-9 of each half of a nib64 pair.
-__device__ __forceinline__ uint32_t add_hi2(uint32_t raw, uint32_t h, int y) {
-    const uint32_t t = ((h >> (2 * y)) & 0x303u) * 0x00010100u;
-    return (t & 0x03000300u) | raw;
-}
-// nib64 with a run-time pair index x (0..3): a funnel shift brings nibbles x, x+4 to bits 4-7, 20-23.
-__device__ __forceinline__ uint32_t nib64_rt(uint32_t w, int x) {
-    const uint32_t t = __funnelshift_r(w << 4, w >> 28, 4 * x);
-    return (t & 0x00F000F0u) | 0x54005400u;
-}
+// The two high bits of 8 tq6_0 codes (16 bits, code i at bits 2i) spread for hi2_at: codes
+// 0..3 at bits 0-7, codes 4..7 at bits 16-23.
+__device__ __forceinline__ uint32_t hi2_spread(uint32_t h16) { return (h16 & 0xFFu) | ((h16 & 0xFF00u) << 8); }
+// Adds the high bits of codes x and x+4 (from hi2_spread) to a nib64 pair: mantissa bits 8-9.
+template <int X>
+__device__ __forceinline__ uint32_t hi2_at(uint32_t raw, uint32_t u) { return ((u << (8 - 2 * X)) & 0x03000300u) | raw; }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
@@ -119,9 +121,12 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
     uint64_t* empty = full + 4;
     uint8_t* cur = smem + Gm::AREA + 128;
-    uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += 2 * Gm::QB_BYTES;   // bf16 rows: hi, lo
+    const bool has_bf = (L.tail_fmt == KVQ_BF16) || (L.journal == KVQ_BF16);
+    uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += (has_bf ? 2 : 1) * Gm::QB_BYTES;   // bf16: hi, lo
     uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
     float* red = reinterpret_cast<float*>(cur);           // [NQ][warp] maxima, then sums; m at 2 NQ 8
+    cur += Gm::RED_FLOATS * 4;
+    uint8_t* vbuf = cur;                                  // [warp][VROWS][VRS] decoded tq6_0 values
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ int s_abort;
@@ -361,11 +366,17 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                 const uint32_t H0[2] = {h0.x, h0.y}, H1[2] = {h1.x, h1.y};
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {
-                    const int m = jj >> 1, x = 2 * (jj & 1), y = 8 * (m & 1) + x;
-                    const uint32_t a0 = add_hi2(nib64(W0[m], x), H0[m >> 1], y);
-                    const uint32_t a2 = add_hi2(nib64(W0[m], x + 1), H0[m >> 1], y + 1);
-                    const uint32_t a1 = add_hi2(nib64(W1[m], x), H1[m >> 1], y);
-                    const uint32_t a3 = add_hi2(nib64(W1[m], x + 1), H1[m >> 1], y + 1);
+                    const int m = jj >> 1;
+                    const uint32_t u0 = hi2_spread((H0[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
+                    const uint32_t u1 = hi2_spread((H1[m >> 1] >> (16 * (m & 1))) & 0xFFFFu);
+                    uint32_t a0, a1, a2, a3;
+                    if (jj & 1) {
+                        a0 = hi2_at<2>(nib64(W0[m], 2), u0); a2 = hi2_at<3>(nib64(W0[m], 3), u0);
+                        a1 = hi2_at<2>(nib64(W1[m], 2), u1); a3 = hi2_at<3>(nib64(W1[m], 3), u1);
+                    } else {
+                        a0 = hi2_at<0>(nib64(W0[m], 0), u0); a2 = hi2_at<1>(nib64(W0[m], 1), u0);
+                        a1 = hi2_at<0>(nib64(W1[m], 0), u1); a3 = hi2_at<1>(nib64(W1[m], 1), u1);
+                    }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const uint2 bq = qb2[((nt * KS + bk * 8 + jj) * 8 + g) * 4 + tq];
@@ -517,27 +528,43 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                 bp[nt] = pb2[((pv * 8 + kk) * NT + nt) * 32 + lane];
                 if (ring) mma16816(a1s[nt], ONE2, ONE2, ONE2, ONE2, bp[nt].x, bp[nt].y);
             }
+            // tq6_0 values: this warp decodes VROWS positions x its D/8 channels per fill (a full
+            // word per lane: nibble pairs and high bits in a few operations) into its buffer, and
+            // ldmatrix.trans reads the A fragments of V^T back (rows hold channels 0,4,1,5,2,6,3,7)
+            uint32_t ar[MT][4];
+            if (ring) {
+                constexpr int WPP = Gm::WPP, VROWS = Gm::VROWS, VRS = Gm::VRS, NF = 16 / Gm::VROWS;
+                uint8_t* vb = vbuf + warp * Gm::VB_BYTES;
+                const int prow = lane / WPP, qd = lane % WPP;
+                const int cw = warp * Gm::CPW + 8 * qd;
+                const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+                for (int f = 0; f < NF; ++f) {
+                    const uint8_t* rowp = vr + (16 * kk + VROWS * f + prow) * CLD + 96 * (cw >> 7);
+                    const uint32_t wq = *reinterpret_cast<const uint32_t*>(rowp + ((cw & 127) >> 1));
+                    const uint32_t u = hi2_spread(*reinterpret_cast<const uint16_t*>(rowp + 64 + ((cw & 127) >> 2)));
+                    *reinterpret_cast<uint4*>(vb + prow * VRS + 16 * qd) =
+                        make_uint4(hi2_at<0>(nib64(wq, 0), u), hi2_at<1>(nib64(wq, 1), u), hi2_at<2>(nib64(wq, 2), u),
+                                   hi2_at<3>(nib64(wq, 3), u));
+                    __syncwarp();
+                    uint32_t r0, r1, r2, r3;
+                    if (VROWS == 8) {   // 8 positions, chunks 0..3 of 8 channels: m-tile chunk pairs
+                        ldsm_x4_t(su32(vb + rr * VRS + 16 * mi), r0, r1, r2, r3);
+                        ar[0][2 * f] = r0; ar[0][2 * f + 1] = r1;
+                        ar[MT - 1][2 * f] = r2; ar[MT - 1][2 * f + 1] = r3;
+                    } else {            // 16 positions, 16 channels: the four 8 x 8 tiles of one m-tile
+                        ldsm_x4_t(su32(vb + (8 * (mi >> 1) + rr) * VRS + 16 * (mi & 1)), r0, r1, r2, r3);
+                        ar[0][0] = r0; ar[0][1] = r1; ar[0][2] = r2; ar[0][3] = r3;
+                    }
+                    __syncwarp();
+                }
+            }
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 const int c0 = warp * (D / 8) + 16 * mt;
                 uint32_t a0, a1, a2, a3;
                 if (ring) {
-                    // 8 x 8 tiles (positions x channels) decoded in A-fragment order, then transposed
-                    const int pa = 16 * kk + g, pb = pa + 8;
-                    // channels c0..c0+15 (c0 a multiple of 16): one 8-byte ql load and one qh word per row
-                    const uint8_t* ra = vr + pa * CLD + 96 * (c0 >> 7);
-                    const uint8_t* rb = vr + pb * CLD + 96 * (c0 >> 7);
-                    const int qa = (c0 & 127) >> 1, ha = 64 + ((c0 & 127) >> 4) * 4;
-                    const int ya = tq, ya1 = 8 + tq;
-                    const uint2 wa = *reinterpret_cast<const uint2*>(ra + qa);
-                    const uint2 wb = *reinterpret_cast<const uint2*>(rb + qa);
-                    const uint32_t xa0 = *reinterpret_cast<const uint32_t*>(ra + ha), xa1 = xa0;
-                    const uint32_t xb0 = *reinterpret_cast<const uint32_t*>(rb + ha), xb1 = xb0;
-                    const uint32_t wa0 = wa.x, wa1 = wa.y, wb0 = wb.x, wb1 = wb.y;
-                    a0 = movtrans(add_hi2(nib64_rt(wa0, tq), xa0, ya));
-                    a1 = movtrans(add_hi2(nib64_rt(wa1, tq), xa1, ya1));
-                    a2 = movtrans(add_hi2(nib64_rt(wb0, tq), xb0, ya));
-                    a3 = movtrans(add_hi2(nib64_rt(wb1, tq), xb1, ya1));
+                    a0 = ar[mt][0]; a1 = ar[mt][1]; a2 = ar[mt][2]; a3 = ar[mt][3];
                 } else {
                     const int mi = lane >> 3, rr = lane & 7;
                     const int pos = 16 * kk + 8 * (mi >> 1) + rr, ch = c0 + 8 * (mi & 1);
@@ -615,8 +642,9 @@ template <int D, int NQ>
 int launch_region_t(const Layout& L, const AttnParams& p, cudaStream_t st) {
     using Gm = RGeo<D, NQ>;
     auto kern = decode_region_kernel<D, NQ>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Gm::SMEM);
-    kern<<<p.n_region_items, kBodyThreads, Gm::SMEM, st>>>(L, p);
+    const int smem = Gm::smem(L.tail_fmt == KVQ_BF16 || L.journal == KVQ_BF16);
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kern<<<p.n_region_items, kBodyThreads, smem, st>>>(L, p);
     return (int)cudaGetLastError();
 }
 
