@@ -42,9 +42,12 @@ struct RGeo {
     static constexpr int RUNF = (16384 / D < 128) ? 16384 / D : 128;    // fp16 rows per run (64 KB stage)
     static constexpr int F_HALF = RUNF * FLD;
     static constexpr int F_STAGE = 2 * F_HALF;
-    static constexpr int AREA = (2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE;
+    // head_dim 512 takes 16-bit rows only (no tq6_0 ring; the host routes rings at 512 to the
+    // generic kernel), so its staging area is one 64 KB fp16 stage
+    static constexpr bool RING = D <= 256;
+    static constexpr int AREA = !RING ? F_STAGE : ((2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE);
     static constexpr int QB_BYTES = NT * KS * 256;                      // one fragment set
-    static constexpr int PC = NB > 2 ? NB : 2;                          // P' copies (bf16 rows: hi, lo)
+    static constexpr int PC = (RING && NB > 2) ? NB : 2;                // P' copies (bf16 rows: hi, lo)
     static constexpr int P_BYTES = PC * 8 * NT * 256;
     static constexpr int RED_FLOATS = 2 * NQ * 8 + 2 * NQ;
     // tq6_0 values: per-warp buffer of decoded rows (ROWS positions x the warp's D/8 channels,
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     const int kind = sp.kind[r];
     const int t0 = sp.lo[r] + cidx * p.chunk;
     const int t1 = min(t0 + p.chunk, sp.hi[r]);
-    const bool ring = (kind == RK_RING);
+    const bool ring = Gm::RING && (kind == RK_RING);
     // bf16 exact rows: bf16 mma, the query and P' each split into bf16 high and low parts
     const bool bf = !ring && kind != RK_SINK && ((kind == RK_TAIL ? L.tail_fmt : L.journal) == KVQ_BF16);
     const int RUN = ring ? 128 : Gm::RUNF;                // positions per run
@@ -117,6 +120,10 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     const uint32_t stage_bytes = ring ? Gm::TQ_STAGE : Gm::F_STAGE;
     const uint32_t half_bytes = ring ? Gm::TQ_HALF : Gm::F_HALF;
     const int nst = min(4, Gm::AREA / (int)stage_bytes);
+    if (nst < 1 || (!Gm::RING && kind == RK_RING)) {   // a ring at head_dim 512 is not routed here: refuse
+        if (threadIdx.x == 0) atomicOr(status_word(L, p.pool), 4u);
+        return;
+    }
     uint8_t* stages = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
     uint64_t* empty = full + 4;
@@ -654,10 +661,11 @@ int upload_tables_region(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-// 1 when the streaming region kernel takes this layout's region items: head_dim 128 or 256,
-// the ring (when present) in runs of whole 128-slot chunks.
+// 1 when the streaming region kernel takes this layout's region items: head_dim 128 or 256
+// (the ring, when present, in runs of whole 128-slot chunks), or 512 with 16-bit rows only.
 int region_kernel_ok(const Layout& L) {
-    if (L.D != 128 && L.D != 256) return 0;
+    if (L.D != 128 && L.D != 256 && L.D != 512) return 0;
+    if (L.D == 512 && L.journal == KVQ_TQ6_0) return 0;
     if (L.journal == KVQ_TQ6_0 && L.R % 128 != 0) return 0;
     return 1;
 }
@@ -668,9 +676,11 @@ int launch_decode_region(const Layout& L, const AttnParams& p, void* stream) {
     if (L.NQ == 8) {
         if (L.D == 128) return launch_region_t<128, 8>(L, p, s);
         if (L.D == 256) return launch_region_t<256, 8>(L, p, s);
+        if (L.D == 512) return launch_region_t<512, 8>(L, p, s);
     } else {
         if (L.D == 128) return launch_region_t<128, 16>(L, p, s);
         if (L.D == 256) return launch_region_t<256, 16>(L, p, s);
+        if (L.D == 512) return launch_region_t<512, 16>(L, p, s);
     }
     return (int)cudaErrorInvalidValue;
 }
