@@ -43,9 +43,9 @@ struct RGeo {
     static constexpr int F_HALF = RUNF * FLD;
     static constexpr int F_STAGE = 2 * F_HALF;
     // head_dim 512 takes 16-bit rows only (no tq6_0 ring; the host routes rings at 512 to the
-    // generic kernel), so its staging area is one 64 KB fp16 stage
+    // generic kernel); its staging area is two 64 KB fp16 stages (one CTA per SM)
     static constexpr bool RING = D <= 256;
-    static constexpr int AREA = !RING ? F_STAGE : ((2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE);
+    static constexpr int AREA = !RING ? 2 * F_STAGE : ((2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE);
     static constexpr int QB_BYTES = NT * KS * 256;                      // one fragment set
     static constexpr int PC = (RING && NB > 2) ? NB : 2;                // P' copies (bf16 rows: hi, lo)
     static constexpr int P_BYTES = PC * 8 * NT * 256;
