@@ -286,7 +286,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
                      "traffic": MEASURED_TRAFFIC.get(w.name),
-                     "kernel": "one kv_decode_attn call: decode_region_kernel beside decode_body_kernel, then "
+                     "kernel": "one kv_decode_attn call: decode_attn_kernel (body and region items), then "
                                "decode_merge_kernel (timed by events on the calling stream)",
                      "peak_source": f"{peak_src} hbm_gbs",
                      "launches_timed": len(attn_times),

@@ -27,7 +27,6 @@ UNITS = {
     "kernels_codec.cu": ["-fmad=false"],
     "kernels_attn.cu": [],
     "kernels_body.cu": [],
-    "kernels_region.cu": [],
     "synth.cu": [],
 }
 

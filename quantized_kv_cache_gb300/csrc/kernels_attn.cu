@@ -593,8 +593,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
 }
 
 template <int D, int NQ>
-int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaStream_t aux, cudaEvent_t evf,
-                    cudaEvent_t evj) {
+int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
     using C = Cfg<D, NQ>;
     static bool attr = false;
     if (!attr) {
@@ -602,32 +601,20 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, cudaSt
         attr = true;
     }
     const int n_body = p.total_items - p.n_region_items;
-    // the streaming region kernel takes the region items when the body kernel takes the body
-    // (so no body positions are among them) and the layout is one it covers. With body work too,
-    // the body kernel is launched first (its items are the long ones) and the region kernel runs
-    // beside it on the auxiliary stream, which joins the caller's stream before the merge.
-    const bool streaming = p.n_region_items > 0 && region_kernel_ok(L) && body_ctas_per_sm(L) > 0;
-    const bool fork = streaming && aux && evf && evj && n_body > 0;
-    if (fork) {
-        if (cudaEventRecord(evf, s) != cudaSuccess || cudaStreamWaitEvent(aux, evf, 0) != cudaSuccess)
-            return (int)cudaGetLastError();
+    // the streaming decode kernel takes the body items (when it has an instance for the layout)
+    // and, where it covers the layout, the region items too, in one launch; otherwise the region
+    // items go through the generic kernel
+    const bool streaming = body_ctas_per_sm(L) > 0;
+    const bool fused_regions = streaming && region_kernel_ok(L);
+    if (streaming) {
+        const int e = launch_decode_fused(L, p, n_body, fused_regions ? p.n_region_items : 0, s);
+        if (e != 0) return e;
     }
-    int eb = 0, er = 0;
-    if (n_body > 0) eb = launch_decode_body(L, p, n_body, s);
-    if (p.n_region_items > 0) {
-        if (streaming) {
-            er = launch_decode_region(L, p, fork ? aux : s);
-        } else {
-            decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
-            er = (int)cudaGetLastError();
-        }
+    if (p.n_region_items > 0 && !fused_regions) {
+        decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return (int)e;
     }
-    if (fork) {
-        cudaEventRecord(evj, aux);
-        cudaStreamWaitEvent(s, evj, 0);
-    }
-    if (eb != 0) return eb;
-    if (er != 0) return er;
     int max_cnt = 0;
     for (int i = 0; i < p.n_seq; ++i)
         max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
@@ -646,18 +633,17 @@ int upload_tables_attn(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-int launch_decode(const Layout& L, const AttnParams& p, void* stream, void* aux, void* ev_fork, void* ev_join) {
+int launch_decode(const Layout& L, const AttnParams& p, void* stream) {
     if (p.total_items == 0) return 0;
-    cudaStream_t s = (cudaStream_t)stream, a = (cudaStream_t)aux;
-    cudaEvent_t f = (cudaEvent_t)ev_fork, j = (cudaEvent_t)ev_join;
+    cudaStream_t s = (cudaStream_t)stream;
     if (L.NQ == 8) {
-        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s, a, f, j);
-        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s, a, f, j);
-        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s, a, f, j);
+        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s);
+        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s);
+        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s);
     } else {
-        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s, a, f, j);
-        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s, a, f, j);
-        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s, a, f, j);
+        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s);
+        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s);
+        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s);
     }
     return (int)cudaErrorInvalidValue;
 }

@@ -25,6 +25,7 @@
 // The partial (m, l, o) is rotated back to the original domain and merged with the region
 // partials by decode_merge_kernel (kernels_attn.cu).
 #include "stream_common.cuh"
+#include "region_item.cuh"
 
 namespace kvq {
 namespace {
@@ -59,6 +60,7 @@ struct Geo {
     static constexpr int STAGE = (V_OFF + REC_V + 127) & ~127;
     static constexpr int QB_BYTES = NT * KS * 256;                      // query fragments (= NQ D fp16)
     static constexpr int P_BYTES = NVB * 8 * NT * 256;                  // P' fragments
+    static_assert(P_BYTES >= 2 * D, "the P' area stages the codes of a fused append");
     static constexpr int RED_FLOATS = (NVB + 2) * NQ * 8 + NQ;          // [q][warp] exchange rows, m, l
     static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QB_BYTES + P_BYTES + RED_FLOATS * 4;
     // resident CTAs per SM: three when two stages fit in a third of shared memory, else two,
@@ -100,17 +102,16 @@ __device__ __forceinline__ void load_row_f(const uint16_t* row, float (&f)[N]) {
     }
 }
 
-// ------------------------------------------------------------------------------ the kernel
+// ------------------------------------------------------------------------------ a body item
+// One body work item (partial index `item`: body items follow the region items), run by a CTA
+// of 8 warps on the dynamic shared memory `smem` with nst stages; s_abort is the CTA's abort flag.
 template <int D, int NQ, int KF, int VF, int KB, int VB>
-__global__ void __launch_bounds__(kCT, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
-decode_body_kernel(Layout L, AttnParams p, int nst) {
+__device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, const int item, const int nst,
+                                          uint8_t* smem, int& s_abort) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     constexpr int NT = Gm::NT, KS = Gm::KS, NBK = Gm::NBK, KSPB = Gm::KSPB, WK = Gm::WK;
     constexpr int NVB = Gm::NVB, WV = Gm::WV, MT = Gm::MT, TPT = Gm::TPT;
-    extern __shared__ __align__(128) uint8_t smem[];
 
-    // ---- work item: body items follow the region items
-    const int item = p.n_region_items + (int)blockIdx.x;
     int b = 0;
     while (b + 1 < p.n_seq && p.seq[b + 1].body_first <= item) ++b;
     const SeqSpan& sp = p.seq[b];
@@ -136,7 +137,6 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
     float* zsm = red + NQ * 8;                            // [NVB][NQ][warp] value zero-point sums
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ int s_abort;
     // thread 0 streams the records: group i into stage i % nst, issued once stage i % nst is
     // free (the first barrier of group i - nst + 1 follows every read of group i - nst)
     const uint8_t* kb = body_rec(L, p.pool, 0, unit, g0);
@@ -157,6 +157,15 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
         for (; issued < min(nst, ngroups); ++issued) issue(issued);
     }
     __syncthreads();
+    if (p.knew != nullptr && kb_ == 0) {
+        // fused decode step: the head's first body item appends the newest position (threads
+        // 0-127 the K row, 128-255 the V row; codes staged in the P' area, unused yet) while its
+        // first records are in flight. No item of this launch reads the slots written (the region
+        // item that holds the newest position reads its row from the input).
+        const int w = threadIdx.x >> 7;
+        append_newest(L, p.pool, unit, w, sp.n_tok - 1, (w ? p.vnew : p.knew) + ((int64_t)b * L.H + h) * D,
+                      threadIdx.x & 127, reinterpret_cast<uint8_t*>(pbuf) + w * D);
+    }
 
     // ================================================================== consumers: set-up
     const int g = lane >> 2, tq = lane & 3;
@@ -766,6 +775,20 @@ decode_body_kernel(Layout L, AttnParams p, int nst) {
                          p.partials + (size_t)item * (2 * NQ + NQ * D), L.rot);
 }
 
+// ------------------------------------------------------------------------------ the kernel
+// Decode attention over one call's work list: CTAs [0, n_body) take the body items (the long
+// ones, so they start first), the rest the region items (tq6_0 ring, 16-bit rows).
+template <int D, int NQ, int KF, int VF, int KB, int VB>
+__global__ void __launch_bounds__(kCT, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
+decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ AttnParams p, int n_body, int nst) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ int s_abort;
+    if ((int)blockIdx.x < n_body)
+        body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
+    else
+        region_item<D, NQ>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
+}
+
 // ------------------------------------------------------------------------------ launch
 template <int D, int NQ, int KF, int VF, int KB, int VB>
 int nstages(const Layout& L) {
@@ -781,15 +804,19 @@ int nstages(const Layout& L) {
 }
 
 template <int D, int NQ, int KF, int VF, int KB, int VB>
-int launch_t(const Layout& L, const AttnParams& p, int n_body, cudaStream_t st) {
+int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cudaStream_t st) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
     if (nst == 0) return (int)cudaErrorInvalidConfiguration;
-    const size_t smem = (size_t)nst * Gm::STAGE + Gm::FIXED;
-    auto kern = decode_body_kernel<D, NQ, KF, VF, KB, VB>;
+    size_t smem = (size_t)nst * Gm::STAGE + Gm::FIXED;
+    if (n_region > 0) {
+        const size_t sr = (size_t)RGeo<D, NQ>::smem(L.tail_fmt == KVQ_BF16 || L.journal == KVQ_BF16);
+        smem = smem > sr ? smem : sr;
+    }
+    auto kern = decode_attn_kernel<D, NQ, KF, VF, KB, VB>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    kern<<<n_body, kCT, smem, st>>>(L, p, nst);
+    kern<<<n_body + n_region, kCT, smem, st>>>(L, p, n_body, nst);
     return (int)cudaGetLastError();
 }
 
@@ -815,16 +842,28 @@ int dispatch(const Layout& L, F&& f) {
 
 struct CtasFn {
     const Layout& L;
+    bool regions;
     template <int D, int NQ, int KF, int VF, int KB, int VB>
-    int run() { return nstages<D, NQ, KF, VF, KB, VB>(L) > 0 ? Geo<D, NQ, KF, VF, KB, VB>::MINB : 0; }
+    int run() {
+        using Gm = Geo<D, NQ, KF, VF, KB, VB>;
+        const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
+        if (nst == 0) return 0;
+        if (!regions) return Gm::MINB;
+        // the SM's 228 KB less 1 KB per CTA, shared by CTAs of the larger of the two footprints
+        size_t smem = (size_t)nst * Gm::STAGE + Gm::FIXED;
+        const size_t sr = (size_t)RGeo<D, NQ>::smem(L.tail_fmt == KVQ_BF16 || L.journal == KVQ_BF16);
+        smem = smem > sr ? smem : sr;
+        const int by_smem = (int)((228 * 1024) / (smem + 1024));
+        return by_smem < Gm::MINB ? by_smem : Gm::MINB;
+    }
 };
 struct LaunchFn {
     const Layout& L;
     const AttnParams& p;
-    int n;
+    int n_body, n_region;
     cudaStream_t s;
     template <int D, int NQ, int KF, int VF, int KB, int VB>
-    int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n, s); }
+    int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n_body, n_region, s); }
 };
 
 }  // namespace
@@ -833,17 +872,33 @@ int upload_tables_body(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-// Resident body-kernel CTAs per SM for this layout (1 or 2), 0 when no instance fits it.
+// Resident decode-kernel CTAs per SM for this layout (1 to 3), 0 when no instance fits it.
 int body_ctas_per_sm(const Layout& L) {
-    CtasFn f{L};
+    CtasFn f{L, false};
     const int r = dispatch(L, f);
     return r > 0 ? r : 0;
 }
 
-// Launches the body kernel over the body items (those after the region items of p).
-int launch_decode_body(const Layout& L, const AttnParams& p, int n_body, void* stream) {
-    if (n_body <= 0) return 0;
-    LaunchFn f{L, p, n_body, (cudaStream_t)stream};
+// Resident CTAs per SM of the decode kernel when it also takes the region items.
+int decode_ctas_per_sm(const Layout& L) {
+    CtasFn f{L, true};
+    const int r = dispatch(L, f);
+    return r > 0 ? r : 0;
+}
+
+// 1 when the streaming kernel takes this layout's region items: head_dim 128 or 256 (the ring,
+// when present, in runs of whole 128-slot chunks), or 512 with 16-bit rows only.
+int region_kernel_ok(const Layout& L) {
+    if (L.D != 128 && L.D != 256 && L.D != 512) return 0;
+    if (L.D == 512 && L.journal == KVQ_TQ6_0) return 0;
+    if (L.journal == KVQ_TQ6_0 && L.R % 128 != 0) return 0;
+    return 1;
+}
+
+// Launches the decode kernel over the body items and the first n_region region items of p.
+int launch_decode_fused(const Layout& L, const AttnParams& p, int n_body, int n_region, void* stream) {
+    if (n_body + n_region <= 0) return 0;
+    LaunchFn f{L, p, n_body, n_region, (cudaStream_t)stream};
     const int r = dispatch(L, f);
     return r < 0 ? (int)cudaErrorInvalidValue : r;
 }

@@ -6,24 +6,13 @@
 // multiply-add is contracted and records are reproducible bit for bit: one IEEE fp32
 // rounding per operation, halving-tree sums, round-half-even rint and fp16/bf16 casts.
 #include <cuda_runtime.h>
-#include "device_common.cuh"
+#include "append_row.cuh"
 
 namespace kvq {
 namespace {
 
-constexpr float kTbqScale = 0.0883883461356163f;   // fp32(1/sqrt(128)) = 0x3DB504F3
-constexpr float kHad256Scale = 0.0625f;             // 1/16, exact
-constexpr unsigned kFull = 0xffffffffu;
+using namespace codec;
 
-__device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
-__device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
-__device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
-__device__ __forceinline__ float fdiv(float a, float b) { return __fdiv_rn(a, b); }
-
-__device__ __forceinline__ float warp_max(float v) {
-    for (int s = 16; s >= 1; s >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, s));
-    return v;
-}
 __device__ __forceinline__ float warp_min(float v) {
     for (int s = 16; s >= 1; s >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, s));
     return v;
@@ -67,30 +56,6 @@ __device__ void block_rotate(float* xs, int D, int rot) {
             xs[i] = fmul(y, kTbqScale);
         }
         __syncthreads();
-    }
-}
-
-// In-warp FWHT of a block of 32 * NK values, value index i = lane + 32 k held in v[k].
-template <int NK>
-__device__ __forceinline__ void warp_fwht(float (&v)[NK], int lane) {
-#pragma unroll
-    for (int s = 1; s < 32; s <<= 1) {
-        const bool upper = lane & s;
-#pragma unroll
-        for (int k = 0; k < NK; ++k) {
-            const float p = __shfl_xor_sync(kFull, v[k], s);
-            v[k] = upper ? fsub(p, v[k]) : fadd(v[k], p);
-        }
-    }
-#pragma unroll
-    for (int m = 1; m < NK; m <<= 1) {
-#pragma unroll
-        for (int k = 0; k < NK; ++k) {
-            if (k & m) continue;
-            const float a = v[k], b = v[k + m];
-            v[k] = fadd(a, b);
-            v[k + m] = fsub(a, b);
-        }
     }
 }
 
@@ -158,103 +123,18 @@ __device__ __forceinline__ void load_journal_row(const Layout& L, const void* po
     }
 }
 
-// One tq6_0 block (values lane + 32 m, m = 0..3, taken from v[k0 + m]) of a journal slot:
-// scale, codes through shared memory, then the ql / qh planes.
-template <int NK>
-__device__ __forceinline__ void tq6_block(const float (&v)[NK], int k0, int blk, int lane, uint8_t* cs, uint8_t* row,
-                                          uint16_t* sc) {
-    float a = 0.f;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) a = fmaxf(a, fabsf(v[k0 + m]));
-    a = warp_max(a);
-    const uint16_t d16 = f2h_bits(fdiv(a, 31.0f));
-    const float d = h2f(d16);
-    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        float q = (d == 0.f) ? 0.f : rintf(fmul(v[k0 + m], inv));
-        q = fminf(fmaxf(q, -31.f), 31.f);
-        cs[128 * blk + lane + 32 * m] = (uint8_t)((int)q + 32);
-    }
-    __syncwarp();
-    const uint8_t* c = cs + 128 * blk;
-    uint8_t* out = row + 96 * blk;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int j = lane + 32 * r;
-        out[j] = (uint8_t)((c[2 * j] & 15) | ((c[2 * j + 1] & 15) << 4));
-    }
-    out[64 + lane] = (uint8_t)((c[4 * lane] >> 4) | ((c[4 * lane + 1] >> 4) << 2) | ((c[4 * lane + 2] >> 4) << 4) |
-                               ((c[4 * lane + 3] >> 4) << 6));
-    if (lane == 0) sc[blk] = d16;
-}
-
 // ---------------------------------------------------------------------------- append
 // grid (n_seq * n_tok, H, 2), block D / 4 threads (one warp per 128 values); dynamic smem D bytes.
 __global__ void append_kernel(Layout L, AppendParams p) {
+    extern __shared__ uint8_t cs[];                   // D codes
     const int b = blockIdx.x / p.n_tok, t = blockIdx.x % p.n_tok;
     const int h = blockIdx.y, w = blockIdx.z, D = L.D;
     const int pos = p.n0[b] + t;
-    const int64_t unit = L.unit(p.layer, p.slot[b], h);
     const uint16_t* src = (w ? p.v : p.k) + (((int64_t)b * p.n_tok + t) * L.H + h) * D;
-    if (pos < kSink) {
-        uint16_t* dst = sink_row(L, p.pool, w, unit, pos);
-        for (int i = threadIdx.x; i < D; i += blockDim.x) dst[i] = src[i];
-        return;
-    }
-    const int slot = journal_slot(L, pos);
-    if (L.journal != KVQ_TQ6_0) {
-        uint16_t* dst = jexact_row(L, p.pool, w, unit, slot);
-        for (int i = threadIdx.x; i < D; i += blockDim.x)
-            dst[i] = (L.journal == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
-        return;
-    }
-    // Exact tail copy. Positions of one append that share a tail slot (pos mod T) would
-    // race; only the newest T positions of the append write it.
-    if (pos + L.T >= p.n0[b] + p.n_tok) {
-        uint16_t* tl = tail_row(L, p.pool, w, unit, pos % L.T);
-        for (int i = threadIdx.x; i < D; i += blockDim.x)
-            tl[i] = (L.tail_fmt == KVQ_BF16) ? f2bf_bits(h2f(src[i])) : src[i];
-    }
-
-    // rotation: one warp per rotation block (256 values for HAD256, else 128), value
-    // i = lane + 32 k of the block in v[k]; the butterflies, signs and scale are those of the
-    // block-wide rotation, in the same order
-    extern __shared__ uint8_t cs[];                   // D codes
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    uint8_t* row = jcode_row(L, p.pool, w, unit, slot);
-    uint16_t* sc = jscale_row(L, p.pool, w, unit, slot);
-    if (L.rot == ROT_HAD256) {
-        for (int u = warp; u < D / 256; u += nw) {
-            float v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = h2f(src[256 * u + lane + 32 * k]);
-            warp_fwht<8>(v, lane);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
-            tq6_block(v, 0, 2 * u, lane, cs, row, sc);
-            tq6_block(v, 4, 2 * u + 1, lane, cs, row, sc);
-        }
-    } else {
-        for (int u = warp; u < D / 128; u += nw) {
-            float v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = h2f(src[128 * u + lane + 32 * k]);
-            if (L.rot == ROT_TBQ128) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    if (sign_neg(0, lane + 32 * k)) v[k] = -v[k];
-                warp_fwht<4>(v, lane);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float y = v[k];
-                    if (sign_neg(1, lane + 32 * k)) y = -y;
-                    v[k] = fmul(y, kTbqScale);
-                }
-            }
-            tq6_block(v, 0, u, lane, cs, row, sc);
-        }
-    }
+    // positions of one append that share a tail slot (pos mod T) would race: only the newest T
+    // positions of the append write it
+    append_row(L, p.pool, L.unit(p.layer, p.slot[b], h), w, pos, src, pos + L.T >= p.n0[b] + p.n_tok,
+               (int)threadIdx.x, (int)blockDim.x, cs);
 }
 
 // ---------------------------------------------------------------------------- seal task

@@ -23,10 +23,6 @@ struct kvq_cache {
     int sm_count;
     std::vector<int64_t> n_tok;   // [L][max_seqs]
     std::vector<int64_t> sealed;  // [L][max_seqs]
-    // decode attention runs its region kernel on `aux`, forked from and joined back into the
-    // caller's stream through the two events (so it overlaps the body kernel)
-    cudaStream_t aux = nullptr;
-    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace kvq {
@@ -103,9 +99,7 @@ kvq_status ensure_tables(int device) {
     std::lock_guard<std::mutex> lk(g_tab_mu);
     if (g_tab_devices.count(device)) return KVQ_OK;
     const FormatTables& t = host_tables();
-    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0 ||
-        upload_tables_region(t) != 0)
-        return KVQ_ECUDA;
+    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0) return KVQ_ECUDA;
     g_tab_devices.insert(device);
     return KVQ_OK;
 }
@@ -212,19 +206,7 @@ kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes
     if (cudaMemset(device_pool, 0, 256) != cudaSuccess) return KVQ_ECUDA;
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return KVQ_ECUDA;
-    cudaStream_t aux = nullptr;
-    cudaEvent_t evf = nullptr, evj = nullptr;
-    if (cudaStreamCreateWithFlags(&aux, cudaStreamNonBlocking) != cudaSuccess) return KVQ_ECUDA;
-    if (cudaEventCreateWithFlags(&evf, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&evj, cudaEventDisableTiming) != cudaSuccess) {
-        if (evf) cudaEventDestroy(evf);
-        cudaStreamDestroy(aux);
-        return KVQ_ECUDA;
-    }
     kvq_cache* c = new kvq_cache;
-    c->aux = aux;
-    c->ev_fork = evf;
-    c->ev_join = evj;
     c->cfg = *cfg;
     c->lay = L;
     c->pool = device_pool;
@@ -239,10 +221,6 @@ kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes
 
 kvq_status kv_destroy(kvq_cache* c) {
     if (!c) return KVQ_EINVAL;
-    if (c->aux) cudaStreamSynchronize(c->aux);
-    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
-    if (c->ev_join) cudaEventDestroy(c->ev_join);
-    if (c->aux) cudaStreamDestroy(c->aux);
     delete c;
     return KVQ_OK;
 }
@@ -345,8 +323,12 @@ kvq_status kv_seal(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, i
     return KVQ_OK;
 }
 
-kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
-                          void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+// Decode attention of one layer; with knew / vnew (the newest position's rows, fp16, already
+// counted in N) the decode kernel also appends them (the fused decode step).
+kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
+                       void* workspace, size_t ws_bytes, const void* knew, const void* vnew, void* stream) {
     kvq_status st = check_cache(c);
     if (st != KVQ_OK) return st;
     if (layer < 0 || layer >= c->cfg.n_layers || !q || !out || !workspace) return KVQ_EINVAL;
@@ -362,35 +344,40 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     p.q = (const uint16_t*)q;
     p.out = (uint16_t*)out;
     p.partials = (float*)workspace;
+    p.knew = (const uint16_t*)knew;
+    p.vnew = (const uint16_t*)vnew;
     p.layer = layer;
     p.n_seq = n_seq;
     const bool body_kernel = body_ctas_per_sm(L) > 0;
+    const bool fused = body_kernel && region_kernel_ok(L);
     int64_t region_tok = 0, body_groups = 0;
     for (int i = 0; i < n_seq; ++i) {
-        const int64_t N = NT(c, layer, seq_ids[i]);
+        SeqSpan& s = p.seq[i];
+        s.slot = seq_ids[i];
+        const int64_t N = NT(c, layer, s.slot);
         if (N <= 0) return KVQ_EINVAL;
-        const int64_t S = ST(c, layer, seq_ids[i]);
+        const int64_t S = ST(c, layer, s.slot);
+        s.n_tok = (int32_t)N;
+        s.body_groups = body_kernel ? (int32_t)((S - kSink) / kGroup) : 0;
+        spans(L, N, S, s.lo, s.hi, s.kind, !body_kernel);
         region_tok += body_kernel ? N - (S - kSink) : N;
-        body_groups += body_kernel ? (S - kSink) / kGroup : 0;
+        body_groups += s.body_groups;
     }
-    // region items: chunks (multiples of 128) giving about two waves of the region kernel;
-    // body items: runs of groups giving about one wave of resident body-kernel CTAs
+    // Work items. Body items split each (sequence, head)'s groups evenly, in number proportional
+    // to its groups, one wave of resident CTAs in all: they start first and carry most of the
+    // bytes. Region items are chunks (multiples of 128 positions) of each span, about two waves'
+    // worth, taken up as body items finish. (One common wave sized by estimated cost measured
+    // slower: 16-bit rows cost 3 to 5 times a sealed group per position, and the minimum of one
+    // item per span makes the region items too coarse.)
     const int per_sm = (L.D == 512) ? 1 : (L.D == 256 ? 2 : 4);
     const int64_t target = (int64_t)c->sm_count * per_sm;
     int64_t chunk = (region_tok * L.H + target - 1) / target;
     chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
-    // body items: per (sequence, head), a number of items proportional to its groups, in all
-    // at most the resident body-kernel CTAs (one wave, no tail); groups split evenly
-    const int body_slots = std::max(1, body_ctas_per_sm(L)) * c->sm_count;
-    int64_t slots_per_head = std::max<int64_t>(1, body_slots / L.H);
+    int64_t body_items = (int64_t)std::max(1, fused ? decode_ctas_per_sm(L) : body_ctas_per_sm(L)) * c->sm_count;
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
-            s.slot = seq_ids[i];
-            s.n_tok = (int32_t)NT(c, layer, s.slot);
-            const int64_t S = ST(c, layer, s.slot);
-            spans(L, s.n_tok, S, s.lo, s.hi, s.kind, !body_kernel);
             s.items_per_head = 0;
             for (int r = 0; r < 4; ++r) {
                 s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + chunk - 1) / chunk);
@@ -400,12 +387,33 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
             items += (int64_t)s.items_per_head * L.H;
         }
         const int64_t n_region = items;
+        // body items per head: largest remainders of body_items / H x groups / all groups
+        const int64_t per_head = std::max<int64_t>(1, body_items / L.H);
+        int64_t given = 0;
+        double rem[kMaxSeqPerCall];
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
-            s.body_groups = body_kernel ? (int32_t)((ST(c, layer, s.slot) - kSink) / kGroup) : 0;
-            int64_t nb = s.body_groups > 0 ? slots_per_head * s.body_groups / std::max<int64_t>(1, body_groups) : 0;
-            if (s.body_groups > 0) nb = std::min<int64_t>(std::max<int64_t>(nb, 1), s.body_groups);
-            s.body_per_head = (int32_t)nb;
+            s.body_per_head = 0;
+            rem[i] = -1.0;
+            if (s.body_groups <= 0) continue;
+            const double share = (double)per_head * s.body_groups / (double)std::max<int64_t>(1, body_groups);
+            s.body_per_head = (int32_t)std::max<int64_t>(1, (int64_t)share);
+            rem[i] = share - (double)s.body_per_head;
+            given += s.body_per_head;
+        }
+        while (given < per_head) {
+            int best = -1;
+            for (int i = 0; i < n_seq; ++i)
+                if (rem[i] > -0.5 && p.seq[i].body_per_head < p.seq[i].body_groups && (best < 0 || rem[i] > rem[best]))
+                    best = i;
+            if (best < 0) break;
+            ++p.seq[best].body_per_head;
+            rem[best] = -1.0;
+            ++given;
+        }
+        for (int i = 0; i < n_seq; ++i) {
+            SeqSpan& s = p.seq[i];
+            s.body_per_head = std::min(s.body_per_head, s.body_groups);
             s.body_first = (int32_t)items;
             items += (int64_t)s.body_per_head * L.H;
         }
@@ -415,12 +423,31 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
             break;
         }
         chunk *= 2;
-        slots_per_head = std::max<int64_t>(1, slots_per_head / 2);
+        body_items = std::max<int64_t>(L.H, body_items / 2);
     }
     p.body_chunk = 0;
     p.chunk = (int32_t)chunk;
-    const int e = launch_decode(L, p, stream, c->aux, c->ev_fork, c->ev_join);
+    const int e = launch_decode(L, p, stream);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;
+}
+
+// 1 when the decode kernel of this layout can append the newest position itself: it takes the
+// region items, and the row that holds position N - 1 (after the append) is fp16 in every
+// sequence (the sink always; else the exact tail, or an exact journal).
+bool fused_append_ok(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq) {
+    const Layout& L = c->lay;
+    if (body_ctas_per_sm(L) <= 0 || !region_kernel_ok(L)) return false;
+    const int row_fmt = (L.journal == KVQ_TQ6_0) ? L.tail_fmt : L.journal;
+    for (int i = 0; i < n_seq; ++i)
+        if (NT(c, layer, seq_ids[i]) + 1 > kSink && row_fmt != KVQ_F16) return false;
+    return true;
+}
+
+}  // namespace
+
+kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
+                          void* workspace, size_t ws_bytes, void* stream) {
+    return decode_attn(c, layer, seq_ids, n_seq, q, out, workspace, ws_bytes, nullptr, nullptr, stream);
 }
 
 kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
@@ -434,9 +461,29 @@ kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, in
     const size_t qb = (size_t)n_seq * L.Hq * L.D * 2, kb = (size_t)n_seq * L.H * L.D * 2;
     int64_t total = 0;
     int32_t need[kMaxSeqPerCall];
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !workspace) return KVQ_EINVAL;
+    size_t ws_need = 0;
+    kv_required_bytes(&c->cfg, nullptr, &ws_need);
+    if (ws_bytes < ws_need) return KVQ_EINVAL;
     for (int l = 0; l < n_layers; ++l) {
-        st = kv_append(c, l, seq_ids, n_seq, 1, (const char*)k + l * kb, (const char*)v + l * kb, stream);
-        if (st != KVQ_OK) return st;
+        const char* kl = (const char*)k + l * kb;
+        const char* vl = (const char*)v + l * kb;
+        // the append goes into the decode kernel where it can (no separate launch); the seal,
+        // when due, reads only positions at least `keep` (>= T) behind the newest one, so it
+        // may run before that append
+        const bool fuse = fused_append_ok(c, l, seq_ids, n_seq);
+        if (fuse) {
+            for (int i = 0; i < n_seq; ++i) {
+                const int s = seq_ids[i];
+                const int64_t N = NT(c, l, s), S = ST(c, l, s);
+                if (N + 1 > c->cfg.max_ctx) return KVQ_ENOSPC;
+                if (std::max<int64_t>(N + 1, kSink) - S > c->cfg.ring_capacity) return KVQ_ENOSPC;
+            }
+            for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) += 1;
+        } else {
+            st = kv_append(c, l, seq_ids, n_seq, 1, kl, vl, stream);
+            if (st != KVQ_OK) return st;
+        }
         int nn = 0;
         for (int i = 0; i < n_seq; ++i) {
             const int s = seq_ids[i];
@@ -454,9 +501,13 @@ kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, in
         }
         if (events && cudaEventRecord((cudaEvent_t)events[2 * l], (cudaStream_t)stream) != cudaSuccess)
             return KVQ_ECUDA;
-        st = kv_decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace,
-                            ws_bytes, stream);
-        if (st != KVQ_OK) return st;
+        st = decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace, ws_bytes,
+                         fuse ? kl : nullptr, fuse ? vl : nullptr, stream);
+        if (st != KVQ_OK) {
+            if (fuse)   // the launch that was to append the position did not go out
+                for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) -= 1;
+            return st;
+        }
         if (events && cudaEventRecord((cudaEvent_t)events[2 * l + 1], (cudaStream_t)stream) != cudaSuccess)
             return KVQ_ECUDA;
     }

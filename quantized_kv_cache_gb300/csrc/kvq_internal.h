@@ -102,6 +102,10 @@ struct AttnParams {
     const uint16_t* q;       // [n_seq][Hq][D] fp16
     uint16_t* out;           // [n_seq][Hq][D] fp16
     float* partials;         // workspace: per item [2 * NQ + NQ * D] floats
+    // fused decode step: the newest position's K and V rows ([n_seq][H][D] fp16, appended by
+    // the region item that holds that position, which also reads them from here), else null
+    const uint16_t* knew;
+    const uint16_t* vnew;
     int32_t layer, n_seq, chunk, total_items;
     int32_t n_region_items;  // region items come first, body items after them
     int32_t body_chunk;      // unused (body items split each head's groups evenly)
@@ -144,15 +148,12 @@ const FormatTables& host_tables();   // derived once per process (tables.cpp)
 // Kernel launchers (kernels_*.cu). Each returns cudaError_t as int.
 int launch_append(const Layout& lay, const AppendParams& p, void* stream);
 int launch_seal(const Layout& lay, const SealParams& p, void* stream);
-// Region kernel on `aux` (forked from / joined into `stream` by the two events) when all three
-// are given, else everything on `stream`.
-int launch_decode(const Layout& lay, const AttnParams& p, void* stream, void* aux, void* ev_fork, void* ev_join);
-int launch_decode_body(const Layout& lay, const AttnParams& p, int n_body, void* stream);
+int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
+int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream);
 int upload_tables_body(const FormatTables& t);
-int upload_tables_region(const FormatTables& t);
-int body_ctas_per_sm(const Layout& lay);
-int region_kernel_ok(const Layout& lay);   // 1 if the streaming region kernel takes the region items
-int launch_decode_region(const Layout& lay, const AttnParams& p, void* stream);   // resident body-kernel CTAs per SM (0 if unsupported)
+int body_ctas_per_sm(const Layout& lay);     // resident body-item CTAs per SM (0: no instance)
+int decode_ctas_per_sm(const Layout& lay);   // the same with the region items in the kernel
+int region_kernel_ok(const Layout& lay);     // 1 if the streaming kernel takes the region items
 int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
                    int kind, int64_t p0, int64_t n, float* out, void* stream);
 int upload_tables_codec(const FormatTables& t);

@@ -2,30 +2,40 @@
 // 16-bit rows of the sink, the exact tail and an exact journal (original domain). bf16 rows use
 // the bf16 mma with the query and P' each split into bf16 high and low parts (16 significant bits).
 //
-// One CTA per region work item (sequence, KV head, run of positions inside one region), in
-// runs of up to 128 positions. Warp 8 streams each run into shared memory with cp.async.bulk:
+// One CTA of 8 warps per region work item (sequence, KV head, run of positions inside one
+// region), in runs of up to 128 positions; the fused decode kernel (kernels_body.cu) runs these
+// items after its body items. Thread 0 streams each run into shared memory with cp.async.bulk:
 // one copy per contiguous slot range of the K rows, V rows and tq6_0 scale rows (many small
-// copies per run cost far more TMA time than a few large ones). Warps 0-7 consume each run
-// like the body kernel:
+// copies per run cost far more TMA time than a few large ones). The warps consume each run like
+// the body items:
 //   1. scores: warp w takes positions [16w, 16w + 16) and all D channels. tq6_0 K rows are
 //      decoded straight into mma.sync m16n8k16 A fragments (6-bit code c: nibble in mantissa
 //      bits 4-7 and the two high bits in bits 8-9 of a half with exponent 6, i.e. 64 + c);
 //      fp16 K rows are the A fragments as they stand. Positions past the run's end score -inf.
 //   2. group maximum, p = 2^(s - m), running sums, P' = p x (tq6_0 value scale of the block);
 //      movmatrix gives the B fragments of step 3 (one 8-byte store per lane).
-//   3. values: warp w takes channels [wD/8, (w+1)D/8) (fp16 rows come in runs of 16384 / D
-//      positions at most, so a stage stays at 64 KB; warps past the run skip step 1). The rows are token-major, so the A
+//   3. values: warp w takes channels [wD/8, (w+1)D/8) (fp16 rows come in runs of 48 positions
+//      beside a ring, 32 at head_dim 512; warps past the run skip step 1). The rows are token-major, so the A
 //      fragments of V^T come from transposes: ldmatrix.trans of the fp16 rows, or of a small
 //      per-warp buffer of decoded tq6_0 rows for the ring (whose fragment rows then hold channels
 //      in the order 0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
 //      removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
 // The partial (m, l, o) of a ring item is rotated back to the original domain; the merge
 // kernel (kernels_attn.cu) combines all partials of a (sequence, KV head) under one softmax.
+#pragma once
 #include <cuda_bf16.h>
 #include "stream_common.cuh"
+#include "append_row.cuh"
 
 namespace kvq {
 namespace {
+
+// The fused decode step's append of the newest position (128 threads per row, see
+// codec::append_row), out of line: cold code kept out of the decode loops' instruction stream.
+__device__ __noinline__ void append_newest(const Layout& L, const void* pool, int64_t unit, int w, int pos,
+                                           const uint16_t* src, int tid, uint8_t* cs) {
+    codec::append_row(L, pool, unit, w, pos, src, true, tid, 128, cs);
+}
 
 template <int D, int NQ>
 struct RGeo {
@@ -39,16 +49,20 @@ struct RGeo {
     static constexpr int TQ_HALF = 128 * CLD + SC_BYTES;                // K (or V) part of a ring stage
     static constexpr int TQ_STAGE = 2 * TQ_HALF;
     static constexpr int FLD = 2 * D;                                   // fp16 row stride (dense)
-    static constexpr int RUNF = (16384 / D < 128) ? 16384 / D : 128;    // fp16 rows per run (64 KB stage)
+    // head_dim 512 takes 16-bit rows only (no tq6_0 ring; the host routes rings at 512 to the
+    // generic kernel); its staging area is two 64 KB fp16 stages (one CTA per SM). With a ring the
+    // staging area is two tq6_0 stages, and the fp16 runs are sized so that two of them fit too
+    // (thread 0 refills a stage only after the next run's first barrier: two stages at least).
+    static constexpr bool RING = D <= 256;
+    static constexpr int RUNF = !RING ? 16384 / D : (TQ_STAGE / (4 * D)) & ~15;   // fp16 rows per run
     static constexpr int F_HALF = RUNF * FLD;
     static constexpr int F_STAGE = 2 * F_HALF;
-    // head_dim 512 takes 16-bit rows only (no tq6_0 ring; the host routes rings at 512 to the
-    // generic kernel); its staging area is two 64 KB fp16 stages (one CTA per SM)
-    static constexpr bool RING = D <= 256;
-    static constexpr int AREA = !RING ? 2 * F_STAGE : ((2 * TQ_STAGE > F_STAGE) ? 2 * TQ_STAGE : F_STAGE);
+    static constexpr int AREA = !RING ? 2 * F_STAGE : 2 * TQ_STAGE;
+    static_assert(RUNF >= 16 && RUNF <= 128 && AREA >= 2 * F_STAGE, "two fp16 stages of whole k-steps");
     static constexpr int QB_BYTES = NT * KS * 256;                      // one fragment set
     static constexpr int PC = (RING && NB > 2) ? NB : 2;                // P' copies (bf16 rows: hi, lo)
     static constexpr int P_BYTES = PC * 8 * NT * 256;
+    static_assert(P_BYTES >= 2 * D, "the P' area stages the codes of a fused append");
     static constexpr int RED_FLOATS = 2 * NQ * 8 + 2 * NQ;
     // tq6_0 values: per-warp buffer of decoded rows (ROWS positions x the warp's D/8 channels,
     // fp16, padded rows) read back transposed by ldmatrix
@@ -90,15 +104,16 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
+// One region work item, run by a CTA of 8 warps on the dynamic shared memory `smem`; s_abort is
+// the CTA's abort flag (a __shared__ int).
 template <int D, int NQ>
-__global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L, AttnParams p) {
+__device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p, const int item, uint8_t* smem,
+                                            int& s_abort) {
     using Gm = RGeo<D, NQ>;
     constexpr int NT = Gm::NT, KS = Gm::KS, MT = Gm::MT, NB = Gm::NB, TPT = Gm::TPT;
     constexpr int CLD = Gm::CLD, FLD = Gm::FLD;
-    extern __shared__ __align__(128) uint8_t smem[];
 
     // ---- work item (same enumeration as the generic region kernel)
-    const int item = (int)blockIdx.x;
     int b = 0;
     while (b + 1 < p.n_seq && p.seq[b + 1].first_item <= item) ++b;
     const SeqSpan& sp = p.seq[b];
@@ -120,13 +135,12 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     const uint32_t stage_bytes = ring ? Gm::TQ_STAGE : Gm::F_STAGE;
     const uint32_t half_bytes = ring ? Gm::TQ_HALF : Gm::F_HALF;
     const int nst = min(4, Gm::AREA / (int)stage_bytes);
-    if (nst < 1 || (!Gm::RING && kind == RK_RING)) {   // a ring at head_dim 512 is not routed here: refuse
+    if (nst < 2 || (!Gm::RING && kind == RK_RING)) {   // a ring at head_dim 512 is not routed here: refuse
         if (threadIdx.x == 0) atomicOr(status_word(L, p.pool), 4u);
         return;
     }
     uint8_t* stages = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
-    uint64_t* empty = full + 4;
     uint8_t* cur = smem + Gm::AREA + 128;
     const bool has_bf = (L.tail_fmt == KVQ_BF16) || (L.journal == KVQ_BF16);
     uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += (has_bf ? 2 : 1) * Gm::QB_BYTES;   // bf16: hi, lo
@@ -136,79 +150,75 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
     uint8_t* vbuf = cur;                                  // [warp][VROWS][VRS] decoded tq6_0 values
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ int s_abort;
-    if (threadIdx.x == 0) {
-        s_abort = 0;
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(su32(&full[i]), 1);
-            mbar_init(su32(&empty[i]), kConsumers);
-        }
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    __syncthreads();
-
-    // ================================================================== producer warp
-    if (warp == kConsumers) {
-        int issued = 0;
-        bool ok = true;
-        for (int i = 0; i < nrun; ++i) {
-            const int sl = i % nst;
-            if (i >= nst) {
-                int good = 1;
-                if (lane == 0) good = mbar_wait(su32(&empty[sl]), ((i / nst) - 1) & 1, status, &s_abort) ? 1 : 0;
-                good = __shfl_sync(0xffffffffu, good, 0);
-                if (!good) { ok = false; break; }
-            }
-            const int pc = t0 + RUN * i, n = min(RUN, t1 - pc);
-            uint8_t* st = stages + (size_t)sl * stage_bytes;
-            const uint32_t fb = su32(&full[sl]);
-            // contiguous slot runs: one copy each (a run of the ring never wraps; the tail and an
-            // exact journal wrap at most once)
-            if (lane == 0) {
-                if (ring) {
-                    mbar_expect_tx(fb, 2u * (n * Gm::CODE_ROW + Gm::SC_BYTES));
-                    for (int w = 0; w < 2; ++w) {
-                        uint8_t* dst = st + w * half_bytes;
-                        const int s0 = journal_slot(L, pc);
-                        bulk_g2s(su32(dst), jcode_row(L, p.pool, w, unit, s0), n * Gm::CODE_ROW, fb);
-                        bulk_g2s(su32(dst + 128 * CLD), jscale_row(L, p.pool, w, unit, s0), Gm::SC_BYTES, fb);
-                    }
-                } else {
-                    mbar_expect_tx(fb, 2u * n * 2 * D);
-                    for (int w = 0; w < 2; ++w) {
-                        uint8_t* dst = st + w * half_bytes;
-                        int done = 0;
-                        while (done < n) {
-                            const int pos = pc + done;
-                            const uint16_t* src;
-                            int cnt;
-                            if (kind == RK_SINK) {
-                                src = sink_row(L, p.pool, w, unit, pos);
-                                cnt = n - done;
-                            } else if (kind == RK_TAIL) {
-                                const int sl0 = pos % L.T;
-                                src = tail_row(L, p.pool, w, unit, sl0);
-                                cnt = min(n - done, L.T - sl0);
-                            } else {
-                                const int sl0 = journal_slot(L, pos);
-                                src = jexact_row(L, p.pool, w, unit, sl0);
-                                cnt = min(n - done, L.R - sl0);
-                            }
-                            bulk_g2s(su32(dst + done * FLD), src, cnt * 2 * D, fb);
-                            done += cnt;
+    // thread 0 streams the runs: run i into stage i % nst, issued once stage i % nst is free
+    // (the first barrier of run i - nst + 1 follows every read of run i - nst)
+    auto issue = [&](int i) {
+        const int sl = i % nst;
+        const int pc = t0 + RUN * i, n = min(RUN, t1 - pc);
+        uint8_t* st = stages + (size_t)sl * stage_bytes;
+        const uint32_t fb = su32(&full[sl]);
+        // contiguous slot runs: one copy each (a run of the ring never wraps; the tail and an
+        // exact journal wrap at most once)
+        {
+            if (ring) {
+                mbar_expect_tx(fb, 2u * (n * Gm::CODE_ROW + Gm::SC_BYTES));
+                for (int w = 0; w < 2; ++w) {
+                    uint8_t* dst = st + w * half_bytes;
+                    const int s0 = journal_slot(L, pc);
+                    bulk_g2s(su32(dst), jcode_row(L, p.pool, w, unit, s0), n * Gm::CODE_ROW, fb);
+                    bulk_g2s(su32(dst + 128 * CLD), jscale_row(L, p.pool, w, unit, s0), Gm::SC_BYTES, fb);
+                }
+            } else {
+                mbar_expect_tx(fb, 2u * n * 2 * D);
+                // a fused decode step's newest position (the last row of the sequence) comes
+                // from the caller's input row (fp16, which the host checks)
+                const bool newest = (p.knew != nullptr) && (pc + n == sp.n_tok);
+                for (int w = 0; w < 2; ++w) {
+                    uint8_t* dst = st + w * half_bytes;
+                    const int ncache = newest ? n - 1 : n;
+                    if (newest)
+                        bulk_g2s(su32(dst + ncache * FLD), (w ? p.vnew : p.knew) + ((int64_t)b * L.H + h) * D, 2 * D, fb);
+                    int done = 0;
+                    while (done < ncache) {
+                        const int pos = pc + done;
+                        const uint16_t* src;
+                        int cnt;
+                        if (kind == RK_SINK) {
+                            src = sink_row(L, p.pool, w, unit, pos);
+                            cnt = ncache - done;
+                        } else if (kind == RK_TAIL) {
+                            const int sl0 = pos % L.T;
+                            src = tail_row(L, p.pool, w, unit, sl0);
+                            cnt = min(ncache - done, L.T - sl0);
+                        } else {
+                            const int sl0 = journal_slot(L, pos);
+                            src = jexact_row(L, p.pool, w, unit, sl0);
+                            cnt = min(ncache - done, L.R - sl0);
                         }
+                        bulk_g2s(su32(dst + done * FLD), src, cnt * 2 * D, fb);
+                        done += cnt;
                     }
                 }
             }
-            __syncwarp();
-            ++issued;
         }
-        if (!ok && lane == 0) {   // a wait timed out: wait (bounded, fresh limit) for copies in flight
-            s_abort = 0;
-            for (int i = max(0, issued - nst); i < issued; ++i)
-                mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
-        }
-        return;
+    };
+    int issued = 0;
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < 4; ++i) mbar_init(su32(&full[i]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        for (; issued < min(nst, nrun); ++issued) issue(issued);
+    }
+    __syncthreads();
+    if (p.knew != nullptr && t1 == sp.n_tok && sp.body_per_head == 0) {
+        // fused decode step, sequence without body items: the item that holds the newest
+        // position appends it to the cache (threads 0-127 the K row, 128-255 the V row; codes
+        // staged in the P' area, unused yet). Nothing in this launch reads the slots written:
+        // the newest row is read from the input above, and its ring slot holds no position of
+        // the ring span (the journal never holds more than R positions)
+        const int w = threadIdx.x >> 7;
+        append_newest(L, p.pool, unit, w, sp.n_tok - 1, (w ? p.vnew : p.knew) + ((int64_t)b * L.H + h) * D,
+                      threadIdx.x & 127, reinterpret_cast<uint8_t*>(pbuf) + w * D);
     }
 
     // ================================================================== consumers: set-up
@@ -465,6 +475,7 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
             }
         }
         csync();
+        if (threadIdx.x == 0 && gi >= 1 && issued < nrun) issue(issued++);
 
         // ---------------- step 2: group maximum, p, running sums, P' fragments
         float al[NT][2], pr[NT][4];
@@ -603,12 +614,15 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                 O[mt][nt][3] = al[nt][1] * O[mt][nt][3] + (r[3] - z1);
             }
         if (!ring) fence_async_smem();    // the zero fill above precedes the next bulk copy into this stage
-        __syncwarp();
-        if (lane == 0) mbar_arrive(su32(&empty[sl]));
     }
 
     // ---- partial: sums over rows and warps, o (ring: rotated back), m and l
     csync();
+    if (threadIdx.x == 0 && s_abort) {   // a wait timed out: wait (bounded, fresh limit) for copies in flight
+        s_abort = 0;
+        for (int i = max(0, issued - nst); i < issued; ++i)
+            mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -645,44 +659,5 @@ __global__ void __launch_bounds__(kBodyThreads, 2) decode_region_kernel(Layout L
                          ring ? L.rot : (int)ROT_NONE);
 }
 
-template <int D, int NQ>
-int launch_region_t(const Layout& L, const AttnParams& p, cudaStream_t st) {
-    using Gm = RGeo<D, NQ>;
-    auto kern = decode_region_kernel<D, NQ>;
-    const int smem = Gm::smem(L.tail_fmt == KVQ_BF16 || L.journal == KVQ_BF16);
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kern<<<p.n_region_items, kBodyThreads, smem, st>>>(L, p);
-    return (int)cudaGetLastError();
-}
-
 }  // namespace
-
-int upload_tables_region(const FormatTables& t) {
-    return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
-}
-
-// 1 when the streaming region kernel takes this layout's region items: head_dim 128 or 256
-// (the ring, when present, in runs of whole 128-slot chunks), or 512 with 16-bit rows only.
-int region_kernel_ok(const Layout& L) {
-    if (L.D != 128 && L.D != 256 && L.D != 512) return 0;
-    if (L.D == 512 && L.journal == KVQ_TQ6_0) return 0;
-    if (L.journal == KVQ_TQ6_0 && L.R % 128 != 0) return 0;
-    return 1;
-}
-
-int launch_decode_region(const Layout& L, const AttnParams& p, void* stream) {
-    if (p.n_region_items <= 0) return 0;
-    cudaStream_t s = (cudaStream_t)stream;
-    if (L.NQ == 8) {
-        if (L.D == 128) return launch_region_t<128, 8>(L, p, s);
-        if (L.D == 256) return launch_region_t<256, 8>(L, p, s);
-        if (L.D == 512) return launch_region_t<512, 8>(L, p, s);
-    } else {
-        if (L.D == 128) return launch_region_t<128, 16>(L, p, s);
-        if (L.D == 256) return launch_region_t<256, 16>(L, p, s);
-        if (L.D == 512) return launch_region_t<512, 16>(L, p, s);
-    }
-    return (int)cudaErrorInvalidValue;
-}
-
 }  // namespace kvq

@@ -14,7 +14,7 @@ import pytest
 from oracle import attention
 from quantized_kv_cache_gb300 import synth, _lib
 
-from gpu_cases import FAMILIES, Pair
+from gpu_cases import FAMILIES, Family, Pair, inputs
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -87,9 +87,12 @@ def _q(p: Pair, layer, step, scale_mult=1.0):
     return np.stack(qs)
 
 
-def _check_attention(p: Pair, layer, q, atol=ATOL, rtol=RTOL):
+def _check_attention(p: Pair, layer, q, atol=ATOL, rtol=RTOL, got=None):
+    """got: the GPU output for q (default: one kv_decode_attn call now)."""
     f = p.f
-    got = p.attend(layer, p.seqs, q).astype(np.float64)
+    if got is None:
+        got = p.attend(layer, p.seqs, q)
+    got = got.astype(np.float64)
     G = f.Hq // f.H
     worst = 0.0
     for bi, s in enumerate(p.seqs):
@@ -136,3 +139,58 @@ def test_decode_steps_match_oracle(pair):
             _check_attention(pair, layer, _q(pair, layer, step + 1))
     _check_bytes(pair)
     _check_dequant(pair)
+
+
+def _step_calls(p: Pair, steps, step0, keep):
+    """Decode steps through kv_decode_step (one call per step over all layers; seal policy
+    'whenever a full group is older than keep'), each layer's output checked against the
+    oracle after the same append and seal. Layouts whose decode kernel takes the region items
+    append inside that kernel (the newest row read from the call's input)."""
+    f = p.f
+    dev = p.dev
+    for step in range(step0, step0 + steps):
+        K = np.zeros((f.L, len(p.seqs), f.H, f.D), np.float16)
+        V = np.zeros_like(K)
+        Q = np.stack([_q(p, layer, step) for layer in range(f.L)])
+        for layer in range(f.L):
+            for bi, s in enumerate(p.seqs):
+                n = p.gpu.state(layer, s)[0]
+                k, v = inputs(f, layer, s, n, 1)
+                K[layer, bi], V[layer, bi] = k[0], v[0]
+                for h in range(f.H):
+                    p.hc[(layer, s, h)].append(k[:, h], v[:, h])
+                    p.hc[(layer, s, h)].seal(keep)
+        Kd, Vd, Qd = (torch.from_numpy(x).to(dev) for x in (K, V, Q))
+        out = torch.empty_like(Qd)
+        _lib.kv_decode_step(p.gpu.h, f.L, p.seqs, Qd.data_ptr(), Kd.data_ptr(), Vd.data_ptr(), out.data_ptr(), 0,
+                            keep, p.gpu.ws.data_ptr(), p.gpu.ws_bytes)
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        for layer in range(f.L):
+            _check_attention(p, layer, Q[layer], got=got[layer])
+
+
+def test_decode_step_call_matches_oracle(pair):
+    # the same decode steps through the one-call entry point (after the per-call steps above)
+    _step_calls(pair, pair.f.steps, pair.f.steps + 1, pair.f.keep)
+    _check_bytes(pair)
+    _check_dequant(pair)
+
+
+@pytest.mark.parametrize("base", ["tbq4_f16", "kvarn4_ring", "kvarn5_wide", "q8q4_bf16"])
+def test_decode_step_call_across_sink_edge(base):
+    # short sequences stepped across position 128: the newest position moves from the sink
+    # into the exact journal / tail while the decode kernel appends it
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f0 = FAMILIES[base]
+    f = Family(f0.name + "_edge", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T, R=f0.R,
+               contexts=[124, 101], keep=f0.keep, steps=6, n_out=f0.n_out, factor=f0.factor)
+    p = Pair(f)
+    try:
+        p.prefill()
+        _step_calls(p, f.steps, 1, f.keep)
+        _check_bytes(p)
+        _check_dequant(p)
+    finally:
+        p.gpu.close()
