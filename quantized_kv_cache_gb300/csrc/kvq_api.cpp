@@ -364,8 +364,8 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
         body_groups += s.body_groups;
     }
     // Work items. Body items split each (sequence, head)'s groups evenly, in number proportional
-    // to its groups, one wave of resident CTAs in all: they start first and carry most of the
-    // bytes. Region items are chunks (multiples of 128 positions) of each span, about two waves'
+    // to its groups, at most one wave of resident CTAs in all: they start first and carry most
+    // of the bytes. Region items are chunks (multiples of 128 positions) of each span, about two waves'
     // worth, taken up as body items finish. (One common wave sized by estimated cost measured
     // slower: 16-bit rows cost 3 to 5 times a sealed group per position, and the minimum of one
     // item per span makes the region items too coarse.)
@@ -374,6 +374,10 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     int64_t chunk = (region_tok * L.H + target - 1) / target;
     chunk = std::max<int64_t>(kGroup, (chunk + kGroup - 1) / kGroup * kGroup);
     int64_t body_items = (int64_t)std::max(1, fused ? decode_ctas_per_sm(L) : body_ctas_per_sm(L)) * c->sm_count;
+    // at least kMinBodyGroups groups per body item where the wave would give fewer: a shorter
+    // item spends most of its time on per-item set-up (query rotation, pipeline fill, partial)
+    constexpr int64_t kMinBodyGroups = 6;
+    body_items = std::min(body_items, std::max<int64_t>(L.H, (body_groups * L.H + kMinBodyGroups - 1) / kMinBodyGroups));
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {

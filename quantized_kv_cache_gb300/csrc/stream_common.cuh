@@ -171,7 +171,6 @@ __device__ __forceinline__ void warp_unrotate(float (&v)[NK], int lane, int rot)
     }
 }
 
-
 // Writes a work item's partial: m and l per query row, then o (rows [NQ][D] in shared memory,
 // fp32) rotated back to the original domain by warp shuffles (one warp per row block) and
 // stored straight to global memory. Called by the consumer threads after a consumer barrier.
