@@ -143,13 +143,28 @@ kvq_status kv_decode_attn(kvq_cache* cache, int layer, const int32_t* seq_ids, i
  * keep exists; seal_trigger < 0 never seals. Layouts: q [n_layers][n_seq][Hq][D], k and v
  * [n_layers][n_seq][1][H][D], out [n_layers][n_seq][Hq][D], all device fp16.
  * events (may be NULL): 2 * n_layers caller-created cudaEvent_t handles; events[2l] and
- * events[2l+1] are recorded on `stream` just before and after layer l's attention.
- * groups_sealed (host, may be NULL) receives the groups sealed in this step. Stops at the
- * first failing call and returns its status; earlier layers stay applied. */
+ * events[2l+1] are recorded on `stream` just before and just after layer l's decode kernel
+ * (the streaming kernel, or the generic split kernel; the merge kernel follows them).
+ * groups_sealed (host, may be NULL) receives the groups sealed in this step.
+ * Where the decode kernel takes a layout's region items and the newest row is fp16, the
+ * append runs inside that layer's attention launch (same results, one launch less).
+ * By default (kv_set_graph_mode) the step's launches are captured on a stream private to the
+ * cache and replayed on `stream` as one CUDA graph; an argument or capacity error then leaves
+ * the cache as it was (nothing launched). With graph mode off the calls go straight to
+ * `stream`, and a failing call stops the step with earlier layers applied. */
 kvq_status kv_decode_step(kvq_cache* cache, int n_layers, const int32_t* seq_ids, int n_seq,
                           const void* q, const void* k, const void* v, void* out,
                           int seal_trigger, int keep, void* workspace, size_t ws_bytes,
                           void* const* events, int64_t* groups_sealed, void* stream);
+
+/* kv_set_graph_mode — whether kv_decode_step replays its launches as one CUDA graph (enable
+ * != 0, the default) or issues them one by one. A step is launch-bound where its kernels are
+ * short: on GB300 a dependent launch costs 2 to 4 us on a stream, about 1 us as a graph node.
+ * The graph is re-captured each step and applied to the cached executable graph with
+ * cudaGraphExecUpdate, instantiated anew when the launch topology changes (a seal, another
+ * layer count). If a capture or a graph launch fails, the cache switches to direct launches.
+ * A library convenience with no counterpart in the source pages. */
+kvq_status kv_set_graph_mode(kvq_cache* cache, int enable);
 
 /* kv_snapshot_size / kv_snapshot / kv_restore — copy the host-side lengths of every slot
  * out of, or back into, a cache handle (host memory of kv_snapshot_size bytes). Restoring

@@ -67,6 +67,7 @@ _SIGS = {
     "kv_decode_step": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
                        P, SZ, ctypes.POINTER(P), ctypes.POINTER(I64), P],
     "kv_decode_attn_noalloc": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P],
+    "kv_set_graph_mode": [P, ctypes.c_int],
     "kv_snapshot_size": [P, ctypes.POINTER(SZ)],
     "kv_snapshot": [P, P, SZ],
     "kv_restore": [P, P, SZ],
@@ -162,6 +163,11 @@ def kv_decode_step(h, n_layers, seq_ids, q_ptr, k_ptr, v_ptr, out_ptr, seal_trig
                                                    seal_trigger, keep, P(ws_ptr), ws_bytes, ev, ctypes.byref(g),
                                                    P(stream)))
     return g.value
+
+
+def kv_set_graph_mode(h, enable):
+    """Whether kv_decode_step replays its launches as one CUDA graph (default on)."""
+    _check("kv_set_graph_mode", load().kv_set_graph_mode(h, 1 if enable else 0))
 
 
 def kv_decode_attn_noalloc(h, layer, seq_ids, q_ptr, out_ptr, stream=0):

@@ -593,7 +593,7 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
 }
 
 template <int D, int NQ>
-int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
+int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const LaunchMarks& mk) {
     using C = Cfg<D, NQ>;
     static bool attr = false;
     if (!attr) {
@@ -606,6 +606,8 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
     // items go through the generic kernel
     const bool streaming = body_ctas_per_sm(L) > 0;
     const bool fused_regions = streaming && region_kernel_ok(L);
+    if (mk.before && cudaEventRecordWithFlags((cudaEvent_t)mk.before, s, mk.flags) != cudaSuccess)
+        return (int)cudaErrorInvalidResourceHandle;
     if (streaming) {
         const int e = launch_decode_fused(L, p, n_body, fused_regions ? p.n_region_items : 0, s);
         if (e != 0) return e;
@@ -615,6 +617,8 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s) {
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return (int)e;
     }
+    if (mk.after && cudaEventRecordWithFlags((cudaEvent_t)mk.after, s, mk.flags) != cudaSuccess)
+        return (int)cudaErrorInvalidResourceHandle;
     int max_cnt = 0;
     for (int i = 0; i < p.n_seq; ++i)
         max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
@@ -633,17 +637,17 @@ int upload_tables_attn(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
 }
 
-int launch_decode(const Layout& L, const AttnParams& p, void* stream) {
+int launch_decode(const Layout& L, const AttnParams& p, void* stream, const LaunchMarks& mk) {
     if (p.total_items == 0) return 0;
     cudaStream_t s = (cudaStream_t)stream;
     if (L.NQ == 8) {
-        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s);
-        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s);
-        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s);
+        if (L.D == 128) return launch_decode_t<128, 8>(L, p, s, mk);
+        if (L.D == 256) return launch_decode_t<256, 8>(L, p, s, mk);
+        if (L.D == 512) return launch_decode_t<512, 8>(L, p, s, mk);
     } else {
-        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s);
-        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s);
-        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s);
+        if (L.D == 128) return launch_decode_t<128, 16>(L, p, s, mk);
+        if (L.D == 256) return launch_decode_t<256, 16>(L, p, s, mk);
+        if (L.D == 512) return launch_decode_t<512, 16>(L, p, s, mk);
     }
     return (int)cudaErrorInvalidValue;
 }

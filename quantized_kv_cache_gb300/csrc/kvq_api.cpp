@@ -23,6 +23,12 @@ struct kvq_cache {
     int sm_count;
     std::vector<int64_t> n_tok;   // [L][max_seqs]
     std::vector<int64_t> sealed;  // [L][max_seqs]
+    // kv_decode_step replays its launches as one CUDA graph: captured on a private stream each
+    // call and applied to the cached executable graph with cudaGraphExecUpdate (instantiated
+    // anew when the launches' topology changes: a seal, another layer count)
+    int graph_mode = 1;
+    cudaStream_t cap_stream = nullptr;
+    cudaGraphExec_t step_exec = nullptr;
 };
 
 namespace kvq {
@@ -221,6 +227,8 @@ kvq_status kv_create(const kvq_config* cfg, void* device_pool, size_t pool_bytes
 
 kvq_status kv_destroy(kvq_cache* c) {
     if (!c) return KVQ_EINVAL;
+    if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
+    if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
     delete c;
     return KVQ_OK;
 }
@@ -328,7 +336,8 @@ namespace {
 // Decode attention of one layer; with knew / vnew (the newest position's rows, fp16, already
 // counted in N) the decode kernel also appends them (the fused decode step).
 kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
-                       void* workspace, size_t ws_bytes, const void* knew, const void* vnew, void* stream) {
+                       void* workspace, size_t ws_bytes, const void* knew, const void* vnew, void* stream,
+                       const LaunchMarks& marks = LaunchMarks()) {
     kvq_status st = check_cache(c);
     if (st != KVQ_OK) return st;
     if (layer < 0 || layer >= c->cfg.n_layers || !q || !out || !workspace) return KVQ_EINVAL;
@@ -431,7 +440,7 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     }
     p.body_chunk = 0;
     p.chunk = (int32_t)chunk;
-    const int e = launch_decode(L, p, stream);
+    const int e = launch_decode(L, p, stream, marks);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;
 }
 
@@ -454,21 +463,21 @@ kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n
     return decode_attn(c, layer, seq_ids, n_seq, q, out, workspace, ws_bytes, nullptr, nullptr, stream);
 }
 
-kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
-                          const void* k, const void* v, void* out, int seal_trigger, int keep, void* workspace,
-                          size_t ws_bytes, void* const* events, int64_t* groups_sealed, void* stream) {
-    kvq_status st = check_cache(c);
-    if (st != KVQ_OK) return st;
-    if (n_layers <= 0 || n_layers > c->cfg.n_layers || !q || !k || !v || !out) return KVQ_EINVAL;
-    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+namespace {
+
+// The launches of one decode step on `stream` (arguments checked by the caller). The caller's
+// events bracket each layer's decode kernel; ev_flags: cudaEventRecordExternal while the step
+// is captured into a graph (the events then become event-record nodes it can time), else
+// cudaEventRecordDefault.
+kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
+                         const void* k, const void* v, void* out, int seal_trigger, int keep, void* workspace,
+                         size_t ws_bytes, void* const* events, int64_t* groups_sealed, void* stream,
+                         unsigned ev_flags) {
+    kvq_status st = KVQ_OK;
     const Layout& L = c->lay;
     const size_t qb = (size_t)n_seq * L.Hq * L.D * 2, kb = (size_t)n_seq * L.H * L.D * 2;
     int64_t total = 0;
     int32_t need[kMaxSeqPerCall];
-    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !workspace) return KVQ_EINVAL;
-    size_t ws_need = 0;
-    kv_required_bytes(&c->cfg, nullptr, &ws_need);
-    if (ws_bytes < ws_need) return KVQ_EINVAL;
     for (int l = 0; l < n_layers; ++l) {
         const char* kl = (const char*)k + l * kb;
         const char* vl = (const char*)v + l * kb;
@@ -503,19 +512,85 @@ kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, in
             if (st != KVQ_OK) return st;
             total += g;
         }
-        if (events && cudaEventRecord((cudaEvent_t)events[2 * l], (cudaStream_t)stream) != cudaSuccess)
-            return KVQ_ECUDA;
+        LaunchMarks marks;
+        if (events) {
+            marks.before = events[2 * l];
+            marks.after = events[2 * l + 1];
+            marks.flags = ev_flags;
+        }
         st = decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace, ws_bytes,
-                         fuse ? kl : nullptr, fuse ? vl : nullptr, stream);
+                         fuse ? kl : nullptr, fuse ? vl : nullptr, stream, marks);
         if (st != KVQ_OK) {
             if (fuse)   // the launch that was to append the position did not go out
                 for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) -= 1;
             return st;
         }
-        if (events && cudaEventRecord((cudaEvent_t)events[2 * l + 1], (cudaStream_t)stream) != cudaSuccess)
-            return KVQ_ECUDA;
     }
     if (groups_sealed) *groups_sealed = total;
+    return KVQ_OK;
+}
+
+}  // namespace
+
+kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
+                          const void* k, const void* v, void* out, int seal_trigger, int keep, void* workspace,
+                          size_t ws_bytes, void* const* events, int64_t* groups_sealed, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (n_layers <= 0 || n_layers > c->cfg.n_layers || !q || !k || !v || !out) return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !workspace) return KVQ_EINVAL;
+    size_t ws_need = 0;
+    kv_required_bytes(&c->cfg, nullptr, &ws_need);
+    if (ws_bytes < ws_need) return KVQ_EINVAL;
+    if (groups_sealed) *groups_sealed = 0;
+    if (!c->graph_mode)
+        return step_launches(c, n_layers, seq_ids, n_seq, q, k, v, out, seal_trigger, keep, workspace, ws_bytes,
+                             events, groups_sealed, stream, cudaEventRecordDefault);
+    // one graph per step: the host-side lengths advance while the launches are captured, and
+    // go back to where they were if the step cannot be launched
+    if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return KVQ_ECUDA;
+    const std::vector<int64_t> n_tok0 = c->n_tok, sealed0 = c->sealed;
+    if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KVQ_ECUDA;
+    int64_t g = 0;
+    st = step_launches(c, n_layers, seq_ids, n_seq, q, k, v, out, seal_trigger, keep, workspace, ws_bytes, events, &g,
+                       c->cap_stream, cudaEventRecordExternal);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(c->cap_stream, &graph);
+    bool launched = false;
+    if (st == KVQ_OK && ce == cudaSuccess && graph) {
+        bool ready = false;
+        if (c->step_exec) {
+            cudaGraphExecUpdateResultInfo info;
+            ready = cudaGraphExecUpdate(c->step_exec, graph, &info) == cudaSuccess;
+            if (!ready) {
+                cudaGetLastError();
+                cudaGraphExecDestroy(c->step_exec);
+                c->step_exec = nullptr;
+            }
+        }
+        if (!ready) ready = cudaGraphInstantiate(&c->step_exec, graph, 0) == cudaSuccess;
+        launched = ready && cudaGraphLaunch(c->step_exec, (cudaStream_t)stream) == cudaSuccess;
+    }
+    if (graph) cudaGraphDestroy(graph);
+    if (launched) {
+        if (groups_sealed) *groups_sealed = g;
+        return KVQ_OK;
+    }
+    c->n_tok = n_tok0;
+    c->sealed = sealed0;
+    if (st != KVQ_OK) return st;   // an argument or capacity error: nothing was launched
+    // the graph path failed: launch directly from now on
+    cudaGetLastError();
+    c->graph_mode = 0;
+    return step_launches(c, n_layers, seq_ids, n_seq, q, k, v, out, seal_trigger, keep, workspace, ws_bytes, events,
+                         groups_sealed, stream, cudaEventRecordDefault);
+}
+
+kvq_status kv_set_graph_mode(kvq_cache* c, int enable) {
+    if (!c) return KVQ_EINVAL;
+    c->graph_mode = enable ? 1 : 0;
     return KVQ_OK;
 }
 

@@ -148,7 +148,14 @@ const FormatTables& host_tables();   // derived once per process (tables.cpp)
 // Kernel launchers (kernels_*.cu). Each returns cudaError_t as int.
 int launch_append(const Layout& lay, const AppendParams& p, void* stream);
 int launch_seal(const Layout& lay, const SealParams& p, void* stream);
-int launch_decode(const Layout& lay, const AttnParams& p, void* stream);
+// Events recorded around the decode kernel's launch (both null: none); flags for
+// cudaEventRecordWithFlags (cudaEventRecordExternal while a graph is captured).
+struct LaunchMarks {
+    void* before = nullptr;
+    void* after = nullptr;
+    unsigned flags = 0;
+};
+int launch_decode(const Layout& lay, const AttnParams& p, void* stream, const LaunchMarks& marks = LaunchMarks());
 int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream);
 int upload_tables_body(const FormatTables& t);
 int body_ctas_per_sm(const Layout& lay);     // resident body-item CTAs per SM (0: no instance)

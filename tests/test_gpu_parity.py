@@ -194,3 +194,55 @@ def test_decode_step_call_across_sink_edge(base):
         _check_dequant(p)
     finally:
         p.gpu.close()
+
+
+def test_decode_step_graph_and_direct_agree():
+    # the same steps through one CUDA graph per step and through direct launches: outputs and
+    # every stored byte agree exactly (a seal step changes the graph's topology mid-run)
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f = FAMILIES["kvarn4_ring"]
+    pairs = [Pair(f), Pair(f)]
+    try:
+        for p in pairs:
+            p.gpu.pool.zero_()   # kv_create leaves unwritten slots as allocated: compare from zero
+            p.prefill()
+        _lib.kv_set_graph_mode(pairs[1].gpu.h, False)
+        outs = [[], []]
+        for step in range(1, 7):
+            K = np.zeros((f.L, len(pairs[0].seqs), f.H, f.D), np.float16)
+            V = np.zeros_like(K)
+            Q = np.stack([_q(pairs[0], layer, step) for layer in range(f.L)])
+            for layer in range(f.L):
+                for bi, s in enumerate(pairs[0].seqs):
+                    k, v = inputs(f, layer, s, pairs[0].gpu.state(layer, s)[0], 1)
+                    K[layer, bi], V[layer, bi] = k[0], v[0]
+            for i, p in enumerate(pairs):
+                Kd, Vd, Qd = (torch.from_numpy(x).to(p.dev) for x in (K, V, Q))
+                out = torch.empty_like(Qd)
+                # keep 128 below the family's: a seal in some steps
+                _lib.kv_decode_step(p.gpu.h, f.L, p.seqs, Qd.data_ptr(), Kd.data_ptr(), Vd.data_ptr(),
+                                    out.data_ptr(), 0, f.keep - 128, p.gpu.ws.data_ptr(), p.gpu.ws_bytes)
+                torch.cuda.synchronize()
+                outs[i].append(out.cpu().numpy())
+        for a, b in zip(*outs):
+            assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+        for layer in range(f.L):
+            for s in pairs[0].seqs:
+                assert pairs[0].gpu.state(layer, s) == pairs[1].gpu.state(layer, s)
+        torch.cuda.synchronize()
+        regions = [(r, getattr(_lib, r)) for r in dir(_lib) if r.startswith("REGION_")]
+        for layer in range(f.L):
+            for s in pairs[0].seqs:
+                for h in range(f.H):
+                    for which in (0, 1):
+                        for name, r in regions:
+                            a = pairs[0].region_bytes(layer, s, h, which, r)
+                            b = pairs[1].region_bytes(layer, s, h, which, r)
+                            bad = np.flatnonzero(a != b)
+                            assert bad.size == 0, f"{name} l{layer} s{s} h{h} w{which}: {bad.size} bytes, first {bad[:6]}"
+        diff = torch.nonzero(pairs[0].gpu.pool != pairs[1].gpu.pool).flatten()
+        assert diff.numel() == 0, f"{diff.numel()} pool bytes differ outside the regions, first {diff[:6].tolist()}"
+    finally:
+        for p in pairs:
+            p.gpu.close()
