@@ -25,6 +25,7 @@ UNITS = {
     "kvq_api.cpp": [],
     "tables.cpp": [],
     "kernels_codec.cu": ["-fmad=false"],
+    "kernels_seal.cu": ["-fmad=false"],
     "kernels_attn.cu": [],
     "kernels_body.cu": [],
     "synth.cu": [],

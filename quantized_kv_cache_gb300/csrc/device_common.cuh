@@ -54,4 +54,25 @@ __device__ __forceinline__ bool sign_neg(int set, int i) {
     return (c_tab.sign_words[2 * set + (i >> 6)] >> (i & 63)) & 1ULL;
 }
 
+// One sealed group of a seal launch: group index gidx counts the layers' groups in order,
+// the sequences of the batch in order inside a layer.
+struct SealTaskPos { int layer, slot, g, pos0; };
+
+__device__ __forceinline__ SealTaskPos seal_task(const SealParams& p, int gidx) {
+    SealTaskPos t;
+    t.layer = p.layer0 + gidx / p.groups_per_layer;
+    const int r = gidx % p.groups_per_layer;
+    int b = 0;
+    while (b + 1 < p.n_seq && p.seq[b + 1].prefix <= r) ++b;
+    const int gi = r - p.seq[b].prefix;
+    t.slot = p.seq[b].slot;
+    t.g = p.seq[b].first_group + gi;
+    t.pos0 = p.seq[b].first_pos + kGroup * gi;
+    return t;
+}
+
+__device__ __forceinline__ void flag_nonfinite(const Layout& L, const void* pool, float x) {
+    if (!isfinite(x)) atomicOr(status_word(L, pool), 1u);
+}
+
 }  // namespace kvq

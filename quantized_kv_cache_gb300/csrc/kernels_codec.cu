@@ -1,5 +1,5 @@
 // Codec kernels of the rotated low-bit KV cache: append (rotate + tq6_0 staging, exact
-// copies), seal (TBQ4 / Q8_0 / Q4_0 / KVarN body records) and dequant.
+// copies), the KVarN seal and dequant. The TBQ4 / Q8_0 / Q4_0 seal is in kernels_seal.cu.
 //
 // Every floating-point step uses the explicit round-to-nearest intrinsics (__fadd_rn,
 // __fmul_rn, __fdiv_rn, __fsqrt_rn) and this file is built with -fmad=false, so no
@@ -135,171 +135,6 @@ __global__ void append_kernel(Layout L, AppendParams p) {
     // positions of the append write it
     append_row(L, p.pool, L.unit(p.layer, p.slot[b], h), w, pos, src, pos + L.T >= p.n0[b] + p.n_tok,
                (int)threadIdx.x, (int)blockDim.x, cs);
-}
-
-// ---------------------------------------------------------------------------- seal task
-struct SealTaskPos { int layer, slot, g, pos0; };
-
-__device__ __forceinline__ SealTaskPos seal_task(const SealParams& p, int gidx) {
-    SealTaskPos t;
-    t.layer = p.layer0 + gidx / p.groups_per_layer;
-    const int r = gidx % p.groups_per_layer;
-    int b = 0;
-    while (b + 1 < p.n_seq && p.seq[b + 1].prefix <= r) ++b;
-    const int gi = r - p.seq[b].prefix;
-    t.slot = p.seq[b].slot;
-    t.g = p.seq[b].first_group + gi;
-    t.pos0 = p.seq[b].first_pos + kGroup * gi;
-    return t;
-}
-
-__device__ __forceinline__ void flag_nonfinite(const Layout& L, const void* pool, float x) {
-    if (!isfinite(x)) atomicOr(status_word(L, pool), 1u);
-}
-
-// ---------------------------------------------------------------------------- scalar seal
-// TBQ4 (per 128: tree sum of squares, fp16 norm, boundary count), Q8_0 / Q4_0 (per 32:
-// absmax scale, rint). grid (groups, H, 2), 256 threads. A tq6_0 journal chunk (128 rows,
-// contiguous slots) is first staged in shared memory with 16-byte loads; a warp then encodes
-// one row at a time. Codes go to shared memory in the record's order (K token-major [128][D],
-// V channel-major [D][kVS] with a padded stride so a warp's byte writes hit distinct banks),
-// and the record is written with 4- or 16-byte stores.
-constexpr int kVS = 132;
-
-template <int D>
-struct SealSmem {
-    static constexpr int JROW = (D / 128) * 96;                       // tq6_0 code row bytes
-    static constexpr int CODES = (D * kVS > 128 * D ? D * kVS : 128 * D);
-    static constexpr int SCALES = 128 * (D / 32) * 2;
-    static constexpr int JBUF = 128 * JROW + 128 * (D / 128) * 2;
-    static constexpr int BYTES = CODES + SCALES + JBUF;
-};
-
-template <int D>
-__global__ void __launch_bounds__(256) seal_scalar_kernel(Layout L, SealParams p) {
-    constexpr int NK = D / 32;
-    using SS = SealSmem<D>;
-    const SealTaskPos tk = seal_task(p, blockIdx.x);
-    const int h = blockIdx.y, w = blockIdx.z, fmt = L.fmt[w];
-    const int64_t unit = L.unit(tk.layer, tk.slot, h);
-    extern __shared__ __align__(16) uint8_t sm[];
-    uint8_t* codes = sm;
-    uint16_t* scales = reinterpret_cast<uint16_t*>(sm + SS::CODES);      // [128][nb]
-    uint8_t* jbuf = sm + SS::CODES + SS::SCALES;                         // staged tq6_0 chunk
-    __shared__ float bnd[15];
-    if (threadIdx.x < 15) bnd[threadIdx.x] = c_tab.bnd[threadIdx.x];
-    const bool tq6 = (L.journal == KVQ_TQ6_0);
-    if (tq6) {   // the group's 128 slots are contiguous (it starts at a multiple of 128; R is one)
-        const int s0 = journal_slot(L, tk.pos0);
-        const uint4* src = reinterpret_cast<const uint4*>(jcode_row(L, p.pool, w, unit, s0));
-        uint4* dst = reinterpret_cast<uint4*>(jbuf);
-        for (int i = threadIdx.x; i < 128 * SS::JROW / 16; i += blockDim.x) dst[i] = src[i];
-        const uint4* ssrc = reinterpret_cast<const uint4*>(jscale_row(L, p.pool, w, unit, s0));
-        uint4* sdst = reinterpret_cast<uint4*>(jbuf + 128 * SS::JROW);
-        for (int i = threadIdx.x; i < 128 * (D / 128) * 2 / 16; i += blockDim.x) sdst[i] = ssrc[i];
-    }
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nb = (fmt == KVQ_TBQ4) ? D / 128 : D / 32;
-    const bool vmaj = (w == 1);                         // V records are channel-major
-    auto put = [&](int t, int c, uint8_t code) {
-        if (vmaj) codes[c * kVS + t] = code;
-        else codes[t * D + c] = code;
-    };
-    for (int t = warp; t < kGroup; t += 8) {
-        float v[NK];
-        if (tq6) {   // same arithmetic as the journal reader: (code - 32) x fp32(d)
-            const uint8_t* row = jbuf + t * SS::JROW;
-            const uint16_t* sc = reinterpret_cast<const uint16_t*>(jbuf + 128 * SS::JROW) + t * (D / 128);
-#pragma unroll
-            for (int k = 0; k < NK; ++k) {
-                const int c = lane + 32 * k;
-                const int b = c >> 7, j = c & 127;
-                const float d = h2f(sc[b]);
-                v[k] = fmul((float)(tq6_code_at(row + 96 * b, j) - 32), d);
-            }
-        } else {
-            load_journal_row<NK>(L, p.pool, w, unit, tk.pos0 + t, 0, lane, v);
-        }
-        if (fmt == KVQ_TBQ4) {
-#pragma unroll
-            for (int m = 0; m < NK / 4; ++m) {
-                // halving tree over 128: strides 64, 32 in-lane, then 16..1 across lanes
-                const float a0 = fadd(fmul(v[4 * m], v[4 * m]), fmul(v[4 * m + 2], v[4 * m + 2]));
-                const float a1 = fadd(fmul(v[4 * m + 1], v[4 * m + 1]), fmul(v[4 * m + 3], v[4 * m + 3]));
-                const float ss = warp_tree_tail(fadd(a0, a1));
-                const uint16_t n16 = f2h_bits(__fsqrt_rn(ss));
-                const float n = h2f(n16);
-                const float inv = (n == 0.f) ? 0.f : fdiv(1.0f, n);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float u = fmul(v[4 * m + k], inv);
-                    int idx = (u > bnd[7]) ? 8 : 0;
-                    idx += (u > bnd[idx + 3]) ? 4 : 0;
-                    idx += (u > bnd[idx + 1]) ? 2 : 0;
-                    idx += (u > bnd[idx]) ? 1 : 0;
-                    put(t, 128 * m + lane + 32 * k, (uint8_t)idx);
-                }
-                if (lane == 0) {
-                    scales[t * nb + m] = n16;
-                    flag_nonfinite(L, p.pool, n);
-                }
-            }
-        } else {
-            const float qmax = (fmt == KVQ_Q8_0) ? 127.f : 7.f;
-#pragma unroll
-            for (int k = 0; k < NK; ++k) {
-                const float a = warp_max(fabsf(v[k]));
-                const uint16_t d16 = f2h_bits(fdiv(a, qmax));
-                const float d = h2f(d16);
-                const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
-                float q = (d == 0.f) ? 0.f : rintf(fmul(v[k], inv));
-                q = fminf(fmaxf(q, -qmax), qmax);
-                const int qi = (int)q;
-                put(t, lane + 32 * k, (fmt == KVQ_Q8_0) ? (uint8_t)(int8_t)qi : (uint8_t)(qi + 8));
-                if (lane == 0) {
-                    scales[t * nb + k] = d16;
-                    flag_nonfinite(L, p.pool, d);
-                }
-            }
-        }
-    }
-    __syncthreads();
-    uint8_t* rec = body_rec(L, p.pool, w, unit, tk.g);
-    const bool nib = (fmt != KVQ_Q8_0);
-    const int code_bytes = nib ? 64 * D : 128 * D;
-    if (!vmaj) {   // K: token-major rows
-        if (nib) {   // 4 output bytes (8 channels of one row) per thread
-            for (int i = threadIdx.x; i < code_bytes / 4; i += blockDim.x) {
-                const int t = i / (D / 8), c = 8 * (i % (D / 8));
-                const uint2 x = *reinterpret_cast<const uint2*>(codes + t * D + c);
-                const uint32_t lo = (x.x & 0x0F0F0F0Fu) | ((x.x >> 4) & 0xF0F0F0F0u), hi = (x.y & 0x0F0F0F0Fu) | ((x.y >> 4) & 0xF0F0F0F0u);
-                const uint32_t out = __byte_perm(lo, hi, 0x6420);
-                reinterpret_cast<uint32_t*>(rec)[i] = out;
-            }
-        } else {
-            for (int i = threadIdx.x; i < code_bytes / 16; i += blockDim.x)
-                reinterpret_cast<uint4*>(rec)[i] = reinterpret_cast<const uint4*>(codes)[i];
-        }
-    } else {       // V: channel-major rows of 128 positions
-        if (nib) {   // 4 output bytes (positions 8j..8j+7 of one channel) per thread
-            for (int i = threadIdx.x; i < code_bytes / 4; i += blockDim.x) {
-                const int c = i / 16, t = 8 * (i % 16);
-                const uint32_t x0 = *reinterpret_cast<const uint32_t*>(codes + c * kVS + t);
-                const uint32_t x1 = *reinterpret_cast<const uint32_t*>(codes + c * kVS + t + 4);
-                const uint32_t lo = (x0 & 0x0F0F0F0Fu) | ((x0 >> 4) & 0xF0F0F0F0u), hi = (x1 & 0x0F0F0F0Fu) | ((x1 >> 4) & 0xF0F0F0F0u);
-                reinterpret_cast<uint32_t*>(rec)[i] = __byte_perm(lo, hi, 0x6420);
-            }
-        } else {     // 16 output bytes per thread
-            for (int i = threadIdx.x; i < code_bytes / 16; i += blockDim.x) {
-                const int c = i / 8, t = 16 * (i % 8);
-                const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + c * kVS + t);
-                reinterpret_cast<uint4*>(rec)[i] = make_uint4(src[0], src[1], src[2], src[3]);
-            }
-        }
-    }
-    uint16_t* srec = reinterpret_cast<uint16_t*>(rec + code_bytes);
-    for (int i = threadIdx.x; i < kGroup * nb; i += blockDim.x) srec[i] = scales[i];
 }
 
 // ---------------------------------------------------------------------------- KVarN seal
@@ -562,23 +397,7 @@ int launch_seal(const Layout& L, const SealParams& p, void* stream) {
         seal_kvarn_kernel<<<grid, 512, smem, s>>>(L, p);
         return (int)cudaGetLastError();
     }
-    dim3 grid(groups, L.H, 2);
-    switch (L.D) {
-        case 128:
-            cudaFuncSetAttribute(seal_scalar_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, SealSmem<128>::BYTES);
-            seal_scalar_kernel<128><<<grid, 256, SealSmem<128>::BYTES, s>>>(L, p);
-            break;
-        case 256:
-            cudaFuncSetAttribute(seal_scalar_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, SealSmem<256>::BYTES);
-            seal_scalar_kernel<256><<<grid, 256, SealSmem<256>::BYTES, s>>>(L, p);
-            break;
-        case 512:
-            cudaFuncSetAttribute(seal_scalar_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, SealSmem<512>::BYTES);
-            seal_scalar_kernel<512><<<grid, 256, SealSmem<512>::BYTES, s>>>(L, p);
-            break;
-        default: return (int)cudaErrorInvalidValue;
-    }
-    return (int)cudaGetLastError();
+    return launch_seal_rows(L, p, stream);   // TBQ4, Q8_0, Q4_0 (kernels_seal.cu)
 }
 
 int launch_dequant(const Layout& L, const void* pool, int layer, int slot, int head, int which, int kind,

@@ -1,0 +1,481 @@
+// Seal of the scalar body formats (TBQ4, Q8_0, Q4_0): a persistent kernel in which every
+// thread encodes one position of a 128-position group (SJ-KVaRN §2.1 item 4: full groups
+// leave the journal as compact body records).
+//
+// Work unit ("tile"): one group x one KV head x K or V x one 128-channel block. The tile's
+// 128 journal rows are staged in shared memory with 16-byte cp.async copies issued by all
+// threads, rows padded to an odd multiple of 16 bytes so that the thread-per-row 16-byte
+// reads are free of bank conflicts, three stages deep (two tiles in flight while one is
+// encoded). Thread t decodes row t into 128 fp32 registers (tq6_0 codes spread a word at a
+// time; 16-bit rows widened and, for TBQ4, rotated by an in-register FWHT), encodes it and
+// writes its codes straight to the record: K (token-major) with 16-byte stores, V
+// (channel-major) after a lane-shuffle transpose of 8 x 8 nibbles (4-bit codes) or 4 x 4
+// bytes (Q8_0).
+//
+// Arithmetic is the codec's (tq6_0: SJ-KVaRN §2.1; TBQ4, Q8_0, Q4_0: KV cache math, table,
+// "Worked example" and "rotate first"; HAL #582 §1): one IEEE fp32 rounding per operation
+// through the _rn intrinsics (the unit is also built with -fmad=false), halving-tree sums,
+// round-half-even. The TBQ4 index, the number of boundaries beta_k with u > beta_k, is read
+// from a 2,048-bucket table indexed by the top 11 bits of u (sign, exponent, two mantissa
+// bits): a bucket spans a value ratio of at most 1.25 and the boundaries of the 16-level
+// Lloyd-Max table differ by a ratio of at least 1.28, so a bucket holds at most one
+// boundary and idx = base[bucket] + (u > thr[bucket]), the same fp32 comparison.
+#include <cuda_runtime.h>
+#include <algorithm>
+#include "append_row.cuh"
+
+namespace kvq {
+namespace {
+
+using namespace codec;
+
+constexpr int kRows = 128;          // positions of a group = threads of a CTA
+constexpr int kStages = 3;          // staged tiles per CTA
+constexpr int kTq6Stride = 112;     // 96-byte tq6_0 block row + 16 bytes of padding
+constexpr int kX16Stride = 272;     // 256-byte row of 128 16-bit values + 16 bytes of padding
+constexpr int kBuckets = 2048;      // TBQ4 decision buckets (top 11 bits of an fp32 value)
+
+enum JournalKind { J_TQ6 = 0, J_F16 = 1, J_BF16 = 2 };
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// A tile's addresses, decoded once by thread 0 into a shared slot (the runtime divisions
+// stay out of the other threads' path): rows = its first journal row (block offset
+// included), scales = the tq6_0 scale rows, rec = the body record.
+struct TileSlot {
+    const uint8_t* rows;
+    const uint8_t* scales;
+    uint8_t* rec;
+    int w, b;
+};
+constexpr int kSlots = 64;       // ring of decoded tiles (iteration k in slot k % kSlots)
+constexpr int kSlotBatch = 32;   // slots decoded together, by threads 4j (8 lanes in each warp)
+
+// tile = ((group * H + head) * 2 + w) * (D / 128) + block
+__device__ __forceinline__ TileSlot tile_slot(const Layout& L, const SealParams& p, int tile) {
+    const int nb = L.D / 128;
+    TileSlot t;
+    t.b = tile % nb;
+    int r = tile / nb;
+    t.w = r & 1;
+    r >>= 1;
+    const int h = r % L.H;
+    const SealTaskPos tk = seal_task(p, r / L.H);
+    const int64_t unit = L.unit(tk.layer, tk.slot, h);
+    const int s0 = journal_slot(L, tk.pos0);   // a group's 128 slots are contiguous
+    if (L.journal == KVQ_TQ6_0) {
+        t.rows = jcode_row(L, p.pool, t.w, unit, s0) + 96 * t.b;
+        t.scales = reinterpret_cast<const uint8_t*>(jscale_row(L, p.pool, t.w, unit, s0));
+    } else {
+        t.rows = reinterpret_cast<const uint8_t*>(jexact_row(L, p.pool, t.w, unit, s0)) + 256 * t.b;
+        t.scales = nullptr;
+    }
+    t.rec = body_rec(L, p.pool, t.w, unit, tk.g);
+    return t;
+}
+
+// Issues a tile's 128 journal rows (its 128-channel block) into a stage.
+template <int JK>
+__device__ __forceinline__ void issue_tile(const Layout& L, const TileSlot& t, uint8_t* st) {
+    const int tid = threadIdx.x;
+    if constexpr (JK == J_TQ6) {
+        const int64_t jr = L.jrow_bytes;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            const int c = tid + kRows * i, r = c / 6, k = c - 6 * r;
+            cp_async16(st + r * kTq6Stride + 16 * k, t.rows + r * jr + 16 * k);
+        }
+        // the 128 rows' scales of every block ([128][D/128] fp16, 2D bytes)
+        for (int c = tid; c < L.D / 8; c += kRows) cp_async16(st + kRows * kTq6Stride + 16 * c, t.scales + 16 * c);
+    } else {
+        const int64_t rs = 2LL * L.D;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = (tid >> 4) + 8 * i, k = tid & 15;
+            cp_async16(st + r * kX16Stride + 16 * k, t.rows + r * rs + 16 * k);
+        }
+    }
+}
+
+// Row t of a staged tq6_0 tile: y_i = (code_i - 32) x fp32(d), an exact product.
+// A 32-bit word of the ql plane holds 8 channels' low nibbles; the matching 16 bits of the
+// qh plane their 2-bit high parts, spread here so that each channel's pair lands in bits
+// 4-5 of the byte that holds its nibble. A byte c placed in bits 8-15 under exponent 15
+// reads as the float f = 2^15 + c, and y = fma(f, d, -(2^15 + 32) d): the addend is exact
+// ((2^15 + 32) = 32 x 1025 has 11 significant bits, d at most 11) and so is the result, the
+// representable (c - 32) d, whatever the rounding. (A non-finite d, which only non-finite
+// inputs produce and the status word flags, gives NaN rows here.)
+__device__ __forceinline__ void decode_tq6(const uint8_t* st, int D, int b, float (&y)[128]) {
+    const int t = threadIdx.x;
+    const uint4* rp = reinterpret_cast<const uint4*>(st + t * kTq6Stride);
+    uint32_t q[16], h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint4 x = rp[i];
+        q[4 * i] = x.x; q[4 * i + 1] = x.y; q[4 * i + 2] = x.z; q[4 * i + 3] = x.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint4 x = rp[4 + i];
+        h[4 * i] = x.x; h[4 * i + 1] = x.y; h[4 * i + 2] = x.z; h[4 * i + 3] = x.w;
+    }
+    const float d = h2f(reinterpret_cast<const uint16_t*>(st + kRows * kTq6Stride)[t * (D / 128) + b]);
+    const float a = fmul(-32800.0f, d);
+#pragma unroll
+    for (int w = 0; w < 16; ++w) {
+        uint32_t x = (w & 1) ? (h[w >> 1] >> 16) : (h[w >> 1] & 0xFFFFu);
+        x = (x | (x << 8)) & 0x00FF00FFu;
+        x = (x | (x << 4)) & 0x0F0F0F0Fu;
+        x = (x | (x << 2)) & 0x33333333u;     // channel 8w + e: high pair at bits 4e, 4e + 1
+        const uint32_t ev = (q[w] & 0x0F0F0F0Fu) | ((x << 4) & 0xF0F0F0F0u);   // channels 8w + 2k
+        const uint32_t od = ((q[w] >> 4) & 0x0F0F0F0Fu) | (x & 0xF0F0F0F0u);   // channels 8w + 2k + 1
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float ce = __uint_as_float(__byte_perm(ev, 0x47000000u, 0x7404 + 16 * k));
+            const float co = __uint_as_float(__byte_perm(od, 0x47000000u, 0x7404 + 16 * k));
+            y[8 * w + 2 * k] = __fmaf_rn(ce, d, a);
+            y[8 * w + 2 * k + 1] = __fmaf_rn(co, d, a);
+        }
+    }
+}
+
+// Row t of a staged 16-bit tile, widened exactly.
+template <int JK>
+__device__ __forceinline__ void decode_x16(const uint8_t* st, float (&y)[128]) {
+    const uint4* rp = reinterpret_cast<const uint4*>(st + threadIdx.x * kX16Stride);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint4 x = rp[i];
+        const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int j = 8 * i + 2 * k;
+            if constexpr (JK == J_BF16) {
+                y[j] = __uint_as_float(wv[k] << 16);
+                y[j + 1] = __uint_as_float(wv[k] & 0xFFFF0000u);
+            } else {
+                y[j] = h2f((uint16_t)(wv[k] & 0xFFFFu));
+                y[j + 1] = h2f((uint16_t)(wv[k] >> 16));
+            }
+        }
+    }
+}
+
+// TBQ128 of one 128-channel block in registers: s2 . FWHT_128(s1 . x) x fp32(1/sqrt(128)),
+// butterflies in ascending stride order (the same operations as any other FWHT of the codec).
+__device__ __forceinline__ void rotate_tbq128(float (&y)[128]) {
+#pragma unroll
+    for (int i = 0; i < 128; ++i)
+        if (sign_neg(0, i)) y[i] = -y[i];
+#pragma unroll
+    for (int s = 1; s < 128; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+            if (i & s) continue;
+            const float a = y[i], c = y[i + s];
+            y[i] = fadd(a, c);
+            y[i + s] = fsub(a, c);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+        const float v = sign_neg(1, i) ? -y[i] : y[i];
+        y[i] = fmul(v, kTbqScale);
+    }
+}
+
+// ---------------------------------------------------------------------------- encoders
+// Node (K, I) of the halving tree of y_i^2 over 128 values: node(0, i) = y_i^2 and
+// node(K, i) = node(K-1, i) + node(K-1, i + 128 / 2^K); node(7, 0) is the sum. Evaluated
+// depth first so that few partial sums are live beside the 128 values.
+template <int K, int I>
+__device__ __forceinline__ float sq_tree(const float (&y)[128]) {
+    if constexpr (K == 0) {
+        return fmul(y[I], y[I]);
+    } else {
+        return fadd(sq_tree<K - 1, I>(y), sq_tree<K - 1, I + (128 >> K)>(y));
+    }
+}
+
+// TBQ4 block: n16 = fp16(sqrt(sum y^2)), u = y x (1 / fp32(n16)) (0 when n16 is 0), idx =
+// #{k : u > beta_k}; nibble e of P[m] is the index of channel 8m + e.
+__device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const float2* qt, uint32_t (&P)[16]) {
+    const uint16_t n16 = f2h_bits(__fsqrt_rn(sq_tree<7, 0>(y)));
+    const float n = h2f(n16);
+    const float inv = (n == 0.f) ? 0.f : fdiv(1.0f, n);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        uint32_t acc = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float u = fmul(y[8 * m + e], inv);
+            const float2 ent = qt[__float_as_uint(u) >> 21];
+            const uint32_t idx = (uint32_t)__float_as_int(ent.y) + (u > ent.x ? 1u : 0u);
+            acc |= idx << (4 * e);
+        }
+        P[m] = acc;
+    }
+    return n16;
+}
+
+// Q8_0 (QMAX 127) or Q4_0 (QMAX 7) block of 32 values starting at channel j0: d = fp16(max|x|
+// / QMAX), q = clamp(rint(x x (1 / fp32(d))), -QMAX, QMAX) (inv 0 when d is 0). The clamp is
+// taken before the rounding, which gives the same integer for an integer QMAX; adding
+// 1.5 x 2^23 (+ 8, the Q4_0 zero point) rounds half to even and leaves the code in the low
+// byte. c[k] holds the code bytes of channels j0 + 4k .. j0 + 4k + 3.
+template <int QMAX>
+__device__ __forceinline__ uint16_t encode_q32(const float (&y)[128], int j0, uint32_t (&c)[8]) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(y[j0 + i]));
+    const uint16_t d16 = f2h_bits(fdiv(a, (float)QMAX));
+    const float d = h2f(d16);
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+    constexpr float magic = (QMAX == 127) ? 12582912.0f : 12582920.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float z = fminf(fmaxf(fmul(y[j0 + 4 * k + i], inv), -(float)QMAX), (float)QMAX);
+            r[i] = __float_as_uint(fadd(z, magic));
+        }
+        c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
+    }
+    return d16;
+}
+
+// Two words of code bytes (8 channels, values < 16) as one word of nibbles, the even channel
+// in the low nibble.
+__device__ __forceinline__ uint32_t nibbles_of(uint32_t c0, uint32_t c1) {
+    return __byte_perm(c0 | (c0 >> 4), c1 | (c1 >> 4), 0x6420);
+}
+
+// 8 x 8 transpose of nibbles inside groups of 8 lanes: lane j holds row j (nibble e =
+// column e) on entry and column j (nibble i = row i) on exit. Block swaps of 4 x 4 (16-bit
+// halves), 2 x 2 (bytes) and 1 x 1 (nibbles).
+__device__ __forceinline__ uint32_t transpose_nib8(uint32_t x, int lane) {
+    uint32_t y = __shfl_xor_sync(kFull, x, 4);
+    x = __byte_perm(x, y, (lane & 4) ? 0x3276 : 0x5410);
+    y = __shfl_xor_sync(kFull, x, 2);
+    x = __byte_perm(x, y, (lane & 2) ? 0x3715 : 0x6240);
+    y = __shfl_xor_sync(kFull, x, 1);
+    y = __funnelshift_l(y, y, (lane & 1) ? 28 : 4);
+    const uint32_t keep = (lane & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;
+    return (x & keep) | (y & ~keep);
+}
+
+// 4 x 4 transpose of bytes inside groups of 4 lanes (the same block swaps).
+__device__ __forceinline__ uint32_t transpose_byte4(uint32_t x, int lane) {
+    uint32_t y = __shfl_xor_sync(kFull, x, 2);
+    x = __byte_perm(x, y, (lane & 2) ? 0x3276 : 0x5410);
+    y = __shfl_xor_sync(kFull, x, 1);
+    return __byte_perm(x, y, (lane & 1) ? 0x3715 : 0x6240);
+}
+
+// 4-bit codes of row t, block b: K rows of D/2 bytes; V channel rows of 64 bytes.
+__device__ __forceinline__ void store_nibbles(uint8_t* rec, int D, int b, int w, const uint32_t (&P)[16]) {
+    const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+    if (w == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(rec + (int64_t)t * (D / 2) + 64 * b);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(P[4 * i], P[4 * i + 1], P[4 * i + 2], P[4 * i + 3]);
+    } else {
+        // lane 8a + e ends with channel 8m + e of positions 32 wp + 8a .. + 7
+        uint8_t* base = rec + (int64_t)(128 * b + (lane & 7)) * 64 + 16 * wp + 4 * (lane >> 3);
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+            *reinterpret_cast<uint32_t*>(base + 8 * m * 64) = transpose_nib8(P[m], lane);
+    }
+}
+
+// Q8_0 codes of row t, block b: K rows of D bytes; V channel rows of 128 bytes.
+__device__ __forceinline__ void store_bytes(uint8_t* rec, int D, int b, int w, const uint32_t (&B)[32]) {
+    const int t = threadIdx.x, lane = t & 31, wp = t >> 5;
+    if (w == 0) {
+        uint4* dst = reinterpret_cast<uint4*>(rec + (int64_t)t * D + 128 * b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(B[4 * i], B[4 * i + 1], B[4 * i + 2], B[4 * i + 3]);
+    } else {
+        // lane 4a + e ends with channel 4m + e of positions 32 wp + 4a .. + 3
+        uint8_t* base = rec + (int64_t)(128 * b + (lane & 3)) * 128 + 32 * wp + 4 * (lane >> 2);
+#pragma unroll
+        for (int m = 0; m < 32; ++m)
+            *reinterpret_cast<uint32_t*>(base + 4 * m * 128) = transpose_byte4(B[m], lane);
+    }
+}
+
+// Decision table of the TBQ4 index: bucket k = the floats whose top 11 bits are k. base =
+// boundaries below the bucket's smallest value, thr = the boundary inside it (+inf if none);
+// buckets of infinities and NaNs give 0 (a NaN exceeds no boundary).
+__device__ void build_qtab(float2* qt) {
+    for (int k = threadIdx.x; k < kBuckets; k += blockDim.x) {
+        const uint32_t lo = (uint32_t)k << 21, hi = lo | 0x1FFFFFu;
+        float thr = __uint_as_float(0x7F800000u);
+        int base = 0;
+        if (((lo >> 23) & 0xFF) != 0xFF) {
+            const bool neg = lo >> 31;
+            const float vmin = __uint_as_float(neg ? hi : lo), vmax = __uint_as_float(neg ? lo : hi);
+            for (int j = 0; j < 15; ++j) {
+                const float bj = c_tab.bnd[j];
+                if (bj < vmin) ++base;
+                else if (bj <= vmax) thr = bj;
+            }
+        }
+        qt[k] = make_float2(thr, __int_as_float(base));
+    }
+}
+
+// ---------------------------------------------------------------------------- kernel
+// One instance per journal kind and body family: TBQ4 layouts (K and V TBQ4: the rotation
+// is per layout) or Q8_0 / Q4_0 layouts, so that each instance holds one encoder's code.
+enum BodyFamily { F_TBQ4 = 0, F_Q = 1 };
+
+// Decodes the tiles of iterations k0 .. k0 + kSlotBatch - 1 into the slot ring (threads 4j).
+__device__ __forceinline__ void fill_slots(const Layout& L, const SealParams& p, int n_tiles, TileSlot* slot, int k0) {
+    const int t = threadIdx.x;
+    if ((t & 3) == 0) {
+        const int k = k0 + (t >> 2);
+        const int tile = blockIdx.x + k * gridDim.x;
+        if (tile < n_tiles) slot[k % kSlots] = tile_slot(L, p, tile);
+    }
+}
+
+template <int JK, int FAM>
+__global__ void __launch_bounds__(kRows, JK == J_TQ6 ? 3 : 2)
+seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
+    extern __shared__ __align__(16) uint8_t sm[];
+    __shared__ TileSlot slot[kSlots];
+    float2* qt = reinterpret_cast<float2*>(sm + kStages * stage_bytes);
+    if constexpr (FAM == F_TBQ4) build_qtab(qt);    // read after the first barrier below
+    const int t = threadIdx.x, D = L.D;
+    // Iteration it encodes tile blockIdx.x + it * gridDim.x from stage it % kStages. After the
+    // iteration's barrier every thread has finished iteration it - 1, so its stage takes tile
+    // it + kStages - 1 and the slots it read may be rewritten.
+    fill_slots(L, p, n_tiles, slot, 0);
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+        if ((int)blockIdx.x + k * (int)gridDim.x < n_tiles) issue_tile<JK>(L, slot[k], sm + k * stage_bytes);
+        cp_async_commit();
+    }
+    for (int it = 0;; ++it) {
+        const int tile = blockIdx.x + it * gridDim.x;
+        if (tile >= n_tiles) break;
+        cp_async_wait<kStages - 2>();   // this thread's copies of tile `it` have landed
+        __syncthreads();                // and everyone else's; iteration it - 1 is done
+        const int ahead = it + kStages - 1;
+        if (tile + (kStages - 1) * (int)gridDim.x < n_tiles)
+            issue_tile<JK>(L, slot[ahead % kSlots], sm + (ahead % kStages) * stage_bytes);
+        cp_async_commit();
+        // slots of iterations it + kStages .. (read from iteration it + 1 on) while the ring
+        // holds it .. it + kStages - 1
+        if (it % kSlotBatch == 0) fill_slots(L, p, n_tiles, slot, it + kStages);
+
+        const TileSlot tl = slot[it % kSlots];
+        const uint8_t* st = sm + (it % kStages) * stage_bytes;
+        float y[128];
+        if constexpr (JK == J_TQ6) {
+            decode_tq6(st, D, tl.b, y);
+        } else {
+            decode_x16<JK>(st, y);
+            if constexpr (FAM == F_TBQ4) rotate_tbq128(y);
+        }
+        uint8_t* rec = tl.rec;
+        const int fmt = L.fmt[tl.w];
+        if constexpr (FAM == F_TBQ4) {
+            uint32_t P[16];
+            const uint16_t n16 = encode_tbq4(y, qt, P);
+            store_nibbles(rec, D, tl.b, tl.w, P);
+            reinterpret_cast<uint16_t*>(rec + 64LL * D)[t * (D / 128) + tl.b] = n16;
+            flag_nonfinite(L, p.pool, h2f(n16));
+        } else {
+            uint16_t d16[4];
+            uint32_t C[32];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t c[8];
+                d16[j] = (fmt == KVQ_Q8_0) ? encode_q32<127>(y, 32 * j, c) : encode_q32<7>(y, 32 * j, c);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) C[8 * j + k] = c[k];
+            }
+            int64_t sc_off;
+            if (fmt == KVQ_Q8_0) {
+                store_bytes(rec, D, tl.b, tl.w, C);
+                sc_off = 128LL * D;
+            } else {
+                uint32_t P[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) P[m] = nibbles_of(C[2 * m], C[2 * m + 1]);
+                store_nibbles(rec, D, tl.b, tl.w, P);
+                sc_off = 64LL * D;
+            }
+            *reinterpret_cast<uint2*>(rec + sc_off + 2LL * (t * (D / 32) + 4 * tl.b)) =
+                make_uint2(d16[0] | ((uint32_t)d16[1] << 16), d16[2] | ((uint32_t)d16[3] << 16));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) flag_nonfinite(L, p.pool, h2f(d16[j]));
+        }
+    }
+}
+
+template <int JK, int FAM>
+int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
+    const int stage = (JK == J_TQ6) ? kRows * kTq6Stride + 2 * L.D : kRows * kX16Stride;
+    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? kBuckets * sizeof(float2) : 0);
+    auto fn = seal_rows_kernel<JK, FAM>;
+    int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e) return e;
+    int per_sm = 0, dev = 0;
+    e = (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kRows, smem);
+    if (e) return e;
+    e = (int)cudaGetDevice(&dev);
+    if (e) return e;
+    const int grid = std::min(n_tiles, std::max(per_sm, 1) * query_sm_count(dev));
+    fn<<<grid, kRows, smem, s>>>(L, p, n_tiles, stage);
+    return (int)cudaGetLastError();
+}
+
+template <int FAM>
+int launch_family(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
+    if (L.journal == KVQ_TQ6_0) return launch_rows<J_TQ6, FAM>(L, p, n_tiles, s);
+    if (L.journal == KVQ_BF16) return launch_rows<J_BF16, FAM>(L, p, n_tiles, s);
+    return launch_rows<J_F16, FAM>(L, p, n_tiles, s);
+}
+
+}  // namespace
+
+int launch_seal_rows(const Layout& L, const SealParams& p, void* stream) {
+    const int groups = p.n_layers * p.groups_per_layer;
+    if (groups == 0) return 0;
+    if (L.D % 128) return (int)cudaErrorInvalidValue;
+    const int n_tiles = groups * L.H * 2 * (L.D / 128);
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool tbq = (L.fmt[0] == KVQ_TBQ4);
+    if (tbq != (L.fmt[1] == KVQ_TBQ4)) return (int)cudaErrorInvalidValue;   // one rotation per layout
+    return tbq ? launch_family<F_TBQ4>(L, p, n_tiles, s) : launch_family<F_Q>(L, p, n_tiles, s);
+}
+
+int query_sm_count(int device) {
+    static int cached[64] = {0};
+    if (device < 0 || device >= 64) return 1;
+    if (cached[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0) return 1;
+        cached[device] = n;
+    }
+    return cached[device];
+}
+
+int upload_tables_seal(const FormatTables& t) {
+    return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));
+}
+
+}  // namespace kvq

@@ -105,7 +105,7 @@ kvq_status ensure_tables(int device) {
     std::lock_guard<std::mutex> lk(g_tab_mu);
     if (g_tab_devices.count(device)) return KVQ_OK;
     const FormatTables& t = host_tables();
-    if (upload_tables_codec(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0) return KVQ_ECUDA;
+    if (upload_tables_codec(t) != 0 || upload_tables_seal(t) != 0 || upload_tables_attn(t) != 0 || upload_tables_body(t) != 0) return KVQ_ECUDA;
     g_tab_devices.insert(device);
     return KVQ_OK;
 }

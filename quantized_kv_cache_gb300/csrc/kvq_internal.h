@@ -148,6 +148,7 @@ const FormatTables& host_tables();   // derived once per process (tables.cpp)
 // Kernel launchers (kernels_*.cu). Each returns cudaError_t as int.
 int launch_append(const Layout& lay, const AppendParams& p, void* stream);
 int launch_seal(const Layout& lay, const SealParams& p, void* stream);
+int launch_seal_rows(const Layout& lay, const SealParams& p, void* stream);   // TBQ4 / Q8_0 / Q4_0
 // Events recorded around the decode kernel's launch (both null: none); flags for
 // cudaEventRecordWithFlags (cudaEventRecordExternal while a graph is captured).
 struct LaunchMarks {
@@ -164,6 +165,7 @@ int region_kernel_ok(const Layout& lay);     // 1 if the streaming kernel takes 
 int launch_dequant(const Layout& lay, const void* pool, int layer, int slot, int head, int which,
                    int kind, int64_t p0, int64_t n, float* out, void* stream);
 int upload_tables_codec(const FormatTables& t);
+int upload_tables_seal(const FormatTables& t);
 const kvq_config* cache_config(const kvq_cache* c);   // the config a handle was created with
 int upload_tables_attn(const FormatTables& t);
 int query_sm_count(int device);
