@@ -338,6 +338,15 @@ def seal_launches(w, states):
     return n
 
 
+# fp32 operations of the KVarN seal per encoded value: 16 balancing passes x (sum, deviation,
+# square, variance sum, scale) + rounding (divide by C, subtract Z, scale by 1/S, rint, and the
+# row min / max); plus the tq6_0 dequantize (1) or the HAD256 rotation of a 16-bit row (8 + 1)
+KVARN_OPS_PER_VALUE = 16 * 5 + 6
+KVARN_TQ6_OPS = 1
+KVARN_ROT_OPS = 9
+FP32_PEAK_TOPS = round(152 * 128 * 2.070e9 / 1e12, 2)
+
+
 def bulk_seal_prefill(w, cache, ds, seq_ids, stream, max_groups=32):
     """Appends, to every sequence of every layer, as many whole groups (at most max_groups)
     as its journal has room for beyond the newest keep positions. Returns the groups added."""
@@ -423,9 +432,18 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
     write = H * (record_bytes(w.k_body, D) + record_bytes(w.v_body, D))
     hbm, _ = peaks()
     gps = groups / t if t > 0 else None
-    return {"groups_per_s": round(gps, 1) if gps else None, "groups": groups, "seconds": round(t, 6),
-            "bytes_per_group": read + write, "hbm_frac": round(gps * (read + write) / 1e9 / hbm, 4) if gps else None,
-            "kind": kind, "group": "128 positions x 1 layer x all KV heads x K and V"}
+    res = {"groups_per_s": round(gps, 1) if gps else None, "groups": groups, "seconds": round(t, 6),
+           "bytes_per_group": read + write, "hbm_frac": round(gps * (read + write) / 1e9 / hbm, 4) if gps else None,
+           "kind": kind, "group": "128 positions x 1 layer x all KV heads x K and V"}
+    if w.k_body.startswith("kvarn") and gps:
+        # KVarN's balancing is bound by fp32 arithmetic: the method's fp32 operations per value
+        # (no fused multiply-adds in the codec) against the fp32 lanes' issue rate
+        per_value = KVARN_OPS_PER_VALUE + (KVARN_ROT_OPS if w.journal != "tq6_0" else KVARN_TQ6_OPS)
+        ops = gps * 128 * H * 2 * D * per_value
+        res["alu"] = {"bound": "alu", "ops_per_value": per_value, "achieved_tops": round(ops / 1e12, 3),
+                      "peak_tops": FP32_PEAK_TOPS, "frac": round(ops / 1e12 / FP32_PEAK_TOPS, 4),
+                      "peak_source": "152 SMs x 128 fp32 lanes x 2,070 MHz, one operation per lane per cycle"}
+    return res
 
 
 def measure_e2e(w, cache, inp, seq_ids, out, stream, K, total_bytes, world):

@@ -450,7 +450,279 @@ int launch_family(const Layout& L, const SealParams& p, int n_tiles, cudaStream_
     return launch_rows<J_F16, FAM>(L, p, n_tiles, s);
 }
 
+// ---------------------------------------------------------------------------- KVarN seal
+// One 128 x 256 tile (SJ-KVaRN §2.2): HAD256-rotated journal rows, 16 alternating row/column
+// passes of spread balancing (rows first), per-row b-bit rounding with fp16 scales (SJ-KVaRN
+// §2.2, §3). CTA = 16 warps on one tile = (group, KV head, K or V, 256-channel half). The
+// tile's journal rows are staged once with cp.async; both reads of the rows (into the fp32
+// tile Y, and again for the codes, which use the unbalanced values) decode them from shared
+// memory. A balancing pass gives each row to 4 threads (each column to 2) holding 64 values
+// apiece, so most levels of the halving sums run in registers. The arithmetic is the
+// codec's, operation for operation.
+constexpr int kYS = 260;            // Y row stride (floats): 4 t + q covers the 32 banks in a row pass
+constexpr int kKvThreads = 512;
+constexpr int kKvWarps = kKvThreads / 32;
+
+__device__ __forceinline__ float warp_min(float v) {
+    for (int s = 16; s >= 1; s >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, s));
+    return v;
+}
+template <int JK>
+struct KvStage {
+    static constexpr int ROW = (JK == J_TQ6) ? 192 : 512;    // one row of the half (2 tq6_0 blocks / 256 x 16 bit)
+};
+
+// Values of channels lane + 32k (k < 8) of row t of the staged half, in the body's domain:
+// tq6_0 codes dequantized (the ring rows are rotated at append), 16-bit rows widened and
+// rotated here by HAD256.
+template <int JK>
+__device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, int t, int nsc, int half, int lane,
+                                       float (&v)[8]) {
+    const uint8_t* row = st + t * KvStage<JK>::ROW;
+    if constexpr (JK == J_TQ6) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int b = k >> 2, j = lane + 32 * (k & 3);
+            const uint8_t* blk = row + 96 * b;
+            const int lo = (blk[j >> 1] >> ((j & 1) * 4)) & 15;
+            const int hi = (blk[64 + (j >> 2)] >> ((j & 3) * 2)) & 3;
+            v[k] = fmul((float)((lo | (hi << 4)) - 32), h2f(sc[t * nsc + 2 * half + b]));
+        }
+    } else {
+        const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = x16_to_f(r16[lane + 32 * k], JK == J_BF16 ? KVQ_BF16 : KVQ_F16);
+        warp_fwht<8>(v, lane);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
+    }
+}
+
+// One balancing pass over the tile, lines of n = 256 (rows) or 128 (columns) values: mean
+// and population spread by halving trees, sigma <= 2^-20 counts as 1, line /= sigma, the
+// line's scale *= sigma. A line belongs to P = n / 64 threads (adjacent lanes); thread q
+// holds the values q + P i (i < 64), so the tree levels of stride >= P are in-thread and the
+// last log2(P) levels cross the P lanes (every lane ends with the same sum, the adds being
+// commutative). ROWS: 128 rows x 4 threads; else 256 columns x 2 threads.
+template <bool ROWS>
+__device__ __forceinline__ void kv_pass(float* Y, float* scale) {
+    constexpr int P = ROWS ? 4 : 2;
+    constexpr float INV_N = ROWS ? 1.0f / 256.0f : 1.0f / 128.0f;
+    const int line = threadIdx.x / P, q = threadIdx.x % P;
+    // element i of this thread: row-major index of value q + P i of the line
+    auto at = [&](int i) -> float& {
+        return ROWS ? Y[line * kYS + q + P * i] : Y[(q + P * i) * kYS + line];
+    };
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 64; ++i) x[i] = at(i);
+    // halving-tree sum over the line of leaf(i): first level x-pairs (i, i + 32) in-thread
+    auto line_sum = [&](auto leaf) {
+        float a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = fadd(leaf(i), leaf(i + 32));
+#pragma unroll
+        for (int n = 16; n >= 1; n >>= 1) {
+#pragma unroll
+            for (int i = 0; i < n; ++i) a[i] = fadd(a[i], a[i + n]);
+        }
+        float t = a[0];
+#pragma unroll
+        for (int sft = P / 2; sft >= 1; sft >>= 1) t = fadd(t, __shfl_xor_sync(kFull, t, sft));
+        return t;
+    };
+    const float mu = fmul(line_sum([&](int i) { return x[i]; }), INV_N);
+    const float var = line_sum([&](int i) { const float d = fsub(x[i], mu); return fmul(d, d); });
+    float sig = __fsqrt_rn(fmul(var, INV_N));
+    if (sig <= 9.5367431640625e-07f) sig = 1.f;     // 2^-20
+    const float inv = fdiv(1.0f, sig);
+#pragma unroll
+    for (int i = 0; i < 64; ++i) at(i) = fmul(x[i], inv);
+    if (q == 0) scale[line] = fmul(scale[line], sig);
+}
+
+// grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: Y [128][257] fp32 and
+// the staged rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit:
+// [128][512]). Once the row parameters are taken, Y is dead and holds the codes, one byte
+// per value in rows of 1,028 bytes (257 words): a walk down a column (the V record is
+// channel-major) then touches a different bank for every other row.
+template <int JK>
+__global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
+    constexpr int ROW = KvStage<JK>::ROW;
+    constexpr int CS = 1028;                                // code row stride (bytes, 257 words)
+    const SealTaskPos tk = seal_task(p, blockIdx.x);
+    const int nh = L.D / 256;
+    const int h = blockIdx.y, w = blockIdx.z / nh, half = blockIdx.z % nh;
+    const int fmt = L.fmt[w];
+    const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+    const float Q = (float)((1 << bits) - 1);
+    const int64_t unit = L.unit(tk.layer, tk.slot, h);
+    extern __shared__ __align__(16) uint8_t kv_sm[];
+    float* Y = reinterpret_cast<float*>(kv_sm);                      // [128][kYS]
+    uint8_t* st = kv_sm + 128 * kYS * sizeof(float);                 // staged rows
+    uint16_t* sc = reinterpret_cast<uint16_t*>(st + 128 * ROW);      // tq6_0 scales [128][D/128]
+    uint8_t* codes = kv_sm;                                          // [128][CS], over Y
+    __shared__ float r[128], c[256], invS[128], Zs[128], invC[256];
+    __shared__ uint16_t S16[128], Z16[128], C16[256];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nsc = L.D / 128;
+
+    // stage the half's 128 journal rows (contiguous slots)
+    {
+        const int s0 = journal_slot(L, tk.pos0);
+        if constexpr (JK == J_TQ6) {
+            const uint8_t* src = jcode_row(L, p.pool, w, unit, s0) + 192 * half;
+            const int64_t jr = L.jrow_bytes;
+            for (int ci = threadIdx.x; ci < 128 * 12; ci += kKvThreads) {
+                const int rr = ci / 12, k = ci - 12 * rr;
+                cp_async16(st + rr * ROW + 16 * k, src + rr * jr + 16 * k);
+            }
+            const uint8_t* ss = reinterpret_cast<const uint8_t*>(jscale_row(L, p.pool, w, unit, s0));
+            for (int ci = threadIdx.x; ci < L.D / 8; ci += kKvThreads)
+                cp_async16(reinterpret_cast<uint8_t*>(sc) + 16 * ci, ss + 16 * ci);
+        } else {
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(jexact_row(L, p.pool, w, unit, s0)) + 512 * half;
+            const int64_t rs = 2LL * L.D;
+            for (int ci = threadIdx.x; ci < 128 * 32; ci += kKvThreads) {
+                const int rr = ci >> 5, k = ci & 31;
+                cp_async16(st + rr * ROW + 16 * k, src + rr * rs + 16 * k);
+            }
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+    }
+    for (int j = threadIdx.x; j < 256; j += kKvThreads) c[j] = 1.f;
+    if (threadIdx.x < 128) r[threadIdx.x] = 1.f;
+    __syncthreads();
+    for (int t = warp; t < 128; t += kKvWarps) {
+        float v[8];
+        kv_row<JK>(st, sc, t, nsc, half, lane, v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) Y[t * kYS + lane + 32 * k] = v[k];
+    }
+    __syncthreads();
+
+    for (int pass = 0; pass < 16; ++pass) {
+        if ((pass & 1) == 0) kv_pass<true>(Y, r);
+        else kv_pass<false>(Y, c);
+        __syncthreads();
+    }
+
+    // row rounding parameters
+    for (int t = warp; t < 128; t += kKvWarps) {
+        float lo = 3.4e38f, hi = -3.4e38f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float y = Y[t * kYS + lane + 32 * k];
+            lo = fminf(lo, y);
+            hi = fmaxf(hi, y);
+        }
+        lo = warp_min(lo);
+        hi = warp_max(hi);
+        if (lane == 0) {
+            const uint16_t s16 = f2h_bits(fdiv(fmul(r[t], fsub(hi, lo)), Q));
+            const uint16_t z16 = f2h_bits(fmul(r[t], lo));
+            S16[t] = s16;
+            Z16[t] = z16;
+            const float sv = h2f(s16);
+            invS[t] = (sv == 0.f) ? 0.f : fdiv(1.0f, sv);
+            Zs[t] = h2f(z16);
+            flag_nonfinite(L, p.pool, sv);
+            flag_nonfinite(L, p.pool, Zs[t]);
+        }
+    }
+    for (int j = threadIdx.x; j < 256; j += kKvThreads) {
+        const uint16_t c16 = f2h_bits(c[j]);
+        C16[j] = c16;
+        invC[j] = fdiv(1.0f, h2f(c16));
+        flag_nonfinite(L, p.pool, h2f(c16));
+    }
+    __syncthreads();
+
+    // codes from the unbalanced rows (decoded again from the stage: identical bits) and the
+    // stored scales
+    for (int t = warp; t < 128; t += kKvWarps) {
+        float v[8];
+        kv_row<JK>(st, sc, t, nsc, half, lane, v);
+        const float is = invS[t], z = Zs[t];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int j = lane + 32 * k;
+            float q = 0.f;
+            if (is != 0.f) {
+                q = rintf(fmul(fsub(fmul(v[k], invC[j]), z), is));
+                q = fminf(fmaxf(q, 0.f), Q);
+            }
+            codes[t * CS + j] = (uint8_t)q;
+        }
+    }
+    __syncthreads();
+
+    uint8_t* rec = body_rec(L, p.pool, w, unit, tk.g) + (int64_t)half * (4096 * bits + 1152);
+    if (w == 0) {           // K: token-major low plane [128][128], high plane [128][32]
+        for (int i = threadIdx.x; i < 128 * 128; i += kKvThreads) {
+            const int t = i >> 7, j = 2 * (i & 127);
+            rec[i] = (uint8_t)((codes[t * CS + j] & 15) | ((codes[t * CS + j + 1] & 15) << 4));
+        }
+        if (bits == 5) {
+            for (int i = threadIdx.x; i < 128 * 32; i += kKvThreads) {
+                const int t = i >> 5, j0 = 8 * (i & 31);
+                uint8_t b = 0;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) b |= (uint8_t)(((codes[t * CS + j0 + m] >> 4) & 1) << m);
+                rec[16384 + i] = b;
+            }
+        }
+    } else {                // V: channel-major low plane [256][64], high plane [256][16]
+        for (int i = threadIdx.x; i < 256 * 64; i += kKvThreads) {
+            const int j = i >> 6, t = 2 * (i & 63);
+            rec[i] = (uint8_t)((codes[t * CS + j] & 15) | ((codes[(t + 1) * CS + j] & 15) << 4));
+        }
+        if (bits == 5) {
+            for (int i = threadIdx.x; i < 256 * 16; i += kKvThreads) {
+                const int j = i >> 4, t0 = 8 * (i & 15);
+                uint8_t b = 0;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) b |= (uint8_t)(((codes[(t0 + m) * CS + j] >> 4) & 1) << m);
+                rec[16384 + i] = b;
+            }
+        }
+    }
+    uint16_t* sb = reinterpret_cast<uint16_t*>(rec + 4096 * bits);
+    for (int i = threadIdx.x; i < 576; i += kKvThreads) {
+        uint16_t x = 0;
+        if (i < 128) x = S16[i];
+        else if (i < 256) x = Z16[i - 128];
+        else if (i < 512) x = C16[i - 256];
+        sb[i] = x;
+    }
+}
+
+template <int JK>
+int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
+    constexpr int ROW = KvStage<JK>::ROW;
+    const size_t smem = 128 * kYS * sizeof(float) + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
+    int e = (int)cudaFuncSetAttribute(seal_kvarn_kernel<JK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e) return e;
+    dim3 grid(groups, L.H, 2 * (L.D / 256));
+    seal_kvarn_kernel<JK><<<grid, kKvThreads, smem, s>>>(L, p);
+    return (int)cudaGetLastError();
+}
+
 }  // namespace
+
+int launch_seal(const Layout& L, const SealParams& p, void* stream) {
+    const int groups = p.n_layers * p.groups_per_layer;
+    if (groups == 0) return 0;
+    if (L.fmt[0] == KVQ_KVARN4 || L.fmt[0] == KVQ_KVARN5) {
+        if (L.D % 256) return (int)cudaErrorInvalidValue;
+        cudaStream_t s = (cudaStream_t)stream;
+        if (L.journal == KVQ_TQ6_0) return launch_kvarn<J_TQ6>(L, p, groups, s);
+        if (L.journal == KVQ_BF16) return launch_kvarn<J_BF16>(L, p, groups, s);
+        return launch_kvarn<J_F16>(L, p, groups, s);
+    }
+    return launch_seal_rows(L, p, stream);
+}
 
 int launch_seal_rows(const Layout& L, const SealParams& p, void* stream) {
     const int groups = p.n_layers * p.groups_per_layer;

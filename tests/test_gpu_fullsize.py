@@ -9,7 +9,7 @@ the same appends and seals from the host-side generator (the same counter-based 
 the test compares:
 
 - the sequence's lengths (N, S);
-- sampled body records (first, middle and last group, K and V) byte for byte;
+- every body record of the sampled heads (K and V) byte for byte;
 - the newest journal rows (tq6_0 codes and scales, or exact rows) and exact-tail rows;
 - the decode output of the head's query group against the fp64 oracle attention over the
   same regions, within the decode tolerance |gpu - oracle| <= 1e-3 + 2e-3 |oracle|.
@@ -99,6 +99,14 @@ def _replay(w, seq, h):
     return hc
 
 
+def _check_records(w, hc, body, role, groups, where):
+    rb = len(hc.record_bytes(0, role))
+    for g in groups:
+        got = body[g * rb:(g + 1) * rb]
+        diff = np.flatnonzero(got != hc.record_bytes(g, role))
+        assert diff.size == 0, f"{w.name} {where} {role} group {g}: {diff.size} bytes differ, first {diff[:6]}"
+
+
 def _region_bytes(cache, seq, head, which, region):
     ptr, nb = _lib.kv_region_ptr(cache.h, 0, seq, head, which, region)
     off = ptr - cache.pool.data_ptr()
@@ -136,12 +144,7 @@ def test_fullsize_sampled_records_and_rows(run):
         for wi, role in ((0, "K"), (1, "V")):
             if ng:
                 body = _region_bytes(cache, seq, h, wi, _lib.REGION_BODY)
-                rb = len(hc.record_bytes(0, role))
-                for g in sorted({0, ng // 2, ng - 1}):
-                    ref = hc.record_bytes(g, role)
-                    got = body[g * rb:(g + 1) * rb]
-                    diff = np.flatnonzero(got != ref)
-                    assert diff.size == 0, f"{w.name} seq {seq} head {h} {role} group {g}: {diff.size} bytes differ"
+                _check_records(w, hc, body, role, range(ng), f"seq {seq} head {h}")
             # the newest positions of the journal (and the exact tail with a tq6_0 ring)
             newest = range(max(hc.S, hc.N - 4), hc.N)
             if w.journal == "tq6_0":
@@ -172,3 +175,26 @@ def test_fullsize_sampled_attention(run):
         got = out[seq, h * G:(h + 1) * G].astype(np.float64)
         err = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
         assert np.all(err <= 0), f"{w.name} seq {seq} head {h}: excess {err.max():.3g}"
+
+
+def test_fullsize_bulk_seal(run):
+    """The bulk seal of longctx_tbq4 (every sequence's groups older than the newest keep, one
+    launch): the sampled heads' new records against the oracle's seal of the same groups."""
+    w, cache, inp, out, status = run
+    if w.name != "longctx_tbq4":
+        pytest.skip("the bulk seal belongs to longctx_tbq4")
+    seq_ids = list(range(len(w.contexts)))
+    before = {seq: cache.state(0, seq)[1] for seq in seq_ids}
+    groups = _lib.kv_seal(cache.h, -1, seq_ids, w.keep, 0)
+    torch.cuda.synchronize()
+    assert _lib.kv_get_status(cache.h) == 0
+    assert groups == sum((cache.state(0, s)[1] - before[s]) // 128 for s in seq_ids) == 512
+    for seq, h in SAMPLES[w.name]:
+        hc = _oracle_head(w, seq, h)
+        g0 = (hc.S - 128) // 128
+        hc.seal(w.keep)
+        assert cache.state(0, seq) == (hc.N, hc.S)
+        g1 = (hc.S - 128) // 128
+        for wi, role in ((0, "K"), (1, "V")):
+            body = _region_bytes(cache, seq, h, wi, _lib.REGION_BODY)
+            _check_records(w, hc, body, role, range(g0, g1), f"bulk seal seq {seq} head {h}")
