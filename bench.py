@@ -61,9 +61,9 @@ def peaks():
 # profiles/decode_attn_launches.md gives the command and the per-kernel split.
 MEASURED_TRAFFIC = {
     "hybrid27b_kvarn44": 42.83e6,
-    "fa14b_q8q4": 221.15e6,
-    "longctx_tbq4": 749.89e6,
-    "widehead_kvarn55": 191.55e6,
+    "fa14b_q8q4": 221.25e6,
+    "longctx_tbq4": 749.88e6,
+    "widehead_kvarn55": 190.68e6,
 }
 
 
