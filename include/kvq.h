@@ -93,6 +93,27 @@ typedef struct kvq_cache kvq_cache;  /* opaque host-side handle */
  * Pure host arithmetic; out is a host pointer. KVQ_EINVAL on a bad config. */
 kvq_status kv_bytes_per_token(const kvq_config* cfg, kvq_bytes* out);
 
+/* kv_auto_tier — the least compression that keeps a whole cache of `tokens` positions inside
+ * `budget_bytes` (HAL #582 §5 P1, "auto KV-tier policy at boot": walk the ladder f16 ->
+ * q8_0 K / q8_0 V -> q8_0 K / q4_0 V and take the first rung whose cost fits; the floor rung
+ * when none does). A rung's cost is tokens x layers x KV heads x head_dim x (bytes per K value
+ * + bytes per V value), the per-cell byte sum the page budgets with (f16 2 B, q8_0 34/32 B,
+ * q4_0 18/32 B per value). Reading: the page's last rung, q5_1 K / q4_0 V, is not one of this
+ * library's body formats, so the floor here is q8_0 / q4_0; the f16 rung means an
+ * uncompressed cache (*k_fmt = *v_fmt = KVQ_F16: an F16 journal that holds the context,
+ * never sealed). Only n_layers, n_kv_heads and head_dim of cfg are read. Host arithmetic,
+ * host pointers out: the chosen formats and their cost in bytes. KVQ_OK when the chosen rung
+ * fits, KVQ_ENOSPC with the floor rung when none fits, KVQ_EINVAL on a null pointer, a
+ * non-positive shape or tokens < 0. */
+kvq_status kv_auto_tier(const kvq_config* cfg, int64_t tokens, uint64_t budget_bytes, int32_t* k_fmt,
+                        int32_t* v_fmt, uint64_t* cost_bytes);
+
+/* kv_tier_budget — the cache budget of that policy (HAL #582 §5 P1): the device's free bytes,
+ * capped by a total target (0: no target), less the bytes already resident and a 1.5 GiB
+ * compute reserve; 0 when that is negative. Host arithmetic; budget is a host pointer.
+ * KVQ_EINVAL on a null pointer. */
+kvq_status kv_tier_budget(uint64_t free_bytes, uint64_t resident_bytes, uint64_t target_bytes, uint64_t* budget);
+
 /* kv_required_bytes — device pool bytes for kv_create and workspace bytes for
  * kv_decode_attn with up to cfg->max_seqs sequences per call. Host pointers out. */
 kvq_status kv_required_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* workspace_bytes);

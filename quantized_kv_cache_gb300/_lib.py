@@ -17,6 +17,7 @@ FMT_NAMES = {"f16": F16, "bf16": BF16, "tq6_0": TQ6_0, "tbq4": TBQ4, "q8_0": Q8_
              "kvarn4": KVARN4, "kvarn5": KVARN5}
 # regions
 REGION_SINK, REGION_JOURNAL, REGION_JOURNAL_SCALE, REGION_TAIL, REGION_BODY = range(5)
+ENOSPC = 2
 STATUS = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ENOSPC", 3: "KVQ_EUNSUPPORTED", 4: "KVQ_ECUDA", 5: "KVQ_EDEVICE"}
 
 
@@ -51,6 +52,9 @@ SZ = ctypes.c_size_t
 _SIGS = {
     "kv_bytes_per_token": [ctypes.POINTER(kvq_config), ctypes.POINTER(kvq_bytes)],
     "kv_required_bytes": [ctypes.POINTER(kvq_config), ctypes.POINTER(SZ), ctypes.POINTER(SZ)],
+    "kv_auto_tier": [ctypes.POINTER(kvq_config), I64, ctypes.c_uint64, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                     ctypes.POINTER(ctypes.c_uint64)],
+    "kv_tier_budget": [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)],
     "kv_create": [ctypes.POINTER(kvq_config), P, SZ, ctypes.c_int, ctypes.POINTER(P)],
     "kv_destroy": [P],
     "kv_reset": [P, ctypes.c_int, ctypes.c_int],
@@ -111,6 +115,22 @@ def kv_bytes_per_token(cfg):
     out = kvq_bytes()
     _check("kv_bytes_per_token", load().kv_bytes_per_token(ctypes.byref(cfg), ctypes.byref(out)))
     return {f: getattr(out, f) for f, _ in kvq_bytes._fields_}
+
+
+def kv_auto_tier(cfg, tokens, budget_bytes):
+    """(k_fmt, v_fmt, cost_bytes, fits): the ladder rung kv_auto_tier picks."""
+    k, v, cost = I32(), I32(), ctypes.c_uint64()
+    code = load().kv_auto_tier(ctypes.byref(cfg), tokens, budget_bytes, ctypes.byref(k), ctypes.byref(v),
+                               ctypes.byref(cost))
+    if code not in (0, ENOSPC):
+        raise KVQError("kv_auto_tier", code)
+    return k.value, v.value, cost.value, code == 0
+
+
+def kv_tier_budget(free_bytes, resident_bytes, target_bytes=0):
+    out = ctypes.c_uint64()
+    _check("kv_tier_budget", load().kv_tier_budget(free_bytes, resident_bytes, target_bytes, ctypes.byref(out)))
+    return out.value
 
 
 def kv_required_bytes(cfg):

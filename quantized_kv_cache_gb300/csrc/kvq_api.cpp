@@ -192,6 +192,37 @@ kvq_status kv_bytes_per_token(const kvq_config* cfg, kvq_bytes* out) {
     return KVQ_OK;
 }
 
+kvq_status kv_auto_tier(const kvq_config* cfg, int64_t tokens, uint64_t budget_bytes, int32_t* k_fmt,
+                        int32_t* v_fmt, uint64_t* cost_bytes) {
+    if (!cfg || !k_fmt || !v_fmt || !cost_bytes || tokens < 0) return KVQ_EINVAL;
+    if (cfg->n_layers <= 0 || cfg->n_kv_heads <= 0 || cfg->head_dim <= 0) return KVQ_EINVAL;
+    // bytes per 32 values of each rung's K and V format: f16 64, q8_0 34, q4_0 18
+    struct Rung { int32_t k, v; uint64_t k32, v32; };
+    static const Rung ladder[] = {{KVQ_F16, KVQ_F16, 64, 64}, {KVQ_Q8_0, KVQ_Q8_0, 34, 34},
+                                  {KVQ_Q8_0, KVQ_Q4_0, 34, 18}};
+    const uint64_t cells = (uint64_t)tokens * (uint64_t)cfg->n_layers * (uint64_t)cfg->n_kv_heads *
+                           (uint64_t)cfg->head_dim;   // values per K (and per V)
+    const int n = (int)(sizeof(ladder) / sizeof(ladder[0]));
+    for (int i = 0; i < n; ++i) {
+        const uint64_t cost = cells / 32 * (ladder[i].k32 + ladder[i].v32) +
+                              cells % 32 * (ladder[i].k32 + ladder[i].v32) / 32;
+        *k_fmt = ladder[i].k;
+        *v_fmt = ladder[i].v;
+        *cost_bytes = cost;
+        if (cost <= budget_bytes) return KVQ_OK;
+    }
+    return KVQ_ENOSPC;   // the floor rung, which does not fit either
+}
+
+kvq_status kv_tier_budget(uint64_t free_bytes, uint64_t resident_bytes, uint64_t target_bytes, uint64_t* budget) {
+    if (!budget) return KVQ_EINVAL;
+    constexpr uint64_t kReserve = 3ull << 29;   // 1.5 GiB compute reserve
+    const uint64_t cap = (target_bytes > 0 && target_bytes < free_bytes) ? target_bytes : free_bytes;
+    const uint64_t used = resident_bytes + kReserve;
+    *budget = cap > used ? cap - used : 0;
+    return KVQ_OK;
+}
+
 kvq_status kv_required_bytes(const kvq_config* cfg, size_t* pool_bytes, size_t* workspace_bytes) {
     if (!cfg) return KVQ_EINVAL;
     Layout L;
