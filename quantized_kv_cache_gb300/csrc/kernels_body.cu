@@ -149,11 +149,19 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
         bulk_g2s(dst, kb + (size_t)i * recK, recK, fb);
         bulk_g2s(dst + v_off, vb + (size_t)i * recV, recV, fb);
     };
+    // the query rows of the head (G x D fp16, contiguous) land in the fragment area first: the
+    // set-up waits on them (full[4]) while the first groups' records stream in behind them
+    const int G = L.G;
+    const uint16_t* qsrc = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
+    const uint32_t qbar = su32(&full[4]);
     int issued = 0;
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int i = 0; i < nst; ++i) mbar_init(su32(&full[i]), 1);
+        mbar_init(qbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+        mbar_expect_tx(qbar, (uint32_t)(G * D * 2));
+        bulk_g2s(su32(qb), qsrc, (uint32_t)(G * D * 2), qbar);
         for (; issued < min(nst, ngroups); ++issued) issue(issued);
     }
     __syncthreads();
@@ -169,16 +177,16 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
 
     // ================================================================== consumers: set-up
     const int g = lane >> 2, tq = lane & 3;
-    const int G = L.G;
     if (Gm::LUT) {
         for (int i = threadIdx.x; i < 256 * 32; i += kCT) {
             const int by = i >> 5;
             lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
         }
     }
-    __half* qr = reinterpret_cast<__half*>(qb);           // rotated query rows, fp16 [NQ][D]
+    __half* qr = reinterpret_cast<__half*>(qb);           // query rows, fp16 [NQ][D], rotated in place
+    mbar_wait(qbar, 0, status, &s_abort);
     {
-        const uint16_t* q = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
+        const uint16_t* q = reinterpret_cast<const uint16_t*>(qr);
         const int rot = L.rot;
         if (rot == ROT_HAD256) {
             if constexpr (D >= 256) {
@@ -738,6 +746,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     csync();
     if (threadIdx.x == 0 && s_abort) {   // a wait timed out: wait (bounded, fresh limit) for copies in flight
         s_abort = 0;
+        mbar_wait(qbar, 0, status, &s_abort);
         for (int i = max(0, issued - nst); i < issued; ++i)
             mbar_wait(su32(&full[i % nst]), (i / nst) & 1, status, &s_abort);
     }
