@@ -114,8 +114,9 @@ __device__ __forceinline__ Item decode_item(const AttnParams& p, int item) {
     int r = 0;
     while (r < 3 && c >= s.nchunk[r]) { c -= s.nchunk[r]; ++r; }
     it.kind = s.kind[r];
-    it.t0 = s.lo[r] + c * p.chunk;
-    it.t1 = min(it.t0 + p.chunk, s.hi[r]);
+    const int ck = (it.kind == RK_RING) ? p.ring_chunk : p.chunk;
+    it.t0 = s.lo[r] + c * ck;
+    it.t1 = min(it.t0 + ck, s.hi[r]);
     it.slot = s.slot;
     return it;
 }

@@ -418,13 +418,34 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     // item spends most of its time on per-item set-up (query rotation, pipeline fill, partial)
     constexpr int64_t kMinBodyGroups = 6;
     body_items = std::min(body_items, std::max<int64_t>(L.H, (body_groups * L.H + kMinBodyGroups - 1) / kMinBodyGroups));
+    // tq6_0 ring spans take chunks twice as long when that keeps the whole launch within one
+    // wave of resident CTAs: a second, partial wave of region items costs a whole item's time
+    // while most slots idle (measured on the 32k-position hybrid shape: +5.6%), whereas a launch
+    // that spans several waves anyway balances better with the finer chunks
+    int64_t ring_chunk = chunk;
+    if (fused) {
+        auto count = [&](int64_t rc) {
+            int64_t n = 0;
+            for (int i = 0; i < n_seq; ++i) {
+                const SeqSpan& s = p.seq[i];
+                for (int r = 0; r < 4; ++r) {
+                    const int64_t ck = (s.kind[r] == RK_RING) ? rc : chunk;
+                    n += (s.hi[r] - s.lo[r] + ck - 1) / ck;
+                }
+            }
+            return n * L.H;
+        };
+        const int64_t slots = (int64_t)std::max(1, decode_ctas_per_sm(L)) * c->sm_count;
+        if (body_items + count(chunk) > slots && body_items + count(2 * chunk) <= slots) ring_chunk = 2 * chunk;
+    }
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {
             SeqSpan& s = p.seq[i];
             s.items_per_head = 0;
             for (int r = 0; r < 4; ++r) {
-                s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + chunk - 1) / chunk);
+                const int64_t ck = (s.kind[r] == RK_RING) ? ring_chunk : chunk;
+                s.nchunk[r] = (int32_t)((s.hi[r] - s.lo[r] + ck - 1) / ck);
                 s.items_per_head += s.nchunk[r];
             }
             s.first_item = (int32_t)items;
@@ -467,9 +488,10 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
             break;
         }
         chunk *= 2;
+        ring_chunk *= 2;
         body_items = std::max<int64_t>(L.H, body_items / 2);
     }
-    p.body_chunk = 0;
+    p.ring_chunk = (int32_t)ring_chunk;
     p.chunk = (int32_t)chunk;
     const int e = launch_decode(L, p, stream, marks);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;

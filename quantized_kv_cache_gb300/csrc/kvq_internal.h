@@ -108,7 +108,7 @@ struct AttnParams {
     const uint16_t* vnew;
     int32_t layer, n_seq, chunk, total_items;
     int32_t n_region_items;  // region items come first, body items after them
-    int32_t body_chunk;      // unused (body items split each head's groups evenly)
+    int32_t ring_chunk;      // positions per region item of a tq6_0 ring span (others: chunk)
     SeqSpan seq[kMaxSeqPerCall];
 };
 

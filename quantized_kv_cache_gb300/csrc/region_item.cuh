@@ -122,8 +122,9 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     int cidx = local % sp.items_per_head, r = 0;
     while (r < 3 && cidx >= sp.nchunk[r]) { cidx -= sp.nchunk[r]; ++r; }
     const int kind = sp.kind[r];
-    const int t0 = sp.lo[r] + cidx * p.chunk;
-    const int t1 = min(t0 + p.chunk, sp.hi[r]);
+    const int ck = (kind == RK_RING) ? p.ring_chunk : p.chunk;
+    const int t0 = sp.lo[r] + cidx * ck;
+    const int t1 = min(t0 + ck, sp.hi[r]);
     const bool ring = Gm::RING && (kind == RK_RING);
     // bf16 exact rows: bf16 mma, the query and P' each split into bf16 high and low parts
     const bool bf = !ring && kind != RK_SINK && ((kind == RK_TAIL ? L.tail_fmt : L.journal) == KVQ_BF16);
