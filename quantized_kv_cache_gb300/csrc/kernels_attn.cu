@@ -515,6 +515,20 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
     auto item_of = [&](int c) { return c < cnt_r ? first + c : bfirst + (c - cnt_r); };
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t stride = 2 * NQ + NQ * D;
+    // this thread's first U output slices are loaded now: they do not depend on the weights, so
+    // their latency overlaps the round trip of m and l below
+    const int c0 = blockIdx.y * 8;
+    const int il = threadIdx.x / FPI, f = threadIdx.x % FPI;
+    const int qi = f >> 1, half = f & 1;
+    constexpr int U = 8;
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int c = il + IL * u;
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (qi < G && c < cnt)
+            v[u] = *reinterpret_cast<const float4*>(p.partials + item_of(c) * stride + 2 * NQ + qi * D + c0 + 4 * half);
+    }
     for (int c = threadIdx.x; c < cnt; c += blockDim.x) {
         const float4* pc = reinterpret_cast<const float4*>(p.partials + item_of(c) * stride);
         float4 mv[NQ / 4], lv[NQ / 4];
@@ -530,38 +544,35 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams 
         }
     }
     __syncthreads();
-    for (int qi = warp; qi < G; qi += 8) {
+    for (int qw = warp; qw < G; qw += 8) {
         float m = -INFINITY;
-        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, wgt[c * NQ + qi]);
+        for (int c = lane; c < cnt; c += 32) m = fmaxf(m, wgt[c * NQ + qw]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
         for (int c = lane; c < cnt; c += 32) {
-            const float mc = wgt[c * NQ + qi];
+            const float mc = wgt[c * NQ + qw];
             const float w = (mc == -INFINITY) ? 0.f : exp2f(mc - m);
-            wgt[c * NQ + qi] = w;
-            l += w * lsm[c * NQ + qi];
+            wgt[c * NQ + qw] = w;
+            l += w * lsm[c * NQ + qw];
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) lstar[qi] = l;
+        if (lane == 0) lstar[qw] = l;
     }
     __syncthreads();
-    const int c0 = blockIdx.y * 8;
-    const int il = threadIdx.x / FPI, f = threadIdx.x % FPI;
-    const int qi = f >> 1, half = f & 1;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (qi < G) {
-        constexpr int U = 8;
         for (int cb = il; cb < cnt; cb += IL * U) {
-            float4 v[U];
+            if (cb != il) {   // slices past the first U (prefetched above)
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int c = cb + IL * u;
-                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c < cnt)
-                    v[u] = *reinterpret_cast<const float4*>(p.partials + item_of(c) * stride + 2 * NQ + qi * D + c0 +
-                                                            4 * half);
+                for (int u = 0; u < U; ++u) {
+                    const int c = cb + IL * u;
+                    v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (c < cnt)
+                        v[u] = *reinterpret_cast<const float4*>(p.partials + item_of(c) * stride + 2 * NQ + qi * D +
+                                                                c0 + 4 * half);
+                }
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
