@@ -318,11 +318,9 @@ def run_ours(args, rank, world, local_rank):
 
 
 def launches_per_layer(w):
-    """Kernel launches of one layer's decode step outside seals: the decode kernel and the merge;
-    plus the append kernel where the decode kernel cannot append itself (16-bit newest rows in
-    bf16: the fused append takes fp16 rows only)."""
-    newest_fmt = w.tail_fmt if w.journal == "tq6_0" else w.journal
-    return 2 if newest_fmt == "f16" else 3
+    """Kernel launches of one layer's decode step outside seals: the decode kernel (which also
+    appends the step's position) and the merge."""
+    return 2
 
 
 def seal_launches(w, states):

@@ -498,15 +498,12 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
 }
 
 // 1 when the decode kernel of this layout can append the newest position itself: it takes the
-// region items, and the row that holds position N - 1 (after the append) is fp16 in every
-// sequence (the sink always; else the exact tail, or an exact journal).
+// region items (the item that holds position N - 1 reads that row from the caller's fp16 input,
+// rounded to bf16 where the row it stands for is bf16).
 bool fused_append_ok(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq) {
+    (void)layer; (void)seq_ids; (void)n_seq;
     const Layout& L = c->lay;
-    if (body_ctas_per_sm(L) <= 0 || !region_kernel_ok(L)) return false;
-    const int row_fmt = (L.journal == KVQ_TQ6_0) ? L.tail_fmt : L.journal;
-    for (int i = 0; i < n_seq; ++i)
-        if (NT(c, layer, seq_ids[i]) + 1 > kSink && row_fmt != KVQ_F16) return false;
-    return true;
+    return body_ctas_per_sm(L) > 0 && region_kernel_ok(L);
 }
 
 }  // namespace

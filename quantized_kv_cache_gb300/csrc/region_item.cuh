@@ -361,6 +361,15 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
         const int n = min(RUN, t1 - (t0 + RUN * gi));
         uint8_t* kr = stages + (size_t)sl * stage_bytes;
         uint8_t* vr = kr + half_bytes;
+        if (bf && p.knew != nullptr && t0 + RUN * gi + n == sp.n_tok) {
+            // fused decode step, bf16 rows: the newest row came from the caller's fp16 input;
+            // round it to bf16, the value the cache stores, before any warp reads it
+            for (int e = threadIdx.x; e < 2 * D; e += kCT) {
+                uint16_t* x = reinterpret_cast<uint16_t*>((e < D ? kr : vr) + (n - 1) * FLD) + (e % D);
+                *x = f2bf_bits(h2f(*x));
+            }
+            csync();
+        }
         if (!ring && n < RUN) {   // rows past the run's end: zeros, so 0 x row stays 0 in P.V
             for (int e = threadIdx.x; e < (RUN - n) * (2 * D / 16); e += kCT) {
                 const int rr = n + e / (2 * D / 16), u = e % (2 * D / 16);
