@@ -118,8 +118,15 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     const int local = item - sp.body_first;
     const int h = local / sp.body_per_head;
     const int kb_ = local % sp.body_per_head;             // the head's groups split evenly over its items
-    const int g0 = (int)((int64_t)kb_ * sp.body_groups / sp.body_per_head);
-    const int ngroups = (int)((int64_t)(kb_ + 1) * sp.body_groups / sp.body_per_head) - g0;
+    // the head's groups split evenly: 32-bit products while they fit (items per head < 2^16)
+    int g0, ngroups;
+    if (sp.body_groups < (1 << 15)) {
+        g0 = (kb_ * sp.body_groups) / sp.body_per_head;
+        ngroups = ((kb_ + 1) * sp.body_groups) / sp.body_per_head - g0;
+    } else {
+        g0 = (int)((int64_t)kb_ * sp.body_groups / sp.body_per_head);
+        ngroups = (int)((int64_t)(kb_ + 1) * sp.body_groups / sp.body_per_head) - g0;
+    }
     const int64_t unit = L.unit(p.layer, sp.slot, h);
     uint32_t* status = status_word(L, p.pool);
 
