@@ -386,6 +386,7 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
     if w.bulk_seal_step >= 0:
         target = ("bulk", w.bulk_seal_step)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    after = None
     if target is None:
         # no seal in the measured steps: append up to 32 more groups per sequence and layer
         # (seeded synthetic rows) and time one seal of them over all layers
@@ -409,6 +410,7 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
         torch.cuda.synchronize()
         t = ev0.elapsed_time(ev1) / 1e3
         kind = "bulk seal, all layers, one launch"
+        after = decode_after(w, cache, inp, seq_ids, out, stream, target[1])
     else:
         for s in range(target):
             _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
@@ -441,7 +443,40 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
         res["alu"] = {"bound": "alu", "ops_per_value": per_value, "achieved_tops": round(ops / 1e12, 3),
                       "peak_tops": FP32_PEAK_TOPS, "frac": round(ops / 1e12 / FP32_PEAK_TOPS, 4),
                       "peak_source": "152 SMs x 128 fp32 lanes x 2,070 MHz, one operation per lane per cycle"}
+    if after:
+        res["decode_after_seal"] = after
     return res
+
+
+def decode_after(w, cache, inp, seq_ids, out, stream, s0, max_steps=16):
+    """Decode throughput after the bulk seal (the headline steps run before it): the steps
+    s0 .. of the same inputs, the first one untimed (the graph is rebuilt after the seal)."""
+    import torch
+    from quantized_kv_cache_gb300 import _lib
+    n = min(max_steps, inp.q.shape[0] - s0)
+    if n < 2:
+        return None
+    def run(s):
+        _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
+                            inp.v[s].data_ptr(), out.data_ptr(), w.seal_trigger, w.keep, cache.ws.data_ptr(),
+                            cache.ws_bytes, None, stream)
+    run(s0)
+    torch.cuda.synchronize()
+    # lengths before each timed step (no seal falls in them: the bulk-seal workload never seals
+    # during decode), after its append
+    st0 = [cache.state(0, q) for q in seq_ids]
+    byts = sum(layer_step_bytes(w, [(N + 1 + i, S) for N, S in st0]) for i in range(n - 1)) * w.n_layers
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(s0 + 1, s0 + n):
+        run(s)
+    e1.record()
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3
+    hbm, _ = peaks()
+    return {"value": round(byts / t / 1e9, 2), "unit": UNIT, "steps": n - 1, "ms_per_step": round(t / (n - 1) * 1e3, 4),
+            "pct_of_hbm_peak": round(100 * byts / t / 1e9 / hbm, 2),
+            "note": "decode steps after the bulk seal (all but the newest 4,096 positions of each sequence sealed)"}
 
 
 def measure_e2e(w, cache, inp, seq_ids, out, stream, K, total_bytes, world):
