@@ -138,6 +138,20 @@ kvq_status kv_reset(kvq_cache* cache, int layer, int seq);
 kvq_status kv_append(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq, int n_tok,
                      const void* k, const void* v, void* stream);
 
+/* kv_prefill — a prefill chunk in one call (SJ-KVaRN §2.1: positions staged, then every full
+ * group older than the newest `keep` committed in one batch): for each listed sequence of
+ * `layer`, positions N..N+n_tok-1 from k / v ([n_seq][n_tok][H][D] fp16, device, as kv_append),
+ * then the seal of every full group g with S + 128 <= N + n_tok - keep (as kv_seal). The cache
+ * ends byte for byte as kv_append followed by kv_seal would leave it; a group that lies wholly in
+ * the chunk and is sealed by this call is encoded straight from the input rows, through the
+ * values the journal would have returned (bf16 rounding for a BF16 journal, the rotation, and
+ * with a tq6_0 ring its quantize-dequantize), so it never occupies the journal: n_tok is bounded
+ * by max_ctx, not by the ring. Refused with nothing written: KVQ_ENOSPC when N + n_tok exceeds
+ * max_ctx or the positions the call leaves unsealed exceed ring_capacity; KVQ_EINVAL on a bad
+ * layer, sequence list, keep < tail or null pointer. groups_sealed: host out (may be null). */
+kvq_status kv_prefill(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq, int n_tok, const void* k,
+                      const void* v, int keep, int64_t* groups_sealed, void* stream);
+
 /* kv_seal — SJ-KVaRN §2.1 item 4 and §4.3: for each listed sequence of `layer` (-1: all
  * layers) seal every full 128-position group g with S + 128 <= N - keep into body records,
  * oldest first, and advance S. keep >= T. groups_sealed (host, may be NULL) receives the

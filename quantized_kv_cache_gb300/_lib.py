@@ -60,6 +60,8 @@ _SIGS = {
     "kv_reset": [P, ctypes.c_int, ctypes.c_int],
     "kv_append": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, ctypes.c_int, P, P, P],
     "kv_seal": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, ctypes.c_int, ctypes.POINTER(I64), P],
+    "kv_prefill": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+                   ctypes.POINTER(I64), P],
     "kv_decode_attn": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P, SZ, P],
     "kv_state": [P, ctypes.c_int, ctypes.c_int, ctypes.POINTER(I64), ctypes.POINTER(I64)],
     "kv_get_status": [P, ctypes.POINTER(ctypes.c_uint32)],
@@ -156,6 +158,14 @@ def kv_reset(h, layer, seq):
 def kv_append(h, layer, seq_ids, n_tok, k_ptr, v_ptr, stream=0):
     ids, n = _ids(seq_ids)
     _check("kv_append", load().kv_append(h, layer, ids, n, n_tok, P(k_ptr), P(v_ptr), P(stream)))
+
+
+def kv_prefill(h, layer, seq_ids, n_tok, k_ptr, v_ptr, keep, stream=0):
+    ids, n = _ids(seq_ids)
+    g = I64()
+    _check("kv_prefill", load().kv_prefill(h, layer, ids, n, n_tok, P(k_ptr), P(v_ptr), keep, ctypes.byref(g),
+                                           P(stream)))
+    return g.value
 
 
 def kv_seal(h, layer, seq_ids, keep, stream=0):

@@ -56,7 +56,7 @@ __device__ __forceinline__ bool sign_neg(int set, int i) {
 
 // One sealed group of a seal launch: group index gidx counts the layers' groups in order,
 // the sequences of the batch in order inside a layer.
-struct SealTaskPos { int layer, slot, g, pos0; };
+struct SealTaskPos { int layer, slot, g, pos0, b; };   // b: index in the launch's sequence list
 
 __device__ __forceinline__ SealTaskPos seal_task(const SealParams& p, int gidx) {
     SealTaskPos t;
@@ -68,6 +68,7 @@ __device__ __forceinline__ SealTaskPos seal_task(const SealParams& p, int gidx) 
     t.slot = p.seq[b].slot;
     t.g = p.seq[b].first_group + gi;
     t.pos0 = p.seq[b].first_pos + kGroup * gi;
+    t.b = b;
     return t;
 }
 

@@ -22,15 +22,18 @@ __device__ __forceinline__ int tq6_code_at(const uint8_t* blk, int j) {
 
 // ---------------------------------------------------------------------------- append
 // grid (n_seq * n_tok, H, 2), block D / 4 threads (one warp per 128 values); dynamic smem D bytes.
+// Sequence b appends count[b] (<= n_tok) positions, read from its input rows src_off[b] on (the
+// input holds src_stride rows per sequence).
 __global__ void append_kernel(Layout L, AppendParams p) {
     extern __shared__ uint8_t cs[];                   // D codes
     const int b = blockIdx.x / p.n_tok, t = blockIdx.x % p.n_tok;
+    if (t >= p.count[b]) return;
     const int h = blockIdx.y, w = blockIdx.z, D = L.D;
     const int pos = p.n0[b] + t;
-    const uint16_t* src = (w ? p.v : p.k) + (((int64_t)b * p.n_tok + t) * L.H + h) * D;
+    const uint16_t* src = (w ? p.v : p.k) + (((int64_t)b * p.src_stride + p.src_off[b] + t) * L.H + h) * D;
     // positions of one append that share a tail slot (pos mod T) would race: only the newest T
-    // positions of the append write it
-    append_row(L, p.pool, L.unit(p.layer, p.slot[b], h), w, pos, src, pos + L.T >= p.n0[b] + p.n_tok,
+    // positions (pos >= tail_from) write it
+    append_row(L, p.pool, L.unit(p.layer, p.slot[b], h), w, pos, src, pos >= p.tail_from[b],
                (int)threadIdx.x, (int)blockDim.x, cs);
 }
 

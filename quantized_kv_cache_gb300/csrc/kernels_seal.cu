@@ -35,7 +35,9 @@ constexpr int kTq6Stride = 112;     // 96-byte tq6_0 block row + 16 bytes of pad
 constexpr int kX16Stride = 272;     // 256-byte row of 128 16-bit values + 16 bytes of padding
 constexpr int kBuckets = 2048;      // TBQ4 decision buckets (top 11 bits of an fp32 value)
 
-enum JournalKind { J_TQ6 = 0, J_F16 = 1, J_BF16 = 2 };
+// Row sources: the journal (tq6_0, F16 or BF16 rows), or the caller's fp16 input rows of a
+// prefill chunk (J_IN: the values the journal would have held are formed from them on the way).
+enum JournalKind { J_TQ6 = 0, J_F16 = 1, J_BF16 = 2, J_IN = 3 };
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
@@ -54,6 +56,7 @@ struct TileSlot {
     const uint8_t* rows;
     const uint8_t* scales;
     uint8_t* rec;
+    int64_t rs;     // bytes from one position's 16-bit row to the next (16-bit sources)
     int w, b;
 };
 constexpr int kSlots = 64;       // ring of decoded tiles (iteration k in slot k % kSlots)
@@ -71,7 +74,13 @@ __device__ __forceinline__ TileSlot tile_slot(const Layout& L, const SealParams&
     const SealTaskPos tk = seal_task(p, r / L.H);
     const int64_t unit = L.unit(tk.layer, tk.slot, h);
     const int s0 = journal_slot(L, tk.pos0);   // a group's 128 slots are contiguous
-    if (L.journal == KVQ_TQ6_0) {
+    t.rs = 2LL * L.D;
+    if (p.k_src != nullptr) {
+        const int64_t row = p.seq[tk.b].src_row + (tk.pos0 - p.seq[tk.b].first_pos);
+        t.rows = reinterpret_cast<const uint8_t*>((t.w ? p.v_src : p.k_src) + (row * L.H + h) * L.D) + 256 * t.b;
+        t.scales = nullptr;
+        t.rs = 2LL * L.H * L.D;
+    } else if (L.journal == KVQ_TQ6_0) {
         t.rows = jcode_row(L, p.pool, t.w, unit, s0) + 96 * t.b;
         t.scales = reinterpret_cast<const uint8_t*>(jscale_row(L, p.pool, t.w, unit, s0));
     } else {
@@ -96,12 +105,29 @@ __device__ __forceinline__ void issue_tile(const Layout& L, const TileSlot& t, u
         // the 128 rows' scales of every block ([128][D/128] fp16, 2D bytes)
         for (int c = tid; c < L.D / 8; c += kRows) cp_async16(st + kRows * kTq6Stride + 16 * c, t.scales + 16 * c);
     } else {
-        const int64_t rs = 2LL * L.D;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = (tid >> 4) + 8 * i, k = tid & 15;
-            cp_async16(st + r * kX16Stride + 16 * k, t.rows + r * rs + 16 * k);
+            cp_async16(st + r * kX16Stride + 16 * k, t.rows + r * t.rs + 16 * k);
         }
+    }
+}
+
+// The tq6_0 staging of one 128-value block, in place: d = fp16(max|y| / 31), q = clamp(rint(y x
+// (1 / fp32(d))), -31, 31) (0 when d is 0), y = q x fp32(d): what the journal would return for
+// these values (the append's block quantizer and the seal's dequantizer, operation for
+// operation).
+__device__ __forceinline__ void tq6_roundtrip(float (&y)[128]) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) a = fmaxf(a, fabsf(y[i]));
+    const float d = h2f(f2h_bits(fdiv(a, 31.0f)));
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+#pragma unroll
+    for (int i = 0; i < 128; ++i) {
+        float q = (d == 0.f) ? 0.f : rintf(fmul(y[i], inv));
+        q = fminf(fmaxf(q, -31.f), 31.f);
+        y[i] = fmul(q, d);
     }
 }
 
@@ -385,6 +411,17 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
         float y[128];
         if constexpr (JK == J_TQ6) {
             decode_tq6(st, D, tl.b, y);
+        } else if constexpr (JK == J_IN) {
+            // a prefill chunk's fp16 rows, turned into what the journal would hold for them: the
+            // stored 16-bit values (bf16-rounded for a BF16 journal), rotated; with a tq6_0 ring
+            // the rotated rows are staged and dequantized
+            decode_x16<J_F16>(st, y);
+            if (L.journal == KVQ_BF16) {
+#pragma unroll
+                for (int i = 0; i < 128; ++i) y[i] = bf2f(f2bf_bits(y[i]));
+            }
+            if constexpr (FAM == F_TBQ4) rotate_tbq128(y);
+            if (L.journal == KVQ_TQ6_0) tq6_roundtrip(y);
         } else {
             decode_x16<JK>(st, y);
             if constexpr (FAM == F_TBQ4) rotate_tbq128(y);
@@ -445,6 +482,7 @@ int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t 
 
 template <int FAM>
 int launch_family(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
+    if (p.k_src != nullptr) return launch_rows<J_IN, FAM>(L, p, n_tiles, s);
     if (L.journal == KVQ_TQ6_0) return launch_rows<J_TQ6, FAM>(L, p, n_tiles, s);
     if (L.journal == KVQ_BF16) return launch_rows<J_BF16, FAM>(L, p, n_tiles, s);
     return launch_rows<J_F16, FAM>(L, p, n_tiles, s);
@@ -472,14 +510,47 @@ struct KvStage {
     static constexpr int ROW = (JK == J_TQ6) ? 192 : 512;    // one row of the half (2 tq6_0 blocks / 256 x 16 bit)
 };
 
+// The tq6_0 staging of one 128-value block held by a warp, 4 values per lane (v[k0 .. k0+3]), in
+// place: the same arithmetic as tq6_roundtrip.
+__device__ __forceinline__ void tq6_roundtrip_warp(float (&v)[8], int k0) {
+    float a = 0.f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) a = fmaxf(a, fabsf(v[k0 + m]));
+    a = warp_max(a);
+    const float d = h2f(f2h_bits(fdiv(a, 31.0f)));
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        float q = (d == 0.f) ? 0.f : rintf(fmul(v[k0 + m], inv));
+        q = fminf(fmaxf(q, -31.f), 31.f);
+        v[k0 + m] = fmul(q, d);
+    }
+}
+
 // Values of channels lane + 32k (k < 8) of row t of the staged half, in the body's domain:
 // tq6_0 codes dequantized (the ring rows are rotated at append), 16-bit rows widened and
 // rotated here by HAD256.
 template <int JK>
 __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, int t, int nsc, int half, int lane,
-                                       float (&v)[8]) {
+                                       float (&v)[8], int journal) {
     const uint8_t* row = st + t * KvStage<JK>::ROW;
-    if constexpr (JK == J_TQ6) {
+    if constexpr (JK == J_IN) {
+        // a prefill chunk's fp16 row: the stored value (bf16-rounded for a BF16 journal),
+        // rotated, and with a tq6_0 ring staged and dequantized per 128-channel block
+        const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            v[k] = h2f(r16[lane + 32 * k]);
+            if (journal == KVQ_BF16) v[k] = bf2f(f2bf_bits(v[k]));
+        }
+        warp_fwht<8>(v, lane);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
+        if (journal == KVQ_TQ6_0) {
+            tq6_roundtrip_warp(v, 0);
+            tq6_roundtrip_warp(v, 4);
+        }
+    } else if constexpr (JK == J_TQ6) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int b = k >> 2, j = lane + 32 * (k & 3);
@@ -570,7 +641,16 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     // stage the half's 128 journal rows (contiguous slots)
     {
         const int s0 = journal_slot(L, tk.pos0);
-        if constexpr (JK == J_TQ6) {
+        if constexpr (JK == J_IN) {
+            const int64_t row0 = p.seq[tk.b].src_row + (tk.pos0 - p.seq[tk.b].first_pos);
+            const uint8_t* src = reinterpret_cast<const uint8_t*>((w ? p.v_src : p.k_src) + (row0 * L.H + h) * L.D) +
+                                 512 * half;
+            const int64_t rs = 2LL * L.H * L.D;
+            for (int ci = threadIdx.x; ci < 128 * 32; ci += kKvThreads) {
+                const int rr = ci >> 5, k = ci & 31;
+                cp_async16(st + rr * ROW + 16 * k, src + rr * rs + 16 * k);
+            }
+        } else if constexpr (JK == J_TQ6) {
             const uint8_t* src = jcode_row(L, p.pool, w, unit, s0) + 192 * half;
             const int64_t jr = L.jrow_bytes;
             for (int ci = threadIdx.x; ci < 128 * 12; ci += kKvThreads) {
@@ -596,7 +676,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     __syncthreads();
     for (int t = warp; t < 128; t += kKvWarps) {
         float v[8];
-        kv_row<JK>(st, sc, t, nsc, half, lane, v);
+        kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
 #pragma unroll
         for (int k = 0; k < 8; ++k) Y[t * kYS + lane + 32 * k] = v[k];
     }
@@ -643,7 +723,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     // stored scales
     for (int t = warp; t < 128; t += kKvWarps) {
         float v[8];
-        kv_row<JK>(st, sc, t, nsc, half, lane, v);
+        kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
         const float is = invS[t], z = Zs[t];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -717,6 +797,7 @@ int launch_seal(const Layout& L, const SealParams& p, void* stream) {
     if (L.fmt[0] == KVQ_KVARN4 || L.fmt[0] == KVQ_KVARN5) {
         if (L.D % 256) return (int)cudaErrorInvalidValue;
         cudaStream_t s = (cudaStream_t)stream;
+        if (p.k_src != nullptr) return launch_kvarn<J_IN>(L, p, groups, s);
         if (L.journal == KVQ_TQ6_0) return launch_kvarn<J_TQ6>(L, p, groups, s);
         if (L.journal == KVQ_BF16) return launch_kvarn<J_BF16>(L, p, groups, s);
         return launch_kvarn<J_F16>(L, p, groups, s);

@@ -289,6 +289,7 @@ kvq_status kv_append(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq,
     p.layer = layer;
     p.n_seq = n_seq;
     p.n_tok = n_tok;
+    p.src_stride = n_tok;
     for (int i = 0; i < n_seq; ++i) {
         const int s = seq_ids[i];
         const int64_t N = NT(c, layer, s), S = ST(c, layer, s);
@@ -296,10 +297,144 @@ kvq_status kv_append(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq,
         if (std::max<int64_t>(N + n_tok, kSink) - S > c->cfg.ring_capacity) return KVQ_ENOSPC;
         p.slot[i] = s;
         p.n0[i] = (int32_t)N;
+        p.count[i] = n_tok;
+        p.src_off[i] = 0;
+        p.tail_from[i] = (int32_t)(N + n_tok - c->cfg.tail);
     }
     const int e = launch_append(c->lay, p, stream);
     if (e != 0) return KVQ_ECUDA;
     for (int i = 0; i < n_seq; ++i) NT(c, layer, seq_ids[i]) += n_tok;
+    return KVQ_OK;
+}
+
+namespace {
+
+// Seals counts[i] groups of each listed sequence of one layer, from its sealed end on: from the
+// journal (k_src null) or from input rows (src_row[i]: the input row of the first group's first
+// position; the input holds src_stride rows per sequence). Advances the sealed ends.
+int seal_counts(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const int64_t* counts,
+                const void* k_src, const void* v_src, int src_stride, const int64_t* src_row, void* stream) {
+    SealParams p{};
+    p.pool = c->pool;
+    p.k_src = (const uint16_t*)k_src;
+    p.v_src = (const uint16_t*)v_src;
+    p.layer0 = layer;
+    p.n_layers = 1;
+    p.src_stride = src_stride;
+    int32_t acc = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        if (counts[i] <= 0) continue;
+        const int s = seq_ids[i];
+        SealSeq& q = p.seq[p.n_seq++];
+        q.slot = s;
+        q.first_pos = (int32_t)ST(c, layer, s);
+        q.first_group = (int32_t)((ST(c, layer, s) - kSink) / kGroup);
+        q.n_groups = (int32_t)counts[i];
+        q.prefix = acc;
+        q.src_row = src_row ? src_row[i] : 0;
+        acc += (int32_t)counts[i];
+    }
+    p.groups_per_layer = acc;
+    if (acc == 0) return 0;
+    const int e = launch_seal(c->lay, p, stream);
+    if (e != 0) return e;
+    for (int i = 0; i < n_seq; ++i)
+        if (counts[i] > 0) ST(c, layer, seq_ids[i]) += (int64_t)kGroup * counts[i];
+    return 0;
+}
+
+// Appends, for each listed sequence, count[i] positions from its N on, read from input rows
+// src_off[i] on (src_stride rows per sequence); positions >= tail_from[i] also write the tail.
+int append_ranges(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* k, const void* v,
+                  int src_stride, const int64_t* count, const int64_t* src_off, const int64_t* tail_from,
+                  void* stream) {
+    AppendParams p{};
+    p.pool = c->pool;
+    p.k = (const uint16_t*)k;
+    p.v = (const uint16_t*)v;
+    p.layer = layer;
+    p.n_seq = n_seq;
+    p.src_stride = src_stride;
+    int64_t most = 0;
+    for (int i = 0; i < n_seq; ++i) {
+        p.slot[i] = seq_ids[i];
+        p.n0[i] = (int32_t)NT(c, layer, seq_ids[i]);
+        p.count[i] = (int32_t)count[i];
+        p.src_off[i] = (int32_t)src_off[i];
+        p.tail_from[i] = (int32_t)std::min<int64_t>(tail_from[i], 0x7fffffff);
+        most = std::max(most, count[i]);
+    }
+    if (most == 0) return 0;
+    p.n_tok = (int32_t)most;
+    const int e = launch_append(c->lay, p, stream);
+    if (e != 0) return e;
+    for (int i = 0; i < n_seq; ++i) NT(c, layer, seq_ids[i]) += count[i];
+    return 0;
+}
+
+}  // namespace
+
+kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, int n_tok, const void* k,
+                      const void* v, int keep, int64_t* groups_sealed, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (layer < 0 || layer >= c->cfg.n_layers || n_tok <= 0 || !k || !v || !aligned16(k) || !aligned16(v) ||
+        keep < c->cfg.tail)
+        return KVQ_EINVAL;
+    if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
+    // Per sequence (N0, S0 before; N1, S1 after): positions [N0, N1) split into
+    //   head   [N0, max(N0, M))  the journal (and the sink): the chunk's part of groups that
+    //                            started before N0, sealed from the journal right after
+    //   direct [M, S1)           groups wholly in the chunk, sealed straight from the input
+    //   rest   [max(N0, S1), N1) the journal and, for the newest T, the exact tail
+    // with M = min(first group start >= N0, S1, N1). (S1 exceeds N1 only while the sequence is
+    // still inside the sink: S1 = 128 > N1.)
+    int64_t n0[kMaxSeqPerCall], s1[kMaxSeqPerCall], m[kMaxSeqPerCall];
+    for (int i = 0; i < n_seq; ++i) {
+        const int s = seq_ids[i];
+        const int64_t N0 = NT(c, layer, s), S0 = ST(c, layer, s), N1 = N0 + n_tok;
+        if (N1 > c->cfg.max_ctx) return KVQ_ENOSPC;
+        const int64_t lim = N1 - keep - S0;
+        const int64_t S1 = S0 + (lim >= kGroup ? lim / kGroup * kGroup : 0);
+        if (std::max<int64_t>(N1, kSink) - S1 > c->cfg.ring_capacity) return KVQ_ENOSPC;
+        const int64_t first_in = N0 <= kSink ? kSink : kSink + (N0 - kSink + kGroup - 1) / kGroup * kGroup;
+        n0[i] = N0;
+        s1[i] = S1;
+        m[i] = std::min(std::min(first_in, S1), N1);
+    }
+    int64_t cnt[kMaxSeqPerCall], off[kMaxSeqPerCall], tfrom[kMaxSeqPerCall], groups[kMaxSeqPerCall];
+    int64_t row[kMaxSeqPerCall];
+    int64_t total = 0;
+    // head, then the groups it completes (from the journal)
+    for (int i = 0; i < n_seq; ++i) {
+        cnt[i] = std::max<int64_t>(n0[i], m[i]) - n0[i];
+        off[i] = 0;
+        tfrom[i] = INT64_MAX;               // older than the newest T: no tail writes
+    }
+    if (append_ranges(c, layer, seq_ids, n_seq, k, v, n_tok, cnt, off, tfrom, stream)) return KVQ_ECUDA;
+    for (int i = 0; i < n_seq; ++i) {
+        groups[i] = std::max<int64_t>(0, m[i] - ST(c, layer, seq_ids[i])) / kGroup;
+        total += groups[i];
+    }
+    if (seal_counts(c, layer, seq_ids, n_seq, groups, nullptr, nullptr, 0, nullptr, stream)) return KVQ_ECUDA;
+    // the groups wholly in the chunk, from the input rows
+    for (int i = 0; i < n_seq; ++i) {
+        groups[i] = std::max<int64_t>(0, s1[i] - ST(c, layer, seq_ids[i])) / kGroup;
+        row[i] = (int64_t)i * n_tok + (ST(c, layer, seq_ids[i]) - n0[i]);
+        total += groups[i];
+    }
+    if (seal_counts(c, layer, seq_ids, n_seq, groups, k, v, n_tok, row, stream)) return KVQ_ECUDA;
+    // the rest: the direct groups' positions count as appended (their journal slots stay unwritten)
+    for (int i = 0; i < n_seq; ++i) {
+        const int s = seq_ids[i];
+        const int64_t start = std::max(n0[i], std::min(s1[i], n0[i] + n_tok));
+        NT(c, layer, s) = start;
+        cnt[i] = n0[i] + n_tok - start;
+        off[i] = start - n0[i];
+        tfrom[i] = n0[i] + n_tok - c->cfg.tail;
+    }
+    if (append_ranges(c, layer, seq_ids, n_seq, k, v, n_tok, cnt, off, tfrom, stream)) return KVQ_ECUDA;
+    if (groups_sealed) *groups_sealed = total;
     return KVQ_OK;
 }
 

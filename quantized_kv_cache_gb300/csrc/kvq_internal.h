@@ -114,11 +114,14 @@ struct AttnParams {
 
 struct AppendParams {
     const void* pool;
-    const uint16_t* k;       // [n_seq][n_tok][H][D]
+    const uint16_t* k;       // [n_seq][src_stride][H][D]
     const uint16_t* v;
-    int32_t layer, n_seq, n_tok, pad;
+    int32_t layer, n_seq, n_tok, src_stride;   // n_tok: the largest count; src_stride: input rows per sequence
     int32_t slot[kMaxSeqPerCall];
     int32_t n0[kMaxSeqPerCall];       // N before this append
+    int32_t count[kMaxSeqPerCall];    // positions appended to this sequence (<= n_tok)
+    int32_t src_off[kMaxSeqPerCall];  // input row of position n0
+    int32_t tail_from[kMaxSeqPerCall];   // positions >= tail_from also write the exact tail
 };
 
 struct SealSeq {             // one sequence's batch of consecutive groups (same in every sealed layer)
@@ -127,11 +130,18 @@ struct SealSeq {             // one sequence's batch of consecutive groups (same
     int32_t first_group;     // its body group index
     int32_t n_groups;
     int32_t prefix;          // groups of the earlier sequences of this launch
+    int32_t pad;
+    int64_t src_row;         // input source: input row of first_pos ([n_seq][src_stride][H][D])
 };
 
 struct SealParams {
     const void* pool;
+    // input source (a prefill chunk sealed straight from the caller's fp16 rows), else null: the
+    // rows come from the journal
+    const uint16_t* k_src;
+    const uint16_t* v_src;
     int32_t layer0, n_layers, n_seq, groups_per_layer;
+    int32_t src_stride, pad;
     SealSeq seq[kMaxSeqPerCall];
 };
 
