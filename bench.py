@@ -36,7 +36,7 @@ DEFAULT_WORKLOAD = "hybrid27b_kvarn44"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=0, help="timed decode steps (default: the workload's own count)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
@@ -44,7 +44,15 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (a smaller case for profiling; the line names it)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps <= 0 and args.workload in _workloads():
+        args.steps = _workloads()[args.workload].steps
+    return args
+
+
+def _workloads():
+    from quantized_kv_cache_gb300 import configs
+    return configs.WORKLOADS
 
 
 def peaks():
@@ -281,6 +289,8 @@ def run_ours(args, rank, world, local_rank):
     # seal throughput: time the seals of the policy's first seal point (or the bulk seal)
     seal = measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds)
 
+    prefill = measure_prefill(w, ds, seq_ids, stream)
+
     e2e = None
     if not args.no_e2e:
         restore()
@@ -305,6 +315,7 @@ def run_ours(args, rank, world, local_rank):
                      "mean_launch_us": round(1e6 * sum(attn_times) / len(attn_times), 3),
                      "algorithmic_bytes_per_launch": int(sum(attn_bytes) / len(attn_bytes))},
         "seal": seal,
+        "prefill": prefill,
         "groups_sealed_in_timed_region": sealed,
         "gpu_launches": launches,
         "clocks": clocks.summary(),
@@ -445,6 +456,89 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
                       "peak_source": "152 SMs x 128 fp32 lanes x 2,070 MHz, one operation per lane per cycle"}
     if after:
         res["decode_after_seal"] = after
+    return res
+
+
+def prefill_bytes(w, n0, S1):
+    """Algorithmic bytes of one kv_prefill of n0 positions of one layer (all KV heads) from an
+    empty sequence that ends with S1 sealed: the fp16 input read once; the sealed groups'
+    records, the sink, the journal rows of the unsealed positions past the sink and the exact
+    tail (a tq6_0 ring only) written once."""
+    from quantized_kv_cache_gb300.configs import record_bytes
+    H, D = w.n_kv_heads, w.head_dim
+    rows = 2 * H                                              # K and V rows of all heads
+    b = n0 * rows * 2 * D                                     # input
+    b += (S1 - 128) // 128 * H * (record_bytes(w.k_body, D) + record_bytes(w.v_body, D))
+    b += min(n0, 128) * rows * 2 * D                          # sink
+    unsealed = max(0, n0 - max(S1, 128))
+    if w.journal == "tq6_0":
+        b += unsealed * rows * (D // 128) * 98 + min(unsealed, w.tail) * rows * 2 * D
+    else:
+        b += unsealed * rows * 2 * D
+    return b
+
+
+def measure_prefill(w, ds, seq_ids, stream, reps=3):
+    """kv_prefill of every sequence's whole context into a fresh one-layer cache (the layers
+    are independent and alike), one call per sequence, timed with CUDA events after an untimed
+    run; the inputs are generated in HBM first. Positions/s count positions of one layer, all
+    KV heads."""
+    import torch
+    import quantized_kv_cache_gb300 as pkg
+    from quantized_kv_cache_gb300 import synth, _lib
+    H, D = w.n_kv_heads, w.head_dim
+    cfg = w.config(n_layers=1)
+    cache = pkg.KVCache(cfg, ds.dev.index)
+    bufs = []
+    for seq in seq_ids:
+        n0 = w.contexts[seq]
+        k = torch.empty((1, n0, H, D), dtype=torch.float16, device=ds.dev)
+        v = torch.empty_like(k)
+        ds.kv(synth.T_K, 0, seq, 0, n0, k, stream)
+        ds.kv(synth.T_V, 0, seq, 0, n0, v, stream)
+        bufs.append((k, v))
+    torch.cuda.synchronize()
+
+    def run():
+        g = 0
+        for seq, (k, v) in zip(seq_ids, bufs):
+            g += cache.prefill(0, [seq], k, v, w.keep, stream)
+        return g
+
+    def reset():
+        for seq in seq_ids:
+            _lib.kv_reset(cache.h, 0, seq)
+
+    run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(reps):
+        reset()
+        torch.cuda.synchronize()
+        e0.record()
+        groups = run()
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    status = _lib.kv_get_status(cache.h)
+    states = [cache.state(0, seq) for seq in seq_ids]
+    cache.close()
+    t = sorted(times)[len(times) // 2]
+    pos = sum(w.contexts[s] for s in seq_ids)
+    byts = sum(prefill_bytes(w, w.contexts[s], S) for s, (_, S) in zip(seq_ids, states))
+    hbm, _ = peaks()
+    res = {"positions_per_s": round(pos / t, 1), "positions": pos, "groups_sealed": groups,
+           "seconds": round(t, 6), "algorithmic_bytes": byts, "achieved_gbs": round(byts / t / 1e9, 2),
+           "hbm_frac": round(byts / t / 1e9 / hbm, 4), "status": status,
+           "kind": "kv_prefill of each sequence's whole context (keep = the workload's), one layer, "
+                   "one call per sequence, median of 3"}
+    if w.k_body.startswith("kvarn"):
+        per_value = KVARN_OPS_PER_VALUE + (KVARN_ROT_OPS if w.journal != "tq6_0" else KVARN_TQ6_OPS)
+        ops = groups * 128 * H * 2 * D * per_value / t
+        res["alu"] = {"bound": "alu", "ops_per_value": per_value, "achieved_tops": round(ops / 1e12, 3),
+                      "peak_tops": FP32_PEAK_TOPS, "frac": round(ops / 1e12 / FP32_PEAK_TOPS, 4),
+                      "note": "the sealed groups' balancing only"}
     return res
 
 

@@ -9,7 +9,7 @@ call raises.
 
 from . import _lib, configs, synth  # noqa: F401
 from ._lib import (KVQError, kvq_config, kv_bytes_per_token, kv_required_bytes, kv_create,  # noqa: F401
-                   kv_destroy, kv_reset, kv_append, kv_seal, kv_decode_attn, kv_state, kv_get_status,
+                   kv_destroy, kv_reset, kv_append, kv_prefill, kv_seal, kv_decode_attn, kv_state, kv_get_status,
                    kv_dequant, kv_region_ptr, kv_format_tables, kvq_synth_fill)
 
 
@@ -42,6 +42,12 @@ class KVCache:
         """k, v: fp16 CUDA tensors [n_seq, n_tok, H, D] (contiguous)."""
         assert k.is_contiguous() and v.is_contiguous()
         kv_append(self.h, layer, seq_ids, k.shape[1], k.data_ptr(), v.data_ptr(), stream)
+
+    def prefill(self, layer, seq_ids, k, v, keep, stream=0):
+        """kv_prefill: k, v fp16 CUDA tensors [n_seq, n_tok, H, D] (contiguous). Returns the
+        number of groups sealed."""
+        assert k.is_contiguous() and v.is_contiguous()
+        return kv_prefill(self.h, layer, seq_ids, k.shape[1], k.data_ptr(), v.data_ptr(), keep, stream)
 
     def seal(self, layer, seq_ids, keep, stream=0):
         return kv_seal(self.h, layer, seq_ids, keep, stream)

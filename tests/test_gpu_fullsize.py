@@ -12,9 +12,13 @@ the test compares:
 - every body record of the sampled heads (K and V) byte for byte;
 - the newest journal rows (tq6_0 codes and scales, or exact rows) and exact-tail rows;
 - the decode output of the head's query group against the fp64 oracle attention over the
-  same regions, within the decode tolerance |gpu - oracle| <= 1e-3 + 2e-3 |oracle|.
+  same regions, within the decode tolerance |gpu - oracle| <= 1e-3 + 2e-3 |oracle|;
+- the bench's prefill measurement: kv_prefill of a sampled sequence's whole context into a fresh
+  one-layer cache; lengths, the sealed records (a record depends only on its group's rows, so
+  the oracle's cache above, sealed on, holds the same ones) and the newest journal and tail rows.
 """
 
+import copy
 import dataclasses
 
 import numpy as np
@@ -198,3 +202,64 @@ def test_fullsize_bulk_seal(run):
         for wi, role in ((0, "K"), (1, "V")):
             body = _region_bytes(cache, seq, h, wi, _lib.REGION_BODY)
             _check_records(w, hc, body, role, range(g0, g1), f"bulk seal seq {seq} head {h}")
+
+
+def test_fullsize_prefill(run):
+    """kv_prefill of the sampled sequences' whole contexts (the bench's prefill measurement)."""
+    from quantized_kv_cache_gb300 import KVCache
+    from quantized_kv_cache_gb300.runner import DeviceSynth
+    w = run[0]
+    H, D = w.n_kv_heads, w.head_dim
+    ds = DeviceSynth(w, 0)
+    cache = KVCache(w.config(n_layers=1), 0)
+    try:
+        seqs = sorted({seq for seq, _ in SAMPLES[w.name]})
+        for seq in seqs:
+            n0 = w.contexts[seq]
+            k = torch.empty((1, n0, H, D), dtype=torch.float16, device=ds.dev)
+            v = torch.empty_like(k)
+            ds.kv(synth.T_K, 0, seq, 0, n0, k)
+            ds.kv(synth.T_V, 0, seq, 0, n0, v)
+            g = cache.prefill(0, [seq], k, v, w.keep)
+            torch.cuda.synchronize()
+            lim = n0 - w.keep - 128
+            S1 = 128 + (lim // 128 * 128 if lim >= 128 else 0)
+            assert cache.state(0, seq) == (n0, S1)
+            assert g == (S1 - 128) // 128
+            del k, v
+        assert _lib.kv_get_status(cache.h) == 0
+        for seq, h in SAMPLES[w.name]:
+            n0 = w.contexts[seq]
+            S1 = cache.state(0, seq)[1]
+            hc = copy.deepcopy(_oracle_head(w, seq, h))   # n0 + 1 positions
+            if hc.S < S1:
+                hc.seal(w.keep)
+            assert hc.S >= S1
+            ng = (S1 - 128) // 128
+            for wi, role in ((0, "K"), (1, "V")):
+                if ng:
+                    body = _region_bytes(cache, seq, h, wi, _lib.REGION_BODY)
+                    _check_records(w, hc, body, role, sorted({0, ng // 2, ng - 1}) if ng > 3 else range(ng),
+                                   f"prefill seq {seq} head {h}")
+                    if ng > 3:   # every record, cheaply: the whole sealed body in one comparison
+                        rb = len(hc.record_bytes(0, role))
+                        ref = np.concatenate([hc.record_bytes(gg, role) for gg in range(ng)])
+                        assert np.array_equal(body[:ng * rb], ref), f"prefill seq {seq} head {h} {role} body"
+                newest = range(max(S1, n0 - 4), n0)
+                if w.journal == "tq6_0":
+                    codes = _region_bytes(cache, seq, h, wi, _lib.REGION_JOURNAL).reshape(w.ring, D // 128, 96)
+                    sc = _region_bytes(cache, seq, h, wi, _lib.REGION_JOURNAL_SCALE).view(np.uint16).reshape(w.ring, D // 128)
+                    tail = _region_bytes(cache, seq, h, wi, _lib.REGION_TAIL).view(np.uint16).reshape(w.tail, D)
+                    for p in newest:
+                        d, ql, qh = hc.tq6_slot_bytes(p, role)
+                        slot = (p - 128) % w.ring
+                        assert np.array_equal(codes[slot], np.concatenate([ql, qh], axis=1)), (seq, h, role, p)
+                        assert np.array_equal(sc[slot], d.view(np.uint16)), (seq, h, role, p)
+                        assert np.array_equal(tail[p % w.tail], hc.tail[role][p % w.tail]), (seq, h, role, p)
+                else:
+                    jx = _region_bytes(cache, seq, h, wi, _lib.REGION_JOURNAL).view(np.uint16).reshape(w.ring, D)
+                    for p in newest:
+                        slot = (p - 128) % w.ring
+                        assert np.array_equal(jx[slot], hc.jx[role][slot]), (seq, h, role, p)
+    finally:
+        cache.close()
