@@ -498,6 +498,7 @@ constexpr int kMergeMaxItems = 1024;
 // accumulating them.
 template <int D, int NQ>
 __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
+    grid_dep_wait();          // the partials of the launch ahead are complete and visible
     const int bh = blockIdx.x;
     const int b = bh / L.H, h = bh % L.H;
     const SeqSpan& s = p.seq[b];
@@ -621,7 +622,7 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
     if (mk.before && cudaEventRecordWithFlags((cudaEvent_t)mk.before, s, mk.flags) != cudaSuccess)
         return (int)cudaErrorInvalidResourceHandle;
     if (streaming) {
-        const int e = launch_decode_fused(L, p, n_body, fused_regions ? p.n_region_items : 0, s);
+        const int e = launch_decode_fused(L, p, n_body, fused_regions ? p.n_region_items : 0, s, mk.pdl);
         if (e != 0) return e;
     }
     if (p.n_region_items > 0 && !fused_regions) {
@@ -639,8 +640,11 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
     const size_t msmem = (size_t)max_cnt * NQ * 2 * sizeof(float);
     if (msmem > 48 * 1024)
         cudaFuncSetAttribute(decode_merge_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
-    decode_merge_kernel<D, NQ><<<mg, 256, msmem, s>>>(L, p);
-    return (int)cudaGetLastError();
+    // programmatic serialization only where the launch ahead is the decode kernel (no event
+    // record or generic kernel between them)
+    const bool pdl = mk.pdl && streaming && fused_regions && !mk.after;
+    const cudaError_t e = launch_k(decode_merge_kernel<D, NQ>, mg, dim3(256), msmem, s, pdl, L, p);
+    return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
 
 }  // namespace

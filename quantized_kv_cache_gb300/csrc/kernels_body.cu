@@ -799,6 +799,9 @@ __global__ void __launch_bounds__(kCT, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
 decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ AttnParams p, int n_body, int nst) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
+    // launched with programmatic serialization, the CTAs may be placed while the launch ahead
+    // drains: nothing is read or written in global memory before it has completed
+    grid_dep_wait();
     if ((int)blockIdx.x < n_body)
         body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
     else
@@ -820,7 +823,7 @@ int nstages(const Layout& L) {
 }
 
 template <int D, int NQ, int KF, int VF, int KB, int VB>
-int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cudaStream_t st) {
+int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cudaStream_t st, bool pdl) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
     if (nst == 0) return (int)cudaErrorInvalidConfiguration;
@@ -832,8 +835,8 @@ int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cud
     auto kern = decode_attn_kernel<D, NQ, KF, VF, KB, VB>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
-    kern<<<n_body + n_region, kCT, smem, st>>>(L, p, n_body, nst);
-    return (int)cudaGetLastError();
+    const cudaError_t e = launch_k(kern, dim3(n_body + n_region), dim3(kCT), smem, st, pdl, L, p, n_body, nst);
+    return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
 
 // Instantiated combinations (head_dim, query tile, K format, V format); other layouts keep
@@ -878,8 +881,9 @@ struct LaunchFn {
     const AttnParams& p;
     int n_body, n_region;
     cudaStream_t s;
+    bool pdl;
     template <int D, int NQ, int KF, int VF, int KB, int VB>
-    int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n_body, n_region, s); }
+    int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n_body, n_region, s, pdl); }
 };
 
 }  // namespace
@@ -912,9 +916,9 @@ int region_kernel_ok(const Layout& L) {
 }
 
 // Launches the decode kernel over the body items and the first n_region region items of p.
-int launch_decode_fused(const Layout& L, const AttnParams& p, int n_body, int n_region, void* stream) {
+int launch_decode_fused(const Layout& L, const AttnParams& p, int n_body, int n_region, void* stream, bool pdl) {
     if (n_body + n_region <= 0) return 0;
-    LaunchFn f{L, p, n_body, n_region, (cudaStream_t)stream};
+    LaunchFn f{L, p, n_body, n_region, (cudaStream_t)stream, pdl};
     const int r = dispatch(L, f);
     return r < 0 ? (int)cudaErrorInvalidValue : r;
 }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <set>
@@ -643,9 +644,24 @@ bool fused_append_ok(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq)
 
 }  // namespace
 
+namespace {
+// The decode and merge kernels go out with programmatic stream serialization (their CTAs are
+// placed while the launch ahead drains, and wait for it before touching memory), unless the
+// environment sets KVQ_PDL=0.
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("KVQ_PDL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+}  // namespace
+
 kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
                           void* workspace, size_t ws_bytes, void* stream) {
-    return decode_attn(c, layer, seq_ids, n_seq, q, out, workspace, ws_bytes, nullptr, nullptr, stream);
+    LaunchMarks marks;
+    marks.pdl = pdl_enabled();
+    return decode_attn(c, layer, seq_ids, n_seq, q, out, workspace, ws_bytes, nullptr, nullptr, stream, marks);
 }
 
 namespace {
@@ -702,6 +718,8 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
             marks.before = events[2 * l];
             marks.after = events[2 * l + 1];
             marks.flags = ev_flags;
+        } else {
+            marks.pdl = pdl_enabled();
         }
         st = decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace, ws_bytes,
                          fuse ? kl : nullptr, fuse ? vl : nullptr, stream, marks);

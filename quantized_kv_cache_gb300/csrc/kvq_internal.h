@@ -165,9 +165,11 @@ struct LaunchMarks {
     void* before = nullptr;
     void* after = nullptr;
     unsigned flags = 0;
+    bool pdl = false;      // launch the decode and merge kernels with programmatic stream serialization
 };
 int launch_decode(const Layout& lay, const AttnParams& p, void* stream, const LaunchMarks& marks = LaunchMarks());
-int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream);
+int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream,
+                        bool pdl = false);
 int upload_tables_body(const FormatTables& t);
 int body_ctas_per_sm(const Layout& lay);     // resident body-item CTAs per SM (0: no instance)
 int decode_ctas_per_sm(const Layout& lay);   // the same with the region items in the kernel
