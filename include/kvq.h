@@ -43,8 +43,8 @@ typedef enum {
     KVQ_EDEVICE = 5        /* device status word reports a problem (see kv_get_status) */
 } kvq_status;
 
-/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, KVARN4, KVARN5. Journal: TQ6_0, F16, BF16.
- * Exact tail: F16, BF16. */
+/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, KVARN2..KVARN8. Journal: TQ6_0, F16, BF16.
+ * Exact tail: F16, BF16. K and V bodies may differ (e.g. KVARN3 keys, KVARN2 values). */
 typedef enum {
     KVQ_F16 = 0,
     KVQ_BF16 = 1,
@@ -53,7 +53,11 @@ typedef enum {
     KVQ_Q8_0 = 4,    /* 34 B per 32 values */
     KVQ_Q4_0 = 5,    /* 18 B per 32 values */
     KVQ_KVARN4 = 6,  /* SJ-KVaRN §2.2: 256-pt Hadamard, 16-pass balancing, 4-bit rows */
-    KVQ_KVARN5 = 7   /* same, 5-bit rows */
+    KVQ_KVARN5 = 7,  /* same, 5-bit rows */
+    KVQ_KVARN2 = 8,  /* same, 2-bit rows (SJ-KVaRN §2.3 scalar body, §3: the 3/2 and 2/2 caches) */
+    KVQ_KVARN3 = 9,  /* same, 3-bit rows */
+    KVQ_KVARN6 = 10, /* same, 6-bit rows */
+    KVQ_KVARN8 = 11  /* same, 8-bit rows (KVarN8, the pages' ceiling check) */
 } kvq_fmt;
 
 typedef struct {

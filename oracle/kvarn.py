@@ -20,7 +20,6 @@ error bound.
 import numpy as np
 
 from .fp import f32, to_f16, tree_sum
-from .codecs import pack_nibbles, unpack_nibbles, pack_bitplane, unpack_bitplane
 
 ROWS, COLS = 128, 256
 PASSES = 16
@@ -91,26 +90,52 @@ def scale_block(S, Z, C):
     return np.concatenate([S, Z, C, pad], axis=-1).astype(np.float16)
 
 
+# Code planes of a b-bit code, low plane first (FORMAT.md section 5): plane widths summing to b.
+PLANES = {2: (2,), 3: (2, 1), 4: (4,), 5: (4, 1), 6: (4, 2), 8: (8,)}
+
+
+def _pack_plane(vals, w):
+    """vals [..., n] (< 2^w) -> bytes [..., n w / 8]: element i at bit w (i mod 8/w) of byte i // (8/w)."""
+    per = 8 // w
+    v = vals.astype(np.uint16)
+    out = np.zeros(v.shape[:-1] + (v.shape[-1] // per,), dtype=np.uint16)
+    for m in range(per):
+        out |= v[..., m::per] << (w * m)
+    return out.astype(np.uint8)
+
+
+def _unpack_plane(b, w):
+    per = 8 // w
+    out = np.empty(b.shape[:-1] + (per * b.shape[-1],), dtype=np.uint8)
+    for m in range(per):
+        out[..., m::per] = (b >> (w * m)) & ((1 << w) - 1)
+    return out
+
+
 def pack_codes(code, bits, role):
     """Code bytes of one tile [..., 128, 256] by role: K token-major, V channel-major.
 
-    4-bit: nibble stream along the row; 5-bit: the 4-bit low plane, then a one-bit high
-    plane with the same row order.
+    The b-bit codes are split into planes (PLANES[b], low bits first); each plane holds
+    every row in order, the row's codes packed LSB-first. 4-bit: one nibble stream along the
+    row (pack_nibbles); 5-bit: that nibble plane, then a one-bit plane (pack_bitplane).
     """
     rows = code if role == "K" else np.swapaxes(code, -1, -2)
-    lo = pack_nibbles(rows & 0x0F)
-    if bits == 4:
-        return lo.reshape(lo.shape[:-2] + (-1,))
-    assert bits == 5
-    hi = pack_bitplane((rows >> 4) & 1)
-    return np.concatenate([lo.reshape(lo.shape[:-2] + (-1,)), hi.reshape(hi.shape[:-2] + (-1,))], axis=-1)
+    parts, sh = [], 0
+    for w in PLANES[bits]:
+        p = _pack_plane((rows >> sh) & ((1 << w) - 1), w)
+        parts.append(p.reshape(p.shape[:-2] + (-1,)))
+        sh += w
+    return np.concatenate(parts, axis=-1)
 
 
 def unpack_codes(b, bits, role):
-    shape_rows = (ROWS, COLS) if role == "K" else (COLS, ROWS)
-    nlo = ROWS * COLS // 2
-    lo = unpack_nibbles(b[..., :nlo].reshape(b.shape[:-1] + (shape_rows[0], shape_rows[1] // 2)))
-    if bits == 5:
-        hi = unpack_bitplane(b[..., nlo:].reshape(b.shape[:-1] + (shape_rows[0], shape_rows[1] // 8)))
-        lo = lo | (hi << 4)
-    return lo if role == "K" else np.swapaxes(lo, -1, -2)
+    n_rows = ROWS if role == "K" else COLS
+    code = None
+    off = sh = 0
+    for w in PLANES[bits]:
+        nb = ROWS * COLS * w // 8
+        p = _unpack_plane(b[..., off:off + nb].reshape(b.shape[:-1] + (n_rows, -1)), w).astype(np.uint8)
+        code = (p << sh) if code is None else (code | (p << sh))
+        off += nb
+        sh += w
+    return code if role == "K" else np.swapaxes(code, -1, -2)

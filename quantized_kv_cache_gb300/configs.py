@@ -22,6 +22,11 @@ recipe (seed, K outlier channels and factor).
   heads x 256, 24 query heads; TBQ4 body (16,896 B per position), tq6_0 ring, 1,024-position
   tail; each sequence starts with 128 groups + 4,096 positions unsealed; 32 decode steps
   with a bulk seal of 4 x 128 = 512 groups per layer after step 16.
+
+A sixth workload measures the KVarN widths beyond 4 and 5 (SJ-KVaRN §7, the 3/2 cache of the
+12 GB-card run, here with the scalar body: trellis and scalar records have the same size):
+- hybrid27b_kvarn32_200k: the hybrid27b shape at 204,800 positions with KVarN 3-bit K and
+  2-bit V, tq6_0 ring, the same seal policy; 64 decode steps.
 """
 
 from dataclasses import dataclass, field
@@ -94,14 +99,16 @@ WORKLOADS = {
                              ring=20608, contexts=[262144, 196608, 131072, 65536], steps=32, seed=4, n_out=8,
                              out_factor=16.0, keep=4096, seal_trigger=-2, prefill_unsealed=128 * 128 + 4096,
                              bulk_seal_step=16),
+    "hybrid27b_kvarn32_200k": Workload("hybrid27b_kvarn32_200k", 16, 4, 256, 24, "kvarn3", "kvarn2", "tq6_0",
+                                       "f16", tail=1024, ring=8448, contexts=[204800], steps=64, seed=5, n_out=8,
+                                       out_factor=16.0, keep=4096, seal_trigger=8192),
 }
 
 
 def record_bytes(fmt, head_dim):
     """Bytes of one 128-position body record of one KV head (K or V) in the given format."""
     return {"tbq4": 66 * head_dim, "q8_0": 136 * head_dim, "q4_0": 72 * head_dim,
-            "kvarn4": (head_dim // 256) * (4096 * 4 + 1152),
-            "kvarn5": (head_dim // 256) * (4096 * 5 + 1152)}[fmt]
+            **{f"kvarn{b}": (head_dim // 256) * (4096 * b + 1152) for b in (2, 3, 4, 5, 6, 8)}}[fmt]
 
 
 def journal_len(n_tok, sealed):

@@ -203,6 +203,26 @@ __device__ void fill_ring(const Layout& L, const void* pool, int w, int64_t unit
     }
 }
 
+// Codes e0 .. e0 + 7 (e0 a multiple of 8) of row `row` of a KVarN tile's code planes (rows of
+// len codes; see kvarn_planes): each plane's 8 codes are w consecutive bytes, one aligned load.
+__device__ __forceinline__ uint64_t load_wbytes(const uint8_t* p, int w) {
+    switch (w) {
+        case 1: return *p;
+        case 2: return *reinterpret_cast<const uint16_t*>(p);
+        case 4: return *reinterpret_cast<const uint32_t*>(p);
+        default: return *reinterpret_cast<const uint64_t*>(p);
+    }
+}
+__device__ __forceinline__ void kvarn_codes8(const uint8_t* tile, int bits, int len, int row, int e0, int (&code)[8]) {
+    const int w0 = bits >= 4 ? (bits == 8 ? 8 : 4) : 2, w1 = bits - w0;
+    const int64_t at = (int64_t)row * len + e0;
+    const uint64_t a = load_wbytes(tile + at * w0 / 8, w0);
+    const uint64_t b = w1 ? load_wbytes(tile + 4096 * w0 + at * w1 / 8, w1) : 0;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+        code[m] = (int)(((a >> (w0 * m)) & ((1u << w0) - 1)) | (((b >> (w1 * m)) & ((1u << w1) - 1)) << w0));
+}
+
 // Body K records (token-major) of one tile: positions [tstart, tstart + TILE) of group g.
 template <int D, int TILE, int LD>
 __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
@@ -230,19 +250,16 @@ __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int
             const float d = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 32) + (c0 >> 5)]);
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = (float)((int)((w4 >> (4 * k)) & 15) - 8) * d;
-        } else {   // KVarN
-            const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+        } else {   // KVarN (any code width: kvarn_code reads the planes)
+            const int bits = kvarn_bits(fmt);
             const int hh = c0 >> 8, j0 = c0 & 255;
             const uint8_t* tr = rec + (int64_t)hh * (4096 * bits + 1152);
-            const uint32_t lo = *reinterpret_cast<const uint32_t*>(tr + t * 128 + (j0 >> 1));
-            const uint32_t hi = (bits == 5) ? tr[16384 + t * 32 + (j0 >> 3)] : 0u;
             const uint16_t* sb = reinterpret_cast<const uint16_t*>(tr + 4096 * bits);
             const float S = h2f(sb[t]), Z = h2f(sb[128 + t]);
+            int code[8];
+            kvarn_codes8(tr, bits, 256, t, j0, code);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int code = ((lo >> (4 * k)) & 15) | (((hi >> k) & 1) << 4);
-                v[k] = ((float)code * S + Z) * h2f(sb[256 + j0 + k]);
-            }
+            for (int k = 0; k < 8; ++k) v[k] = ((float)code[k] * S + Z) * h2f(sb[256 + j0 + k]);
         }
         store8(dst + i * LD + c0, v);
     }
@@ -276,19 +293,16 @@ __device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int
             const uint16_t* dr = reinterpret_cast<const uint16_t*>(rec + 128 * D);
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = (float)q[k] * h2f(dr[(t0 + k) * (D / 32) + (c >> 5)]);
-        } else {   // KVarN
-            const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+        } else {   // KVarN (any code width)
+            const int bits = kvarn_bits(fmt);
             const int hh = c >> 8, j = c & 255;
             const uint8_t* tr = rec + (int64_t)hh * (4096 * bits + 1152);
-            const uint32_t lo = *reinterpret_cast<const uint32_t*>(tr + j * 64 + (t0 >> 1));
-            const uint32_t hi = (bits == 5) ? tr[16384 + j * 16 + (t0 >> 3)] : 0u;
             const uint16_t* sb = reinterpret_cast<const uint16_t*>(tr + 4096 * bits);
             const float C = h2f(sb[256 + j]);
+            int code[8];
+            kvarn_codes8(tr, bits, 128, j, t0, code);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int code = ((lo >> (4 * k)) & 15) | (((hi >> k) & 1) << 4);
-                v[k] = ((float)code * h2f(sb[t0 + k]) + h2f(sb[128 + t0 + k])) * C;
-            }
+            for (int k = 0; k < 8; ++k) v[k] = ((float)code[k] * h2f(sb[t0 + k]) + h2f(sb[128 + t0 + k])) * C;
         }
         store8(dst + c * LDV + t0 - rel, v);
     }

@@ -62,7 +62,13 @@ struct Geo {
     static constexpr int P_BYTES = NVB * 8 * NT * 256;                  // P' fragments
     static_assert(P_BYTES >= 2 * D, "the P' area stages the codes of a fused append");
     static constexpr int RED_FLOATS = (NVB + 2) * NQ * 8 + NQ;          // [q][warp] exchange rows, m, l
-    static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QB_BYTES + P_BYTES + RED_FLOATS * 4;
+    // KVarN codes of 2 or 3 bits: each group's code planes are expanded in shared memory into
+    // the 4-bit nibble image of a KVarN4 tile (16 KB per 256-channel tile), which the 4-bit
+    // fragment decoders read; the scales are read from the staged record
+    static constexpr bool KIMG = (KF == KF_KVARN) && (KB < 4);
+    static constexpr bool VIMG = (VF == KF_KVARN) && (VB < 4);
+    static constexpr int IMG_BYTES = ((KIMG ? 1 : 0) + (VIMG ? 1 : 0)) * 16384 * (D / 256);
+    static constexpr int FIXED = 128 + (LUT ? kLutBytes : 0) + QB_BYTES + P_BYTES + RED_FLOATS * 4 + IMG_BYTES;
     // resident CTAs per SM: three when two stages fit in a third of shared memory, else two,
     // else one (the per-CTA budgets leave the 1 KB per CTA the SM reserves)
     static constexpr int THREE_CTA_BYTES = 74 * 1024;
@@ -99,6 +105,33 @@ __device__ __forceinline__ void load_row_f(const uint16_t* row, float (&f)[N]) {
                 f[8 * k + 2 * i + 1] = a.y;
             }
         }
+    }
+}
+
+// 8 codes of a 2-bit plane (16 bits, code m at bits 2m) spread to bits 4m, 4m + 1.
+__device__ __forceinline__ uint32_t spread2(uint32_t x) {
+    x = (x | (x << 8)) & 0x00FF00FFu;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    return (x | (x << 2)) & 0x33333333u;
+}
+// 8 codes of a 1-bit plane (a byte, code m at bit m) spread to bit 4m.
+__device__ __forceinline__ uint32_t spread1(uint32_t x) {
+    x = (x | (x << 12)) & 0x000F000Fu;
+    x = (x | (x << 6)) & 0x03030303u;
+    return (x | (x << 3)) & 0x11111111u;
+}
+// The nibble image (KVarN4 layout) of the codes of ntile 2- or 3-bit KVarN tiles at rec: word u
+// of a tile's image holds the 8 codes whose low bits are uint16 u of the 2-bit plane and whose
+// third bits are byte u of the 1-bit plane; this is so for the token rows of K and the channel
+// rows of V alike (the planes are row-major with the same codes per row). All threads.
+template <int B>
+__device__ __forceinline__ void nibble_image(const uint8_t* rec, int ntile, uint8_t* img) {
+    for (int u = threadIdx.x; u < 4096 * ntile; u += kCT) {
+        const uint8_t* tb = rec + (size_t)(u >> 12) * (4096 * B + 1152);
+        const int uu = u & 4095;
+        uint32_t x = spread2(reinterpret_cast<const uint16_t*>(tb)[uu]);
+        if (B == 3) x |= spread1(tb[8192 + uu]) << 2;
+        reinterpret_cast<uint32_t*>(img + (size_t)(u >> 12) * 16384)[uu] = x;
     }
 }
 
@@ -142,6 +175,8 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
     float* red = reinterpret_cast<float*>(cur);
     float* zsm = red + NQ * 8;                            // [NVB][NQ][warp] value zero-point sums
+    uint8_t* kimg = reinterpret_cast<uint8_t*>(red + Gm::RED_FLOATS);   // nibble images (2/3-bit codes)
+    uint8_t* vimg = kimg + (Gm::KIMG ? 16384 * (D / 256) : 0);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // thread 0 streams the records: group i into stage i % nst, issued once stage i % nst is
@@ -331,6 +366,11 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
         mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
         const uint8_t* kr = stages + (size_t)sl * stage_bytes;
         const uint8_t* vr = kr + v_off;
+        if constexpr (Gm::KIMG || Gm::VIMG) {
+            csync();   // the previous group's reads of the images are done
+            if constexpr (Gm::KIMG) nibble_image<KB>(kr, D / 256, kimg);
+            if constexpr (Gm::VIMG) nibble_image<VB>(vr, D / 256, vimg);
+        }
         if (KF == KF_KVARN) {
             write_qb(kr);
             csync();
@@ -373,11 +413,12 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                     // this thread's 64 channels of the 256-channel tile bk: 32 bytes per row; odd
                     // rows read the two halves in the other order so a quarter warp hits 32 banks
                     const uint8_t* tb = kr + (size_t)bk * (4096 * KB + 1152);
+                    const uint8_t* tc = Gm::KIMG ? kimg + (size_t)bk * 16384 : tb;     // nibble codes
                     const int odd = g & 1;
-                    uint4 x0a = *reinterpret_cast<const uint4*>(tb + t0 * 128 + 32 * tq + 16 * odd);
-                    uint4 x0b = *reinterpret_cast<const uint4*>(tb + t0 * 128 + 32 * tq + 16 * (1 - odd));
-                    uint4 x1a = *reinterpret_cast<const uint4*>(tb + t1 * 128 + 32 * tq + 16 * odd);
-                    uint4 x1b = *reinterpret_cast<const uint4*>(tb + t1 * 128 + 32 * tq + 16 * (1 - odd));
+                    uint4 x0a = *reinterpret_cast<const uint4*>(tc + t0 * 128 + 32 * tq + 16 * odd);
+                    uint4 x0b = *reinterpret_cast<const uint4*>(tc + t0 * 128 + 32 * tq + 16 * (1 - odd));
+                    uint4 x1a = *reinterpret_cast<const uint4*>(tc + t1 * 128 + 32 * tq + 16 * odd);
+                    uint4 x1b = *reinterpret_cast<const uint4*>(tc + t1 * 128 + 32 * tq + 16 * (1 - odd));
                     if (odd) {
                         const uint4 t = x0a; x0a = x0b; x0b = t;
                         const uint4 u = x1a; x1a = x1b; x1b = u;
@@ -656,8 +697,9 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
             vt[mt] = vr;
             if (VF == KF_KVARN) {
                 vt[mt] = vr + (size_t)(c0 >> 8) * (4096 * VB + 1152);
-                const uint4 y0 = *reinterpret_cast<const uint4*>(vt[mt] + (c0 & 255) * 64 + 16 * tq);
-                const uint4 y1 = *reinterpret_cast<const uint4*>(vt[mt] + (c1 & 255) * 64 + 16 * tq);
+                const uint8_t* vc = Gm::VIMG ? vimg + (size_t)(c0 >> 8) * 16384 : vt[mt];   // nibble codes
+                const uint4 y0 = *reinterpret_cast<const uint4*>(vc + (c0 & 255) * 64 + 16 * tq);
+                const uint4 y1 = *reinterpret_cast<const uint4*>(vc + (c1 & 255) * 64 + 16 * tq);
                 X0[mt][0] = y0.x; X0[mt][1] = y0.y; X0[mt][2] = y0.z; X0[mt][3] = y0.w;
                 X1[mt][0] = y1.x; X1[mt][1] = y1.y; X1[mt][2] = y1.z; X1[mt][3] = y1.w;
                 if (VB == 5) {
@@ -853,6 +895,7 @@ int dispatch(const Layout& L, F&& f) {
     KVQ_BODY_CASE(128, 16, KF_Q8, KF_Q4, 4, 4, KVQ_Q8_0, KVQ_Q4_0)
     KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4)
     KVQ_BODY_CASE(256, 16, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4)
+    KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 3, 2, KVQ_KVARN3, KVQ_KVARN2)
     KVQ_BODY_CASE(512, 8, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
     KVQ_BODY_CASE(512, 16, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
 #undef KVQ_BODY_CASE

@@ -63,18 +63,11 @@ __global__ void dequant_kernel(Layout L, const void* pool, int layer, int slot, 
             const uint8_t* rec = body_rec(L, pool, w, unit, g);
             const int fmt = L.fmt[w];
             const int D = L.D;
-            if (fmt == KVQ_KVARN4 || fmt == KVQ_KVARN5) {
-                const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+            if (kvarn_bits(fmt)) {
+                const int bits = kvarn_bits(fmt);
                 const int hh = ch >> 8, j = ch & 255;
                 const uint8_t* tr = rec + (int64_t)hh * (4096 * bits + 1152);
-                int code;
-                if (w == 0) {
-                    code = (tr[t * 128 + (j >> 1)] >> ((j & 1) * 4)) & 15;
-                    if (bits == 5) code |= ((tr[16384 + t * 32 + (j >> 3)] >> (j & 7)) & 1) << 4;
-                } else {
-                    code = (tr[j * 64 + (t >> 1)] >> ((t & 1) * 4)) & 15;
-                    if (bits == 5) code |= ((tr[16384 + j * 16 + (t >> 3)] >> (t & 7)) & 1) << 4;
-                }
+                const int code = (w == 0) ? kvarn_code(tr, bits, 256, t, j) : kvarn_code(tr, bits, 128, j, t);
                 const uint16_t* sb = (const uint16_t*)(tr + 4096 * bits);
                 x = fmul(fadd(fmul((float)code, h2f(sb[t])), h2f(sb[128 + t])), h2f(sb[256 + j]));
             } else {

@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     const int nh = L.D / 256;
     const int h = blockIdx.y, w = blockIdx.z / nh, half = blockIdx.z % nh;
     const int fmt = L.fmt[w];
-    const int bits = (fmt == KVQ_KVARN5) ? 5 : 4;
+    const int bits = kvarn_bits(fmt);
     const float Q = (float)((1 << bits) - 1);
     const int64_t unit = L.unit(tk.layer, tk.slot, h);
     extern __shared__ __align__(16) uint8_t kv_sm[];
@@ -739,33 +739,29 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     __syncthreads();
 
     uint8_t* rec = body_rec(L, p.pool, w, unit, tk.g) + (int64_t)half * (4096 * bits + 1152);
-    if (w == 0) {           // K: token-major low plane [128][128], high plane [128][32]
-        for (int i = threadIdx.x; i < 128 * 128; i += kKvThreads) {
-            const int t = i >> 7, j = 2 * (i & 127);
-            rec[i] = (uint8_t)((codes[t * CS + j] & 15) | ((codes[t * CS + j + 1] & 15) << 4));
-        }
-        if (bits == 5) {
-            for (int i = threadIdx.x; i < 128 * 32; i += kKvThreads) {
-                const int t = i >> 5, j0 = 8 * (i & 31);
-                uint8_t b = 0;
+    // code planes (kvarn_planes): K token-major (128 rows of 256 codes), V channel-major (256
+    // rows of 128 codes); byte i of a plane of width pw packs 8 / pw codes of one row
+    {
+        int pw[2];
+        const int np = kvarn_planes(bits, pw);
+        uint8_t* plane = rec;
+        int sh = 0;
+        for (int k = 0; k < np; ++k) {
+            const int wk = pw[k], per = 8 / wk, mask = (1 << wk) - 1;
+            const int row_bytes = (w == 0 ? 256 : 128) / per;
+            for (int i = threadIdx.x; i < 4096 * wk; i += kKvThreads) {
+                const int row = i / row_bytes, e0 = (i % row_bytes) * per;
+                uint32_t b = 0;
 #pragma unroll
-                for (int m = 0; m < 8; ++m) b |= (uint8_t)(((codes[t * CS + j0 + m] >> 4) & 1) << m);
-                rec[16384 + i] = b;
+                for (int m = 0; m < 8; ++m) {
+                    if (m >= per) break;
+                    const uint32_t code = (w == 0) ? codes[row * CS + e0 + m] : codes[(e0 + m) * CS + row];
+                    b |= ((code >> sh) & mask) << (wk * m);
+                }
+                plane[i] = (uint8_t)b;
             }
-        }
-    } else {                // V: channel-major low plane [256][64], high plane [256][16]
-        for (int i = threadIdx.x; i < 256 * 64; i += kKvThreads) {
-            const int j = i >> 6, t = 2 * (i & 63);
-            rec[i] = (uint8_t)((codes[t * CS + j] & 15) | ((codes[(t + 1) * CS + j] & 15) << 4));
-        }
-        if (bits == 5) {
-            for (int i = threadIdx.x; i < 256 * 16; i += kKvThreads) {
-                const int j = i >> 4, t0 = 8 * (i & 15);
-                uint8_t b = 0;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) b |= (uint8_t)(((codes[(t0 + m) * CS + j] >> 4) & 1) << m);
-                rec[16384 + i] = b;
-            }
+            plane += 4096 * wk;
+            sh += wk;
         }
     }
     uint16_t* sb = reinterpret_cast<uint16_t*>(rec + 4096 * bits);
@@ -794,7 +790,7 @@ int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t 
 int launch_seal(const Layout& L, const SealParams& p, void* stream) {
     const int groups = p.n_layers * p.groups_per_layer;
     if (groups == 0) return 0;
-    if (L.fmt[0] == KVQ_KVARN4 || L.fmt[0] == KVQ_KVARN5) {
+    if (kvarn_bits(L.fmt[0])) {
         if (L.D % 256) return (int)cudaErrorInvalidValue;
         cudaStream_t s = (cudaStream_t)stream;
         if (p.k_src != nullptr) return launch_kvarn<J_IN>(L, p, groups, s);

@@ -35,7 +35,7 @@ struct kvq_cache {
 namespace kvq {
 
 static bool is_body(int f) {
-    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || f == KVQ_KVARN4 || f == KVQ_KVARN5;
+    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || kvarn_bits(f) != 0;
 }
 
 bool make_layout(const kvq_config& c, Layout* out) {

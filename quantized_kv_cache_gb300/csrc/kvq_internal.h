@@ -24,14 +24,60 @@ constexpr int kMaxG = 16;       // query heads per KV head handled by the decode
 
 enum Rot : int32_t { ROT_NONE = 0, ROT_HAD256 = 1, ROT_TBQ128 = 2 };
 
+// Code bits of a KVarN body format, 0 for any other format.
+KVQ_HD int kvarn_bits(int fmt) {
+    switch (fmt) {
+        case KVQ_KVARN2: return 2;
+        case KVQ_KVARN3: return 3;
+        case KVQ_KVARN4: return 4;
+        case KVQ_KVARN5: return 5;
+        case KVQ_KVARN6: return 6;
+        case KVQ_KVARN8: return 8;
+        default: return 0;
+    }
+}
+
+// Code planes of a b-bit KVarN code, low plane first: plane i holds bits [s, s + w_i) of every
+// code, s the widths before it (2: 2; 3: 2+1; 4: 4; 5: 4+1; 6: 4+2; 8: 8). A plane of width w
+// packs each row's codes LSB-first, code i at bit w (i mod 8/w) of byte (i w) / 8; it spans
+// 4,096 w bytes of a 128 x 256 tile. Returns the plane count; w[] receives the widths.
+KVQ_HD int kvarn_planes(int bits, int* w) {
+    switch (bits) {
+        case 2: w[0] = 2; return 1;
+        case 3: w[0] = 2; w[1] = 1; return 2;
+        case 4: w[0] = 4; return 1;
+        case 5: w[0] = 4; w[1] = 1; return 2;
+        case 6: w[0] = 4; w[1] = 2; return 2;
+        case 8: w[0] = 8; return 1;
+        default: return 0;
+    }
+}
+
+// Code i of row `row` of a KVarN tile's code planes (rows of `len` codes: 256 for K's token
+// rows, 128 for V's channel rows).
+KVQ_HD int kvarn_code(const uint8_t* tile, int bits, int len, int row, int i) {
+    int w[2];
+    const int np = kvarn_planes(bits, w);
+    int code = 0, s = 0;
+    const uint8_t* plane = tile;
+    for (int k = 0; k < np; ++k) {
+        const int per = 8 / w[k];
+        const uint8_t byte = plane[(int64_t)row * (len / per) + i / per];
+        code |= ((byte >> (w[k] * (i % per))) & ((1 << w[k]) - 1)) << s;
+        s += w[k];
+        plane += 4096 * w[k];
+    }
+    return code;
+}
+
 // Record bytes of one 128-position group of one KV head (K or V), per format.
 KVQ_HD int64_t record_bytes(int fmt, int D) {
     switch (fmt) {
         case KVQ_TBQ4: return 66LL * D;                       // 64 B idx + 2 B norm per 128
         case KVQ_Q8_0: return 136LL * D;                      // 34 B per 32, 128 tokens
         case KVQ_Q4_0: return 72LL * D;                       // 18 B per 32
-        case KVQ_KVARN4: return (int64_t)(D / 256) * (4096 * 4 + 1152);
-        case KVQ_KVARN5: return (int64_t)(D / 256) * (4096 * 5 + 1152);
+        case KVQ_KVARN2: case KVQ_KVARN3: case KVQ_KVARN4: case KVQ_KVARN5: case KVQ_KVARN6: case KVQ_KVARN8:
+            return (int64_t)(D / 256) * (4096 * kvarn_bits(fmt) + 1152);
         default: return -1;
     }
 }
@@ -48,7 +94,7 @@ KVQ_HD int64_t record_code_bytes(int fmt, int D) {
 
 KVQ_HD int rotation_of(int fmt) {
     if (fmt == KVQ_TBQ4) return ROT_TBQ128;
-    if (fmt == KVQ_KVARN4 || fmt == KVQ_KVARN5) return ROT_HAD256;
+    if (kvarn_bits(fmt)) return ROT_HAD256;
     return ROT_NONE;
 }
 

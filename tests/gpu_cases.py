@@ -59,6 +59,12 @@ FAMILIES = {
                           contexts=[777, 1200], keep=256, steps=2, factor=12.0, n_out=16),
     "tbq4_ring": Family("tbq4_ring", 256, 2, 12, "tbq4", "tbq4", "tq6_0", "f16", T=96, R=896,
                         contexts=[640, 1900], keep=384, steps=3, n_out=8),
+    # KVarN widths without a streaming instance (the generic decode path): 3-bit keys with
+    # 2-bit values on a tq6_0 ring, and 8-bit keys with 6-bit values on an F16 journal
+    "kvarn32_ring": Family("kvarn32_ring", 256, 2, 8, "kvarn3", "kvarn2", "tq6_0", "f16", T=64, R=768,
+                           contexts=[650, 1300], keep=256, steps=2, factor=16.0, n_out=8),
+    "kvarn86_f16": Family("kvarn86_f16", 256, 1, 6, "kvarn8", "kvarn6", "f16", "f16", T=128, R=768,
+                          contexts=[900, 1250], keep=128, steps=2, factor=16.0, n_out=8),
 }
 
 

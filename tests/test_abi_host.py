@@ -67,6 +67,21 @@ def test_named_bytes_per_token_pins(lib):
     assert _lib.kv_bytes_per_token(configs.WORKLOADS["hybrid27b_kvarn44"].config())["f16_bytes_per_token"] == 65536
 
 
+def test_kvarn_widths_bytes_per_token(lib):
+    """KVarN-b bodies of any width (and K / V widths that differ): the library's bytes per token
+    are the oracle's closed form (SJ-KVaRN §3: 4,096 b code bytes + 1,152 B of scales per tile)."""
+    from oracle import sizes
+    base = configs.WORKLOADS["hybrid27b_kvarn44"]
+    for kb, vb in ((2, 2), (3, 3), (3, 2), (6, 6), (8, 8), (8, 6), (4, 5)):
+        c = base.config()
+        c.k_body, c.v_body = _lib.FMT_NAMES[f"kvarn{kb}"], _lib.FMT_NAMES[f"kvarn{vb}"]
+        got = _lib.kv_bytes_per_token(c)["body_bytes_per_token"]
+        assert got == sizes.kv_bytes_per_token(16, 4, 256, f"kvarn{kb}", f"kvarn{vb}")
+    c = base.config()
+    c.k_body, c.v_body = _lib.KVARN3, _lib.KVARN2
+    assert _lib.kv_bytes_per_token(c)["body_bytes_per_token"] == 11392     # the pages' 3/2 cache
+
+
 @pytest.mark.parametrize("field,value", [("head_dim", 192), ("n_q_heads", 4 * 32), ("ring_capacity", 1000),
                                          ("tail_fmt", _lib.TQ6_0), ("k_body", _lib.F16), ("v_body", _lib.TBQ4)])
 def test_invalid_configs_refused(lib, field, value):

@@ -40,6 +40,7 @@ SAMPLES = {
     "fa14b_q8q4": [(0, 5)],
     "widehead_kvarn55": [(2, 1), (7, 0)],
     "longctx_tbq4": [(0, 2), (3, 0)],
+    "hybrid27b_kvarn32_200k": [(0, 2)],
 }
 
 

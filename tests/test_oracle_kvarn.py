@@ -52,7 +52,7 @@ def test_fixed_point_of_sign_tile():
     assert np.allclose(kvarn.decode(code, S, Z, C), X, atol=0.5 * 15 * 2 ** -14 + 1e-3)
 
 
-@pytest.mark.parametrize("bits", [4, 5])
+@pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
 def test_row_rounding_error_bound(bits):
     X = _tile()
     code, S, Z, C = kvarn.encode(X, bits)
@@ -68,7 +68,7 @@ def test_row_rounding_error_bound(bits):
 
 def test_tile_bytes_and_bits_per_value():
     X = _tile()
-    for bits in (4, 5):
+    for bits in (2, 3, 4, 5, 6, 8):
         code, S, Z, C = kvarn.encode(X, bits)
         for role in "KV":
             b = kvarn.pack_codes(code, bits, role)
@@ -92,6 +92,28 @@ def test_role_layouts():
     # high planes: K row t occupies 32 B after the 16 KiB low plane; V row c 16 B
     assert bK[16384 + 32 * 2] & 1 == code[2, 0] >> 4
     assert (bV[16384 + 16 * 3] >> 2) & 1 == code[2, 3] >> 4
+
+
+def test_plane_layouts_of_other_widths():
+    """2-bit: four codes per byte, LSB first; 3-bit: that 2-bit plane, then a one-bit plane;
+    6-bit: the nibble plane, then a 2-bit plane; 8-bit: one byte per code."""
+    rng = np.random.default_rng(3)
+    for bits in (2, 3, 6, 8):
+        code = rng.integers(0, 2 ** bits, (128, 256)).astype(np.uint8)
+        bK = kvarn.pack_codes(code, bits, "K")
+        bV = kvarn.pack_codes(code, bits, "V")
+        if bits in (2, 3):
+            lo = code & 3
+            assert bK[64 * 5 + 2] == lo[5, 8] | (lo[5, 9] << 2) | (lo[5, 10] << 4) | (lo[5, 11] << 6)
+            assert bV[32 * 7 + 1] == lo[4, 7] | (lo[5, 7] << 2) | (lo[6, 7] << 4) | (lo[7, 7] << 6)
+        if bits == 3:   # one-bit plane after the 8 KiB 2-bit plane: K rows of 32 B, V rows of 16 B
+            assert (bK[8192 + 32 * 9 + 1] >> 3) & 1 == code[9, 11] >> 2
+            assert (bV[8192 + 16 * 2 + 3] >> 5) & 1 == code[29, 2] >> 2
+        if bits == 6:   # 2-bit plane after the 16 KiB nibble plane
+            assert bK[128 * 3] == (code[3, 0] & 15) | ((code[3, 1] & 15) << 4)
+            assert (bK[16384 + 64 * 3] >> 2) & 3 == code[3, 1] >> 4
+        if bits == 8:
+            assert np.array_equal(bK.reshape(128, 256), code) and np.array_equal(bV.reshape(256, 128), code.T)
 
 
 def test_constant_rows_and_zero_tile():
