@@ -24,7 +24,7 @@ recipe (seed, K outlier channels and factor).
   with a bulk seal of 4 x 128 = 512 groups per layer after step 16.
 
 A sixth workload measures the KVarN widths beyond 4 and 5 (SJ-KVaRN §7, the 3/2 cache of the
-12 GB-card run, here with the scalar body: trellis and scalar records have the same size):
+12 GB-card run, here with the scalar body, whose records take as many bytes as the trellis ones):
 - hybrid27b_kvarn32_200k: the hybrid27b shape at 204,800 positions with KVarN 3-bit K and
   2-bit V, tq6_0 ring, the same seal policy; 64 decode steps.
 """
