@@ -33,7 +33,7 @@ def rotation_of(fmt):
         return TBQ128
     if fmt.startswith("kvarn"):
         return HAD256
-    if fmt in ("q8_0", "q4_0"):
+    if fmt in ("q8_0", "q4_0", "q5_0", "q6_0", "q4_1", "q5_1"):
         return NONE
     raise ValueError(fmt)
 
@@ -41,7 +41,7 @@ def rotation_of(fmt):
 @dataclass(frozen=True)
 class HeadConfig:
     head_dim: int
-    k_body: str            # tbq4 | q8_0 | q4_0 | kvarn4 | kvarn5
+    k_body: str            # tbq4 | q8_0 | q4_0 | q5_0 | q6_0 | q4_1 | q5_1 | kvarn2..kvarn8
     v_body: str
     journal: str           # tq6_0 | f16 | bf16
     tail_fmt: str          # f16 | bf16 (exact tail store; with an exact journal, its format)
@@ -79,6 +79,12 @@ def encode_body(X, fmt):
     if fmt == "q4_0":
         d, c = codecs.q4_encode(X)
         return {"scale": d, "code": c.reshape(X.shape)}
+    if fmt in QSYM:
+        d, c = codecs.qsym_encode(X, QSYM[fmt])
+        return {"scale": d, "code": c.reshape(X.shape)}
+    if fmt in QMIN:
+        d, m, c = codecs.qmin_encode(X, QMIN[fmt])
+        return {"scale": d, "min": m, "code": c.reshape(X.shape)}
     if fmt.startswith("kvarn"):
         bits = int(fmt[5:])
         D = X.shape[-1]
@@ -86,6 +92,12 @@ def encode_body(X, fmt):
         code, S, Z, C = kvarn.encode(tiles, bits)
         return {"code": code, "S": S, "Z": Z, "C": C, "bits": bits}
     raise ValueError(fmt)
+
+
+# 32-value block formats beyond Q8_0 / Q4_0: symmetric levels L, or min-offset levels Q
+QSYM = {"q5_0": 15, "q6_0": 31}
+QMIN = {"q4_1": 15, "q5_1": 31}
+CODE_BITS = {"q5_0": 5, "q6_0": 6, "q4_1": 4, "q5_1": 5}
 
 
 def decode_body(rec, fmt):
@@ -99,6 +111,12 @@ def decode_body(rec, fmt):
     if fmt == "q4_0":
         D = rec["code"].shape[-1]
         return codecs.q4_decode(rec["scale"], rec["code"].reshape(128, D // 32, 32))
+    if fmt in QSYM:
+        D = rec["code"].shape[-1]
+        return codecs.qsym_decode(rec["scale"], rec["code"].reshape(128, D // 32, 32), QSYM[fmt])
+    if fmt in QMIN:
+        D = rec["code"].shape[-1]
+        return codecs.qmin_decode(rec["scale"], rec["min"], rec["code"].reshape(128, D // 32, 32))
     if fmt.startswith("kvarn"):
         x = kvarn.decode(rec["code"], rec["S"], rec["Z"], rec["C"])   # [half, 128, 256]
         return x.transpose(1, 0, 2).reshape(128, -1)
@@ -114,6 +132,19 @@ def pack_body(rec, fmt, role):
             parts.append(kvarn.scale_block(rec["S"][h], rec["Z"][h], rec["C"][h]).view(np.uint8).reshape(-1))
         return np.concatenate(parts)
     code = rec["code"]                                   # [128 tokens, D]
+    if fmt in CODE_BITS:
+        # token-major for K and V alike: the low nibble plane [128][D/2], the high plane (5-bit:
+        # one bit per code [128][D/8]; 6-bit: two bits [128][D/4]), d [128][D/32], then for the
+        # _1 formats m [128][D/32]
+        parts = [codecs.pack_nibbles(code & 15).reshape(-1)]
+        if CODE_BITS[fmt] == 5:
+            parts.append(codecs.pack_bitplane((code >> 4) & 1).reshape(-1))
+        elif CODE_BITS[fmt] == 6:
+            parts.append(codecs.pack_crumbs((code >> 4) & 3).reshape(-1))
+        parts.append(np.ascontiguousarray(rec["scale"]).astype(np.float16).view(np.uint8).reshape(-1))
+        if fmt in QMIN:
+            parts.append(np.ascontiguousarray(rec["min"]).astype(np.float16).view(np.uint8).reshape(-1))
+        return np.concatenate(parts)
     rows = code if role == "K" else code.T               # K token-major, V channel-major
     if fmt in ("tbq4", "q4_0"):
         cb = codecs.pack_nibbles(rows)

@@ -1,4 +1,5 @@
-"""Block codecs of the oracle (test infrastructure): tq6_0, TBQ4, Q8_0, Q4_0.
+"""Block codecs of the oracle (test infrastructure): tq6_0, TBQ4, Q8_0, Q4_0, Q5_0, Q6_0,
+Q4_1, Q5_1.
 
 All encoders take fp32 values whose last axis is a whole number of blocks and return
 (scale fp16 array, code array of small integers); packers turn code arrays into the
@@ -121,6 +122,50 @@ def q4_decode(d, code):
     return v.reshape(code.shape[:-2] + (code.shape[-2] * 32,))
 
 
+# ----------------------------------------------------------------------------- Q5_0 / Q6_0 / Q4_1 / Q5_1
+# The other 32-value block formats the pages compare against (SJ-KVaRN §4.1, §6: q5_1 "a 5-bit
+# block format with a scale and an offset", 24 B / 32; KV cache math and the Qwen page: q5_0
+# 22 B, q6_0 26 B, q4_1 20 B per 32). Reading (the pages give only sizes and names): the _0
+# formats are symmetric like Q4_0, d = fp16(max|x| / L), code = clamp(rint(x / d), -L, L) + L + 1
+# (L = 15, 31); the _1 formats take the block's minimum as the offset, m = fp16(min x),
+# d = fp16((max x - min x) / Q), code = clamp(rint((x - m) / d), 0, Q) (Q = 15, 31), d = 0 -> 0.
+def qsym_encode(x, L):
+    """x[..., 32k] -> (d fp16 [..., k], code uint8 [..., k, 32] in 1..2L+1; L+1 is zero)."""
+    xb = _blocks(x, 32)
+    d = to_f16(np.max(np.abs(xb), axis=-1) / np.float32(L))
+    d32 = d.astype(np.float32)
+    zero = d32 == 0
+    inv = np.where(zero, np.float32(0), np.float32(1.0) / np.where(zero, np.float32(1), d32))
+    q = np.clip(np.rint(xb * inv[..., None].astype(np.float32)), -L, L)
+    return d, (q + (L + 1)).astype(np.uint8)
+
+
+def qsym_decode(d, code, L):
+    v = (code.astype(np.float32) - np.float32(L + 1)) * d.astype(np.float32)[..., None]
+    return v.reshape(code.shape[:-2] + (code.shape[-2] * 32,))
+
+
+def qmin_encode(x, Q):
+    """x[..., 32k] -> (d fp16, m fp16 [..., k], code uint8 [..., k, 32] in 0..Q)."""
+    xb = _blocks(x, 32)
+    lo = np.min(xb, axis=-1)
+    hi = np.max(xb, axis=-1)
+    m = to_f16(lo)
+    d = to_f16((hi - lo) / np.float32(Q))
+    d32, m32 = d.astype(np.float32), m.astype(np.float32)
+    zero = d32 == 0
+    inv = np.where(zero, np.float32(0), np.float32(1.0) / np.where(zero, np.float32(1), d32))
+    with np.errstate(invalid="ignore"):
+        q = np.clip(np.rint((xb - m32[..., None]) * inv[..., None].astype(np.float32)), 0, Q)
+    q = np.where(zero[..., None], 0, q)
+    return d, m, q.astype(np.uint8)
+
+
+def qmin_decode(d, m, code):
+    v = code.astype(np.float32) * d.astype(np.float32)[..., None] + m.astype(np.float32)[..., None]
+    return v.reshape(code.shape[:-2] + (code.shape[-2] * 32,))
+
+
 # ----------------------------------------------------------------------------- nibble packing
 def pack_nibbles(code):
     """code [..., 2m] (values < 16) -> bytes [..., m]: element 2i low nibble, 2i+1 high."""
@@ -148,4 +193,20 @@ def unpack_bitplane(b):
     out = np.empty(b.shape[:-1] + (8 * b.shape[-1],), dtype=np.uint8)
     for j in range(8):
         out[..., j::8] = (b >> j) & 1
+    return out
+
+
+def pack_crumbs(vals):
+    """vals [..., 4m] (values < 4) -> bytes [..., m]: element 4k + j at bits 2j of byte k."""
+    v = vals.astype(np.uint8)
+    out = np.zeros(v.shape[:-1] + (v.shape[-1] // 4,), dtype=np.uint8)
+    for j in range(4):
+        out |= (v[..., j::4] << (2 * j)).astype(np.uint8)
+    return out
+
+
+def unpack_crumbs(b):
+    out = np.empty(b.shape[:-1] + (4 * b.shape[-1],), dtype=np.uint8)
+    for j in range(4):
+        out[..., j::4] = (b >> (2 * j)) & 3
     return out

@@ -22,6 +22,8 @@ BYTES_PER_VALUE = {
     "q5_1": Fraction(24, 32),
     "q5_0": Fraction(22, 32),
     "q6_0": Fraction(26, 32),
+    # the pages name q4_1 without its size: reading, two fp16 (d, m) + 16 B of nibbles per 32
+    "q4_1": Fraction(20, 32),
 }
 
 

@@ -173,3 +173,63 @@ def test_tbq4_ties_go_low():
     assert idx[0, 1] == 8 and idx[0, 0] == 15
     y[1] = np.nextafter(bnd[8], np.float32(1))
     assert codecs.tbq4_encode(y)[1][0, 1] == 9
+
+
+# ----------------------------------------------------------------------------- Q5_0 / Q6_0 / Q4_1 / Q5_1
+@pytest.mark.parametrize("L", [15, 31])
+def test_qsym_error_bound_zero_and_grid(L):
+    x = (RNG.standard_normal((400, 32)) * RNG.uniform(0.01, 50, (400, 1))).astype(np.float32)
+    d, code = codecs.qsym_encode(x, L)
+    xr = codecs.qsym_decode(d, code, L)
+    d32 = d.astype(np.float32)          # [400, 1]: one block per row
+    assert code.min() >= 1 and code.max() <= 2 * L + 1
+    # half a step, plus the fp16 rounding of d over the block's range (|x| <= L d (1 + 2^-11))
+    assert np.all(np.abs(xr.reshape(x.shape) - x) <= 0.5 * d32 + L * d32 * 2 ** -10)
+    # the largest magnitude of each block is coded at level +-L (or next to it)
+    assert np.all(np.abs(code.astype(int) - (L + 1)).max(axis=-1) >= L - 1)
+    # values on the grid come back exactly, and their codes are stable
+    d2, c2 = codecs.qsym_encode(xr, L)
+    assert np.array_equal(codecs.qsym_decode(d2, c2, L), xr)
+    # a zero block: d = 0 and every code the zero level L + 1
+    dz, cz = codecs.qsym_encode(np.zeros(32, np.float32), L)
+    assert dz[0] == 0 and np.all(cz == L + 1)
+
+
+@pytest.mark.parametrize("Q", [15, 31])
+def test_qmin_error_bound_extremes_and_constants(Q):
+    x = (RNG.standard_normal((400, 32)) * RNG.uniform(0.01, 50, (400, 1)) + RNG.uniform(-5, 5, (400, 1))).astype(np.float32)
+    d, m, code = codecs.qmin_encode(x, Q)
+    xr = codecs.qmin_decode(d, m, code).reshape(x.shape)
+    d32, m32 = d.astype(np.float32), m.astype(np.float32)      # [400, 1]: one block per row
+    assert code.max() <= Q
+    # half a step, plus the fp16 roundings of m and d (relative 2^-11) over the block's values
+    bound = 0.5 * d32 + 2 ** -11 * np.abs(m32) + Q * d32 * 2 ** -10 + 1e-6
+    assert np.all(np.abs(xr - x) <= bound)
+    # the block's minimum takes code 0 and its maximum code Q (or next to them)
+    lo = np.argmin(x, axis=-1)
+    hi = np.argmax(x, axis=-1)
+    assert np.all(code[np.arange(400), 0, lo] <= 1) and np.all(code[np.arange(400), 0, hi] >= Q - 1)
+    # a constant block: d = 0, every code 0, decoded as fp16(c)
+    dc, mc, cc = codecs.qmin_encode(np.full(32, 0.3, np.float32), Q)
+    assert dc[0] == 0 and np.all(cc == 0)
+    assert np.all(codecs.qmin_decode(dc, mc, cc) == np.float32(np.float16(0.3)))
+
+
+def test_block_format_sizes_are_the_pages():
+    """Packed record sizes per 32 values: q5_0 22 B, q6_0 26 B, q4_1 20 B, q5_1 24 B (the pages'
+    block sizes, also in the oracle's byte table)."""
+    from oracle.cache import encode_body, pack_body
+    from oracle import sizes
+    X = RNG.standard_normal((128, 256)).astype(np.float32)
+    for fmt, b in (("q5_0", 22), ("q6_0", 26), ("q4_1", 20), ("q5_1", 24)):
+        rec = encode_body(X, fmt)
+        for role in "KV":
+            assert pack_body(rec, fmt, role).size == 128 * 256 // 32 * b
+        assert sizes.record_bytes(fmt, 256) == 128 * 256 // 32 * b
+
+
+def test_crumb_packing_exhaustive():
+    v = np.array([[a, b, c, d] for a in range(4) for b in range(4) for c in range(4) for d in range(4)], np.uint8)
+    p = codecs.pack_crumbs(v)
+    assert np.array_equal(p[:, 0], v[:, 0] | (v[:, 1] << 2) | (v[:, 2] << 4) | (v[:, 3] << 6))
+    assert np.array_equal(codecs.unpack_crumbs(p), v)
