@@ -43,7 +43,8 @@ typedef enum {
     KVQ_EDEVICE = 5        /* device status word reports a problem (see kv_get_status) */
 } kvq_status;
 
-/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, KVARN2..KVARN8. Journal: TQ6_0, F16, BF16.
+/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, Q5_0, Q6_0, Q4_1, Q5_1, KVARN2..KVARN8.
+ * Journal: TQ6_0, F16, BF16.
  * Exact tail: F16, BF16. K and V bodies may differ (e.g. KVARN3 keys, KVARN2 values). */
 typedef enum {
     KVQ_F16 = 0,
@@ -57,7 +58,14 @@ typedef enum {
     KVQ_KVARN2 = 8,  /* same, 2-bit rows (SJ-KVaRN §2.3 scalar body, §3: the 3/2 and 2/2 caches) */
     KVQ_KVARN3 = 9,  /* same, 3-bit rows */
     KVQ_KVARN6 = 10, /* same, 6-bit rows */
-    KVQ_KVARN8 = 11  /* same, 8-bit rows (KVarN8, the pages' ceiling check) */
+    KVQ_KVARN8 = 11, /* same, 8-bit rows (KVarN8, the pages' ceiling check) */
+    /* 32-value block formats the pages compare against (SJ-KVaRN §4.1, §6; the Qwen page):
+     * symmetric d = fp16(max|x| / L) with codes x/d + L + 1, or the block minimum as offset
+     * m = fp16(min x), d = fp16((max - min) / Q), codes (x - m)/d. Records token-major for K and V. */
+    KVQ_Q5_0 = 12,   /* L = 15: 22 B per 32 values */
+    KVQ_Q6_0 = 13,   /* L = 31: 26 B per 32 values */
+    KVQ_Q4_1 = 14,   /* Q = 15: 20 B per 32 values */
+    KVQ_Q5_1 = 15    /* Q = 31: 24 B per 32 values */
 } kvq_fmt;
 
 typedef struct {
@@ -99,12 +107,11 @@ kvq_status kv_bytes_per_token(const kvq_config* cfg, kvq_bytes* out);
 
 /* kv_auto_tier — the least compression that keeps a whole cache of `tokens` positions inside
  * `budget_bytes` (HAL #582 §5 P1, "auto KV-tier policy at boot": walk the ladder f16 ->
- * q8_0 K / q8_0 V -> q8_0 K / q4_0 V and take the first rung whose cost fits; the floor rung
- * when none does). A rung's cost is tokens x layers x KV heads x head_dim x (bytes per K value
- * + bytes per V value), the per-cell byte sum the page budgets with (f16 2 B, q8_0 34/32 B,
- * q4_0 18/32 B per value). Reading: the page's last rung, q5_1 K / q4_0 V, is not one of this
- * library's body formats, so the floor here is q8_0 / q4_0; the f16 rung means an
- * uncompressed cache (*k_fmt = *v_fmt = KVQ_F16: an F16 journal that holds the context,
+ * q8_0 K / q8_0 V -> q8_0 K / q4_0 V -> q5_1 K / q4_0 V and take the first rung whose cost
+ * fits; the floor rung, q5_1 / q4_0, when none does). A rung's cost is tokens x layers x KV
+ * heads x head_dim x (bytes per K value + bytes per V value), the per-cell byte sum the page
+ * budgets with (f16 2 B, q8_0 34/32 B, q5_1 24/32 B, q4_0 18/32 B per value). Reading: the f16
+ * rung means an uncompressed cache (*k_fmt = *v_fmt = KVQ_F16: an F16 journal that holds the context,
  * never sealed). Only n_layers, n_kv_heads and head_dim of cfg are read. Host arithmetic,
  * host pointers out: the chosen formats and their cost in bytes. KVQ_OK when the chosen rung
  * fits, KVQ_ENOSPC with the floor rung when none fits, KVQ_EINVAL on a null pointer, a

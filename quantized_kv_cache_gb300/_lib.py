@@ -12,10 +12,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libkvq.so")
 
 # kvq_fmt
-F16, BF16, TQ6_0, TBQ4, Q8_0, Q4_0, KVARN4, KVARN5, KVARN2, KVARN3, KVARN6, KVARN8 = range(12)
+F16, BF16, TQ6_0, TBQ4, Q8_0, Q4_0, KVARN4, KVARN5, KVARN2, KVARN3, KVARN6, KVARN8, Q5_0, Q6_0, Q4_1, Q5_1 = range(16)
 FMT_NAMES = {"f16": F16, "bf16": BF16, "tq6_0": TQ6_0, "tbq4": TBQ4, "q8_0": Q8_0, "q4_0": Q4_0,
              "kvarn4": KVARN4, "kvarn5": KVARN5, "kvarn2": KVARN2, "kvarn3": KVARN3, "kvarn6": KVARN6,
-             "kvarn8": KVARN8}
+             "kvarn8": KVARN8, "q5_0": Q5_0, "q6_0": Q6_0, "q4_1": Q4_1, "q5_1": Q5_1}
 # regions
 REGION_SINK, REGION_JOURNAL, REGION_JOURNAL_SCALE, REGION_TAIL, REGION_BODY = range(5)
 ENOSPC = 2

@@ -61,6 +61,22 @@ __device__ __forceinline__ void store8(__half* dst, const float (&v)[8]) {
     u.w = pack_h2(v[6], v[7]);
     *reinterpret_cast<uint4*>(dst) = u;
 }
+// 8 values as fp16 (dst) and, with lo, the fp16 remainders v - fp16(v) (lo): hi + lo carries
+// 22 significant bits of each value.
+__device__ __forceinline__ void store8_split(__half* dst, __half* lo, const float (&v)[8]) {
+    if (!lo) {
+        store8(dst, v);
+        return;
+    }
+    float h[8], r[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        h[k] = __half2float(__float2half_rn(v[k]));
+        r[k] = v[k] - h[k];
+    }
+    store8(dst, h);
+    store8(lo, r);
+}
 
 // Block-wide FWHT over rows of n values (shared fp32), ascending strides.
 __device__ void block_fwht_rows(float* xs, int total, int n) {
@@ -223,10 +239,23 @@ __device__ __forceinline__ void kvarn_codes8(const uint8_t* tile, int bits, int 
         code[m] = (int)(((a >> (w0 * m)) & ((1u << w0) - 1)) | (((b >> (w1 * m)) & ((1u << w1) - 1)) << w0));
 }
 
+// Value of channel c of row t (token-major) of a Q5_0 / Q6_0 / Q4_1 / Q5_1 record.
+__device__ __forceinline__ float qblock_value(const uint8_t* rec, int fmt, int D, int t, int c) {
+    const int bits = qblock_bits(fmt);
+    int code = (rec[t * (D / 2) + (c >> 1)] >> ((c & 1) * 4)) & 15;
+    if (bits == 5) code |= ((rec[64 * D + t * (D / 8) + (c >> 3)] >> (c & 7)) & 1) << 4;
+    else if (bits == 6) code |= ((rec[64 * D + t * (D / 4) + (c >> 2)] >> (2 * (c & 3))) & 3) << 4;
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(rec + record_code_bytes(fmt, D));
+    const float d = h2f(sc[t * (D / 32) + (c >> 5)]);
+    const int L = qblock_sym_levels(fmt);
+    if (L) return (float)(code - (L + 1)) * d;
+    return (float)code * d + h2f(sc[4 * D + t * (D / 32) + (c >> 5)]);
+}
+
 // Body K records (token-major) of one tile: positions [tstart, tstart + TILE) of group g.
 template <int D, int TILE, int LD>
 __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
-                            const float* cent) {
+                            const float* cent, __half* lo) {
     const int fmt = L.fmt[0];
     const uint8_t* rec = body_rec(L, pool, 0, unit, g);
     constexpr int U = D / 8;
@@ -234,7 +263,10 @@ __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int
         const int i = e / U, u = e % U;
         const int t = rel + i, c0 = 8 * u;
         float v[8];
-        if (fmt == KVQ_TBQ4) {
+        if (qblock_bits(fmt)) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = qblock_value(rec, fmt, D, t, c0 + k);
+        } else if (fmt == KVQ_TBQ4) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));
             const float n = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 128) + (c0 >> 7)]);
 #pragma unroll
@@ -261,14 +293,14 @@ __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = ((float)code[k] * S + Z) * h2f(sb[256 + j0 + k]);
         }
-        store8(dst + i * LD + c0, v);
+        store8_split(dst + i * LD + c0, lo ? lo + i * LD + c0 : nullptr, v);
     }
 }
 
 // Body V records (channel-major) of one tile into dst[D][LDV] (channel-major smem).
 template <int D, int TILE, int LDV>
 __device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
-                            const float* cent) {
+                            const float* cent, __half* lo) {
     const int fmt = L.fmt[1];
     const uint8_t* rec = body_rec(L, pool, 1, unit, g);
     constexpr int U = TILE / 8;   // 8-token units per channel
@@ -276,7 +308,10 @@ __device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int
         const int c = e / U, u = e % U;
         const int t0 = rel + 8 * u;
         float v[8];
-        if (fmt == KVQ_TBQ4) {
+        if (qblock_bits(fmt)) {   // token-major V
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = qblock_value(rec, fmt, D, t0 + k, c);
+        } else if (fmt == KVQ_TBQ4) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + c * 64 + (t0 >> 1));
             const uint16_t* nr = reinterpret_cast<const uint16_t*>(rec + 64 * D);
 #pragma unroll
@@ -304,7 +339,7 @@ __device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = ((float)code[k] * h2f(sb[t0 + k]) + h2f(sb[128 + t0 + k])) * C;
         }
-        store8(dst + c * LDV + t0 - rel, v);
+        store8_split(dst + c * LDV + t0 - rel, lo ? lo + c * LDV + t0 - rel : nullptr, v);
     }
 }
 
@@ -321,7 +356,8 @@ struct Cfg {
     static constexpr int S_BYTES = TILE * NQ * 4;
     static constexpr int P_BYTES = NQ * LDP * 2;
     static constexpr int QF_BYTES = NQ * D * 4;    // fp32 staging of q / the output rows
-    static constexpr int SMEM = K_BYTES + V_BYTES + Q_BYTES + S_BYTES + P_BYTES + QF_BYTES + 64 * 4 + 16 * 4;
+    static constexpr int SMEM = K_BYTES + V_BYTES + Q_BYTES + S_BYTES + P_BYTES + QF_BYTES + 64 * 4 + 16 * 4 +
+                                K_BYTES + V_BYTES;   // the fp16 remainders of body K and V tiles
 };
 
 template <int D, int NQ>
@@ -340,8 +376,14 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
     float* l_run = stat + 16;
     float* alpha = stat + 32;
     float* cent = stat + 48;
+    __half* Ks_lo = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(stat + 64 + 16));
+    __half* Vs_lo = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(Ks_lo) + C::K_BYTES);
 
     const Item it = decode_item(p, blockIdx.x);
+    // body tiles of the 32-value block formats beyond Q8_0 / Q4_0 are held as fp16 values plus
+    // fp16 remainders, and both go through the mma: an fp16 value of code x d (+ m) alone is too
+    // coarse for the decode tolerance where the softmax is sharp
+    const bool lo_now = it.kind == RK_BODY && (qblock_bits(L.fmt[0]) || qblock_bits(L.fmt[1]));
     const int G = L.G;
     const int64_t unit = L.unit(p.layer, it.slot, it.h);
     const bool rotated = (it.kind == RK_BODY || it.kind == RK_RING) && L.rot != ROT_NONE;
@@ -384,8 +426,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
         // ---- decode the tile into shared memory
         if (it.kind == RK_BODY) {
             const int g = (tstart - kSink) / kGroup, rel = (tstart - kSink) % kGroup;
-            fill_body_k<D, TILE, LDK>(L, p.pool, unit, g, rel, Ks, cent);
-            fill_body_v<D, TILE, LDV>(L, p.pool, unit, g, rel, Vs, cent);
+            fill_body_k<D, TILE, LDK>(L, p.pool, unit, g, rel, Ks, cent, lo_now ? Ks_lo : nullptr);
+            fill_body_v<D, TILE, LDV>(L, p.pool, unit, g, rel, Vs, cent, lo_now ? Vs_lo : nullptr);
         } else if (it.kind == RK_RING) {
             fill_ring<D, TILE, LDK>(L, p.pool, 0, unit, tstart, nvalid, Ks);
             fill_ring<D, TILE, LDK>(L, p.pool, 1, unit, tstart, nvalid, Vs);
@@ -405,6 +447,10 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
                     ldsm_x4(smem_u32(Ks + (warp * 16 + (lane & 15)) * LDK + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
                     ldsm_x2(smem_u32(Qs + (nt * 8 + (lane & 7)) * LDK + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1);
                     mma16816(c4, a0, a1, a2, a3, b0, b1);
+                    if (lo_now) {
+                        ldsm_x4(smem_u32(Ks_lo + (warp * 16 + (lane & 15)) * LDK + ks * 16 + (lane >> 4) * 8), a0, a1, a2, a3);
+                        mma16816(c4, a0, a1, a2, a3, b0, b1);
+                    }
                 }
                 const int r0 = warp * 16 + gq, qc = nt * 8 + 2 * tq;
                 Ss[r0 * NQ + qc] = (r0 < nvalid) ? c4[0] * sc : -INFINITY;
@@ -462,11 +508,15 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
                 } else {
                     ldsm_x4_t(smem_u32(Vs + (ks * 16 + (mi >> 1) * 8 + ri) * LDK + ch0 + (mi & 1) * 8), a0, a1, a2, a3);
                 }
+                uint32_t e0 = 0, e1 = 0, e2 = 0, e3 = 0;
+                if (lo_now)   // body tiles are channel-major
+                    ldsm_x4(smem_u32(Vs_lo + (ch0 + (mi & 1) * 8 + ri) * LDV + ks * 16 + (mi >> 1) * 8), e0, e1, e2, e3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     uint32_t b0, b1;
                     ldsm_x2(smem_u32(Ps + (nt * 8 + (lane & 7)) * LDP + ks * 16 + ((lane >> 3) & 1) * 8), b0, b1);
                     mma16816(acc[mt][nt], a0, a1, a2, a3, b0, b1);
+                    if (lo_now) mma16816(acc[mt][nt], e0, e1, e2, e3, b0, b1);
                 }
             }
         }

@@ -70,6 +70,16 @@ __global__ void dequant_kernel(Layout L, const void* pool, int layer, int slot, 
                 const int code = (w == 0) ? kvarn_code(tr, bits, 256, t, j) : kvarn_code(tr, bits, 128, j, t);
                 const uint16_t* sb = (const uint16_t*)(tr + 4096 * bits);
                 x = fmul(fadd(fmul((float)code, h2f(sb[t])), h2f(sb[128 + t])), h2f(sb[256 + j]));
+            } else if (qblock_bits(fmt)) {   // token-major for K and V
+                const int bits = qblock_bits(fmt);
+                int code = (rec[t * (D / 2) + (ch >> 1)] >> ((ch & 1) * 4)) & 15;
+                if (bits == 5) code |= ((rec[64 * D + t * (D / 8) + (ch >> 3)] >> (ch & 7)) & 1) << 4;
+                else if (bits == 6) code |= ((rec[64 * D + t * (D / 4) + (ch >> 2)] >> (2 * (ch & 3))) & 3) << 4;
+                const uint16_t* sc = (const uint16_t*)(rec + record_code_bytes(fmt, D));
+                const float d = h2f(sc[t * (D / 32) + (ch >> 5)]);
+                const int Lv = qblock_sym_levels(fmt);
+                x = Lv ? fmul((float)(code - (Lv + 1)), d)
+                       : fadd(fmul((float)code, d), h2f(sc[4 * D + t * (D / 32) + (ch >> 5)]));
             } else {
                 const int64_t cb = record_code_bytes(fmt, D);
                 const uint16_t* sc = (const uint16_t*)(rec + cb);

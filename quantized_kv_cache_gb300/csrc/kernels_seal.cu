@@ -265,7 +265,8 @@ __device__ __forceinline__ uint16_t encode_q32(const float (&y)[128], int j0, ui
     const uint16_t d16 = f2h_bits(fdiv(a, (float)QMAX));
     const float d = h2f(d16);
     const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
-    constexpr float magic = (QMAX == 127) ? 12582912.0f : 12582920.0f;
+    // 1.5 x 2^23 plus the zero level (Q8_0: 0, its codes are signed bytes; else QMAX + 1)
+    constexpr float magic = 12582912.0f + (QMAX == 127 ? 0.f : (float)(QMAX + 1));
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         uint32_t r[4];
@@ -277,6 +278,46 @@ __device__ __forceinline__ uint16_t encode_q32(const float (&y)[128], int j0, ui
         c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
     }
     return d16;
+}
+
+// Q4_1 (Q 15) or Q5_1 (Q 31) block of 32 values starting at channel j0: m = fp16(min x),
+// d = fp16((max x - min x) / Q), code = clamp(rint((x - fp32(m)) x (1 / fp32(d))), 0, Q) (inv 0
+// when d is 0), rounded by adding 1.5 x 2^23. c[k] holds the code bytes of channels j0 + 4k ..
+template <int Q>
+__device__ __forceinline__ uint16_t encode_qmin(const float (&y)[128], int j0, uint32_t (&c)[8], uint16_t& m16) {
+    float lo = y[j0], hi = y[j0];
+#pragma unroll
+    for (int i = 1; i < 32; ++i) {
+        lo = fminf(lo, y[j0 + i]);
+        hi = fmaxf(hi, y[j0 + i]);
+    }
+    m16 = f2h_bits(lo);
+    const uint16_t d16 = f2h_bits(fdiv(fsub(hi, lo), (float)Q));
+    const float d = h2f(d16), m = h2f(m16);
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float z = fminf(fmaxf(fmul(fsub(y[j0 + 4 * k + i], m), inv), 0.f), (float)Q);
+            r[i] = __float_as_uint(fadd(z, 12582912.0f));
+        }
+        c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
+    }
+    return d16;
+}
+
+// Bit 4 of 8 code bytes (two words, channels 8m .. 8m + 7) as one byte, channel e at bit e:
+// the multiply gathers the bits at 0, 8, 16, 24 into bits 21 .. 24 (no two partial products meet).
+__device__ __forceinline__ uint32_t bit4_byte(uint32_t c0, uint32_t c1) {
+    const uint32_t a = (c0 >> 4) & 0x01010101u, b = (c1 >> 4) & 0x01010101u;
+    return (((a * 0x00204081u) >> 21) & 0xFu) | ((((b * 0x00204081u) >> 21) & 0xFu) << 4);
+}
+// Bits 4-5 of 4 code bytes (one word, channels 4m .. 4m + 3) as one byte, channel e at bits 2e.
+__device__ __forceinline__ uint32_t bits45_byte(uint32_t c) {
+    const uint32_t a = (c >> 4) & 0x03030303u;
+    return ((a * 0x00041041u) >> 18) & 0xFFu;
 }
 
 // Two words of code bytes (8 channels, values < 16) as one word of nibbles, the even channel
@@ -435,28 +476,62 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
             reinterpret_cast<uint16_t*>(rec + 64LL * D)[t * (D / 128) + tl.b] = n16;
             flag_nonfinite(L, p.pool, h2f(n16));
         } else {
-            uint16_t d16[4];
+            uint16_t d16[4], m16[4] = {0, 0, 0, 0};
             uint32_t C[32];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t c[8];
-                d16[j] = (fmt == KVQ_Q8_0) ? encode_q32<127>(y, 32 * j, c) : encode_q32<7>(y, 32 * j, c);
+                switch (fmt) {
+                    case KVQ_Q8_0: d16[j] = encode_q32<127>(y, 32 * j, c); break;
+                    case KVQ_Q4_0: d16[j] = encode_q32<7>(y, 32 * j, c); break;
+                    case KVQ_Q5_0: d16[j] = encode_q32<15>(y, 32 * j, c); break;
+                    case KVQ_Q6_0: d16[j] = encode_q32<31>(y, 32 * j, c); break;
+                    case KVQ_Q4_1: d16[j] = encode_qmin<15>(y, 32 * j, c, m16[j]); break;
+                    default: d16[j] = encode_qmin<31>(y, 32 * j, c, m16[j]); break;
+                }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) C[8 * j + k] = c[k];
             }
+            const int qbits = qblock_bits(fmt);
             int64_t sc_off;
             if (fmt == KVQ_Q8_0) {
                 store_bytes(rec, D, tl.b, tl.w, C);
                 sc_off = 128LL * D;
             } else {
+                // Q4_0: K token-major, V channel-major; the other block formats token-major for
+                // both, the low nibbles then the high plane of the 5- and 6-bit codes
                 uint32_t P[16];
 #pragma unroll
-                for (int m = 0; m < 16; ++m) P[m] = nibbles_of(C[2 * m], C[2 * m + 1]);
-                store_nibbles(rec, D, tl.b, tl.w, P);
-                sc_off = 64LL * D;
+                for (int m = 0; m < 16; ++m) P[m] = nibbles_of(C[2 * m] & 0x0F0F0F0Fu, C[2 * m + 1] & 0x0F0F0F0Fu);
+                store_nibbles(rec, D, tl.b, qbits ? 0 : tl.w, P);
+                if (qbits == 5) {
+                    uint32_t hb[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        hb[q] = bit4_byte(C[8 * q], C[8 * q + 1]) | (bit4_byte(C[8 * q + 2], C[8 * q + 3]) << 8) |
+                                (bit4_byte(C[8 * q + 4], C[8 * q + 5]) << 16) | (bit4_byte(C[8 * q + 6], C[8 * q + 7]) << 24);
+                    *reinterpret_cast<uint4*>(rec + 64LL * D + (int64_t)t * (D / 8) + 16 * tl.b) =
+                        make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                } else if (qbits == 6) {
+                    uint32_t hb[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        hb[q] = bits45_byte(C[4 * q]) | (bits45_byte(C[4 * q + 1]) << 8) | (bits45_byte(C[4 * q + 2]) << 16) |
+                                (bits45_byte(C[4 * q + 3]) << 24);
+                    uint4* dst = reinterpret_cast<uint4*>(rec + 64LL * D + (int64_t)t * (D / 4) + 32 * tl.b);
+                    dst[0] = make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                    dst[1] = make_uint4(hb[4], hb[5], hb[6], hb[7]);
+                }
+                sc_off = record_code_bytes(fmt, D);
             }
             *reinterpret_cast<uint2*>(rec + sc_off + 2LL * (t * (D / 32) + 4 * tl.b)) =
                 make_uint2(d16[0] | ((uint32_t)d16[1] << 16), d16[2] | ((uint32_t)d16[3] << 16));
+            if (qbits && qblock_sym_levels(fmt) == 0) {
+                *reinterpret_cast<uint2*>(rec + sc_off + 8LL * D + 2LL * (t * (D / 32) + 4 * tl.b)) =
+                    make_uint2(m16[0] | ((uint32_t)m16[1] << 16), m16[2] | ((uint32_t)m16[3] << 16));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) flag_nonfinite(L, p.pool, h2f(m16[j]));
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) flag_nonfinite(L, p.pool, h2f(d16[j]));
         }

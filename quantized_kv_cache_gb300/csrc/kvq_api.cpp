@@ -35,7 +35,7 @@ struct kvq_cache {
 namespace kvq {
 
 static bool is_body(int f) {
-    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || kvarn_bits(f) != 0;
+    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || qblock_bits(f) != 0 || kvarn_bits(f) != 0;
 }
 
 bool make_layout(const kvq_config& c, Layout* out) {
@@ -197,10 +197,10 @@ kvq_status kv_auto_tier(const kvq_config* cfg, int64_t tokens, uint64_t budget_b
                         int32_t* v_fmt, uint64_t* cost_bytes) {
     if (!cfg || !k_fmt || !v_fmt || !cost_bytes || tokens < 0) return KVQ_EINVAL;
     if (cfg->n_layers <= 0 || cfg->n_kv_heads <= 0 || cfg->head_dim <= 0) return KVQ_EINVAL;
-    // bytes per 32 values of each rung's K and V format: f16 64, q8_0 34, q4_0 18
+    // bytes per 32 values of each rung's K and V format: f16 64, q8_0 34, q5_1 24, q4_0 18
     struct Rung { int32_t k, v; uint64_t k32, v32; };
     static const Rung ladder[] = {{KVQ_F16, KVQ_F16, 64, 64}, {KVQ_Q8_0, KVQ_Q8_0, 34, 34},
-                                  {KVQ_Q8_0, KVQ_Q4_0, 34, 18}};
+                                  {KVQ_Q8_0, KVQ_Q4_0, 34, 18}, {KVQ_Q5_1, KVQ_Q4_0, 24, 18}};
     const uint64_t cells = (uint64_t)tokens * (uint64_t)cfg->n_layers * (uint64_t)cfg->n_kv_heads *
                            (uint64_t)cfg->head_dim;   // values per K (and per V)
     const int n = (int)(sizeof(ladder) / sizeof(ladder[0]));

@@ -70,12 +70,32 @@ KVQ_HD int kvarn_code(const uint8_t* tile, int bits, int len, int row, int i) {
     return code;
 }
 
+// The 32-value block formats beyond Q8_0 / Q4_0: code bits (0 for any other format), the
+// symmetric level count L (_0: codes x/d + L + 1) or 0 for the min-offset formats (_1: codes
+// (x - m)/d in 0..2^bits - 1). Their records are token-major for K and V: the low nibble plane
+// [128][D/2], the high plane (5-bit codes: one bit [128][D/8]; 6-bit: two bits [128][D/4]),
+// d [128][D/32] fp16, then for the _1 formats m [128][D/32] fp16.
+KVQ_HD int qblock_bits(int fmt) {
+    switch (fmt) {
+        case KVQ_Q5_0: return 5;
+        case KVQ_Q6_0: return 6;
+        case KVQ_Q4_1: return 4;
+        case KVQ_Q5_1: return 5;
+        default: return 0;
+    }
+}
+KVQ_HD int qblock_sym_levels(int fmt) { return fmt == KVQ_Q5_0 ? 15 : (fmt == KVQ_Q6_0 ? 31 : 0); }
+
 // Record bytes of one 128-position group of one KV head (K or V), per format.
 KVQ_HD int64_t record_bytes(int fmt, int D) {
     switch (fmt) {
         case KVQ_TBQ4: return 66LL * D;                       // 64 B idx + 2 B norm per 128
         case KVQ_Q8_0: return 136LL * D;                      // 34 B per 32, 128 tokens
         case KVQ_Q4_0: return 72LL * D;                       // 18 B per 32
+        case KVQ_Q5_0: return 88LL * D;                       // 22 B per 32
+        case KVQ_Q6_0: return 104LL * D;                      // 26 B per 32
+        case KVQ_Q4_1: return 80LL * D;                       // 20 B per 32
+        case KVQ_Q5_1: return 96LL * D;                       // 24 B per 32
         case KVQ_KVARN2: case KVQ_KVARN3: case KVQ_KVARN4: case KVQ_KVARN5: case KVQ_KVARN6: case KVQ_KVARN8:
             return (int64_t)(D / 256) * (4096 * kvarn_bits(fmt) + 1152);
         default: return -1;
@@ -88,6 +108,9 @@ KVQ_HD int64_t record_code_bytes(int fmt, int D) {
         case KVQ_TBQ4: return 64LL * D;
         case KVQ_Q8_0: return 128LL * D;
         case KVQ_Q4_0: return 64LL * D;
+        case KVQ_Q5_0: case KVQ_Q5_1: return 80LL * D;       // nibbles + one-bit plane
+        case KVQ_Q6_0: return 96LL * D;                       // nibbles + two-bit plane
+        case KVQ_Q4_1: return 64LL * D;
         default: return -1;
     }
 }

@@ -65,6 +65,14 @@ FAMILIES = {
                            contexts=[650, 1300], keep=256, steps=2, factor=16.0, n_out=8),
     "kvarn86_f16": Family("kvarn86_f16", 256, 1, 6, "kvarn8", "kvarn6", "f16", "f16", T=128, R=768,
                           contexts=[900, 1250], keep=128, steps=2, factor=16.0, n_out=8),
+    # the other 32-value block formats (generic decode path): the tier ladder's floor rung
+    # q5_1 K / q4_0 V on a BF16 journal, q6_0 K / q4_1 V and q5_0 K / q5_0 V on F16 journals
+    "q51q40_bf16": Family("q51q40_bf16", 128, 2, 10, "q5_1", "q4_0", "bf16", "bf16", T=256, R=768,
+                          contexts=[900, 1333], keep=256, steps=2, factor=20.0),
+    "q60q41_f16": Family("q60q41_f16", 128, 1, 4, "q6_0", "q4_1", "f16", "f16", T=128, R=768,
+                         contexts=[800, 1201], keep=128, steps=2, factor=12.0),
+    "q50q50_f16": Family("q50q50_f16", 256, 1, 2, "q5_0", "q5_0", "f16", "f16", T=64, R=512,
+                         contexts=[700], keep=64, steps=2, factor=16.0, n_out=8),
 }
 
 

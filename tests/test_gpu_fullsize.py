@@ -41,6 +41,7 @@ SAMPLES = {
     "widehead_kvarn55": [(2, 1), (7, 0)],
     "longctx_tbq4": [(0, 2), (3, 0)],
     "hybrid27b_kvarn32_200k": [(0, 2)],
+    "fa14b_q51q40": [(0, 3)],
 }
 
 
