@@ -69,9 +69,11 @@ def peaks():
 # profiles/decode_attn_launches.md gives the command and the per-kernel split.
 MEASURED_TRAFFIC = {
     "hybrid27b_kvarn44": 42.83e6,
-    "fa14b_q8q4": 221.25e6,
-    "longctx_tbq4": 749.88e6,
-    "widehead_kvarn55": 190.68e6,
+    "fa14b_q8q4": 221.90e6,
+    "longctx_tbq4": 749.80e6,
+    "widehead_kvarn55": 190.77e6,
+    "hybrid27b_kvarn32_200k": 156.86e6,
+    "fa14b_q51q40": 180.60e6,
 }
 
 
@@ -516,9 +518,11 @@ def measure_prefill(w, ds, seq_ids, stream, reps=3):
     for _ in range(reps):
         reset()
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("prefill")
         e0.record()
         groups = run()
         e1.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         times.append(e0.elapsed_time(e1) / 1e3)
     status = _lib.kv_get_status(cache.h)
