@@ -29,7 +29,7 @@ GROUP = 128
 
 
 def rotation_of(fmt):
-    if fmt == "tbq4":
+    if fmt in ("tbq4", "turbo3", "tq5_0"):
         return TBQ128
     if fmt.startswith("kvarn"):
         return HAD256
@@ -41,7 +41,7 @@ def rotation_of(fmt):
 @dataclass(frozen=True)
 class HeadConfig:
     head_dim: int
-    k_body: str            # tbq4 | q8_0 | q4_0 | q5_0 | q6_0 | q4_1 | q5_1 | kvarn2..kvarn8
+    k_body: str            # tbq4 | turbo3 | tq5_0 | q8_0 | q4_0 | q5_0 | q6_0 | q4_1 | q5_1 | kvarn2..kvarn8
     v_body: str
     journal: str           # tq6_0 | f16 | bf16
     tail_fmt: str          # f16 | bf16 (exact tail store; with an exact journal, its format)
@@ -79,6 +79,12 @@ def encode_body(X, fmt):
     if fmt == "q4_0":
         d, c = codecs.q4_encode(X)
         return {"scale": d, "code": c.reshape(X.shape)}
+    if fmt == "turbo3":
+        n16, idx = codecs.turbo3_encode(X)
+        return {"scale": n16, "code": idx.reshape(X.shape)}
+    if fmt == "tq5_0":
+        d, c = codecs.tq5_encode(X)
+        return {"scale": d, "code": c.reshape(X.shape)}
     if fmt in QSYM:
         d, c = codecs.qsym_encode(X, QSYM[fmt])
         return {"scale": d, "code": c.reshape(X.shape)}
@@ -111,6 +117,12 @@ def decode_body(rec, fmt):
     if fmt == "q4_0":
         D = rec["code"].shape[-1]
         return codecs.q4_decode(rec["scale"], rec["code"].reshape(128, D // 32, 32))
+    if fmt == "turbo3":
+        D = rec["code"].shape[-1]
+        return codecs.turbo3_decode(rec["scale"], rec["code"].reshape(128, D // 128, 128))
+    if fmt == "tq5_0":
+        D = rec["code"].shape[-1]
+        return codecs.tq5_decode(rec["scale"], rec["code"].reshape(128, D // 128, 128))
     if fmt in QSYM:
         D = rec["code"].shape[-1]
         return codecs.qsym_decode(rec["scale"], rec["code"].reshape(128, D // 32, 32), QSYM[fmt])
@@ -132,6 +144,16 @@ def pack_body(rec, fmt, role):
             parts.append(kvarn.scale_block(rec["S"][h], rec["Z"][h], rec["C"][h]).view(np.uint8).reshape(-1))
         return np.concatenate(parts)
     code = rec["code"]                                   # [128 tokens, D]
+    if fmt in ("turbo3", "tq5_0"):
+        # token-major for K and V alike: turbo3 a 2-bit plane [128][D/4] then a one-bit plane
+        # [128][D/8] of the 3-bit indices; tq5_0 the nibble plane [128][D/2] then a one-bit plane
+        # [128][D/8]; then the fp16 norms (turbo3) or scales (tq5_0) [128][D/128]
+        if fmt == "turbo3":
+            parts = [codecs.pack_crumbs(code & 3).reshape(-1), codecs.pack_bitplane((code >> 2) & 1).reshape(-1)]
+        else:
+            parts = [codecs.pack_nibbles(code & 15).reshape(-1), codecs.pack_bitplane((code >> 4) & 1).reshape(-1)]
+        parts.append(np.ascontiguousarray(rec["scale"]).astype(np.float16).view(np.uint8).reshape(-1))
+        return np.concatenate(parts)
     if fmt in CODE_BITS:
         # token-major for K and V alike: the low nibble plane [128][D/2], the high plane (5-bit:
         # one bit per code [128][D/8]; 6-bit: two bits [128][D/4]), d [128][D/32], then for the

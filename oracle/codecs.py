@@ -16,6 +16,7 @@ Sources:
 import numpy as np
 
 from .fp import f32, to_f16, tree_sum
+from . import tables
 from .tables import tbq4_tables
 
 
@@ -81,6 +82,47 @@ def tbq4_encode(y):
     for k in range(15):
         idx += (u > bnd[k]).astype(np.uint8)
     return n16, idx
+
+
+def turbo3_encode(y):
+    """The pages' turbo3 (SJ-KVaRN §2.1, §7.2: a rotated 3-bit format, 50 B per 128 values),
+    read as TBQ4 with 8 levels: y[..., 128k] (rotated) -> (n16 fp16 [..., k], idx [..., k, 128]
+    in 0..7), idx = #{k : u > beta_k} with u = y / fp32(n16)."""
+    cent, bnd = tables.tbq3_tables()
+    yb = _blocks(y, 128)
+    ss = tree_sum(yb * yb, axis=-1)
+    n16 = to_f16(np.sqrt(ss))
+    n32 = n16.astype(np.float32)
+    zero = n32 == 0
+    inv = np.where(zero, np.float32(0), np.float32(1.0) / np.where(zero, np.float32(1), n32))
+    u = yb * inv[..., None].astype(np.float32)
+    idx = np.zeros(u.shape, dtype=np.uint8)
+    for k in range(7):
+        idx += (u > bnd[k]).astype(np.uint8)
+    return n16, idx
+
+
+def turbo3_decode(n16, idx):
+    cent, _ = tables.tbq3_tables()
+    v = cent[idx] * n16.astype(np.float32)[..., None]
+    return v.reshape(idx.shape[:-2] + (idx.shape[-2] * 128,))
+
+
+def tq5_encode(y):
+    """The pages' tq5_0 (a rotated 5-bit format, 82 B per 128 values), read like tq6_0 with 15
+    levels a side: y[..., 128k] -> (d fp16 [..., k], code [..., k, 128] in 1..31; 16 is zero)."""
+    yb = _blocks(y, 128)
+    d = to_f16(np.max(np.abs(yb), axis=-1) / np.float32(15.0))
+    d32 = d.astype(np.float32)
+    zero = d32 == 0
+    inv = np.where(zero, np.float32(0), np.float32(1.0) / np.where(zero, np.float32(1), d32))
+    q = np.clip(np.rint(yb * inv[..., None].astype(np.float32)), -15, 15)
+    return d, (q + 16).astype(np.uint8)
+
+
+def tq5_decode(d, code):
+    v = (code.astype(np.float32) - np.float32(16)) * d.astype(np.float32)[..., None]
+    return v.reshape(code.shape[:-2] + (code.shape[-2] * 128,))
 
 
 def tbq4_decode(n16, idx):

@@ -1,4 +1,5 @@
-"""Format constants of the oracle: TBQ4 sign vectors and Lloyd-Max centroid table.
+"""Format constants of the oracle: TBQ sign vectors and Lloyd-Max centroid tables (16 levels
+for TBQ4, 8 for turbo3).
 
 KV cache math, "How a 4-bit cache gets away with it: rotate first": each 128-value block
 is sign-flipped, Walsh-Hadamard transformed, sign-flipped again, and quantized with 16
@@ -90,4 +91,15 @@ def tbq4_tables():
     cent = np.array([sigma * v for v in C], dtype=np.float64).astype(np.float32)
     bnd = np.array([sigma * (C[k - 1] + C[k]) / 2.0 for k in range(1, 16)],
                    dtype=np.float64).astype(np.float32)
+    return cent, bnd
+
+
+@lru_cache(maxsize=None)
+def tbq3_tables():
+    """turbo3's (centroids[8], boundaries[7]) as float32, the same construction with 8 levels
+    (the pages' turbo3 is the 3-bit relative of turbo4 = TBQ4: 50 B per 128 values)."""
+    sigma = 1.0 / math.sqrt(128.0)
+    C = lloyd_max_gaussian(8)
+    cent = np.array([sigma * v for v in C], dtype=np.float64).astype(np.float32)
+    bnd = np.array([sigma * (C[k - 1] + C[k]) / 2.0 for k in range(1, 8)], dtype=np.float64).astype(np.float32)
     return cent, bnd

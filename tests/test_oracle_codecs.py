@@ -233,3 +233,63 @@ def test_crumb_packing_exhaustive():
     p = codecs.pack_crumbs(v)
     assert np.array_equal(p[:, 0], v[:, 0] | (v[:, 1] << 2) | (v[:, 2] << 4) | (v[:, 3] << 6))
     assert np.array_equal(codecs.unpack_crumbs(p), v)
+
+
+# ----------------------------------------------------------------------------- turbo3 / tq5_0
+def test_eight_level_lloyd_max_table():
+    """turbo3's table: the 8-level Lloyd-Max quantizer of N(0,1) (Max 1960, Table I: levels
+    +-0.2451, +-0.7560, +-1.3440, +-2.1520, distortion 0.03454), scaled by 1/sqrt(128)."""
+    cent, bnd = tables.tbq3_tables()
+    C = np.array(tables.lloyd_max_gaussian(8))
+    assert np.allclose(C[4:], [0.2451, 0.7560, 1.3440, 2.1520], atol=1e-4)
+    assert np.array_equal(cent[:4], -cent[:3:-1]) and bnd[3] == 0
+    # each level is the conditional mean of its cell, boundaries the midpoints (fp64)
+    b = [0.0] + [(C[4 + k - 1] + C[4 + k]) / 2 for k in range(1, 4)] + [math.inf]
+    phi = lambda x: 0.0 if x == math.inf else math.exp(-x * x / 2) / math.sqrt(2 * math.pi)
+    tail = lambda x: 0.0 if x == math.inf else 0.5 * math.erfc(x / math.sqrt(2))
+    for k in range(4):
+        assert abs((phi(b[k]) - phi(b[k + 1])) / (tail(b[k]) - tail(b[k + 1])) - C[4 + k]) < 1e-12
+    # distortion E[(x - Q(x))^2] for N(0,1): 1 - sum_k P_k C_k^2 for the optimal quantizer
+    mse = 1 - 2 * sum((tail(b[k]) - tail(b[k + 1])) * C[4 + k] ** 2 for k in range(4))
+    assert abs(mse - 0.03454) < 1e-4
+
+
+def test_turbo3_nearest_centroid_and_distortion():
+    cent, bnd = tables.tbq3_tables()
+    y = RNG.standard_normal((2000, 128)).astype(np.float32)
+    n16, idx = codecs.turbo3_encode(y)
+    assert idx.max() <= 7
+    u = y * (np.float32(1) / n16.astype(np.float32))
+    nearest = np.argmin(np.abs(u[..., None].astype(np.float64) - cent.astype(np.float64)), axis=-1)
+    assert np.mean(nearest.reshape(idx.shape) == idx) > 0.99999
+    rel_mse = np.mean((y - codecs.turbo3_decode(n16, idx)) ** 2) / np.mean(y ** 2)
+    assert 0.031 < rel_mse < 0.038
+    # a zero block: norm 0, u = 0 exceeds the three negative boundaries only (the boundary at 0
+    # is a tie, which goes to the lower level): index 3
+    z16, zi = codecs.turbo3_encode(np.zeros(128, np.float32))
+    assert z16[0] == 0 and np.all(zi == 3)
+
+
+def test_tq5_error_bound_zero_and_grid():
+    x = (RNG.standard_normal((300, 128)) * RNG.uniform(0.01, 40, (300, 1))).astype(np.float32)
+    d, code = codecs.tq5_encode(x)
+    xr = codecs.tq5_decode(d, code).reshape(x.shape)
+    d32 = d.astype(np.float32)
+    assert code.min() >= 1 and code.max() <= 31
+    assert np.all(np.abs(xr - x) <= 0.5 * d32 + 15 * d32 * 2 ** -10)
+    d2, c2 = codecs.tq5_encode(xr)
+    assert np.array_equal(codecs.tq5_decode(d2, c2), xr.reshape(-1))
+    dz, cz = codecs.tq5_encode(np.zeros(128, np.float32))
+    assert dz[0] == 0 and np.all(cz == 16)
+
+
+def test_rotated_comparator_sizes_are_the_pages():
+    """turbo3 50 B and tq5_0 82 B per 128 values (KV cache math table; SJ-KVaRN §4.1)."""
+    from oracle.cache import encode_body, pack_body
+    from oracle import sizes
+    X = RNG.standard_normal((128, 256)).astype(np.float32)
+    for fmt, b in (("turbo3", 50), ("tq5_0", 82)):
+        rec = encode_body(X, fmt)
+        for role in "KV":
+            assert pack_body(rec, fmt, role).size == 256 * b
+        assert sizes.record_bytes(fmt, 256) == 256 * b
