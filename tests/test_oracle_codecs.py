@@ -278,7 +278,7 @@ def test_tq5_error_bound_zero_and_grid():
     assert code.min() >= 1 and code.max() <= 31
     assert np.all(np.abs(xr - x) <= 0.5 * d32 + 15 * d32 * 2 ** -10)
     d2, c2 = codecs.tq5_encode(xr)
-    assert np.array_equal(codecs.tq5_decode(d2, c2), xr.reshape(-1))
+    assert np.array_equal(codecs.tq5_decode(d2, c2), xr)
     dz, cz = codecs.tq5_encode(np.zeros(128, np.float32))
     assert dz[0] == 0 and np.all(cz == 16)
 
