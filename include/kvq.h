@@ -43,7 +43,8 @@ typedef enum {
     KVQ_EDEVICE = 5        /* device status word reports a problem (see kv_get_status) */
 } kvq_status;
 
-/* Stored formats. Body formats: TBQ4, Q8_0, Q4_0, Q5_0, Q6_0, Q4_1, Q5_1, KVARN2..KVARN8.
+/* Stored formats. Body formats: TBQ4, TURBO3, TQ5_0, Q8_0, Q4_0, Q5_0, Q6_0, Q4_1, Q5_1,
+ * KVARN2..KVARN8.
  * Journal: TQ6_0, F16, BF16.
  * Exact tail: F16, BF16. K and V bodies may differ (e.g. KVARN3 keys, KVARN2 values). */
 typedef enum {
@@ -65,7 +66,12 @@ typedef enum {
     KVQ_Q5_0 = 12,   /* L = 15: 22 B per 32 values */
     KVQ_Q6_0 = 13,   /* L = 31: 26 B per 32 values */
     KVQ_Q4_1 = 14,   /* Q = 15: 20 B per 32 values */
-    KVQ_Q5_1 = 15    /* Q = 31: 24 B per 32 values */
+    KVQ_Q5_1 = 15,   /* Q = 31: 24 B per 32 values */
+    /* rotated comparators of the pages (SJ-KVaRN §2.1, §4.1; KV cache math), TBQ4's rotation:
+     * turbo3 = TBQ with the 8-level Lloyd-Max table (fp16 norm + 3-bit indices, 50 B per 128);
+     * tq5_0 = symmetric 5-bit, d = fp16(max|y| / 15) (82 B per 128). Records token-major. */
+    KVQ_TURBO3 = 16,
+    KVQ_TQ5_0 = 17
 } kvq_fmt;
 
 typedef struct {
@@ -269,6 +275,10 @@ kvq_status kv_region_ptr(const kvq_cache* cache, int layer, int seq, int head, i
  * centroids and boundaries (fp32, Lloyd-Max for N(0, 1/128)) and the four splitmix64 sign
  * words. Host pointers; any may be NULL. */
 kvq_status kv_format_tables(float centroids[16], float boundaries[15], uint64_t sign_words[4]);
+
+/* kv_format_tables_turbo3 — turbo3's 8 centroids and 7 boundaries (fp32, the same Lloyd-Max
+ * construction with 8 levels) as this library derived them. Host pointers; either may be NULL. */
+kvq_status kv_format_tables_turbo3(float centroids[8], float boundaries[7]);
 
 /* kv_status_string — static description of a status code. */
 const char* kv_status_string(kvq_status s);

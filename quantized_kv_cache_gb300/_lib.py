@@ -12,10 +12,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libkvq.so")
 
 # kvq_fmt
-F16, BF16, TQ6_0, TBQ4, Q8_0, Q4_0, KVARN4, KVARN5, KVARN2, KVARN3, KVARN6, KVARN8, Q5_0, Q6_0, Q4_1, Q5_1 = range(16)
+(F16, BF16, TQ6_0, TBQ4, Q8_0, Q4_0, KVARN4, KVARN5, KVARN2, KVARN3, KVARN6, KVARN8, Q5_0, Q6_0, Q4_1, Q5_1,
+ TURBO3, TQ5_0) = range(18)
 FMT_NAMES = {"f16": F16, "bf16": BF16, "tq6_0": TQ6_0, "tbq4": TBQ4, "q8_0": Q8_0, "q4_0": Q4_0,
              "kvarn4": KVARN4, "kvarn5": KVARN5, "kvarn2": KVARN2, "kvarn3": KVARN3, "kvarn6": KVARN6,
-             "kvarn8": KVARN8, "q5_0": Q5_0, "q6_0": Q6_0, "q4_1": Q4_1, "q5_1": Q5_1}
+             "kvarn8": KVARN8, "q5_0": Q5_0, "q6_0": Q6_0, "q4_1": Q4_1, "q5_1": Q5_1, "turbo3": TURBO3,
+             "tq5_0": TQ5_0}
 # regions
 REGION_SINK, REGION_JOURNAL, REGION_JOURNAL_SCALE, REGION_TAIL, REGION_BODY = range(5)
 ENOSPC = 2
@@ -71,6 +73,7 @@ _SIGS = {
                       ctypes.POINTER(P), ctypes.POINTER(SZ)],
     "kv_format_tables": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                          ctypes.POINTER(ctypes.c_uint64)],
+    "kv_format_tables_turbo3": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
     "kv_decode_step": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
                        P, SZ, ctypes.POINTER(P), ctypes.POINTER(I64), P],
     "kv_decode_attn_noalloc": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P],
@@ -251,6 +254,13 @@ def kv_format_tables():
     s = (ctypes.c_uint64 * 4)()
     _check("kv_format_tables", load().kv_format_tables(c, b, s))
     return list(c), list(b), list(s)
+
+
+def kv_format_tables_turbo3():
+    c = (ctypes.c_float * 8)()
+    b = (ctypes.c_float * 7)()
+    _check("kv_format_tables_turbo3", load().kv_format_tables_turbo3(c, b))
+    return list(c), list(b)
 
 
 def kvq_synth_fill(out_ptr, n_pos, n_heads, head_dim, head_keys, pos0, factor_ptr, table_ptr, stream=0):

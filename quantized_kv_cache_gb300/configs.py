@@ -29,6 +29,9 @@ A sixth workload measures the KVarN widths beyond 4 and 5 (SJ-KVaRN §7, the 3/2
   2-bit V, tq6_0 ring, the same seal policy; 64 decode steps.
 And a seventh the block formats beyond Q8_0 / Q4_0 (the auto tier's floor rung, HAL #582 §5):
 - fa14b_q51q40: the fa14b_q8q4 shape and policy with q5_1 K and q4_0 V.
+An eighth the rotated comparator the pages measure SJ-KVaRN against (SJ-KVaRN §4.1):
+- hybrid27b_tq50tbq4_110k: the hybrid27b shape and policy at 110,592 positions with tq5_0 K and
+  TBQ4 (turbo4) V.
 """
 
 from dataclasses import dataclass, field
@@ -104,6 +107,9 @@ WORKLOADS = {
     "fa14b_q51q40": Workload("fa14b_q51q40", 48, 8, 128, 40, "q5_1", "q4_0", "bf16", "bf16", tail=1024, ring=5248,
                              contexts=[131072], steps=64, seed=6, n_out=4, out_factor=20.0, keep=1024,
                              seal_trigger=0),
+    "hybrid27b_tq50tbq4_110k": Workload("hybrid27b_tq50tbq4_110k", 16, 4, 256, 24, "tq5_0", "tbq4", "tq6_0",
+                                        "f16", tail=1024, ring=8448, contexts=[110592], steps=64, seed=7, n_out=8,
+                                        out_factor=16.0, keep=4096, seal_trigger=8192),
     "hybrid27b_kvarn32_200k": Workload("hybrid27b_kvarn32_200k", 16, 4, 256, 24, "kvarn3", "kvarn2", "tq6_0",
                                        "f16", tail=1024, ring=8448, contexts=[204800], steps=64, seed=5, n_out=8,
                                        out_factor=16.0, keep=4096, seal_trigger=8192),
@@ -113,7 +119,8 @@ WORKLOADS = {
 def record_bytes(fmt, head_dim):
     """Bytes of one 128-position body record of one KV head (K or V) in the given format."""
     return {"tbq4": 66 * head_dim, "q8_0": 136 * head_dim, "q4_0": 72 * head_dim, "q5_0": 88 * head_dim,
-            "q6_0": 104 * head_dim, "q4_1": 80 * head_dim, "q5_1": 96 * head_dim,
+            "q6_0": 104 * head_dim, "q4_1": 80 * head_dim, "q5_1": 96 * head_dim, "turbo3": 50 * head_dim,
+            "tq5_0": 82 * head_dim,
             **{f"kvarn{b}": (head_dim // 256) * (4096 * b + 1152) for b in (2, 3, 4, 5, 6, 8)}}[fmt]
 
 

@@ -252,6 +252,18 @@ __device__ __forceinline__ float qblock_value(const uint8_t* rec, int fmt, int D
     return (float)code * d + h2f(sc[4 * D + t * (D / 32) + (c >> 5)]);
 }
 
+// Value of channel c of row t (token-major) of a turbo3 or tq5_0 record (rotated domain).
+__device__ __forceinline__ float rot_block_value(const uint8_t* rec, int fmt, int D, int t, int c) {
+    if (fmt == KVQ_TURBO3) {
+        const int code = ((rec[t * (D / 4) + (c >> 2)] >> (2 * (c & 3))) & 3) |
+                         (((rec[32 * D + t * (D / 8) + (c >> 3)] >> (c & 7)) & 1) << 2);
+        return c_tab.cent3[code] * h2f(reinterpret_cast<const uint16_t*>(rec + 48 * D)[t * (D / 128) + (c >> 7)]);
+    }
+    const int code = ((rec[t * (D / 2) + (c >> 1)] >> ((c & 1) * 4)) & 15) |
+                     (((rec[64 * D + t * (D / 8) + (c >> 3)] >> (c & 7)) & 1) << 4);
+    return (float)(code - 16) * h2f(reinterpret_cast<const uint16_t*>(rec + 80 * D)[t * (D / 128) + (c >> 7)]);
+}
+
 // Body K records (token-major) of one tile: positions [tstart, tstart + TILE) of group g.
 template <int D, int TILE, int LD>
 __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
@@ -266,6 +278,9 @@ __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int
         if (qblock_bits(fmt)) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = qblock_value(rec, fmt, D, t, c0 + k);
+        } else if (fmt == KVQ_TURBO3 || fmt == KVQ_TQ5_0) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = rot_block_value(rec, fmt, D, t, c0 + k);
         } else if (fmt == KVQ_TBQ4) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));
             const float n = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 128) + (c0 >> 7)]);
@@ -311,6 +326,9 @@ __device__ void fill_body_v(const Layout& L, const void* pool, int64_t unit, int
         if (qblock_bits(fmt)) {   // token-major V
 #pragma unroll
             for (int k = 0; k < 8; ++k) v[k] = qblock_value(rec, fmt, D, t0 + k, c);
+        } else if (fmt == KVQ_TURBO3 || fmt == KVQ_TQ5_0) {   // token-major V
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = rot_block_value(rec, fmt, D, t0 + k, c);
         } else if (fmt == KVQ_TBQ4) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + c * 64 + (t0 >> 1));
             const uint16_t* nr = reinterpret_cast<const uint16_t*>(rec + 64 * D);
@@ -380,10 +398,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Layout L, AttnPa
     __half* Vs_lo = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(Ks_lo) + C::K_BYTES);
 
     const Item it = decode_item(p, blockIdx.x);
-    // body tiles of the 32-value block formats beyond Q8_0 / Q4_0 are held as fp16 values plus
+    // body tiles of the 32-value block formats beyond Q8_0 / Q4_0 (and of turbo3, tq5_0) are held as fp16 values plus
     // fp16 remainders, and both go through the mma: an fp16 value of code x d (+ m) alone is too
     // coarse for the decode tolerance where the softmax is sharp
-    const bool lo_now = it.kind == RK_BODY && (qblock_bits(L.fmt[0]) || qblock_bits(L.fmt[1]));
+    auto split_fmt = [](int f) { return qblock_bits(f) != 0 || f == KVQ_TURBO3 || f == KVQ_TQ5_0; };
+    const bool lo_now = it.kind == RK_BODY && (split_fmt(L.fmt[0]) || split_fmt(L.fmt[1]));
     const int G = L.G;
     const int64_t unit = L.unit(p.layer, it.slot, it.h);
     const bool rotated = (it.kind == RK_BODY || it.kind == RK_RING) && L.rot != ROT_NONE;

@@ -70,6 +70,14 @@ __global__ void dequant_kernel(Layout L, const void* pool, int layer, int slot, 
                 const int code = (w == 0) ? kvarn_code(tr, bits, 256, t, j) : kvarn_code(tr, bits, 128, j, t);
                 const uint16_t* sb = (const uint16_t*)(tr + 4096 * bits);
                 x = fmul(fadd(fmul((float)code, h2f(sb[t])), h2f(sb[128 + t])), h2f(sb[256 + j]));
+            } else if (fmt == KVQ_TURBO3) {   // token-major for K and V
+                const int code = ((rec[t * (D / 4) + (ch >> 2)] >> (2 * (ch & 3))) & 3) |
+                                 (((rec[32 * D + t * (D / 8) + (ch >> 3)] >> (ch & 7)) & 1) << 2);
+                x = fmul(c_tab.cent3[code], h2f(((const uint16_t*)(rec + 48 * D))[t * (D / 128) + (ch >> 7)]));
+            } else if (fmt == KVQ_TQ5_0) {     // token-major for K and V
+                const int code = ((rec[t * (D / 2) + (ch >> 1)] >> ((ch & 1) * 4)) & 15) |
+                                 (((rec[64 * D + t * (D / 8) + (ch >> 3)] >> (ch & 7)) & 1) << 4);
+                x = fmul((float)(code - 16), h2f(((const uint16_t*)(rec + 80 * D))[t * (D / 128) + (ch >> 7)]));
             } else if (qblock_bits(fmt)) {   // token-major for K and V
                 const int bits = qblock_bits(fmt);
                 int code = (rec[t * (D / 2) + (ch >> 1)] >> ((ch & 1) * 4)) & 15;

@@ -380,10 +380,12 @@ __device__ __forceinline__ void store_bytes(uint8_t* rec, int D, int b, int w, c
     }
 }
 
-// Decision table of the TBQ4 index: bucket k = the floats whose top 11 bits are k. base =
-// boundaries below the bucket's smallest value, thr = the boundary inside it (+inf if none);
-// buckets of infinities and NaNs give 0 (a NaN exceeds no boundary).
-__device__ void build_qtab(float2* qt) {
+// Decision table of a TBQ index (TBQ4: the 15 boundaries; turbo3: 7): bucket k = the floats
+// whose top 11 bits are k. base = boundaries below the bucket's smallest value, thr = the
+// boundary inside it (+inf if none); buckets of infinities and NaNs give 0 (a NaN exceeds no
+// boundary). Exact where no bucket holds two boundaries (consecutive boundaries differ by a
+// ratio above 1.25: TBQ4 >= 1.28, turbo3 >= 1.66).
+__device__ void build_qtab(float2* qt, const float* bnd, int nb) {
     for (int k = threadIdx.x; k < kBuckets; k += blockDim.x) {
         const uint32_t lo = (uint32_t)k << 21, hi = lo | 0x1FFFFFu;
         float thr = __uint_as_float(0x7F800000u);
@@ -391,14 +393,52 @@ __device__ void build_qtab(float2* qt) {
         if (((lo >> 23) & 0xFF) != 0xFF) {
             const bool neg = lo >> 31;
             const float vmin = __uint_as_float(neg ? hi : lo), vmax = __uint_as_float(neg ? lo : hi);
-            for (int j = 0; j < 15; ++j) {
-                const float bj = c_tab.bnd[j];
+            for (int j = 0; j < nb; ++j) {
+                const float bj = bnd[j];
                 if (bj < vmin) ++base;
                 else if (bj <= vmax) thr = bj;
             }
         }
         qt[k] = make_float2(thr, __int_as_float(base));
     }
+}
+
+// tq5_0 block (128 values): d = fp16(max|y| / 15), code = clamp(rint(y x (1 / fp32(d))), -15, 15)
+// + 16 (inv 0 when d is 0), rounded by adding 1.5 x 2^23 + 16; c[k] holds the code bytes of
+// channels 4k .. 4k + 3.
+__device__ __forceinline__ uint16_t encode_tq5(const float (&y)[128], uint32_t (&c)[32]) {
+    float a = 0.f;
+#pragma unroll
+    for (int i = 0; i < 128; ++i) a = fmaxf(a, fabsf(y[i]));
+    const uint16_t d16 = f2h_bits(fdiv(a, 15.0f));
+    const float d = h2f(d16);
+    const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        uint32_t r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float z = fminf(fmaxf(fmul(y[4 * k + i], inv), -15.f), 15.f);
+            r[i] = __float_as_uint(fadd(z, 12582928.0f));
+        }
+        c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
+    }
+    return d16;
+}
+
+// The low two bits of 8 nibbles (channels 8m .. 8m + 7) as 16 bits, channel e at bits 2e.
+__device__ __forceinline__ uint32_t crumbs_of(uint32_t x) {
+    x &= 0x33333333u;
+    x = (x | (x >> 2)) & 0x0F0F0F0Fu;
+    x = (x | (x >> 4)) & 0x00FF00FFu;
+    return (x | (x >> 8)) & 0x0000FFFFu;
+}
+// Bit 2 of 8 nibbles as one byte, channel e at bit e.
+__device__ __forceinline__ uint32_t bit2_byte(uint32_t x) {
+    x = (x >> 2) & 0x11111111u;
+    x = (x | (x >> 3)) & 0x03030303u;
+    x = (x | (x >> 6)) & 0x000F000Fu;
+    return (x | (x >> 12)) & 0xFFu;
 }
 
 // ---------------------------------------------------------------------------- kernel
@@ -422,7 +462,11 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
     extern __shared__ __align__(16) uint8_t sm[];
     __shared__ TileSlot slot[kSlots];
     float2* qt = reinterpret_cast<float2*>(sm + kStages * stage_bytes);
-    if constexpr (FAM == F_TBQ4) build_qtab(qt);    // read after the first barrier below
+    float2* qt3 = qt + kBuckets;                    // turbo3's table, present when a body is turbo3
+    if constexpr (FAM == F_TBQ4) {                  // read after the first barrier below
+        build_qtab(qt, c_tab.bnd, 15);
+        if (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3) build_qtab(qt3, c_tab.bnd3, 7);
+    }
     const int t = threadIdx.x, D = L.D;
     // Iteration it encodes tile blockIdx.x + it * gridDim.x from stage it % kStages. After the
     // iteration's barrier every thread has finished iteration it - 1, so its stage takes tile
@@ -470,11 +514,44 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
         uint8_t* rec = tl.rec;
         const int fmt = L.fmt[tl.w];
         if constexpr (FAM == F_TBQ4) {
-            uint32_t P[16];
-            const uint16_t n16 = encode_tbq4(y, qt, P);
-            store_nibbles(rec, D, tl.b, tl.w, P);
-            reinterpret_cast<uint16_t*>(rec + 64LL * D)[t * (D / 128) + tl.b] = n16;
-            flag_nonfinite(L, p.pool, h2f(n16));
+            if (fmt == KVQ_TQ5_0) {   // token-major: nibble plane, one-bit plane, scales
+                uint32_t C[32], P[16], hb[4];
+                const uint16_t d16 = encode_tq5(y, C);
+#pragma unroll
+                for (int m = 0; m < 16; ++m) P[m] = nibbles_of(C[2 * m] & 0x0F0F0F0Fu, C[2 * m + 1] & 0x0F0F0F0Fu);
+                store_nibbles(rec, D, tl.b, 0, P);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    hb[q] = bit4_byte(C[8 * q], C[8 * q + 1]) | (bit4_byte(C[8 * q + 2], C[8 * q + 3]) << 8) |
+                            (bit4_byte(C[8 * q + 4], C[8 * q + 5]) << 16) | (bit4_byte(C[8 * q + 6], C[8 * q + 7]) << 24);
+                *reinterpret_cast<uint4*>(rec + 64LL * D + (int64_t)t * (D / 8) + 16 * tl.b) =
+                    make_uint4(hb[0], hb[1], hb[2], hb[3]);
+                reinterpret_cast<uint16_t*>(rec + 80LL * D)[t * (D / 128) + tl.b] = d16;
+                flag_nonfinite(L, p.pool, h2f(d16));
+            } else {
+                uint32_t P[16];
+                const bool t3 = (fmt == KVQ_TURBO3);
+                const uint16_t n16 = encode_tbq4(y, t3 ? qt3 : qt, P);
+                if (t3) {   // token-major: 2-bit plane, one-bit plane, norms
+                    uint32_t cw[8], bw[4];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) cw[q] = crumbs_of(P[2 * q]) | (crumbs_of(P[2 * q + 1]) << 16);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        bw[q] = bit2_byte(P[4 * q]) | (bit2_byte(P[4 * q + 1]) << 8) | (bit2_byte(P[4 * q + 2]) << 16) |
+                                (bit2_byte(P[4 * q + 3]) << 24);
+                    uint4* c2 = reinterpret_cast<uint4*>(rec + (int64_t)t * (D / 4) + 32 * tl.b);
+                    c2[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    c2[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+                    *reinterpret_cast<uint4*>(rec + 32LL * D + (int64_t)t * (D / 8) + 16 * tl.b) =
+                        make_uint4(bw[0], bw[1], bw[2], bw[3]);
+                    reinterpret_cast<uint16_t*>(rec + 48LL * D)[t * (D / 128) + tl.b] = n16;
+                } else {
+                    store_nibbles(rec, D, tl.b, tl.w, P);
+                    reinterpret_cast<uint16_t*>(rec + 64LL * D)[t * (D / 128) + tl.b] = n16;
+                }
+                flag_nonfinite(L, p.pool, h2f(n16));
+            }
         } else {
             uint16_t d16[4], m16[4] = {0, 0, 0, 0};
             uint32_t C[32];
@@ -541,7 +618,8 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
 template <int JK, int FAM>
 int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
     const int stage = (JK == J_TQ6) ? kRows * kTq6Stride + 2 * L.D : kRows * kX16Stride;
-    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? kBuckets * sizeof(float2) : 0);
+    const bool t3 = (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3);
+    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? (t3 ? 2 : 1) * kBuckets * sizeof(float2) : 0);
     auto fn = seal_rows_kernel<JK, FAM>;
     int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
@@ -882,8 +960,8 @@ int launch_seal_rows(const Layout& L, const SealParams& p, void* stream) {
     if (L.D % 128) return (int)cudaErrorInvalidValue;
     const int n_tiles = groups * L.H * 2 * (L.D / 128);
     cudaStream_t s = (cudaStream_t)stream;
-    const bool tbq = (L.fmt[0] == KVQ_TBQ4);
-    if (tbq != (L.fmt[1] == KVQ_TBQ4)) return (int)cudaErrorInvalidValue;   // one rotation per layout
+    const bool tbq = (rotation_of(L.fmt[0]) == ROT_TBQ128);
+    if (tbq != (rotation_of(L.fmt[1]) == ROT_TBQ128)) return (int)cudaErrorInvalidValue;   // one rotation per layout
     return tbq ? launch_family<F_TBQ4>(L, p, n_tiles, s) : launch_family<F_Q>(L, p, n_tiles, s);
 }
 

@@ -35,7 +35,8 @@ struct kvq_cache {
 namespace kvq {
 
 static bool is_body(int f) {
-    return f == KVQ_TBQ4 || f == KVQ_Q8_0 || f == KVQ_Q4_0 || qblock_bits(f) != 0 || kvarn_bits(f) != 0;
+    return f == KVQ_TBQ4 || f == KVQ_TURBO3 || f == KVQ_TQ5_0 || f == KVQ_Q8_0 || f == KVQ_Q4_0 ||
+           qblock_bits(f) != 0 || kvarn_bits(f) != 0;
 }
 
 bool make_layout(const kvq_config& c, Layout* out) {
@@ -887,6 +888,13 @@ kvq_status kv_format_tables(float centroids[16], float boundaries[15], uint64_t 
     if (centroids) std::memcpy(centroids, t.cent, sizeof(t.cent));
     if (boundaries) std::memcpy(boundaries, t.bnd, sizeof(t.bnd));
     if (sign_words) std::memcpy(sign_words, t.sign_words, sizeof(t.sign_words));
+    return KVQ_OK;
+}
+
+kvq_status kv_format_tables_turbo3(float centroids[8], float boundaries[7]) {
+    const FormatTables& t = host_tables();
+    if (centroids) std::memcpy(centroids, t.cent3, sizeof(t.cent3));
+    if (boundaries) std::memcpy(boundaries, t.bnd3, sizeof(t.bnd3));
     return KVQ_OK;
 }
 

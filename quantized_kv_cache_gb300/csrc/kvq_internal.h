@@ -96,6 +96,8 @@ KVQ_HD int64_t record_bytes(int fmt, int D) {
         case KVQ_Q6_0: return 104LL * D;                      // 26 B per 32
         case KVQ_Q4_1: return 80LL * D;                       // 20 B per 32
         case KVQ_Q5_1: return 96LL * D;                       // 24 B per 32
+        case KVQ_TURBO3: return 50LL * D;                     // 48 B idx + 2 B norm per 128
+        case KVQ_TQ5_0: return 82LL * D;                      // 80 B codes + 2 B scale per 128
         case KVQ_KVARN2: case KVQ_KVARN3: case KVQ_KVARN4: case KVQ_KVARN5: case KVQ_KVARN6: case KVQ_KVARN8:
             return (int64_t)(D / 256) * (4096 * kvarn_bits(fmt) + 1152);
         default: return -1;
@@ -111,12 +113,14 @@ KVQ_HD int64_t record_code_bytes(int fmt, int D) {
         case KVQ_Q5_0: case KVQ_Q5_1: return 80LL * D;       // nibbles + one-bit plane
         case KVQ_Q6_0: return 96LL * D;                       // nibbles + two-bit plane
         case KVQ_Q4_1: return 64LL * D;
+        case KVQ_TURBO3: return 48LL * D;                     // 2-bit plane + one-bit plane
+        case KVQ_TQ5_0: return 80LL * D;                      // nibbles + one-bit plane
         default: return -1;
     }
 }
 
 KVQ_HD int rotation_of(int fmt) {
-    if (fmt == KVQ_TBQ4) return ROT_TBQ128;
+    if (fmt == KVQ_TBQ4 || fmt == KVQ_TURBO3 || fmt == KVQ_TQ5_0) return ROT_TBQ128;
     if (kvarn_bits(fmt)) return ROT_HAD256;
     return ROT_NONE;
 }
@@ -220,6 +224,9 @@ struct FormatTables {
     float bnd[15];
     float pad;
     uint64_t sign_words[4];
+    float cent3[8];        // turbo3: 8-level table
+    float bnd3[7];
+    float pad3;
 };
 
 const FormatTables& host_tables();   // derived once per process (tables.cpp)

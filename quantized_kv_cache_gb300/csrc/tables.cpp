@@ -1,5 +1,6 @@
 // Format constants derived by the library itself, once per process, on the host:
-//  - TBQ4 centroids and decision boundaries: 16-level Lloyd-Max quantizer of N(0, 1/128)
+//  - TBQ4 centroids and decision boundaries: 16-level Lloyd-Max quantizer of N(0, 1/128), and
+//    turbo3's 8-level one by the same construction
 //    (KV cache math, "How a 4-bit cache gets away with it": 16 Lloyd-Max centroids fitted
 //    to N(0, 1/sqrt(128)), read as a standard deviation of 1/sqrt(128)), computed in fp64
 //    by Lloyd iteration with closed-form Gaussian cell means and rounded to fp32;
@@ -27,20 +28,21 @@ double normal_upper(double x) { return 0.5 * std::erfc(x / std::sqrt(2.0)); }
 // from c_k = (k + 0.5) * 2.5 / 8. Cell k of the positive half is (b_k, b_{k+1}], with
 // b_0 = 0, b_k = (c_{k-1} + c_k) / 2, b_8 = infinity; its mean is
 // (pdf(b_k) - pdf(b_{k+1})) / (upper(b_k) - upper(b_{k+1})).
-void lloyd_half(double c[8]) {
-    for (int k = 0; k < 8; ++k) c[k] = (k + 0.5) * 2.5 / 8.0;
+// The same with h = 4 half-levels gives turbo3's 8-level table.
+void lloyd_half(double c[8], int h = 8) {
+    for (int k = 0; k < h; ++k) c[k] = (k + 0.5) * 2.5 / h;
     for (int it = 0; it < 50000; ++it) {
         double b[9];
         b[0] = 0.0;
-        for (int k = 1; k < 8; ++k) b[k] = (c[k - 1] + c[k]) / 2.0;
+        for (int k = 1; k < h; ++k) b[k] = (c[k - 1] + c[k]) / 2.0;
         double nc[8];
-        for (int k = 0; k < 8; ++k) {
-            const bool last = (k == 7);
+        for (int k = 0; k < h; ++k) {
+            const bool last = (k == h - 1);
             double num = normal_pdf(b[k]) - (last ? 0.0 : normal_pdf(b[k + 1]));
             double den = normal_upper(b[k]) - (last ? 0.0 : normal_upper(b[k + 1]));
             nc[k] = num / den;
         }
-        for (int k = 0; k < 8; ++k) c[k] = nc[k];
+        for (int k = 0; k < h; ++k) c[k] = nc[k];
     }
 }
 
@@ -56,6 +58,15 @@ FormatTables build() {
     const double sigma = 1.0 / std::sqrt(128.0);
     for (int j = 0; j < 16; ++j) t.cent[j] = (float)(sigma * C[j]);
     for (int k = 1; k < 16; ++k) t.bnd[k - 1] = (float)(sigma * (C[k - 1] + C[k]) / 2.0);
+    double h3[8];
+    lloyd_half(h3, 4);
+    double C3[8];
+    for (int j = 0; j < 4; ++j) {
+        C3[j] = -h3[3 - j];
+        C3[4 + j] = h3[j];
+    }
+    for (int j = 0; j < 8; ++j) t.cent3[j] = (float)(sigma * C3[j]);
+    for (int k = 1; k < 8; ++k) t.bnd3[k - 1] = (float)(sigma * (C3[k - 1] + C3[k]) / 2.0);
     uint64_t st = 0x54425134ULL;
     for (int i = 0; i < 4; ++i) t.sign_words[i] = splitmix_next(st);
     return t;

@@ -73,6 +73,12 @@ FAMILIES = {
                          contexts=[800, 1201], keep=128, steps=2, factor=12.0),
     "q50q50_f16": Family("q50q50_f16", 256, 1, 2, "q5_0", "q5_0", "f16", "f16", T=64, R=512,
                          contexts=[700], keep=64, steps=2, factor=16.0, n_out=8),
+    # the rotated comparators (generic decode path): tq5_0 K with TBQ4 (turbo4) V on a tq6_0
+    # ring, and turbo3 K and V on an F16 journal
+    "tq50tbq4_ring": Family("tq50tbq4_ring", 256, 2, 8, "tq5_0", "tbq4", "tq6_0", "f16", T=96, R=896,
+                            contexts=[700, 1300], keep=384, steps=2, n_out=8),
+    "turbo3_f16": Family("turbo3_f16", 128, 2, 4, "turbo3", "turbo3", "f16", "f16", T=128, R=1024,
+                         contexts=[900, 1413], keep=128, steps=2),
 }
 
 

@@ -44,6 +44,10 @@ def test_library_tables_equal_oracle_tables(lib):
     assert np.array_equal(np.array(cent, np.float32), oc)
     assert np.array_equal(np.array(bnd, np.float32), ob)
     assert tuple(words) == tables.sign_words()
+    c3, b3 = _lib.kv_format_tables_turbo3()
+    oc3, ob3 = tables.tbq3_tables()
+    assert np.array_equal(np.array(c3, np.float32), oc3)
+    assert np.array_equal(np.array(b3, np.float32), ob3)
 
 
 @pytest.mark.parametrize("name", list(configs.WORKLOADS))

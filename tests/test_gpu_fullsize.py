@@ -42,6 +42,7 @@ SAMPLES = {
     "longctx_tbq4": [(0, 2), (3, 0)],
     "hybrid27b_kvarn32_200k": [(0, 2)],
     "fa14b_q51q40": [(0, 3)],
+    "hybrid27b_tq50tbq4_110k": [(0, 1)],
 }
 
 
