@@ -709,7 +709,11 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
         if (e != 0) return e;
     }
     if (p.n_region_items > 0 && !fused_regions) {
-        decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, C::SMEM, s>>>(L, p);
+        // the remainder tiles (the area's last K_BYTES + V_BYTES) only for layouts that use them
+        auto split_fmt = [](int f) { return qblock_bits(f) != 0 || f == KVQ_TURBO3 || f == KVQ_TQ5_0; };
+        const bool lo = split_fmt(L.fmt[0]) || split_fmt(L.fmt[1]);
+        const int smem = C::SMEM - (lo ? 0 : C::K_BYTES + C::V_BYTES);
+        decode_split_kernel<D, NQ><<<p.n_region_items, kThreads, smem, s>>>(L, p);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return (int)e;
     }
