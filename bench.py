@@ -73,7 +73,6 @@ MEASURED_TRAFFIC = {
     "longctx_tbq4": 749.80e6,
     "widehead_kvarn55": 190.77e6,
     "hybrid27b_kvarn32_200k": 156.86e6,
-    "fa14b_q51q40": 180.60e6,
 }
 
 

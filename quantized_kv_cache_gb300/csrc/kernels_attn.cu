@@ -264,6 +264,48 @@ __device__ __forceinline__ float rot_block_value(const uint8_t* rec, int fmt, in
     return (float)(code - 16) * h2f(reinterpret_cast<const uint16_t*>(rec + 80 * D)[t * (D / 128) + (c >> 7)]);
 }
 
+// Channels c0 .. c0 + 7 (c0 a multiple of 8) of row t of a token-major Q5_0 / Q6_0 / Q4_1 /
+// Q5_1 / turbo3 / tq5_0 record: one load per plane and one per scale for the 8 values.
+__device__ __forceinline__ void tok_values8(const uint8_t* rec, int fmt, int D, int t, int c0, float (&v)[8]) {
+    if (fmt == KVQ_TURBO3) {
+        const uint32_t lo = *reinterpret_cast<const uint16_t*>(rec + t * (D / 4) + (c0 >> 2));   // 2 bits each
+        const uint32_t hb = rec[32 * D + t * (D / 8) + (c0 >> 3)];                             // bit 2
+        const float n = h2f(reinterpret_cast<const uint16_t*>(rec + 48 * D)[t * (D / 128) + (c0 >> 7)]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = c_tab.cent3[((lo >> (2 * k)) & 3) | (((hb >> k) & 1) << 2)] * n;
+        return;
+    }
+    const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));    // nibbles
+    const int bits = fmt == KVQ_TQ5_0 ? 5 : qblock_bits(fmt);
+    uint32_t hb = 0;
+    if (bits == 5) hb = rec[64 * D + t * (D / 8) + (c0 >> 3)];
+    else if (bits == 6) hb = *reinterpret_cast<const uint16_t*>(rec + 64 * D + t * (D / 4) + (c0 >> 2));
+    int code[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        code[k] = (int)((w4 >> (4 * k)) & 15);
+        if (bits == 5) code[k] |= (int)((hb >> k) & 1) << 4;
+        else if (bits == 6) code[k] |= (int)((hb >> (2 * k)) & 3) << 4;
+    }
+    if (fmt == KVQ_TQ5_0) {
+        const float d = h2f(reinterpret_cast<const uint16_t*>(rec + 80 * D)[t * (D / 128) + (c0 >> 7)]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = (float)(code[k] - 16) * d;
+        return;
+    }
+    const uint16_t* sc = reinterpret_cast<const uint16_t*>(rec + record_code_bytes(fmt, D));
+    const float d = h2f(sc[t * (D / 32) + (c0 >> 5)]);
+    const int L = qblock_sym_levels(fmt);
+    if (L) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = (float)(code[k] - (L + 1)) * d;
+    } else {
+        const float m = h2f(sc[4 * D + t * (D / 32) + (c0 >> 5)]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = (float)code[k] * d + m;
+    }
+}
+
 // Body K records (token-major) of one tile: positions [tstart, tstart + TILE) of group g.
 template <int D, int TILE, int LD>
 __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int g, int rel, __half* dst,
@@ -275,12 +317,8 @@ __device__ void fill_body_k(const Layout& L, const void* pool, int64_t unit, int
         const int i = e / U, u = e % U;
         const int t = rel + i, c0 = 8 * u;
         float v[8];
-        if (qblock_bits(fmt)) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = qblock_value(rec, fmt, D, t, c0 + k);
-        } else if (fmt == KVQ_TURBO3 || fmt == KVQ_TQ5_0) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] = rot_block_value(rec, fmt, D, t, c0 + k);
+        if (qblock_bits(fmt) || fmt == KVQ_TURBO3 || fmt == KVQ_TQ5_0) {
+            tok_values8(rec, fmt, D, t, c0, v);
         } else if (fmt == KVQ_TBQ4) {
             const uint32_t w4 = *reinterpret_cast<const uint32_t*>(rec + t * (D / 2) + (c0 >> 1));
             const float n = h2f(reinterpret_cast<const uint16_t*>(rec + 64 * D)[t * (D / 128) + (c0 >> 7)]);
