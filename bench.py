@@ -329,10 +329,21 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+# (head_dim, query tile, K body, V body) of the streaming decode kernel's instances
+# (kernels_body.cu, the dispatch table); other layouts take the generic path
+STREAMING = {(128, 8, "tbq4", "tbq4"), (256, 8, "tbq4", "tbq4"), (256, 16, "tbq4", "tbq4"),
+             (128, 8, "q8_0", "q4_0"), (128, 16, "q8_0", "q4_0"), (256, 8, "kvarn4", "kvarn4"),
+             (256, 16, "kvarn4", "kvarn4"), (512, 8, "kvarn5", "kvarn5"), (512, 16, "kvarn5", "kvarn5"),
+             (256, 8, "kvarn3", "kvarn2")}
+
+
 def launches_per_layer(w):
     """Kernel launches of one layer's decode step outside seals: the decode kernel (which also
-    appends the step's position) and the merge."""
-    return 2
+    appends the step's position) and the merge; on the generic path an append, the generic
+    decode kernel and the merge."""
+    nq = 8 if w.G <= 8 else 16
+    fused = (w.head_dim, nq, w.k_body, w.v_body) in STREAMING and not (w.head_dim == 512 and w.journal == "tq6_0")
+    return 2 if fused else 3
 
 
 def seal_launches(w, states):

@@ -142,3 +142,18 @@ def test_decode_seal_points():
     w = configs.WORKLOADS["longctx_tbq4"]
     for n0 in w.contexts:
         assert configs.groups_to_seal(n0 + 16, n0 - 20480, w.keep) == 128
+
+
+def test_bench_streaming_table_matches_the_dispatch_table():
+    """bench.py counts launches by the streaming decode kernel's instances; they must be the
+    instances kernels_body.cu dispatches to (KVQ_BODY_CASE lines)."""
+    import re
+    import bench
+    src = open(os.path.join(os.path.dirname(__file__), "..", "quantized_kv_cache_gb300", "csrc",
+                            "kernels_body.cu")).read()
+    names = {"KVQ_TBQ4": "tbq4", "KVQ_Q8_0": "q8_0", "KVQ_Q4_0": "q4_0", "KVQ_KVARN2": "kvarn2",
+             "KVQ_KVARN3": "kvarn3", "KVQ_KVARN4": "kvarn4", "KVQ_KVARN5": "kvarn5"}
+    cases = set()
+    for m in re.finditer(r"KVQ_BODY_CASE\((\d+), (\d+), \w+, \w+, \d, \d, (\w+), (\w+)\)", src):
+        cases.add((int(m.group(1)), int(m.group(2)), names[m.group(3)], names[m.group(4)]))
+    assert cases == bench.STREAMING
