@@ -169,6 +169,15 @@ kvq_status kv_append(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_
 kvq_status kv_prefill(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq, int n_tok, const void* k,
                       const void* v, int keep, int64_t* groups_sealed, void* stream);
 
+/* kv_prefill_plan — (test call) the host plan kv_prefill makes for one sequence holding
+ * n_tokens positions with sealed end sealed_end: ranges (host, 8 values) receives the head
+ * [r0, r1) appended to the journal and sink, the groups [r2, r3) then sealed from the journal,
+ * the groups [r4, r5) sealed straight from the input rows, and the rest [r6, r7) appended to the
+ * journal and exact tail; r5 is the sealed end after the call. The same refusals as kv_prefill
+ * (KVQ_ENOSPC), KVQ_EINVAL on a null pointer or n_tok <= 0. Pure host arithmetic. */
+kvq_status kv_prefill_plan(int64_t n_tokens, int64_t sealed_end, int64_t n_tok, int32_t keep, int32_t ring_capacity,
+                           int64_t max_ctx, int64_t ranges[8]);
+
 /* kv_seal — SJ-KVaRN §2.1 item 4 and §4.3: for each listed sequence of `layer` (-1: all
  * layers) seal every full 128-position group g with S + 128 <= N - keep into body records,
  * oldest first, and advance S. keep >= T. groups_sealed (host, may be NULL) receives the

@@ -74,6 +74,7 @@ _SIGS = {
     "kv_format_tables": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float),
                          ctypes.POINTER(ctypes.c_uint64)],
     "kv_format_tables_turbo3": [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)],
+    "kv_prefill_plan": [I64, I64, I64, ctypes.c_int32, ctypes.c_int32, I64, ctypes.POINTER(I64)],
     "kv_decode_step": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P, P, ctypes.c_int, ctypes.c_int,
                        P, SZ, ctypes.POINTER(P), ctypes.POINTER(I64), P],
     "kv_decode_attn_noalloc": [P, ctypes.c_int, ctypes.POINTER(I32), ctypes.c_int, P, P, P],
@@ -254,6 +255,13 @@ def kv_format_tables():
     s = (ctypes.c_uint64 * 4)()
     _check("kv_format_tables", load().kv_format_tables(c, b, s))
     return list(c), list(b), list(s)
+
+
+def kv_prefill_plan(n_tokens, sealed_end, n_tok, keep, ring_capacity, max_ctx):
+    """The 8 range bounds of kv_prefill's plan (head, journal seal, direct seal, rest)."""
+    r = (I64 * 8)()
+    _check("kv_prefill_plan", load().kv_prefill_plan(n_tokens, sealed_end, n_tok, keep, ring_capacity, max_ctx, r))
+    return list(r)
 
 
 def kv_format_tables_turbo3():

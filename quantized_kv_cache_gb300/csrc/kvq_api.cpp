@@ -376,6 +376,39 @@ int append_ranges(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, co
 
 }  // namespace
 
+namespace {
+// One sequence's prefill plan: N0 positions held, S0 sealed end, n_tok new positions. S1 is the
+// sealed end after the call (every full group older than the newest keep sealed) and M the end
+// of the head range (see kv_prefill). KVQ_ENOSPC when the call would pass max_ctx or leave more
+// unsealed positions than the ring holds.
+kvq_status prefill_plan(int64_t N0, int64_t S0, int64_t n_tok, int64_t keep, int64_t R, int64_t max_ctx,
+                        int64_t* S1, int64_t* M) {
+    const int64_t N1 = N0 + n_tok;
+    if (N1 > max_ctx) return KVQ_ENOSPC;
+    const int64_t lim = N1 - keep - S0;
+    *S1 = S0 + (lim >= kGroup ? lim / kGroup * kGroup : 0);
+    if (std::max<int64_t>(N1, kSink) - *S1 > R) return KVQ_ENOSPC;
+    const int64_t first_in = N0 <= kSink ? kSink : kSink + (N0 - kSink + kGroup - 1) / kGroup * kGroup;
+    *M = std::min(std::min(first_in, *S1), N1);
+    return KVQ_OK;
+}
+}  // namespace
+
+kvq_status kv_prefill_plan(int64_t n_tokens, int64_t sealed_end, int64_t n_tok, int32_t keep, int32_t ring_capacity,
+                           int64_t max_ctx, int64_t ranges[8]) {
+    if (!ranges || n_tok <= 0 || keep < 0 || ring_capacity <= 0 || n_tokens < 0 || sealed_end < kSink)
+        return KVQ_EINVAL;
+    int64_t S1 = 0, M = 0;
+    const kvq_status st = prefill_plan(n_tokens, sealed_end, n_tok, keep, ring_capacity, max_ctx, &S1, &M);
+    if (st != KVQ_OK) return st;
+    const int64_t N0 = n_tokens, N1 = N0 + n_tok;
+    const int64_t Sj = sealed_end + std::max<int64_t>(0, M - sealed_end) / kGroup * kGroup;
+    const int64_t Sd = Sj + std::max<int64_t>(0, S1 - Sj) / kGroup * kGroup;
+    const int64_t r[8] = {N0, std::max(N0, M), sealed_end, Sj, Sj, Sd, std::max(N0, std::min(S1, N1)), N1};
+    for (int i = 0; i < 8; ++i) ranges[i] = r[i];
+    return KVQ_OK;
+}
+
 kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, int n_tok, const void* k,
                       const void* v, int keep, int64_t* groups_sealed, void* stream) {
     kvq_status st = check_cache(c);
@@ -394,15 +427,10 @@ kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq
     int64_t n0[kMaxSeqPerCall], s1[kMaxSeqPerCall], m[kMaxSeqPerCall];
     for (int i = 0; i < n_seq; ++i) {
         const int s = seq_ids[i];
-        const int64_t N0 = NT(c, layer, s), S0 = ST(c, layer, s), N1 = N0 + n_tok;
-        if (N1 > c->cfg.max_ctx) return KVQ_ENOSPC;
-        const int64_t lim = N1 - keep - S0;
-        const int64_t S1 = S0 + (lim >= kGroup ? lim / kGroup * kGroup : 0);
-        if (std::max<int64_t>(N1, kSink) - S1 > c->cfg.ring_capacity) return KVQ_ENOSPC;
-        const int64_t first_in = N0 <= kSink ? kSink : kSink + (N0 - kSink + kGroup - 1) / kGroup * kGroup;
-        n0[i] = N0;
-        s1[i] = S1;
-        m[i] = std::min(std::min(first_in, S1), N1);
+        n0[i] = NT(c, layer, s);
+        const kvq_status e = prefill_plan(n0[i], ST(c, layer, s), n_tok, keep, c->cfg.ring_capacity,
+                                          c->cfg.max_ctx, &s1[i], &m[i]);
+        if (e != KVQ_OK) return e;
     }
     int64_t cnt[kMaxSeqPerCall], off[kMaxSeqPerCall], tfrom[kMaxSeqPerCall], groups[kMaxSeqPerCall];
     int64_t row[kMaxSeqPerCall];
