@@ -12,7 +12,7 @@ positions, KVarN 4/4 body, tq6_0 ring, 1,024-position exact tail, 256 decode ste
 the seal at the journal's 8,192 mark). Prints one JSON line (rank 0).
 
 --impl reference times the CPU oracle (numpy, fp64 attention) on a bounded sample of the
-same workload: the reference this build is checked against.
+same workload: the reference the CUDA path is checked against.
 """
 
 import argparse

@@ -38,7 +38,7 @@ typedef enum {
     KVQ_OK = 0,
     KVQ_EINVAL = 1,        /* bad argument: null / misaligned pointer, index out of range, bad config */
     KVQ_ENOSPC = 2,        /* journal ring or context capacity would overflow; nothing written */
-    KVQ_EUNSUPPORTED = 3,  /* valid config this build has no kernel for */
+    KVQ_EUNSUPPORTED = 3,  /* valid config this library has no kernel for */
     KVQ_ECUDA = 4,         /* a CUDA runtime call or kernel launch failed */
     KVQ_EDEVICE = 5        /* device status word reports a problem (see kv_get_status) */
 } kvq_status;
