@@ -47,6 +47,7 @@ class HeadConfig:
     tail_fmt: str          # f16 | bf16 (exact tail store; with an exact journal, its format)
     tail: int              # T
     ring: int              # R, journal capacity (positions)
+    kvarn_balance: str = "final16"   # KVarN balancing: "final16" or "best8" (kvarn.BALANCE_MODES)
 
     @property
     def rot(self):
@@ -68,7 +69,7 @@ def _load_exact(bits, fmt):
     return bf16_bits_to_f32(bits)
 
 
-def encode_body(X, fmt):
+def encode_body(X, fmt, kvarn_balance="final16"):
     """Rows X [128, D] fp32 in the body's domain -> unpacked record fields."""
     if fmt == "tbq4":
         n16, idx = codecs.tbq4_encode(X)
@@ -95,7 +96,7 @@ def encode_body(X, fmt):
         bits = int(fmt[5:])
         D = X.shape[-1]
         tiles = X.reshape(128, D // 256, 256).transpose(1, 0, 2)   # [half, 128, 256]
-        code, S, Z, C = kvarn.encode(tiles, bits)
+        code, S, Z, C = kvarn.encode(tiles, bits, kvarn_balance)
         return {"code": code, "S": S, "Z": Z, "C": C, "bits": bits}
     raise ValueError(fmt)
 
@@ -237,7 +238,7 @@ class HeadCache:
         while self.S + GROUP <= self.N - keep:
             for w, fmt in (("K", self.cfg.k_body), ("V", self.cfg.v_body)):
                 X = self.journal_rows(w, self.S, GROUP)
-                self.body[w].append(encode_body(X, fmt))
+                self.body[w].append(encode_body(X, fmt, self.cfg.kvarn_balance))
             self.S += GROUP
             n += 1
         return n

@@ -11,6 +11,12 @@ Readings where the page is silent (the format fixes them): the spread is the pop
 standard deviation (centred), passes start with rows, scales are carried as running
 products, a spread <= 2^-20 counts as 1.
 
+The page also names the KVarN reference configuration: 8 passes, keeping the best scales
+seen (``balance_best``). Reading: a pass's state is measured by the largest |sigma - 1| over
+the lines of the axis that pass did not balance (its columns after a row pass, its rows after
+a column pass), with sigma computed exactly as the next pass would compute it; the kept state
+is the one with the smallest measure, the earliest on a tie.
+
 Parity unpinned: the pages print no worked example of a balanced tile, so the exact
 scales this function picks are pinned only by invariants (final column spreads equal 1,
 X = diag(r) Y diag(c), fixed points of already-balanced tiles) and by the row-rounding
@@ -23,7 +29,9 @@ from .fp import f32, to_f16, tree_sum
 
 ROWS, COLS = 128, 256
 PASSES = 16
+BEST_PASSES = 8
 SIGMA_FLOOR = np.float32(2.0 ** -20)
+BALANCE_MODES = ("final16", "best8")
 
 
 def _spread(v, axis):
@@ -56,11 +64,56 @@ def balance(X, passes=PASSES):
     return Y, r, c
 
 
-def encode(X, bits):
-    """X [..., 128, 256] -> (codes uint8 [..., 128, 256], S, Z fp16 [..., 128], C fp16 [..., 256])."""
+def imbalance(Y, after_row_pass):
+    """Measure of a balancing state: the largest |sigma - 1| (fp32) over the lines of the axis
+    the last pass did not balance, sigma being that line's spread as a pass computes it."""
+    sig = _spread(Y, axis=-2 if after_row_pass else -1)
+    return np.max(np.abs(sig - np.float32(1.0)), axis=-1)
+
+
+def balance_best(X, passes=BEST_PASSES):
+    """The KVarN reference configuration (SJ-KVaRN §2.2): `passes` alternating passes, rows
+    first, keeping the state (Y, r, c) of the pass with the smallest imbalance (the earliest on
+    a tie). X [..., 128, 256] fp32 -> (Y, r, c, best pass [...], imbalance per pass [passes, ...])."""
+    Y = f32(X).copy()
+    r = np.ones(Y.shape[:-1], dtype=np.float32)
+    c = np.ones(Y.shape[:-2] + (Y.shape[-1],), dtype=np.float32)
+    states, eps = [], []
+    for p in range(passes):
+        if p % 2 == 0:
+            sig = _spread(Y, axis=-1)
+            Y = Y * (np.float32(1.0) / sig)[..., :, None]
+            r = r * sig
+        else:
+            sig = _spread(Y, axis=-2)
+            Y = Y * (np.float32(1.0) / sig)[..., None, :]
+            c = c * sig
+        states.append((Y, r, c))
+        eps.append(imbalance(Y, p % 2 == 0))
+    eps = np.stack(eps)                                   # [passes, ...]
+    best = np.argmin(eps, axis=0)                         # first minimum: earliest pass on a tie
+    Ys = np.stack([s_[0] for s_ in states])
+    rs = np.stack([s_[1] for s_ in states])
+    cs = np.stack([s_[2] for s_ in states])
+    sel = best[None, ...]
+    Yb = np.take_along_axis(Ys, sel[..., None, None], axis=0)[0]
+    rb = np.take_along_axis(rs, sel[..., None], axis=0)[0]
+    cb = np.take_along_axis(cs, sel[..., None], axis=0)[0]
+    return Yb, rb, cb, best, eps
+
+
+def encode(X, bits, balance_mode="final16"):
+    """X [..., 128, 256] -> (codes uint8 [..., 128, 256], S, Z fp16 [..., 128], C fp16 [..., 256]).
+
+    balance_mode: "final16" (16 passes, final scales) or "best8" (8 passes, best state)."""
     X = f32(X)
     Q = np.float32(2 ** bits - 1)
-    Y, r, c = balance(X)
+    if balance_mode == "final16":
+        Y, r, c = balance(X)
+    elif balance_mode == "best8":
+        Y, r, c = balance_best(X)[:3]
+    else:
+        raise ValueError(balance_mode)
     lo = np.min(Y, axis=-1)
     hi = np.max(Y, axis=-1)
     S = to_f16((r * (hi - lo)) / Q)

@@ -120,3 +120,108 @@ def test_constant_rows_and_zero_tile():
     X = np.zeros((128, 256), np.float32)
     code, S, Z, C = kvarn.encode(X, 4)
     assert np.all(S == 0) and np.all(code == 0) and np.all(kvarn.decode(code, S, Z, C) == 0)
+
+
+# ------------------------------------------------------------------ 8-pass keep-best balancing
+# SJ-KVaRN §2.2: the KVarN reference configuration runs 8 passes and keeps the best scales
+# seen. Reading (the format fixes it): a state is measured by the largest |sigma - 1| over the
+# lines the last pass did not balance; the kept state is the smallest, the earliest on a tie.
+
+def _alternating_tile(alpha):
+    """32 rows of a balanced sign pattern (x alpha) over 96 zero rows: every sum is exact, the
+    column spreads after a row pass are sqrt(32/128) = 0.5 and the row spreads after a column
+    pass are 2, so the imbalance alternates 0.5, 1, 0.5, 1, ... exactly."""
+    a = np.array([1, -1] * 16, np.float32)
+    b = np.array([1, 1, -1, -1] * 64, np.float32)
+    X = np.zeros((128, 256), np.float32)
+    X[:32] = alpha * a[:, None] * b[None, :]
+    return X, a, b
+
+
+def test_best8_exact_alternation_keeps_the_first_pass():
+    alpha = np.float32(0.25)
+    X, a, b = _alternating_tile(alpha)
+    Y, r, c, best, eps = kvarn.balance_best(X)
+    assert eps.tolist() == [0.5, 1.0] * 4
+    assert int(best) == 0                                   # ties: the earliest state
+    assert np.all(r[:32] == alpha) and np.all(r[32:] == 1) and np.all(c == 1)
+    assert np.array_equal(Y[:32], a[:, None] * b[None, :]) and not Y[32:].any()
+    code, S, Z, C = kvarn.encode(X, 4, "best8")
+    # rows 0..31: lo = -1, hi = 1: S = fp16(0.25 * 2 / 15), Z = fp16(-0.25); zero rows: S = Z = 0
+    assert np.all(S[:32] == np.float16(np.float32(0.5) / np.float32(15))) and np.all(Z[:32] == np.float16(-0.25))
+    assert not S[32:].view(np.uint16).any() and not Z[32:].view(np.uint16).any()
+    assert np.all(C.view(np.uint16) == 0x3C00)
+    assert np.array_equal(code[:32], np.where(X[:32] > 0, 15, 0)) and not code[32:].any()
+    # the 16-pass rule keeps the last (column) pass instead: 8 column passes of 0.5, 7 row
+    # passes of 2 after the first
+    Yf, rf, cf = kvarn.balance(X)
+    assert np.all(cf == 2.0 ** -8) and np.all(rf[:32] == alpha * 2 ** 7)
+
+
+def _balance_fp64(X, passes=8):
+    """Plain fp64 restatement of the passes and the imbalance measure (numpy std, no trees)."""
+    Y = X.astype(np.float64)
+    r, c = np.ones(128), np.ones(256)
+    states, eps = [], []
+    for p in range(passes):
+        if p % 2 == 0:
+            s = Y.std(axis=1)
+            s = np.where(s <= 2.0 ** -20, 1.0, s)
+            Y, r = Y / s[:, None], r * s
+            o = Y.std(axis=0)
+        else:
+            s = Y.std(axis=0)
+            s = np.where(s <= 2.0 ** -20, 1.0, s)
+            Y, c = Y / s[None, :], c * s
+            o = Y.std(axis=1)
+        o = np.where(o <= 2.0 ** -20, 1.0, o)
+        states.append((Y, r, c))
+        eps.append(np.max(np.abs(o - 1)))
+    return states, np.array(eps)
+
+
+def _tiles():
+    rng = np.random.default_rng(17)
+    out = []
+    for i in range(6):
+        x = rng.standard_normal((128, 256)).astype(np.float32)
+        x[:, rng.choice(256, 8, replace=False)] *= 16
+        if i % 2 == 0:
+            x[rng.choice(128, 3, replace=False)] = 0          # dead rows: no joint balance exists
+        if i % 3 == 0:
+            x *= np.exp(2 * rng.standard_normal((128, 1))).astype(np.float32)
+        out.append(x)
+    return out
+
+
+def test_best8_matches_fp64_brute_force():
+    seen_early = False
+    for X in _tiles():
+        Y, r, c, best, eps = kvarn.balance_best(X)
+        states, eps64 = _balance_fp64(X)
+        assert np.allclose(eps, eps64, rtol=1e-4, atol=1e-6)
+        order = np.argsort(eps64, kind="stable")
+        if eps64[order[1]] - eps64[order[0]] > 1e-4 * eps64[order[0]]:
+            assert int(best) == int(order[0])
+        b = int(best)
+        assert eps[b] == eps.min() and b == int(np.flatnonzero(eps == eps.min())[0])
+        Y64, r64, c64 = states[b]
+        assert np.allclose(r, r64, rtol=1e-5) and np.allclose(c, c64, rtol=1e-5)
+        assert np.allclose(Y, Y64, rtol=1e-4, atol=1e-5)
+        # the kept state still factorises the tile
+        recon = r.astype(np.float64)[:, None] * Y.astype(np.float64) * c.astype(np.float64)[None, :]
+        assert np.max(np.abs(recon - X)) <= 1e-5 * np.max(np.abs(X))
+        seen_early |= b < 7
+    assert seen_early          # the dead-row tiles keep an earlier pass than the last
+
+
+@pytest.mark.parametrize("bits", [2, 4, 5])
+def test_best8_row_rounding_error_bound(bits):
+    for X in _tiles()[:3]:
+        code, S, Z, C = kvarn.encode(X, bits, "best8")
+        Xr = kvarn.decode(code, S, Z, C)
+        # every value within half a step of its row (times its column scale), plus the fp16
+        # rounding of the scales
+        step = np.abs(S.astype(np.float64))[:, None] * np.abs(C.astype(np.float64))[None, :]
+        err = np.abs(Xr.astype(np.float64) - X)
+        assert np.all(err <= 0.5 * step + 4e-3 * np.abs(X) + 1e-3 * step + 1e-6)
