@@ -18,8 +18,9 @@
  *  - Ordering: device work is enqueued on the given stream (cudaStream_t passed as void*;
  *    NULL is the legacy default stream). Lengths live on the host and are authoritative,
  *    so refusals (KVQ_ENOSPC, KVQ_EINVAL) happen before anything is enqueued.
- *  - Errors detected on the device (non-finite scales) set bits of a status word that
- *    kv_get_status reads after the caller synchronises.
+ *  - Errors detected on the device (non-finite scales: bit 0; a bounded wait that ran
+ *    out: bit 1) set bits of a status word that kv_get_status reads after the caller
+ *    synchronises.
  *
  * Shapes: L layers, H KV heads, Hq query heads, G = Hq / H, D head_dim. Query head h reads
  * KV head h / G. K/V/q inputs are IEEE fp16, row-major.
@@ -74,13 +75,21 @@ typedef enum {
     KVQ_TQ5_0 = 17
 } kvq_fmt;
 
+/* Balancing rule of KVarN seals (SJ-KVaRN §2.2 "Rotation and balancing"): 16 alternating
+ * row/column passes keeping the final scales, or the KVarN reference configuration's 8 passes
+ * keeping the best scales seen. Reading of "best": the state whose largest |sigma - 1| over
+ * the lines the last pass did not balance (the columns after a row pass, the rows after a
+ * column pass; sigma the line's spread as the next pass would compute it) is the smallest,
+ * the earliest pass on a tie. Records have the same layout either way. */
+enum { KVQ_KVARN_FINAL16 = 0, KVQ_KVARN_BEST8 = 1 };
+
 typedef struct {
     int32_t n_layers;
     int32_t n_kv_heads;
     int32_t head_dim;        /* 128, 256 or 512; KVarN bodies need a multiple of 256 */
     int32_t n_q_heads;       /* a multiple of n_kv_heads, with n_q_heads / n_kv_heads <= 16 */
     int32_t max_seqs;        /* sequence slots */
-    int32_t reserved0;
+    int32_t kvarn_balance;   /* KVarN bodies: KVQ_KVARN_FINAL16 (0) or KVQ_KVARN_BEST8 (1) */
     int64_t max_ctx;         /* positions a slot can hold (sets the body capacity) */
     int32_t k_body;          /* kvq_fmt of K body records */
     int32_t v_body;          /* kvq_fmt of V body records; must share K's rotation */
@@ -191,8 +200,9 @@ kvq_status kv_seal(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_se
  * (body, tq6_0 ring span); one softmax over all positions; the rotated regions' weighted
  * sum rotated back once (KV cache math, "rotate first"; KV Cache Precision Tail §2).
  * q: device fp16 [n_seq][Hq][D]; out: device fp16 [n_seq][Hq][D].
- * workspace: device, >= workspace_bytes of kv_required_bytes, zero-filled before its first
- * use; each call leaves it ready for the next. Calls sharing a workspace must not overlap. */
+ * workspace: device, >= workspace_bytes of kv_required_bytes. It holds the call's per-item
+ * partials (m, l, o), each written before it is read, so its contents need not start at zero.
+ * Calls sharing a workspace must not overlap on the GPU. */
 kvq_status kv_decode_attn(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq,
                           const void* q, void* out, void* workspace, size_t ws_bytes, void* stream);
 
@@ -203,9 +213,12 @@ kvq_status kv_decode_attn(kvq_cache* cache, int layer, const int32_t* seq_ids, i
  * seal back to the newest 4,096); seal_trigger == 0 seals whenever a full group older than
  * keep exists; seal_trigger < 0 never seals. Layouts: q [n_layers][n_seq][Hq][D], k and v
  * [n_layers][n_seq][1][H][D], out [n_layers][n_seq][Hq][D], all device fp16.
- * events (may be NULL): 2 * n_layers caller-created cudaEvent_t handles; events[2l] and
- * events[2l+1] are recorded on `stream` just before and just after layer l's decode kernel
- * (the streaming kernel, or the generic split kernel; the merge kernel follows them).
+ * events (may be NULL): 2 * n_layers caller-created cudaEvent_t handles; events[2l]
+ * completes when everything layer l's decode kernel waits for has completed, events[2l+1]
+ * when that kernel (the streaming kernel, or the generic split kernel; the merge kernel
+ * follows) has. In graph mode they are event-record nodes on a side branch of the step's
+ * graph, so the kernels keep their programmatic launches; with graph mode off they are
+ * recorded inline on `stream` and the decode and merge kernels are launched plainly.
  * groups_sealed (host, may be NULL) receives the groups sealed in this step.
  * Where the decode kernel takes a layout's region items and the newest row is fp16, the
  * append runs inside that layer's attention launch (same results, one launch less).
@@ -242,7 +255,8 @@ kvq_status kv_restore(kvq_cache* cache, const void* buf, size_t bytes);
  * Same arguments and results as kv_decode_attn, minus the workspace: the library uses a
  * fixed 32 MiB device array that every GPU loading the library holds until exit. Configs whose
  * kv_required_bytes workspace exceeds 32 MiB are refused with KVQ_EUNSUPPORTED. All calls
- * share the array (nothing in it needs to start at zero); calls that overlap on the GPU race
+ * share the array (as with kv_decode_attn's workspace, nothing in it needs to start at zero:
+ * every partial is written before it is read); calls that overlap on the GPU race
  * and must be avoided. The first call on each device looks up the array's address with that
  * device current; make that first call before any stream capture begins. Allocates nothing. */
 kvq_status kv_decode_attn_noalloc(kvq_cache* cache, int layer, const int32_t* seq_ids, int n_seq,
@@ -252,7 +266,9 @@ kvq_status kv_decode_attn_noalloc(kvq_cache* cache, int layer, const int32_t* se
 kvq_status kv_state(const kvq_cache* cache, int layer, int seq, int64_t* n_tokens, int64_t* sealed_end);
 
 /* kv_get_status — read (synchronously) and clear the device status word. Bit 0: a
- * non-finite scale was produced by an encoder. Returns KVQ_EDEVICE if any bit was set. */
+ * non-finite scale was produced by an encoder (the record holds it, as the format defines).
+ * Bit 1: a bounded device wait (a streaming kernel's wait for its bulk copies, 2 s) ran out;
+ * the outputs of the launch that set it are invalid. Returns KVQ_EDEVICE if any bit was set. */
 kvq_status kv_get_status(kvq_cache* cache, uint32_t* word);
 
 /* ---------------------------------------------------------------------------------------

@@ -143,7 +143,8 @@ def scale_block(S, Z, C):
     return np.concatenate([S, Z, C, pad], axis=-1).astype(np.float16)
 
 
-# Code planes of a b-bit code, low plane first (FORMAT.md section 5): plane widths summing to b.
+# Code planes of a b-bit code, low plane first (the record layout of the format): plane widths
+# summing to b.
 PLANES = {2: (2,), 3: (2, 1), 4: (4,), 5: (4, 1), 6: (4, 2), 8: (8,)}
 
 

@@ -18,6 +18,8 @@ FMT_NAMES = {"f16": F16, "bf16": BF16, "tq6_0": TQ6_0, "tbq4": TBQ4, "q8_0": Q8_
              "kvarn4": KVARN4, "kvarn5": KVARN5, "kvarn2": KVARN2, "kvarn3": KVARN3, "kvarn6": KVARN6,
              "kvarn8": KVARN8, "q5_0": Q5_0, "q6_0": Q6_0, "q4_1": Q4_1, "q5_1": Q5_1, "turbo3": TURBO3,
              "tq5_0": TQ5_0}
+# KVarN balancing rules (kvq_config.kvarn_balance)
+KVARN_BALANCE = {"final16": 0, "best8": 1}
 # regions
 REGION_SINK, REGION_JOURNAL, REGION_JOURNAL_SCALE, REGION_TAIL, REGION_BODY = range(5)
 ENOSPC = 2
@@ -32,7 +34,7 @@ class KVQError(RuntimeError):
 
 class kvq_config(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
-                ("n_q_heads", ctypes.c_int32), ("max_seqs", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("max_seqs", ctypes.c_int32), ("kvarn_balance", ctypes.c_int32),
                 ("max_ctx", ctypes.c_int64), ("k_body", ctypes.c_int32), ("v_body", ctypes.c_int32),
                 ("journal", ctypes.c_int32), ("tail_fmt", ctypes.c_int32), ("tail", ctypes.c_int32),
                 ("ring_capacity", ctypes.c_int32), ("softmax_scale", ctypes.c_float),

@@ -740,8 +740,16 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
     // items go through the generic kernel
     const bool streaming = body_ctas_per_sm(L) > 0;
     const bool fused_regions = streaming && region_kernel_ok(L);
-    if (mk.before && cudaEventRecordWithFlags((cudaEvent_t)mk.before, s, mk.flags) != cudaSuccess)
-        return (int)cudaErrorInvalidResourceHandle;
+    auto mark = [&](void* ev) -> bool {
+        if (!ev) return true;
+        if (mk.side) {
+            if (cudaEventRecord((cudaEvent_t)mk.fork, s) != cudaSuccess) return false;
+            if (cudaStreamWaitEvent((cudaStream_t)mk.side, (cudaEvent_t)mk.fork, 0) != cudaSuccess) return false;
+            return cudaEventRecordWithFlags((cudaEvent_t)ev, (cudaStream_t)mk.side, mk.flags) == cudaSuccess;
+        }
+        return cudaEventRecordWithFlags((cudaEvent_t)ev, s, mk.flags) == cudaSuccess;
+    };
+    if (!mark(mk.before)) return (int)cudaErrorInvalidResourceHandle;
     if (streaming) {
         const int e = launch_decode_fused(L, p, n_body, fused_regions ? p.n_region_items : 0, s, mk.pdl);
         if (e != 0) return e;
@@ -755,8 +763,7 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return (int)e;
     }
-    if (mk.after && cudaEventRecordWithFlags((cudaEvent_t)mk.after, s, mk.flags) != cudaSuccess)
-        return (int)cudaErrorInvalidResourceHandle;
+    if (!mark(mk.after)) return (int)cudaErrorInvalidResourceHandle;
     int max_cnt = 0;
     for (int i = 0; i < p.n_seq; ++i)
         max_cnt = max(max_cnt, p.seq[i].items_per_head + p.seq[i].body_per_head);
@@ -767,7 +774,7 @@ int launch_decode_t(const Layout& L, const AttnParams& p, cudaStream_t s, const 
         cudaFuncSetAttribute(decode_merge_kernel<D, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)msmem);
     // programmatic serialization only where the launch ahead is the decode kernel (no event
     // record or generic kernel between them)
-    const bool pdl = mk.pdl && streaming && fused_regions && !mk.after;
+    const bool pdl = mk.pdl && streaming && fused_regions && (!mk.after || mk.side);
     const cudaError_t e = launch_k(decode_merge_kernel<D, NQ>, mg, dim3(256), msmem, s, pdl, L, p);
     return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }

@@ -727,9 +727,11 @@ __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, in
 // line's scale *= sigma. A line belongs to P = n / 64 threads (adjacent lanes); thread q
 // holds the values q + P i (i < 64), so the tree levels of stride >= P are in-thread and the
 // last log2(P) levels cross the P lanes (every lane ends with the same sum, the adds being
-// commutative). ROWS: 128 rows x 4 threads; else 256 columns x 2 threads.
-template <bool ROWS>
-__device__ __forceinline__ void kv_pass(float* Y, float* scale) {
+// commutative). ROWS: 128 rows x 4 threads; else 256 columns x 2 threads. Returns |sigma - 1|
+// of this thread's line (the imbalance the state before the pass has on this axis); with
+// APPLY false the pass only measures it.
+template <bool ROWS, bool APPLY = true>
+__device__ __forceinline__ float kv_pass(float* Y, float* scale) {
     constexpr int P = ROWS ? 4 : 2;
     constexpr float INV_N = ROWS ? 1.0f / 256.0f : 1.0f / 128.0f;
     const int line = threadIdx.x / P, q = threadIdx.x % P;
@@ -759,10 +761,26 @@ __device__ __forceinline__ void kv_pass(float* Y, float* scale) {
     const float var = line_sum([&](int i) { const float d = fsub(x[i], mu); return fmul(d, d); });
     float sig = __fsqrt_rn(fmul(var, INV_N));
     if (sig <= 9.5367431640625e-07f) sig = 1.f;     // 2^-20
-    const float inv = fdiv(1.0f, sig);
+    if constexpr (APPLY) {
+        const float inv = fdiv(1.0f, sig);
 #pragma unroll
-    for (int i = 0; i < 64; ++i) at(i) = fmul(x[i], inv);
-    if (q == 0) scale[line] = fmul(scale[line], sig);
+        for (int i = 0; i < 64; ++i) at(i) = fmul(x[i], inv);
+        if (q == 0) scale[line] = fmul(scale[line], sig);
+    }
+    return fabsf(fsub(sig, 1.0f));
+}
+
+// Block maximum of v (non-negative) into *out, every thread calling; wmax: 16 floats of shared
+// memory that no other block reduction uses until the next __syncthreads after this call.
+__device__ __forceinline__ void block_max_to(float v, float* wmax, float* out) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = wmax[0];
+        for (int i = 1; i < kKvWarps; ++i) m = fmaxf(m, wmax[i]);
+        *out = m;
+    }
 }
 
 // grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: Y [128][257] fp32 and
@@ -824,18 +842,49 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         cp_async_commit();
         cp_async_wait<0>();
     }
-    for (int j = threadIdx.x; j < 256; j += kKvThreads) c[j] = 1.f;
-    if (threadIdx.x < 128) r[threadIdx.x] = 1.f;
-    __syncthreads();
-    for (int t = warp; t < 128; t += kKvWarps) {
-        float v[8];
-        kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
+    // the tile Y from the staged rows, unit scales; the barrier first makes every thread's
+    // staged rows (cp.async, each thread waited only for its own copies) visible to all
+    auto load_tile = [&]() {
+        for (int j = threadIdx.x; j < 256; j += kKvThreads) c[j] = 1.f;
+        if (threadIdx.x < 128) r[threadIdx.x] = 1.f;
+        __syncthreads();
+        for (int t = warp; t < 128; t += kKvWarps) {
+            float v[8];
+            kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) Y[t * kYS + lane + 32 * k] = v[k];
-    }
-    __syncthreads();
+            for (int k = 0; k < 8; ++k) Y[t * kYS + lane + 32 * k] = v[k];
+        }
+        __syncthreads();
+    };
+    load_tile();
 
-    for (int pass = 0; pass < 16; ++pass) {
+    int passes = 16;
+    if (L.kvarn_best) {
+        // the KVarN reference configuration: 8 passes, keeping the state with the smallest
+        // imbalance (largest |sigma - 1| over the lines the last pass left unbalanced). Pass p
+        // measures the state of pass p - 1 on its own axis while it balances it; a measuring
+        // row pass after pass 7 takes the last state's. Then the tile is balanced again from
+        // the staged rows up to the kept pass (the same operations, so the same state).
+        __shared__ float s_wmax[kKvWarps], s_eps[8];
+        __shared__ int s_best;
+        for (int pass = 0; pass < 8; ++pass) {
+            const float dev = (pass & 1) == 0 ? kv_pass<true>(Y, r) : kv_pass<false>(Y, c);
+            if (pass == 0) __syncthreads();
+            else block_max_to(dev, s_wmax, &s_eps[pass - 1]);
+            __syncthreads();
+        }
+        block_max_to(kv_pass<true, false>(Y, r), s_wmax, &s_eps[7]);
+        if (threadIdx.x == 0) {
+            int b = 0;
+            for (int i = 1; i < 8; ++i)
+                if (s_eps[i] < s_eps[b]) b = i;
+            s_best = b;
+        }
+        __syncthreads();
+        passes = s_best + 1;
+        load_tile();
+    }
+    for (int pass = 0; pass < passes; ++pass) {
         if ((pass & 1) == 0) kv_pass<true>(Y, r);
         else kv_pass<false>(Y, c);
         __syncthreads();

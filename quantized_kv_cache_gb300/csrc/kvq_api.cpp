@@ -30,6 +30,8 @@ struct kvq_cache {
     int graph_mode = 1;
     cudaStream_t cap_stream = nullptr;
     cudaGraphExec_t step_exec = nullptr;
+    cudaStream_t mark_stream = nullptr;    // side branch of a captured step for the caller's events
+    cudaEvent_t mark_fork = nullptr;
 };
 
 namespace kvq {
@@ -56,6 +58,7 @@ bool make_layout(const kvq_config& c, Layout* out) {
     if (c.ring_capacity < c.tail + kGroup) return false;   // a full group must fit beyond the tail
     if (c.max_ctx < kSink + kGroup || c.max_ctx > (int64_t)1 << 30) return false;
     if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale)) return false;
+    if (c.kvarn_balance != KVQ_KVARN_FINAL16 && c.kvarn_balance != KVQ_KVARN_BEST8) return false;
     L.L = c.n_layers; L.H = c.n_kv_heads; L.D = c.head_dim; L.Hq = c.n_q_heads; L.G = G;
     L.NQ = G <= 8 ? 8 : 16;
     L.max_seqs = c.max_seqs; L.T = c.tail; L.R = c.ring_capacity;
@@ -65,6 +68,7 @@ bool make_layout(const kvq_config& c, Layout* out) {
     L.journal = c.journal; L.tail_fmt = c.tail_fmt; L.rot = rotation_of(c.k_body);
     L.jrow_bytes = (c.journal == KVQ_TQ6_0) ? (c.head_dim / 128) * 96 : c.head_dim * 2;
     L.scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / std::sqrt((float)c.head_dim);
+    L.kvarn_best = c.kvarn_balance == KVQ_KVARN_BEST8 ? 1 : 0;
     const int64_t units = (int64_t)L.L * L.max_seqs * L.H;
     int64_t off = 256;   // status word area
     L.status_off = 0;
@@ -262,6 +266,8 @@ kvq_status kv_destroy(kvq_cache* c) {
     if (!c) return KVQ_EINVAL;
     if (c->step_exec) cudaGraphExecDestroy(c->step_exec);
     if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+    if (c->mark_stream) cudaStreamDestroy(c->mark_stream);
+    if (c->mark_fork) cudaEventDestroy(c->mark_fork);
     delete c;
     return KVQ_OK;
 }
@@ -697,8 +703,9 @@ namespace {
 
 // The launches of one decode step on `stream` (arguments checked by the caller). The caller's
 // events bracket each layer's decode kernel; ev_flags: cudaEventRecordExternal while the step
-// is captured into a graph (the events then become event-record nodes it can time), else
-// cudaEventRecordDefault.
+// is captured into a graph (the events then become event-record nodes it can time, on a side
+// branch of the graph: the kernels keep their programmatic launches), else
+// cudaEventRecordDefault (the events go inline and the launches are plain).
 kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int n_seq, const void* q,
                          const void* k, const void* v, void* out, int seal_trigger, int keep, void* workspace,
                          size_t ws_bytes, void* const* events, int64_t* groups_sealed, void* stream,
@@ -743,12 +750,16 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
             total += g;
         }
         LaunchMarks marks;
+        const bool side = events && ev_flags == cudaEventRecordExternal;
         if (events) {
             marks.before = events[2 * l];
             marks.after = events[2 * l + 1];
             marks.flags = ev_flags;
-        } else {
-            marks.pdl = pdl_enabled();
+        }
+        if (!events || side) marks.pdl = pdl_enabled();
+        if (side) {
+            marks.side = c->mark_stream;
+            marks.fork = c->mark_fork;
         }
         st = decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace, ws_bytes,
                          fuse ? kl : nullptr, fuse ? vl : nullptr, stream, marks);
@@ -757,6 +768,12 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
                 for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) -= 1;
             return st;
         }
+    }
+    if (events && ev_flags == cudaEventRecordExternal) {
+        // join the events' side branch back into the captured stream
+        if (cudaEventRecord(c->mark_fork, c->mark_stream) != cudaSuccess ||
+            cudaStreamWaitEvent((cudaStream_t)stream, c->mark_fork, 0) != cudaSuccess)
+            return KVQ_ECUDA;
     }
     if (groups_sealed) *groups_sealed = total;
     return KVQ_OK;
@@ -783,6 +800,10 @@ kvq_status kv_decode_step(kvq_cache* c, int n_layers, const int32_t* seq_ids, in
     // go back to where they were if the step cannot be launched
     if (!c->cap_stream && cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking) != cudaSuccess)
         return KVQ_ECUDA;
+    if (events && !c->mark_stream) {
+        if (cudaStreamCreateWithFlags(&c->mark_stream, cudaStreamNonBlocking) != cudaSuccess) return KVQ_ECUDA;
+        if (cudaEventCreateWithFlags(&c->mark_fork, cudaEventDisableTiming) != cudaSuccess) return KVQ_ECUDA;
+    }
     const std::vector<int64_t> n_tok0 = c->n_tok, sealed0 = c->sealed;
     if (cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return KVQ_ECUDA;
     int64_t g = 0;

@@ -137,7 +137,7 @@ struct Layout {
     int32_t fmt[2];          // body format of K, V
     int32_t journal, tail_fmt, rot, jrow_bytes;   // jrow_bytes: bytes of one journal code row
     float scale;             // softmax scale
-    int32_t pad;
+    int32_t kvarn_best;      // KVarN seals: 1 = 8 passes keeping the best state, 0 = 16 passes
     int64_t status_off;
     int64_t sink_off[2], sink_stride[2];
     int64_t jcode_off[2], jcode_stride[2];
@@ -242,6 +242,11 @@ struct LaunchMarks {
     void* after = nullptr;
     unsigned flags = 0;
     bool pdl = false;      // launch the decode and merge kernels with programmatic stream serialization
+    // with side (a stream joined to the capture) and fork (an event) set, each mark is recorded
+    // on the side stream after a fork from the launching stream, so no event node sits between
+    // two kernels and their programmatic launch stays in place
+    void* side = nullptr;
+    void* fork = nullptr;
 };
 int launch_decode(const Layout& lay, const AttnParams& p, void* stream, const LaunchMarks& marks = LaunchMarks());
 int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream,

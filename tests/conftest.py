@@ -6,8 +6,21 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+TESTS = os.path.dirname(os.path.abspath(__file__))
+if TESTS not in sys.path:
+    sys.path.insert(0, TESTS)
 
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+
+
+def pytest_terminal_summary(terminalreporter):
+    import tolerance
+    lines = tolerance.report_lines()
+    if lines:
+        terminalreporter.write_sep("-", "decode attention: observed errors against the fp64 oracle")
+        for line in lines:
+            terminalreporter.write_line(line)
+    tolerance.write_report()

@@ -33,6 +33,7 @@ class Family:
     seed: int = 9
     n_out: int = 4
     factor: float = 16.0
+    balance: str = "final16"      # KVarN balancing: "final16" or "best8"
 
     def config(self):
         c = _lib.kvq_config()
@@ -42,10 +43,12 @@ class Family:
         c.k_body, c.v_body = _lib.FMT_NAMES[self.k_body], _lib.FMT_NAMES[self.v_body]
         c.journal, c.tail_fmt = _lib.FMT_NAMES[self.journal], _lib.FMT_NAMES[self.tail_fmt]
         c.tail, c.ring_capacity, c.softmax_scale = self.T, self.R, 0.0
+        c.kvarn_balance = _lib.KVARN_BALANCE[self.balance]
         return c
 
     def head_config(self):
-        return HeadConfig(self.D, self.k_body, self.v_body, self.journal, self.tail_fmt, self.T, self.R)
+        return HeadConfig(self.D, self.k_body, self.v_body, self.journal, self.tail_fmt, self.T, self.R,
+                          self.balance)
 
 
 FAMILIES = {
@@ -79,6 +82,12 @@ FAMILIES = {
                             contexts=[700, 1300], keep=384, steps=2, n_out=8),
     "turbo3_f16": Family("turbo3_f16", 128, 2, 4, "turbo3", "turbo3", "f16", "f16", T=128, R=1024,
                          contexts=[900, 1413], keep=128, steps=2),
+    # the KVarN reference configuration's balancing (8 passes, the best state kept): 4/4 on a
+    # tq6_0 ring (streaming decode instance) and 3/2 on an F16 journal
+    "kvarn4b8_ring": Family("kvarn4b8_ring", 256, 2, 12, "kvarn4", "kvarn4", "tq6_0", "f16", T=64, R=1024,
+                            contexts=[720, 1500], keep=256, steps=2, n_out=8, seed=13, balance="best8"),
+    "kvarn32b8_f16": Family("kvarn32b8_f16", 256, 1, 8, "kvarn3", "kvarn2", "f16", "f16", T=128, R=768,
+                            contexts=[850, 1290], keep=128, steps=2, n_out=8, seed=14, balance="best8"),
 }
 
 

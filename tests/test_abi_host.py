@@ -87,13 +87,24 @@ def test_kvarn_widths_bytes_per_token(lib):
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 192), ("n_q_heads", 4 * 32), ("ring_capacity", 1000),
-                                         ("tail_fmt", _lib.TQ6_0), ("k_body", _lib.F16), ("v_body", _lib.TBQ4)])
+                                         ("tail_fmt", _lib.TQ6_0), ("k_body", _lib.F16), ("v_body", _lib.TBQ4),
+                                         ("kvarn_balance", 2), ("kvarn_balance", -1)])
 def test_invalid_configs_refused(lib, field, value):
     c = configs.WORKLOADS["hybrid27b_kvarn44"].config()
     setattr(c, field, value)
     with pytest.raises(_lib.KVQError) as e:
         _lib.kv_required_bytes(c)
     assert e.value.code == 1
+
+
+def test_kvarn_balance_rules_accepted(lib):
+    # both balancing rules take the same pool: the records have one layout
+    c = configs.WORKLOADS["hybrid27b_kvarn44"].config()
+    sizes = []
+    for rule in (_lib.KVARN_BALANCE["final16"], _lib.KVARN_BALANCE["best8"]):
+        c.kvarn_balance = rule
+        sizes.append(_lib.kv_required_bytes(c))
+    assert sizes[0] == sizes[1]
 
 
 def test_kvarn_needs_256_multiple(lib):

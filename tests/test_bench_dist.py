@@ -62,3 +62,19 @@ def test_single_rank_needs_no_process_group():
     import bench
     assert bench.dist_max(1.25, 1) == 1.25
     assert bench.weak_value(2e9, 0.5, 1) == pytest.approx(4.0)
+
+
+def test_oracle_units_cover_every_head_step_once():
+    # the reference arm's units: every (KV head, step) of the sample exactly once, in ranges
+    # that a unit can replay in order, and no more units than cores (or KV heads)
+    sys.path.insert(0, ROOT)
+    import bench
+    from quantized_kv_cache_gb300 import configs
+    for name in ("longctx_tbq4", "fa14b_q8q4", "hybrid27b_kvarn44"):
+        w = configs.WORKLOADS[name]
+        for steps, cores in [(1, 16), (4, 16), (25, 16), (3, 2), (64, 8), (2, 72)]:
+            units = bench.oracle_units(w, steps, cores)
+            seen = sorted((h, s) for h, s0, s1 in units for s in range(s0, s1))
+            assert seen == [(h, s) for h in range(w.n_kv_heads) for s in range(steps)]
+            assert len(units) <= max(cores, w.n_kv_heads)
+            assert all(s1 > s0 for _, s0, s1 in units)

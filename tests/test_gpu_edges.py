@@ -115,7 +115,7 @@ def test_degenerate_values_bytes_and_dequant(name):
     ctx = 128 + 128 * n_groups + f0.keep + 50
     f = Family(f0.name + "_deg", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T,
                R=f0.R, contexts=[ctx], keep=f0.keep, steps=0, L=1, seed=f0.seed + 5, n_out=f0.n_out,
-               factor=f0.factor)
+               factor=f0.factor, balance=f0.balance)
     p = EdgePair(f, PATTERNS)
     try:
         _fill(p)
@@ -135,12 +135,12 @@ def test_ragged_lengths_attention(name):
     contexts = [1, 127, 128, 129, 256, 257, 600]
     f = Family(f0.name + "_rag", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T,
                R=f0.R, contexts=contexts, keep=f0.keep, steps=2, L=1, seed=f0.seed + 11, n_out=f0.n_out,
-               factor=f0.factor)
+               factor=f0.factor, balance=f0.balance)
     p = EdgePair(f, ["normal", "zero", "const", "normal"])
     try:
         _fill(p, chunk=97)
         for mult in (1.0, 4.0):
-            _check_attention(p, 0, _q(p, 0, 0, mult))
+            _check_attention(p, 0, _q(p, 0, 0, mult), case=f" edges q{mult:g}x")
         _step_calls(p, f.steps, 1, f.keep)      # kv_decode_step over all seven sequences
         _check_bytes(p)
     finally:
@@ -153,7 +153,7 @@ def test_thirty_two_sequences_in_one_call():
     f0 = FAMILIES["tbq4_ring"]
     contexts = [100 + 61 * i for i in range(32)]
     f = Family("tbq4_ring_32", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T,
-               R=f0.R, contexts=contexts, keep=f0.keep, steps=1, L=1, seed=21, n_out=f0.n_out, factor=f0.factor)
+               R=f0.R, contexts=contexts, keep=f0.keep, steps=1, L=1, seed=21, n_out=f0.n_out, factor=f0.factor, balance=f0.balance)
     p = Pair(f)
     try:
         for s, n0 in zip(p.seqs, f.contexts):
@@ -165,7 +165,7 @@ def test_thirty_two_sequences_in_one_call():
                 pos += c
                 p.seal(0, [s], f.keep)
         assert len(p.seqs) == 32
-        _check_attention(p, 0, _q(p, 0, 0))
+        _check_attention(p, 0, _q(p, 0, 0), case=" edges")
         _step_calls(p, 1, 1, f.keep)
         _check_bytes(p)
     finally:
@@ -180,7 +180,7 @@ def test_fp16_scale_overflow_is_flagged(name):
     ctx = 128 + 128 * 2 + f0.keep + 10
     f = Family(f0.name + "_ovf", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T,
                R=f0.R, contexts=[ctx], keep=f0.keep, steps=0, L=1, seed=f0.seed + 17, n_out=f0.n_out,
-               factor=f0.factor)
+               factor=f0.factor, balance=f0.balance)
     p = EdgePair(f, ["normal", "overflow"])
     try:
         _fill(p)

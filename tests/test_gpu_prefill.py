@@ -61,7 +61,7 @@ def test_prefill_matches_append_then_seal(name):
     chunks = (60, n1 - 60, 2 * f0.R + 71, 40)
     f = Family(f0.name + "_pf", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T,
                R=f0.R, contexts=[sum(chunks)] * 2, keep=f0.keep, steps=0, L=2, seed=f0.seed + 23,
-               n_out=f0.n_out, factor=f0.factor)
+               n_out=f0.n_out, factor=f0.factor, balance=f0.balance)
     p = PrefillPair(f)
     try:
         for layer in range(f.L):
@@ -77,7 +77,7 @@ def test_prefill_matches_append_then_seal(name):
         _check_bytes(p)
         _check_dequant(p)
         for layer in range(f.L):
-            _check_attention(p, layer, _q(p, layer, 0))
+            _check_attention(p, layer, _q(p, layer, 0), case=" prefill")
     finally:
         p.gpu.close()
 
@@ -87,7 +87,7 @@ def test_prefill_refusals():
         pytest.skip("no CUDA device")
     f0 = FAMILIES["tbq4_ring"]
     f = Family("pf_refuse", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T, R=f0.R,
-               contexts=[5000], keep=f0.keep, steps=0, L=1, seed=3)
+               contexts=[5000], keep=f0.keep, steps=0, L=1, seed=3, balance=f0.balance)
     p = PrefillPair(f)
     try:
         H, D = f.H, f.D
