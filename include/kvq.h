@@ -282,6 +282,14 @@ kvq_status kv_get_status(kvq_cache* cache, uint32_t* word);
 kvq_status kv_dequant(kvq_cache* cache, int layer, int seq, int head, int which, int64_t p0,
                       int64_t n, float* out, void* stream);
 
+/* kv_test_wait_timeout — (test call) exercises the streaming kernels' bounded-wait path: one
+ * CTA waits on an mbarrier that no copy completes, with a limit of limit_ns (1 us .. 10 s) of
+ * the GPU's global timer instead of the kernels' 2 s, then waits (2 s bound) for the one bulk
+ * copy it did issue and retires. On return the wait has run out, so after the caller
+ * synchronises, kv_get_status reports bit 1; the context stays usable. KVQ_EINVAL on a limit
+ * out of range. A library test hook with no counterpart in the source pages. */
+kvq_status kv_test_wait_timeout(kvq_cache* cache, uint64_t limit_ns, void* stream);
+
 /* Region ids for kv_region_ptr. */
 enum {
     KVQ_REGION_SINK = 0,        /* fp16 [128][D] */

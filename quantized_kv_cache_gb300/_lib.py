@@ -84,6 +84,7 @@ _SIGS = {
     "kv_snapshot_size": [P, ctypes.POINTER(SZ)],
     "kv_snapshot": [P, P, SZ],
     "kv_restore": [P, P, SZ],
+    "kv_test_wait_timeout": [P, ctypes.c_uint64, P],
     "kvq_synth_fill": [P, I64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_uint64), I64, P, P, P],
 }
 
@@ -238,6 +239,10 @@ def kv_get_status(h):
     if code not in (0, 5):
         raise KVQError("kv_get_status", code)
     return w.value
+
+
+def kv_test_wait_timeout(h, limit_ns, stream=0):
+    _check("kv_test_wait_timeout", load().kv_test_wait_timeout(h, limit_ns, P(stream)))
 
 
 def kv_dequant(h, layer, seq, head, which, p0, n, out_ptr, stream=0):

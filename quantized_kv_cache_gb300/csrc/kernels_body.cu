@@ -108,6 +108,16 @@ __device__ __forceinline__ void load_row_f(const uint16_t* row, float (&f)[N]) {
     }
 }
 
+// The centroid pair of byte k (0..3) of y from the lane-replicated table (entry e of lane l at
+// byte offset 128 e + 4 l of lutb): a byte permute extracts e and one multiply-add forms the
+// offset with lw = 4 l, so the integer pipe, which issues at half rate, takes one instruction
+// per lookup and the multiply-add pipe the other.
+template <int K>
+__device__ __forceinline__ uint32_t lut_pair(const uint8_t* lutb, uint32_t y, uint32_t lw) {
+    const uint32_t e = __byte_perm(y, 0u, 0x4440 | K);
+    return *reinterpret_cast<const uint32_t*>(lutb + (e * 128u + lw));
+}
+
 // 8 codes of a 2-bit plane (16 bits, code m at bits 2m) spread to bits 4m, 4m + 1.
 __device__ __forceinline__ uint32_t spread2(uint32_t x) {
     x = (x | (x << 8)) & 0x00FF00FFu;
@@ -165,12 +175,13 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
 
     constexpr uint32_t recK = Gm::REC_K, recV = Gm::REC_V;
     constexpr uint32_t v_off = Gm::V_OFF, stage_bytes = Gm::STAGE;
-    uint8_t* stages = smem;
-    uint8_t* tailp = smem + (size_t)nst * stage_bytes;
+    // the centroid-pair table first, at a fixed offset (its lookups then need no base address
+    // arithmetic), the record stages after it
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem);
+    uint8_t* stages = smem + (Gm::LUT ? kLutBytes : 0);
+    uint8_t* tailp = stages + (size_t)nst * stage_bytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(tailp);
     uint8_t* cur = tailp + 128;
-    uint32_t* lut = reinterpret_cast<uint32_t*>(cur);
-    cur += Gm::LUT ? kLutBytes : 0;
     uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += Gm::QB_BYTES;
     uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
     float* red = reinterpret_cast<float*>(cur);
@@ -225,6 +236,8 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
             lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
         }
     }
+    const uint8_t* lutb = reinterpret_cast<const uint8_t*>(lut);
+    const uint32_t lw = (uint32_t)lane * 4u;
     __half* qr = reinterpret_cast<__half*>(qb);           // query rows, fp16 [NQ][D], rotated in place
     mbar_wait(qbar, 0, status, &s_abort);
     {
@@ -452,12 +465,17 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                 } else if (KF == KF_TBQ4) {
                     const uint4 y0 = tY0[bk], y1 = tY1[bk];
                     const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
-                    const uint32_t* lt = lut + lane;
 #pragma unroll
                     for (int jj = 0; jj < KSPB; ++jj) {
-                        const int m = jj >> 1, sh = 16 * (jj & 1);
-                        const uint32_t a0 = lt[((Y0[m] >> sh) & 0xFF) * 32], a2 = lt[((Y0[m] >> (sh + 8)) & 0xFF) * 32];
-                        const uint32_t a1r = lt[((Y1[m] >> sh) & 0xFF) * 32], a3 = lt[((Y1[m] >> (sh + 8)) & 0xFF) * 32];
+                        const int m = jj >> 1;
+                        uint32_t a0, a2, a1r, a3;
+                        if (jj & 1) {
+                            a0 = lut_pair<2>(lutb, Y0[m], lw); a2 = lut_pair<3>(lutb, Y0[m], lw);
+                            a1r = lut_pair<2>(lutb, Y1[m], lw); a3 = lut_pair<3>(lutb, Y1[m], lw);
+                        } else {
+                            a0 = lut_pair<0>(lutb, Y0[m], lw); a2 = lut_pair<1>(lutb, Y0[m], lw);
+                            a1r = lut_pair<0>(lutb, Y1[m], lw); a3 = lut_pair<1>(lutb, Y1[m], lw);
+                        }
                         const int j = bk * KSPB + jj;
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -727,7 +745,6 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                 X1[mt][4] = y1b.x; X1[mt][5] = y1b.y; X1[mt][6] = y1b.z; X1[mt][7] = y1b.w;
             }
         }
-        const uint32_t* lt = lut + lane;
         // Q8_0 / Q4_0 values: an all-ones mma sums this warp's P' copy (the code offset term)
         float a1v[NT][4];
 #pragma unroll
@@ -753,9 +770,14 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                         a1r = add_bit5(a1r, H1[mt], bx); a3 = add_bit5(a3, H1[mt], bx + 1);
                     }
                 } else if (VF == KF_TBQ4) {
-                    const int m = kk >> 1, sh = 16 * (kk & 1);
-                    a0 = lt[((X0[mt][m] >> sh) & 0xFF) * 32]; a2 = lt[((X0[mt][m] >> (sh + 8)) & 0xFF) * 32];
-                    a1r = lt[((X1[mt][m] >> sh) & 0xFF) * 32]; a3 = lt[((X1[mt][m] >> (sh + 8)) & 0xFF) * 32];
+                    const int m = kk >> 1;
+                    if (kk & 1) {
+                        a0 = lut_pair<2>(lutb, X0[mt][m], lw); a2 = lut_pair<3>(lutb, X0[mt][m], lw);
+                        a1r = lut_pair<2>(lutb, X1[mt][m], lw); a3 = lut_pair<3>(lutb, X1[mt][m], lw);
+                    } else {
+                        a0 = lut_pair<0>(lutb, X0[mt][m], lw); a2 = lut_pair<1>(lutb, X0[mt][m], lw);
+                        a1r = lut_pair<0>(lutb, X1[mt][m], lw); a3 = lut_pair<1>(lutb, X1[mt][m], lw);
+                    }
                 } else {
                     a0 = i8raw(X0[mt][kk], 0x5140); a2 = i8raw(X0[mt][kk], 0x7362);
                     a1r = i8raw(X1[mt][kk], 0x5140); a3 = i8raw(X1[mt][kk], 0x7362);
@@ -929,7 +951,36 @@ struct LaunchFn {
     int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n_body, n_region, s, pdl); }
 };
 
+// The bounded wait's timeout path, exercised on purpose (a test launch): one CTA, thread 0
+// arms barrier a for a 256-byte bulk copy of the pool's status area and issues it, and arms
+// barrier b for 16 bytes that no copy ever delivers. The wait on b runs out after limit_ns
+// (bit 1 of the status word, the CTA's abort flag); the wait on a, with the flag cleared and a
+// fresh limit, completes, so the CTA retires with no copy in flight.
+__global__ void wait_probe_kernel(const __grid_constant__ Layout L, const void* pool, uint64_t limit_ns) {
+    __shared__ __align__(128) uint8_t buf[256];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int s_abort;
+    if (threadIdx.x != 0) return;
+    uint32_t* status = status_word(L, pool);
+    s_abort = 0;
+    const uint32_t a = su32(&bars[0]), b = su32(&bars[1]);
+    mbar_init(a, 1);
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_expect_tx(a, 256);
+    bulk_g2s(su32(buf), pool, 256, a);
+    mbar_expect_tx(b, 16);
+    mbar_wait_ns(b, 0, status, &s_abort, limit_ns);
+    s_abort = 0;
+    mbar_wait_ns(a, 0, status, &s_abort, kWaitNs);
+}
+
 }  // namespace
+
+int launch_wait_probe(const Layout& L, const void* pool, uint64_t limit_ns, void* stream) {
+    wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(L, pool, limit_ns);
+    return (int)cudaGetLastError();
+}
 
 int upload_tables_body(const FormatTables& t) {
     return (int)cudaMemcpyToSymbol(c_tab, &t, sizeof(FormatTables));

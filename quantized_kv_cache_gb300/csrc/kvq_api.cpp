@@ -885,6 +885,13 @@ kvq_status kv_get_status(kvq_cache* c, uint32_t* word) {
     return w ? KVQ_EDEVICE : KVQ_OK;
 }
 
+kvq_status kv_test_wait_timeout(kvq_cache* c, uint64_t limit_ns, void* stream) {
+    kvq_status st = check_cache(c);
+    if (st != KVQ_OK) return st;
+    if (limit_ns < 1000 || limit_ns > 10000000000ull) return KVQ_EINVAL;
+    return launch_wait_probe(c->lay, c->pool, limit_ns, stream) == 0 ? KVQ_OK : KVQ_ECUDA;
+}
+
 kvq_status kv_dequant(kvq_cache* c, int layer, int seq, int head, int which, int64_t p0, int64_t n, float* out,
                       void* stream) {
     kvq_status st = check_cache(c);

@@ -252,6 +252,7 @@ int launch_decode(const Layout& lay, const AttnParams& p, void* stream, const La
 int launch_decode_fused(const Layout& lay, const AttnParams& p, int n_body, int n_region, void* stream,
                         bool pdl = false);
 int upload_tables_body(const FormatTables& t);
+int launch_wait_probe(const Layout& lay, const void* pool, uint64_t limit_ns, void* stream);
 int body_ctas_per_sm(const Layout& lay);     // resident body-item CTAs per SM (0: no instance)
 int decode_ctas_per_sm(const Layout& lay);   // the same with the region items in the kernel
 int region_kernel_ok(const Layout& lay);     // 1 if the streaming kernel takes the region items

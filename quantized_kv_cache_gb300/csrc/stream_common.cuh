@@ -44,21 +44,26 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
-// Bounded wait on an mbarrier phase. On timeout it sets bit 1 of the status word and the
-// CTA's abort flag; once the flag is set no thread waits again (the CTA runs to its end on
-// stale data, reaching every barrier, and the host learns of it from the status word).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status, volatile int* abort_flag) {
+// Bounded wait on an mbarrier phase (limit_ns of %globaltimer). On timeout it sets bit 1 of
+// the status word and the CTA's abort flag; once the flag is set no thread waits again (the
+// CTA runs to its end on stale data, reaching every barrier, and the host learns of it from
+// the status word).
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, uint32_t* status, volatile int* abort_flag,
+                                             uint64_t limit_ns) {
     if (mbar_try(bar, parity)) return true;
     const uint64_t t0 = gtime();
     while (!mbar_try(bar, parity)) {
         if (*abort_flag) return false;
-        if (gtime() - t0 > kWaitNs) {
+        if (gtime() - t0 > limit_ns) {
             atomicOr(status, 2u);
             *abort_flag = 1;
             return false;
         }
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t* status, volatile int* abort_flag) {
+    return mbar_wait_ns(bar, parity, status, abort_flag, kWaitNs);
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"

@@ -189,3 +189,30 @@ def test_fp16_scale_overflow_is_flagged(name):
         _check_bytes(p)    # the stored bytes, infinite scales included, are the oracle's
     finally:
         p.gpu.close()
+
+
+def test_bounded_wait_runs_out_and_sets_status_bit1():
+    """The streaming kernels' bounded wait: a test launch waits 1 ms on an mbarrier that no copy
+    completes; the wait gives up, bit 1 of the status word is set (kv_get_status reports
+    KVQ_EDEVICE), the launch retires, and the same context then decodes correctly."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f = FAMILIES["tbq4_ring"]
+    p = Pair(f)
+    try:
+        p.prefill()
+        assert _lib.kv_get_status(p.gpu.h) == 0
+        _lib.kv_test_wait_timeout(p.gpu.h, 1_000_000)
+        torch.cuda.synchronize()
+        code = _lib.load().kv_get_status(p.gpu.h, None)
+        assert code == 5                                   # KVQ_EDEVICE, and the word is cleared
+        assert _lib.kv_get_status(p.gpu.h) == 0
+        _lib.kv_test_wait_timeout(p.gpu.h, 1_000_000)
+        torch.cuda.synchronize()
+        assert _lib.kv_get_status(p.gpu.h) == 2            # bit 1 alone
+        with pytest.raises(_lib.KVQError):
+            _lib.kv_test_wait_timeout(p.gpu.h, 10)        # limit out of range
+        _check_attention(p, 0, _q(p, 0, 0), case=" after wait timeout")
+        assert _lib.kv_get_status(p.gpu.h) == 0
+    finally:
+        p.gpu.close()
