@@ -372,7 +372,7 @@ def measure_workload(name, args, world, local_rank, clocks, headline):
 STREAMING = {(128, 8, "tbq4", "tbq4"), (256, 8, "tbq4", "tbq4"), (256, 16, "tbq4", "tbq4"),
              (128, 8, "q8_0", "q4_0"), (128, 16, "q8_0", "q4_0"), (256, 8, "kvarn4", "kvarn4"),
              (256, 16, "kvarn4", "kvarn4"), (512, 8, "kvarn5", "kvarn5"), (512, 16, "kvarn5", "kvarn5"),
-             (256, 8, "kvarn3", "kvarn2")}
+             (256, 8, "kvarn3", "kvarn2"), (128, 8, "q5_1", "q4_0"), (256, 8, "tq5_0", "tbq4")}
 
 
 def launches_per_layer(w):

@@ -38,22 +38,27 @@ struct Geo {
     // K fragment block: the channels one set of score accumulators covers. Q8_0 K is dequantised
     // in registers (code x block scale), so one block spans all D channels and each thread quad
     // owns a contiguous quarter of the row
-    static constexpr int WK = (KF == KF_KVARN) ? 256 : (KF == KF_TBQ4 ? 128 : (KF == KF_Q8 ? D : 32));
+    static constexpr int WK = (KF == KF_KVARN) ? 256 : ((KF == KF_TBQ4 || KF == KF_TQ5) ? 128 :
+                                                       ((KF == KF_Q8 || KF == KF_Q51) ? D : 32));
     static constexpr int NBK = D / WK;
     static constexpr int KSPB = WK / 16;                                // k-steps per K block
     static constexpr int WV = (VF == KF_KVARN) ? 256 : (VF == KF_TBQ4 ? 128 : 32);   // V scale block
     static constexpr int NVB = D / WV;                                  // P' copies
     static constexpr int MT = D / 128;                                  // value m-tiles per warp
-    static constexpr bool KNIB = (KF == KF_KVARN || KF == KF_Q4);       // K pairs (x, x+4)
+    static constexpr bool KNIB = (KF == KF_KVARN || KF == KF_Q4 || KF == KF_Q51 || KF == KF_TQ5);   // K pairs (x, x+4)
     static constexpr bool VNIB = (VF == KF_KVARN || VF == KF_Q4);
     // value the raw fp16 operand reads for code 0 (the code's own centre included)
-    static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : 0.f);
+    // Q5_1 keys are dequantised in the fragments (code x d + m); tq5_0 keys read 64 + code, the
+    // code's centre 16 included
+    static constexpr float KOFF = (KF == KF_KVARN) ? 64.f : (KF == KF_Q4 ? 72.f : (KF == KF_TQ5 ? 80.f : 0.f));
     static constexpr float VOFF = (VF == KF_KVARN) ? 64.f : (VF == KF_Q4 ? 72.f : (VF == KF_Q8 ? 1152.f : 0.f));
     static constexpr bool ZV = (VF == KF_KVARN);                        // per-group value zero-point sums
     static constexpr bool PSV = (VF == KF_Q8 || VF == KF_Q4);           // sum of P' per group (offset)
     static constexpr bool LUT = (KF == KF_TBQ4) || (VF == KF_TBQ4);
     static constexpr int rec(int f, int b) {
-        return f == KF_KVARN ? (D / 256) * (4096 * b + 1152) : (f == KF_TBQ4 ? 66 * D : (f == KF_Q8 ? 136 * D : 72 * D));
+        return f == KF_KVARN ? (D / 256) * (4096 * b + 1152)
+                             : (f == KF_TBQ4 ? 66 * D : (f == KF_Q8 ? 136 * D : (f == KF_Q51 ? 96 * D :
+                                                                                 (f == KF_TQ5 ? 82 * D : 72 * D))));
     }
     static constexpr int REC_K = rec(KF, KB), REC_V = rec(VF, VB);
     static constexpr int V_OFF = (REC_K + 127) & ~127;
@@ -407,7 +412,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
             // TBQ4: blocks of 128 channels, 16 bytes of this row and block per thread; with two
             // blocks, odd rows read them in the other order so a quarter warp hits 32 banks
             uint4 tY0[NBK], tY1[NBK];
-            if (KF == KF_TBQ4) {
+            if (KF == KF_TBQ4 || KF == KF_TQ5) {
                 const bool sw = (NBK == 2) && (g & 1);
 #pragma unroll
                 for (int bk = 0; bk < NBK; ++bk) {
@@ -528,6 +533,64 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                             mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
                         }
                     }
+                } else if (KF == KF_TQ5) {
+                    // tq5_0: this thread's 32 channels of the 128-channel block (16 bytes of the
+                    // nibble plane, preloaded) and their fifth bits (4 bytes of the one-bit plane,
+                    // bit 8 m + e for channel 8 m + e): 64 + code, scale after the mma
+                    const uint4 y0 = tY0[bk], y1 = tY1[bk];
+                    const uint32_t Y0[4] = {y0.x, y0.y, y0.z, y0.w}, Y1[4] = {y1.x, y1.y, y1.z, y1.w};
+                    const uint32_t H0 = *reinterpret_cast<const uint32_t*>(kr + 64 * D + t0 * (D / 8) + 16 * bk + 4 * tq);
+                    const uint32_t H1 = *reinterpret_cast<const uint32_t*>(kr + 64 * D + t1 * (D / 8) + 16 * bk + 4 * tq);
+#pragma unroll
+                    for (int jj = 0; jj < KSPB; ++jj) {
+                        const int m = jj >> 1, x = 2 * (jj & 1), bx = 8 * m + x;
+                        const uint32_t a0 = add_bit5(nib64(Y0[m], x), H0, bx), a2 = add_bit5(nib64(Y0[m], x + 1), H0, bx + 1);
+                        const uint32_t a1r = add_bit5(nib64(Y1[m], x), H1, bx), a3 = add_bit5(nib64(Y1[m], x + 1), H1, bx + 1);
+                        const int j = bk * KSPB + jj;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
+                        }
+                    }
+                } else if (KF == KF_Q51) {
+                    // Q5_1 (D = 128): thread quad tq holds the 32-channel block tq (16 bytes of
+                    // nibbles, 4 bytes of fifth bits per row) and dequantises in the fragments:
+                    // (64 + code - 64) x d + m in fp16, one rounding. Odd rows load t1 before t0,
+                    // so a quarter warp's two rows lie 64 bytes apart (all 32 banks).
+                    static_assert(KF != KF_Q51 || D == 128, "Q5_1 keys: one 32-channel block per thread quad");
+                    const int odd = g & 1;
+                    const int ra = odd ? t1 : t0, rb = odd ? t0 : t1;
+                    uint4 ya = *reinterpret_cast<const uint4*>(kr + ra * (D / 2) + 16 * tq);
+                    uint4 yb = *reinterpret_cast<const uint4*>(kr + rb * (D / 2) + 16 * tq);
+                    if (odd) { const uint4 t = ya; ya = yb; yb = t; }
+                    const uint32_t Y0[4] = {ya.x, ya.y, ya.z, ya.w}, Y1[4] = {yb.x, yb.y, yb.z, yb.w};
+                    const uint32_t H0 = *reinterpret_cast<const uint32_t*>(kr + 64 * D + t0 * (D / 8) + 4 * tq);
+                    const uint32_t H1 = *reinterpret_cast<const uint32_t*>(kr + 64 * D + t1 * (D / 8) + 4 * tq);
+                    const uint16_t* dr = reinterpret_cast<const uint16_t*>(kr + 80 * D);
+                    const uint16_t* mr = reinterpret_cast<const uint16_t*>(kr + 88 * D);
+                    const uint32_t d0 = dr[t0 * 4 + tq], d1 = dr[t1 * 4 + tq];
+                    const uint32_t m0 = mr[t0 * 4 + tq], m1 = mr[t1 * 4 + tq];
+                    const __half2 dd0 = as_h2(d0 | (d0 << 16)), dd1 = as_h2(d1 | (d1 << 16));
+                    const __half2 mm0 = as_h2(m0 | (m0 << 16)), mm1 = as_h2(m1 | (m1 << 16));
+                    const __half2 c64 = __float2half2_rn(64.f);
+                    auto deq = [&](uint32_t raw, __half2 d, __half2 mz) {
+                        return as_u(__hfma2(__hsub2(as_h2(raw), c64), d, mz));
+                    };
+#pragma unroll
+                    for (int jj = 0; jj < KSPB; ++jj) {
+                        const int m = jj >> 1, x = 2 * (jj & 1), bx = 8 * m + x;
+                        const uint32_t a0 = deq(add_bit5(nib64(Y0[m], x), H0, bx), dd0, mm0);
+                        const uint32_t a2 = deq(add_bit5(nib64(Y0[m], x + 1), H0, bx + 1), dd0, mm0);
+                        const uint32_t a1r = deq(add_bit5(nib64(Y1[m], x), H1, bx), dd1, mm1);
+                        const uint32_t a3 = deq(add_bit5(nib64(Y1[m], x + 1), H1, bx + 1), dd1, mm1);
+                        const int j = bk * KSPB + jj;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const uint2 bq = QREG ? qf[QREG ? j : 0] : qb2[((nt * KS + j) * 8 + g) * 4 + tq];
+                            mma16816(acc[bk][nt][jj & 1], a0, a1r, a2, a3, bq.x, bq.y);
+                        }
+                    }
                 } else {   // Q4_0 K: one word of 8 nibbles per row and block
                     const uint32_t w0 = *reinterpret_cast<const uint32_t*>(kr + t0 * (D / 2) + 16 * bk + 4 * tq);
                     const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kr + t1 * (D / 2) + 16 * bk + 4 * tq);
@@ -557,9 +620,9 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
             // s = sum over K blocks of e(t) (acc - off sum q') + z(t) sum q', log2 domain; the
             // per-position block scales of TBQ4 / Q8_0 / Q4_0 come in one vector load per row
             float ek0[NBK], ek1[NBK];
-            if (KF != KF_KVARN && KF != KF_Q8) {
+            if (KF != KF_KVARN && KF != KF_Q8 && KF != KF_Q51) {
                 const uint16_t* er = reinterpret_cast<const uint16_t*>(
-                    kr + (KF == KF_TBQ4 ? 64 : (KF == KF_Q8 ? 128 : 64)) * D);
+                    kr + (KF == KF_TBQ4 ? 64 : (KF == KF_TQ5 ? 80 : 64)) * D);
                 load_row_f<NBK>(er + t0 * NBK, ek0);
                 load_row_f<NBK>(er + t1 * NBK, ek1);
             }
@@ -578,7 +641,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
                         zk[bk][nt][0] = a1[bk][nt][0][0];
                         zk[bk][nt][1] = a1[bk][nt][0][1];
                     }
-                } else if (KF == KF_Q8) {
+                } else if (KF == KF_Q8 || KF == KF_Q51) {
                     e0 = e1 = 1.f;                  // dequantised in the fragments
                 } else {
                     e0 = ek0[bk];
@@ -920,6 +983,8 @@ int dispatch(const Layout& L, F&& f) {
     KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 3, 2, KVQ_KVARN3, KVQ_KVARN2)
     KVQ_BODY_CASE(512, 8, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
     KVQ_BODY_CASE(512, 16, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
+    KVQ_BODY_CASE(128, 8, KF_Q51, KF_Q4, 5, 4, KVQ_Q5_1, KVQ_Q4_0)
+    KVQ_BODY_CASE(256, 8, KF_TQ5, KF_TBQ4, 5, 4, KVQ_TQ5_0, KVQ_TBQ4)
 #undef KVQ_BODY_CASE
     return -1;
 }

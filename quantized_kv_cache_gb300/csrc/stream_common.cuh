@@ -19,7 +19,10 @@ constexpr float kTbqScale = 0.0883883461356163f;
 constexpr int kLutBytes = 256 * 32 * 4;
 constexpr uint64_t kWaitNs = 2000000000ull;          // bounded waits: 2 s, then the status word is set
 
-enum { KF_KVARN = 0, KF_TBQ4 = 1, KF_Q8 = 2, KF_Q4 = 3 };
+// fragment decoder families of the streaming decode kernel: KVarN codes, TBQ4 centroid pairs,
+// Q8_0 / Q4_0 blocks, and (keys only) Q5_1 (min-offset 5-bit blocks of 32) and tq5_0 (rotated
+// symmetric 5-bit blocks of 128)
+enum { KF_KVARN = 0, KF_TBQ4 = 1, KF_Q8 = 2, KF_Q4 = 3, KF_Q51 = 4, KF_TQ5 = 5 };
 
 // ------------------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }

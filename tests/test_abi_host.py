@@ -163,7 +163,8 @@ def test_bench_streaming_table_matches_the_dispatch_table():
     src = open(os.path.join(os.path.dirname(__file__), "..", "quantized_kv_cache_gb300", "csrc",
                             "kernels_body.cu")).read()
     names = {"KVQ_TBQ4": "tbq4", "KVQ_Q8_0": "q8_0", "KVQ_Q4_0": "q4_0", "KVQ_KVARN2": "kvarn2",
-             "KVQ_KVARN3": "kvarn3", "KVQ_KVARN4": "kvarn4", "KVQ_KVARN5": "kvarn5"}
+             "KVQ_KVARN3": "kvarn3", "KVQ_KVARN4": "kvarn4", "KVQ_KVARN5": "kvarn5", "KVQ_Q5_1": "q5_1",
+             "KVQ_TQ5_0": "tq5_0"}
     cases = set()
     for m in re.finditer(r"KVQ_BODY_CASE\((\d+), (\d+), \w+, \w+, \d, \d, (\w+), (\w+)\)", src):
         cases.add((int(m.group(1)), int(m.group(2)), names[m.group(3)], names[m.group(4)]))
