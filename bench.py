@@ -78,11 +78,13 @@ def peaks():
 # the line reports null until a new capture replaces it.
 DECODE_SOURCES = ("kernels_body.cu", "region_item.cuh", "stream_common.cuh", "device_common.cuh", "append_row.cuh")
 MEASURED_TRAFFIC = {
-    "hybrid27b_kvarn44": (42.83e6, "e84f547e1507"),
-    "fa14b_q8q4": (221.90e6, "e84f547e1507"),
-    "longctx_tbq4": (749.80e6, "e84f547e1507"),
-    "widehead_kvarn55": (190.77e6, "e84f547e1507"),
-    "hybrid27b_kvarn32_200k": (156.86e6, "e84f547e1507"),
+    "hybrid27b_kvarn44": (42.83e6, "22e1bf295f36"),
+    "fa14b_q8q4": (221.91e6, "22e1bf295f36"),
+    "longctx_tbq4": (750.26e6, "22e1bf295f36"),
+    "widehead_kvarn55": (190.97e6, "22e1bf295f36"),
+    "hybrid27b_kvarn32_200k": (156.71e6, "22e1bf295f36"),
+    "fa14b_q51q40": (180.32e6, "22e1bf295f36"),
+    "hybrid27b_tq50tbq4_110k": (138.13e6, "22e1bf295f36"),
 }
 
 
