@@ -467,9 +467,11 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
                                 inp.v[s].data_ptr(), out.data_ptr(), -1, w.keep, cache.ws.data_ptr(),
                                 cache.ws_bytes, None, stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("bulk_seal")
         ev0.record()
         groups = _lib.kv_seal(cache.h, -1, seq_ids, w.keep, stream)
         ev1.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         t = ev0.elapsed_time(ev1) / 1e3
         kind = "bulk seal, all layers, one launch"
