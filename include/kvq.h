@@ -182,8 +182,10 @@ kvq_status kv_prefill(kvq_cache* cache, int layer, const int32_t* seq_ids, int n
  * n_tokens positions with sealed end sealed_end: ranges (host, 8 values) receives the head
  * [r0, r1) appended to the journal and sink, the groups [r2, r3) then sealed from the journal,
  * the groups [r4, r5) sealed straight from the input rows, and the rest [r6, r7) appended to the
- * journal and exact tail; r5 is the sealed end after the call. The same refusals as kv_prefill
- * (KVQ_ENOSPC), KVQ_EINVAL on a null pointer or n_tok <= 0. Pure host arithmetic. */
+ * journal and exact tail; r5 is the sealed end after the call. kv_prefill takes its counts,
+ * offsets and rows from this same plan. The same refusals as kv_prefill (KVQ_ENOSPC); KVQ_EINVAL
+ * on a null pointer, n_tok <= 0, or a sealed_end that is not 128 plus a multiple of 128. Pure
+ * host arithmetic. */
 kvq_status kv_prefill_plan(int64_t n_tokens, int64_t sealed_end, int64_t n_tok, int32_t keep, int32_t ring_capacity,
                            int64_t max_ctx, int64_t ranges[8]);
 

@@ -213,11 +213,24 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     const uint16_t* qsrc = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
     const uint32_t qbar = su32(&full[4]);
     int issued = 0;
+    const int g = lane >> 2, tq = lane & 3;
+    // set-up that touches no global memory (the item from the launch parameters, the barriers,
+    // the centroid-pair table from constant memory) runs before the wait for the launch ahead:
+    // with programmatic serialization the CTA is placed while that launch drains
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int i = 0; i < nst; ++i) mbar_init(su32(&full[i]), 1);
         mbar_init(qbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (Gm::LUT) {
+        for (int i = threadIdx.x; i < 256 * 32; i += kCT) {
+            const int by = i >> 5;
+            lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
+        }
+    }
+    grid_dep_wait();
+    if (threadIdx.x == 0) {
         mbar_expect_tx(qbar, (uint32_t)(G * D * 2));
         bulk_g2s(su32(qb), qsrc, (uint32_t)(G * D * 2), qbar);
         for (; issued < min(nst, ngroups); ++issued) issue(issued);
@@ -234,13 +247,6 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     }
 
     // ================================================================== consumers: set-up
-    const int g = lane >> 2, tq = lane & 3;
-    if (Gm::LUT) {
-        for (int i = threadIdx.x; i < 256 * 32; i += kCT) {
-            const int by = i >> 5;
-            lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
-        }
-    }
     const uint8_t* lutb = reinterpret_cast<const uint8_t*>(lut);
     const uint32_t lw = (uint32_t)lane * 4u;
     __half* qr = reinterpret_cast<__half*>(qb);           // query rows, fp16 [NQ][D], rotated in place
@@ -927,8 +933,7 @@ decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ Att
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     // launched with programmatic serialization, the CTAs may be placed while the launch ahead
-    // drains: nothing is read or written in global memory before it has completed
-    grid_dep_wait();
+    // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory
     if ((int)blockIdx.x < n_body)
         body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
     else

@@ -383,36 +383,36 @@ int append_ranges(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, co
 }  // namespace
 
 namespace {
-// One sequence's prefill plan: N0 positions held, S0 sealed end, n_tok new positions. S1 is the
-// sealed end after the call (every full group older than the newest keep sealed) and M the end
-// of the head range (see kv_prefill). KVQ_ENOSPC when the call would pass max_ctx or leave more
-// unsealed positions than the ring holds.
+// One sequence's prefill plan: N0 positions held, S0 sealed end (a group boundary), n_tok new
+// positions. r receives the eight bounds kv_prefill works with: the head [r0, r1) appended to the
+// journal and sink, the groups [r2, r3) then sealed from the journal, the groups [r4, r5) sealed
+// straight from the input rows (r5 = S1, the sealed end after the call: every full group older
+// than the newest keep sealed), and the rest [r6, r7) appended to the journal and exact tail.
+// With M = min(first group start >= N0, S1, N1): r1 = max(N0, M); r3 = r4 = the journal seal's
+// end. KVQ_ENOSPC when the call would pass max_ctx or leave more unsealed positions than the
+// ring holds.
 kvq_status prefill_plan(int64_t N0, int64_t S0, int64_t n_tok, int64_t keep, int64_t R, int64_t max_ctx,
-                        int64_t* S1, int64_t* M) {
+                        int64_t r[8]) {
     const int64_t N1 = N0 + n_tok;
     if (N1 > max_ctx) return KVQ_ENOSPC;
     const int64_t lim = N1 - keep - S0;
-    *S1 = S0 + (lim >= kGroup ? lim / kGroup * kGroup : 0);
-    if (std::max<int64_t>(N1, kSink) - *S1 > R) return KVQ_ENOSPC;
+    const int64_t S1 = S0 + (lim >= kGroup ? lim / kGroup * kGroup : 0);
+    if (std::max<int64_t>(N1, kSink) - S1 > R) return KVQ_ENOSPC;
     const int64_t first_in = N0 <= kSink ? kSink : kSink + (N0 - kSink + kGroup - 1) / kGroup * kGroup;
-    *M = std::min(std::min(first_in, *S1), N1);
+    const int64_t M = std::min(std::min(first_in, S1), N1);
+    const int64_t Sj = S0 + std::max<int64_t>(0, M - S0) / kGroup * kGroup;
+    const int64_t plan[8] = {N0, std::max(N0, M), S0, Sj, Sj, S1, std::max(N0, std::min(S1, N1)), N1};
+    for (int i = 0; i < 8; ++i) r[i] = plan[i];
     return KVQ_OK;
 }
 }  // namespace
 
 kvq_status kv_prefill_plan(int64_t n_tokens, int64_t sealed_end, int64_t n_tok, int32_t keep, int32_t ring_capacity,
                            int64_t max_ctx, int64_t ranges[8]) {
-    if (!ranges || n_tok <= 0 || keep < 0 || ring_capacity <= 0 || n_tokens < 0 || sealed_end < kSink)
+    if (!ranges || n_tok <= 0 || keep < 0 || ring_capacity <= 0 || n_tokens < 0 || sealed_end < kSink ||
+        (sealed_end - kSink) % kGroup != 0)
         return KVQ_EINVAL;
-    int64_t S1 = 0, M = 0;
-    const kvq_status st = prefill_plan(n_tokens, sealed_end, n_tok, keep, ring_capacity, max_ctx, &S1, &M);
-    if (st != KVQ_OK) return st;
-    const int64_t N0 = n_tokens, N1 = N0 + n_tok;
-    const int64_t Sj = sealed_end + std::max<int64_t>(0, M - sealed_end) / kGroup * kGroup;
-    const int64_t Sd = Sj + std::max<int64_t>(0, S1 - Sj) / kGroup * kGroup;
-    const int64_t r[8] = {N0, std::max(N0, M), sealed_end, Sj, Sj, Sd, std::max(N0, std::min(S1, N1)), N1};
-    for (int i = 0; i < 8; ++i) ranges[i] = r[i];
-    return KVQ_OK;
+    return prefill_plan(n_tokens, sealed_end, n_tok, keep, ring_capacity, max_ctx, ranges);
 }
 
 kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, int n_tok, const void* k,
@@ -423,19 +423,18 @@ kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq
         keep < c->cfg.tail)
         return KVQ_EINVAL;
     if ((st = check_seqs(c, seq_ids, n_seq)) != KVQ_OK) return st;
-    // Per sequence (N0, S0 before; N1, S1 after): positions [N0, N1) split into
-    //   head   [N0, max(N0, M))  the journal (and the sink): the chunk's part of groups that
-    //                            started before N0, sealed from the journal right after
-    //   direct [M, S1)           groups wholly in the chunk, sealed straight from the input
-    //   rest   [max(N0, S1), N1) the journal and, for the newest T, the exact tail
-    // with M = min(first group start >= N0, S1, N1). (S1 exceeds N1 only while the sequence is
-    // still inside the sink: S1 = 128 > N1.)
-    int64_t n0[kMaxSeqPerCall], s1[kMaxSeqPerCall], m[kMaxSeqPerCall];
+    // Per sequence (N0, S0 before; N1, S1 after), the plan of prefill_plan (the function the
+    // test call kv_prefill_plan exposes): positions [N0, N1) split into
+    //   head   [r0, r1)  the journal (and the sink): the chunk's part of groups that started
+    //                    before N0, whose groups [r2, r3) are sealed from the journal right after
+    //   direct [r4, r5)  groups wholly in the chunk, sealed straight from the input rows
+    //   rest   [r6, r7)  the journal and, for the newest T, the exact tail
+    // (r5 = S1 exceeds N1 only while the sequence is still inside the sink: S1 = 128 > N1.)
+    int64_t r[kMaxSeqPerCall][8];
     for (int i = 0; i < n_seq; ++i) {
         const int s = seq_ids[i];
-        n0[i] = NT(c, layer, s);
-        const kvq_status e = prefill_plan(n0[i], ST(c, layer, s), n_tok, keep, c->cfg.ring_capacity,
-                                          c->cfg.max_ctx, &s1[i], &m[i]);
+        const kvq_status e = prefill_plan(NT(c, layer, s), ST(c, layer, s), n_tok, keep, c->cfg.ring_capacity,
+                                          c->cfg.max_ctx, r[i]);
         if (e != KVQ_OK) return e;
     }
     int64_t cnt[kMaxSeqPerCall], off[kMaxSeqPerCall], tfrom[kMaxSeqPerCall], groups[kMaxSeqPerCall];
@@ -443,31 +442,30 @@ kvq_status kv_prefill(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq
     int64_t total = 0;
     // head, then the groups it completes (from the journal)
     for (int i = 0; i < n_seq; ++i) {
-        cnt[i] = std::max<int64_t>(n0[i], m[i]) - n0[i];
+        cnt[i] = r[i][1] - r[i][0];
         off[i] = 0;
         tfrom[i] = INT64_MAX;               // older than the newest T: no tail writes
     }
     if (append_ranges(c, layer, seq_ids, n_seq, k, v, n_tok, cnt, off, tfrom, stream)) return KVQ_ECUDA;
     for (int i = 0; i < n_seq; ++i) {
-        groups[i] = std::max<int64_t>(0, m[i] - ST(c, layer, seq_ids[i])) / kGroup;
+        groups[i] = (r[i][3] - r[i][2]) / kGroup;
         total += groups[i];
     }
     if (seal_counts(c, layer, seq_ids, n_seq, groups, nullptr, nullptr, 0, nullptr, stream)) return KVQ_ECUDA;
     // the groups wholly in the chunk, from the input rows
     for (int i = 0; i < n_seq; ++i) {
-        groups[i] = std::max<int64_t>(0, s1[i] - ST(c, layer, seq_ids[i])) / kGroup;
-        row[i] = (int64_t)i * n_tok + (ST(c, layer, seq_ids[i]) - n0[i]);
+        groups[i] = (r[i][5] - r[i][4]) / kGroup;
+        row[i] = (int64_t)i * n_tok + (r[i][4] - r[i][0]);
         total += groups[i];
     }
     if (seal_counts(c, layer, seq_ids, n_seq, groups, k, v, n_tok, row, stream)) return KVQ_ECUDA;
     // the rest: the direct groups' positions count as appended (their journal slots stay unwritten)
     for (int i = 0; i < n_seq; ++i) {
         const int s = seq_ids[i];
-        const int64_t start = std::max(n0[i], std::min(s1[i], n0[i] + n_tok));
-        NT(c, layer, s) = start;
-        cnt[i] = n0[i] + n_tok - start;
-        off[i] = start - n0[i];
-        tfrom[i] = n0[i] + n_tok - c->cfg.tail;
+        NT(c, layer, s) = r[i][6];
+        cnt[i] = r[i][7] - r[i][6];
+        off[i] = r[i][6] - r[i][0];
+        tfrom[i] = r[i][7] - c->cfg.tail;
     }
     if (append_ranges(c, layer, seq_ids, n_seq, k, v, n_tok, cnt, off, tfrom, stream)) return KVQ_ECUDA;
     if (groups_sealed) *groups_sealed = total;

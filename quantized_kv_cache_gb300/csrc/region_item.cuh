@@ -137,6 +137,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     const uint32_t half_bytes = ring ? Gm::TQ_HALF : Gm::F_HALF;
     const int nst = min(4, Gm::AREA / (int)stage_bytes);
     if (nst < 2 || (!Gm::RING && kind == RK_RING)) {   // a ring at head_dim 512 is not routed here: refuse
+        grid_dep_wait();
         if (threadIdx.x == 0) atomicOr(status_word(L, p.pool), 4u);
         return;
     }
@@ -209,10 +210,13 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     const uint16_t* qsrc = p.q + ((int64_t)b * L.Hq + (int64_t)h * G) * D;
     const uint32_t qbar = su32(&full[4]);
     int issued = 0;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {   // barriers first: no global memory is touched before the wait
         s_abort = 0;
         for (int i = 0; i < 5; ++i) mbar_init(su32(&full[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    grid_dep_wait();          // the launch ahead (programmatic serialization) has completed
+    if (threadIdx.x == 0) {
         mbar_expect_tx(qbar, (uint32_t)(G * D * 2));
         bulk_g2s(su32(qb), qsrc, (uint32_t)(G * D * 2), qbar);
         for (; issued < min(nst, nrun); ++issued) issue(issued);

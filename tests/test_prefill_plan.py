@@ -85,6 +85,11 @@ def test_plan_refusals(lib):
     with pytest.raises(_lib.KVQError) as e:
         _lib.kv_prefill_plan(0, 128, 0, 128, 512, 1 << 20)
     assert e.value.code == 1
+    # a sealed end off the group grid (the library only ever holds 128 + 128 k)
+    for bad in (129, 200, 255, 127):
+        with pytest.raises(_lib.KVQError) as e:
+            _lib.kv_prefill_plan(1000, bad, 100, 128, 1024, 1 << 20)
+        assert e.value.code == 1
     # the whole context in one call: everything older than keep sealed straight from the input
     r = _lib.kv_prefill_plan(0, 128, 131072, 1024, 5248, 1 << 20)
     assert r[:2] == [0, 128] and r[2:4] == [128, 128] and r[4:6] == [128, 130048] and r[6:] == [130048, 131072]
