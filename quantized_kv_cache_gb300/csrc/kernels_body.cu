@@ -934,10 +934,16 @@ decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ Att
     __shared__ int s_abort;
     // launched with programmatic serialization, the CTAs may be placed while the launch ahead
     // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory
-    if ((int)blockIdx.x < n_body)
+    if (p.region_first) {
+        if ((int)blockIdx.x < p.n_region_items)
+            region_item<D, NQ>(L, p, (int)blockIdx.x, smem, s_abort);
+        else
+            body_item<D, NQ, KF, VF, KB, VB>(L, p, (int)blockIdx.x, nst, smem, s_abort);
+    } else if ((int)blockIdx.x < n_body) {
         body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
-    else
+    } else {
         region_item<D, NQ>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
+    }
 }
 
 // ------------------------------------------------------------------------------ launch

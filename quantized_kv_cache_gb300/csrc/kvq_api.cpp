@@ -533,6 +533,12 @@ kvq_status kv_seal(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, i
 
 namespace {
 
+// An integer from the environment (A/B switches of launch choices), else the default.
+int getenv_int(const char* name, int dflt) {
+    const char* e = std::getenv(name);
+    return (e && e[0]) ? std::atoi(e) : dflt;
+}
+
 // Decode attention of one layer; with knew / vnew (the newest position's rows, fp16, already
 // counted in N) the decode kernel also appends them (the fused decode step).
 kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
@@ -662,6 +668,12 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     }
     p.ring_chunk = (int32_t)ring_chunk;
     p.chunk = (int32_t)chunk;
+    // region items at least a wave of resident CTAs (the long tq6_0 ring spans of longctx) go
+    // first: launched after the body items they formed a tail of their own
+    if (fused && getenv_int("KVQ_REGION_FIRST", 1)) {
+        const int64_t slots = (int64_t)std::max(1, decode_ctas_per_sm(L)) * c->sm_count;
+        p.region_first = p.n_region_items >= slots ? 1 : 0;
+    }
     const int e = launch_decode(L, p, stream, marks);
     return e == 0 ? KVQ_OK : KVQ_ECUDA;
 }

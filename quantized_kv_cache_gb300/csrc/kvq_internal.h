@@ -182,6 +182,7 @@ struct AttnParams {
     int32_t layer, n_seq, chunk, total_items;
     int32_t n_region_items;  // region items come first, body items after them
     int32_t ring_chunk;      // positions per region item of a tq6_0 ring span (others: chunk)
+    int32_t region_first;    // the streaming kernel's first blocks take the region items (else the body items)
     SeqSpan seq[kMaxSeqPerCall];
 };
 
