@@ -645,19 +645,17 @@ int launch_family(const Layout& L, const SealParams& p, int n_tiles, cudaStream_
 // One 128 x 256 tile (SJ-KVaRN §2.2): HAD256-rotated journal rows, 16 alternating row/column
 // passes of spread balancing (rows first), per-row b-bit rounding with fp16 scales (SJ-KVaRN
 // §2.2, §3). CTA = 16 warps on one tile = (group, KV head, K or V, 256-channel half). The
-// tile's journal rows are staged once with cp.async; both reads of the rows (into the fp32
-// tile Y, and again for the codes, which use the unbalanced values) decode them from shared
-// memory. A balancing pass gives each row to 4 threads (each column to 2) holding 64 values
-// apiece, so most levels of the halving sums run in registers. The arithmetic is the
+// tile's journal rows are staged once with cp.async and decoded from shared memory twice (into
+// the balanced tile, and again for the codes, which use the unbalanced values). The balanced
+// tile lives in registers: thread (warp w, lane l) holds the 64 values of rows w + 16 a and
+// columns l + 32 b (a, b < 8). A line's halving-tree sums take their first three levels in the
+// thread (value pairs a, a + 4 / a, a + 2 / a, a + 1, likewise for b); the last five levels of
+// a row cross the warp's lanes (shuffles), the last four of a column cross the 16 warps through
+// 16 KB of shared memory. So a pass moves partial sums, not the tile. The arithmetic is the
 // codec's, operation for operation.
-constexpr int kYS = 260;            // Y row stride (floats): 4 t + q covers the 32 banks in a row pass
 constexpr int kKvThreads = 512;
 constexpr int kKvWarps = kKvThreads / 32;
 
-__device__ __forceinline__ float warp_min(float v) {
-    for (int s = 16; s >= 1; s >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, s));
-    return v;
-}
 template <int JK>
 struct KvStage {
     static constexpr int ROW = (JK == J_TQ6) ? 192 : 512;    // one row of the half (2 tq6_0 blocks / 256 x 16 bit)
@@ -722,52 +720,128 @@ __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, in
     }
 }
 
-// One balancing pass over the tile, lines of n = 256 (rows) or 128 (columns) values: mean
-// and population spread by halving trees, sigma <= 2^-20 counts as 1, line /= sigma, the
-// line's scale *= sigma. A line belongs to P = n / 64 threads (adjacent lanes); thread q
-// holds the values q + P i (i < 64), so the tree levels of stride >= P are in-thread and the
-// last log2(P) levels cross the P lanes (every lane ends with the same sum, the adds being
-// commutative). ROWS: 128 rows x 4 threads; else 256 columns x 2 threads. Returns |sigma - 1|
-// of this thread's line (the imbalance the state before the pass has on this axis); with
-// APPLY false the pass only measures it.
-template <bool ROWS, bool APPLY = true>
-__device__ __forceinline__ float kv_pass(float* Y, float* scale) {
-    constexpr int P = ROWS ? 4 : 2;
-    constexpr float INV_N = ROWS ? 1.0f / 256.0f : 1.0f / 128.0f;
-    const int line = threadIdx.x / P, q = threadIdx.x % P;
-    // element i of this thread: row-major index of value q + P i of the line
-    auto at = [&](int i) -> float& {
-        return ROWS ? Y[line * kYS + q + P * i] : Y[(q + P * i) * kYS + line];
-    };
-    float x[64];
+// The reduction of 8 per-row values (v[k]: row k of this thread's rows) over the warp's 32
+// lanes in the order of a halving tree over lane positions (lane pairs l, l + 16, then l + 8,
+// l + 4, l + 2, l + 1). In the first three levels each lane of a pair keeps the half of the
+// rows its lane bit selects and adds the partner's partial of that half, so every lane ends
+// with the total of row lane / 4 (row 4 (l & 16 ? 1 : 0) + 2 (l & 8 ? 1 : 0) + (l & 4 ? 1 : 0))
+// after 9 shuffles. OP is commutative in its bits (fp32 add, min, max): both lanes of a pair
+// compute the same value.
+template <class OP>
+__device__ __forceinline__ float warp_rows8(const float (&v)[8], int lane, OP op) {
+    const bool h4 = lane & 16, h3 = lane & 8, h2 = lane & 4;
+    float y[4], z[2];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) x[i] = at(i);
-    // halving-tree sum over the line of leaf(i): first level x-pairs (i, i + 32) in-thread
-    auto line_sum = [&](auto leaf) {
-        float a[32];
+    for (int k = 0; k < 4; ++k) y[k] = op(h4 ? v[k + 4] : v[k], __shfl_xor_sync(kFull, h4 ? v[k] : v[k + 4], 16));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = fadd(leaf(i), leaf(i + 32));
+    for (int k = 0; k < 2; ++k) z[k] = op(h3 ? y[k + 2] : y[k], __shfl_xor_sync(kFull, h3 ? y[k] : y[k + 2], 8));
+    float u = op(h2 ? z[1] : z[0], __shfl_xor_sync(kFull, h2 ? z[0] : z[1], 4));
+    u = op(u, __shfl_xor_sync(kFull, u, 2));
+    return op(u, __shfl_xor_sync(kFull, u, 1));
+}
+struct FAdd { __device__ float operator()(float a, float b) const { return fadd(a, b); } };
+struct FMin { __device__ float operator()(float a, float b) const { return fminf(a, b); } };
+struct FMax { __device__ float operator()(float a, float b) const { return fmaxf(a, b); } };
+
+// The spread of a line from its two halving-tree sums, as a pass computes it: sigma =
+// sqrt(var / n), sigma <= 2^-20 counts as 1.
+__device__ __forceinline__ float kv_sigma(float var_sum, float inv_n) {
+    const float sig = __fsqrt_rn(fmul(var_sum, inv_n));
+    return sig <= 9.5367431640625e-07f ? 1.f : sig;     // 2^-20
+}
+
+// A row pass over the warp's 8 rows (n = 256: mean, population spread, row /= sigma, the row
+// scale r[t] *= sigma). Row positions j = l + 32 b: the thread's levels pair b with b + 4
+// (stride 128), b + 2 (64), b + 1 (32); warp_rows8 takes strides 16 .. 1. Returns |sigma - 1|
+// of row w + 16 (lane / 4); with APPLY false the pass only measures.
+template <bool APPLY = true>
+__device__ __forceinline__ float kv_row_pass(float (&x)[8][8], float* r, int warp, int lane) {
+    constexpr float INV_N = 1.0f / 256.0f;
+    float p[8];
+    auto partials = [&](auto leaf) {
 #pragma unroll
-        for (int n = 16; n >= 1; n >>= 1) {
+        for (int a = 0; a < 8; ++a) {
+            float s[4];
 #pragma unroll
-            for (int i = 0; i < n; ++i) a[i] = fadd(a[i], a[i + n]);
+            for (int b = 0; b < 4; ++b) s[b] = fadd(leaf(a, b), leaf(a, b + 4));
+            p[a] = fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
         }
-        float t = a[0];
-#pragma unroll
-        for (int sft = P / 2; sft >= 1; sft >>= 1) t = fadd(t, __shfl_xor_sync(kFull, t, sft));
-        return t;
     };
-    const float mu = fmul(line_sum([&](int i) { return x[i]; }), INV_N);
-    const float var = line_sum([&](int i) { const float d = fsub(x[i], mu); return fmul(d, d); });
-    float sig = __fsqrt_rn(fmul(var, INV_N));
-    if (sig <= 9.5367431640625e-07f) sig = 1.f;     // 2^-20
-    if constexpr (APPLY) {
-        const float inv = fdiv(1.0f, sig);
+    partials([&](int a, int b) { return x[a][b]; });
+    const float mu_own = fmul(warp_rows8(p, lane, FAdd()), INV_N);
+    float mu[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) at(i) = fmul(x[i], inv);
-        if (q == 0) scale[line] = fmul(scale[line], sig);
+    for (int a = 0; a < 8; ++a) mu[a] = __shfl_sync(kFull, mu_own, 4 * a);
+    partials([&](int a, int b) { const float d = fsub(x[a][b], mu[a]); return fmul(d, d); });
+    const float sig = kv_sigma(warp_rows8(p, lane, FAdd()), INV_N);
+    if constexpr (APPLY) {
+        const float inv_own = fdiv(1.0f, sig);
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+            const float inv = __shfl_sync(kFull, inv_own, 4 * a);
+#pragma unroll
+            for (int b = 0; b < 8; ++b) x[a][b] = fmul(x[a][b], inv);
+        }
+        if ((lane & 3) == 0) {
+            const int t = warp + 16 * (lane >> 2);
+            r[t] = fmul(r[t], sig);
+        }
     }
     return fabsf(fsub(sig, 1.0f));
+}
+
+// A column pass (n = 128: column /= sigma, the column scale c[j] *= sigma). Column positions
+// t = w + 16 a: the thread's levels pair a with a + 4 (stride 64), a + 2 (32), a + 1 (16); the
+// warps' partials go to part [16][256] and thread j < 256 finishes column j's tree over the
+// warps (strides 8 .. 1). mu_s, inv_s: [256] of shared memory. Returns |sigma - 1| of column
+// threadIdx.x (threads < 256; 0 for the others). Four barriers: the first publishes the
+// partials, the last the inverses; a column pass's reads of part, mu_s and inv_s all come
+// before the next column pass writes them again (past one or more of these barriers).
+__device__ __forceinline__ float kv_col_pass(float (&x)[8][8], float* c, float* part, float* mu_s, float* inv_s,
+                                             int warp, int lane) {
+    constexpr float INV_N = 1.0f / 128.0f;
+    const int tid = threadIdx.x;
+    auto partials = [&](auto leaf) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            float s[4];
+#pragma unroll
+            for (int a = 0; a < 4; ++a) s[a] = fadd(leaf(a, b), leaf(a + 4, b));
+            part[warp * 256 + lane + 32 * b] = fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
+        }
+    };
+    auto column_total = [&]() {
+        float s[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) s[w] = fadd(part[w * 256 + tid], part[(w + 8) * 256 + tid]);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) s[w] = fadd(s[w], s[w + 4]);
+        return fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
+    };
+    partials([&](int a, int b) { return x[a][b]; });
+    __syncthreads();
+    if (tid < 256) mu_s[tid] = fmul(column_total(), INV_N);
+    __syncthreads();
+    float mu[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) mu[b] = mu_s[lane + 32 * b];
+    partials([&](int a, int b) { const float d = fsub(x[a][b], mu[b]); return fmul(d, d); });
+    __syncthreads();
+    float dev = 0.f;
+    if (tid < 256) {
+        const float sig = kv_sigma(column_total(), INV_N);
+        dev = fabsf(fsub(sig, 1.0f));
+        inv_s[tid] = fdiv(1.0f, sig);
+        c[tid] = fmul(c[tid], sig);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const float inv = inv_s[lane + 32 * b];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) x[a][b] = fmul(x[a][b], inv);
+    }
+    return dev;
 }
 
 // Block maximum of v (non-negative) into *out, every thread calling; wmax: 16 floats of shared
@@ -783,11 +857,11 @@ __device__ __forceinline__ void block_max_to(float v, float* wmax, float* out) {
     }
 }
 
-// grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: Y [128][257] fp32 and
-// the staged rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit:
-// [128][512]). Once the row parameters are taken, Y is dead and holds the codes, one byte
-// per value in rows of 1,028 bytes (257 words): a walk down a column (the V record is
-// channel-major) then touches a different bank for every other row.
+// grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: the column partials
+// [16][256] fp32, then (once the passes are done, over them) the codes, one byte per value in
+// rows of 1,028 bytes (257 words): a walk down a column (the V record is channel-major) then
+// touches a different bank for every other row; after them the staged rows of the half
+// (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]).
 template <int JK>
 __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
     constexpr int ROW = KvStage<JK>::ROW;
@@ -800,11 +874,11 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     const float Q = (float)((1 << bits) - 1);
     const int64_t unit = L.unit(tk.layer, tk.slot, h);
     extern __shared__ __align__(16) uint8_t kv_sm[];
-    float* Y = reinterpret_cast<float*>(kv_sm);                      // [128][kYS]
-    uint8_t* st = kv_sm + 128 * kYS * sizeof(float);                 // staged rows
+    float* part = reinterpret_cast<float*>(kv_sm);                   // [16][256] column partials
+    uint8_t* codes = kv_sm;                                          // [128][CS], over part
+    uint8_t* st = kv_sm + 128 * CS;                                  // staged rows
     uint16_t* sc = reinterpret_cast<uint16_t*>(st + 128 * ROW);      // tq6_0 scales [128][D/128]
-    uint8_t* codes = kv_sm;                                          // [128][CS], over Y
-    __shared__ float r[128], c[256], invS[128], Zs[128], invC[256];
+    __shared__ float r[128], c[256], invS[128], Zs[128], invC[256], mu_s[256], inv_s[256];
     __shared__ uint16_t S16[128], Z16[128], C16[256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nsc = L.D / 128;
@@ -842,19 +916,16 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         cp_async_commit();
         cp_async_wait<0>();
     }
-    // the tile Y from the staged rows, unit scales; the barrier first makes every thread's
-    // staged rows (cp.async, each thread waited only for its own copies) visible to all
+    // the thread's part of the tile from the staged rows (x[a][b] = row warp + 16 a, channel
+    // lane + 32 b), unit scales; the barrier first makes every thread's staged rows (cp.async,
+    // each thread waited only for its own copies) visible to all
+    float x[8][8];
     auto load_tile = [&]() {
         for (int j = threadIdx.x; j < 256; j += kKvThreads) c[j] = 1.f;
         if (threadIdx.x < 128) r[threadIdx.x] = 1.f;
         __syncthreads();
-        for (int t = warp; t < 128; t += kKvWarps) {
-            float v[8];
-            kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) Y[t * kYS + lane + 32 * k] = v[k];
-        }
-        __syncthreads();
+        for (int a = 0; a < 8; ++a) kv_row<JK>(st, sc, warp + 16 * a, nsc, half, lane, x[a], L.journal);
     };
     load_tile();
 
@@ -868,12 +939,14 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         __shared__ float s_wmax[kKvWarps], s_eps[8];
         __shared__ int s_best;
         for (int pass = 0; pass < 8; ++pass) {
-            const float dev = (pass & 1) == 0 ? kv_pass<true>(Y, r) : kv_pass<false>(Y, c);
-            if (pass == 0) __syncthreads();
-            else block_max_to(dev, s_wmax, &s_eps[pass - 1]);
-            __syncthreads();
+            const float dev = (pass & 1) == 0 ? kv_row_pass(x, r, warp, lane)
+                                              : kv_col_pass(x, c, part, mu_s, inv_s, warp, lane);
+            if (pass > 0) {
+                block_max_to(dev, s_wmax, &s_eps[pass - 1]);
+                __syncthreads();
+            }
         }
-        block_max_to(kv_pass<true, false>(Y, r), s_wmax, &s_eps[7]);
+        block_max_to(kv_row_pass<false>(x, r, warp, lane), s_wmax, &s_eps[7]);
         if (threadIdx.x == 0) {
             int b = 0;
             for (int i = 1; i < 8; ++i)
@@ -885,23 +958,27 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         load_tile();
     }
     for (int pass = 0; pass < passes; ++pass) {
-        if ((pass & 1) == 0) kv_pass<true>(Y, r);
-        else kv_pass<false>(Y, c);
-        __syncthreads();
+        if ((pass & 1) == 0) kv_row_pass(x, r, warp, lane);
+        else kv_col_pass(x, c, part, mu_s, inv_s, warp, lane);
     }
 
-    // row rounding parameters
-    for (int t = warp; t < 128; t += kKvWarps) {
-        float lo = 3.4e38f, hi = -3.4e38f;
+    // row rounding parameters: each row's extremes over the balanced values; lanes 4k .. 4k + 3
+    // hold those of row warp + 16 k, whose row scale the same lane 4k updated
+    {
+        float lo8[8], hi8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float y = Y[t * kYS + lane + 32 * k];
-            lo = fminf(lo, y);
-            hi = fmaxf(hi, y);
+        for (int a = 0; a < 8; ++a) {
+            lo8[a] = 3.4e38f;
+            hi8[a] = -3.4e38f;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                lo8[a] = fminf(lo8[a], x[a][b]);
+                hi8[a] = fmaxf(hi8[a], x[a][b]);
+            }
         }
-        lo = warp_min(lo);
-        hi = warp_max(hi);
-        if (lane == 0) {
+        const float lo = warp_rows8(lo8, lane, FMin()), hi = warp_rows8(hi8, lane, FMax());
+        if ((lane & 3) == 0) {
+            const int t = warp + 16 * (lane >> 2);
             const uint16_t s16 = f2h_bits(fdiv(fmul(r[t], fsub(hi, lo)), Q));
             const uint16_t z16 = f2h_bits(fmul(r[t], lo));
             S16[t] = s16;
@@ -979,7 +1056,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
 template <int JK>
 int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
     constexpr int ROW = KvStage<JK>::ROW;
-    const size_t smem = 128 * kYS * sizeof(float) + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
+    const size_t smem = 128 * 1028 + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
     int e = (int)cudaFuncSetAttribute(seal_kvarn_kernel<JK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
     dim3 grid(groups, L.H, 2 * (L.D / 256));
