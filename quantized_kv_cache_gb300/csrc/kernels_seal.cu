@@ -857,15 +857,51 @@ __device__ __forceinline__ void block_max_to(float v, float* wmax, float* out) {
     }
 }
 
+// The codes of a tile in shared memory, one byte each, in the record's row order: K [128
+// tokens][kCodeK bytes], V [256 channels][kCodeV bytes]; the padding word puts consecutive
+// rows one bank apart.
+constexpr int kCodeK = 260;
+constexpr int kCodeV = 132;
+constexpr int kCodeBytes = 256 * kCodeV;     // >= 128 kCodeK, and >= the 16 KB of column partials
+
+// One code plane of width WK (kvarn_planes) from the codes of a tile, rows of NCOLS codes (K
+// 256, V 128) STRIDE bytes apart: byte i of the plane packs 8 / WK codes of one row, code m at
+// bits WK m, each code's bits sh .. sh + WK - 1; so 32-bit word i holds 32 / WK consecutive
+// codes of one row at bits WK m. A thread forms a word from the 32-bit words of its codes: the
+// fields of 4 bytes (each < 2^WK after the shift and mask) are squeezed together by shifts.
+template <int WK, int NCOLS, int STRIDE>
+__device__ __forceinline__ void kv_plane(uint32_t* plane, const uint8_t* codes, int sh) {
+    constexpr int ROW_WORDS = NCOLS * WK / 32, PER_WORD = 32 / WK, NW = 8 / WK;
+    constexpr uint32_t MASK = ((1u << WK) - 1u) * 0x01010101u;
+    for (int i = threadIdx.x; i < 1024 * WK; i += kKvThreads) {
+        const int row = i / ROW_WORDS, e0 = (i % ROW_WORDS) * PER_WORD;
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(codes + row * STRIDE + e0);
+        uint32_t out = 0;
+#pragma unroll
+        for (int k = 0; k < NW; ++k) {
+            uint32_t t = (src[k] >> sh) & MASK;
+            if constexpr (WK == 4) {
+                t = (t | (t >> 4)) & 0x00FF00FFu;
+                t = (t | (t >> 8)) & 0x0000FFFFu;
+            } else if constexpr (WK == 2) {
+                t = (t | (t >> 6)) & 0x000F000Fu;
+                t = (t | (t >> 12)) & 0x000000FFu;
+            } else if constexpr (WK == 1) {
+                t = (t | (t >> 7)) & 0x00030003u;
+                t = (t | (t >> 14)) & 0x0000000Fu;
+            }
+            out |= t << (4 * WK * k);
+        }
+        plane[i] = out;
+    }
+}
+
 // grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: the column partials
-// [16][256] fp32, then (once the passes are done, over them) the codes, one byte per value in
-// rows of 1,028 bytes (257 words): a walk down a column (the V record is channel-major) then
-// touches a different bank for every other row; after them the staged rows of the half
-// (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]).
+// [16][256] fp32, then (once the passes are done, over them) the codes; after them the staged
+// rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]).
 template <int JK>
 __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
     constexpr int ROW = KvStage<JK>::ROW;
-    constexpr int CS = 1028;                                // code row stride (bytes, 257 words)
     const SealTaskPos tk = seal_task(p, blockIdx.x);
     const int nh = L.D / 256;
     const int h = blockIdx.y, w = blockIdx.z / nh, half = blockIdx.z % nh;
@@ -875,8 +911,8 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     const int64_t unit = L.unit(tk.layer, tk.slot, h);
     extern __shared__ __align__(16) uint8_t kv_sm[];
     float* part = reinterpret_cast<float*>(kv_sm);                   // [16][256] column partials
-    uint8_t* codes = kv_sm;                                          // [128][CS], over part
-    uint8_t* st = kv_sm + 128 * CS;                                  // staged rows
+    uint8_t* codes = kv_sm;                                          // codes, over part
+    uint8_t* st = kv_sm + kCodeBytes;                                // staged rows
     uint16_t* sc = reinterpret_cast<uint16_t*>(st + 128 * ROW);      // tq6_0 scales [128][D/128]
     __shared__ float r[128], c[256], invS[128], Zs[128], invC[256], mu_s[256], inv_s[256];
     __shared__ uint16_t S16[128], Z16[128], C16[256];
@@ -999,48 +1035,57 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     __syncthreads();
 
     // codes from the unbalanced rows (decoded again from the stage: identical bits) and the
-    // stored scales
-    for (int t = warp; t < 128; t += kKvWarps) {
-        float v[8];
-        kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
-        const float is = invS[t], z = Zs[t];
+    // stored scales, laid out as the record's rows: K token-major [128][kCodeK], V
+    // channel-major [256][kCodeV] (a warp's 32 channels of one token then fall in 32 banks)
+    {
+        float ic[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int j = lane + 32 * k;
-            float q = 0.f;
-            if (is != 0.f) {
-                q = rintf(fmul(fsub(fmul(v[k], invC[j]), z), is));
-                q = fminf(fmaxf(q, 0.f), Q);
+        for (int b = 0; b < 8; ++b) ic[b] = invC[lane + 32 * b];
+        for (int a = 0; a < 8; ++a) {
+            const int t = warp + 16 * a;
+            float v[8];
+            kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
+            const float is = invS[t], z = Zs[t];
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                const int j = lane + 32 * b;
+                float q = 0.f;
+                if (is != 0.f) {
+                    q = rintf(fmul(fsub(fmul(v[b], ic[b]), z), is));
+                    q = fminf(fmaxf(q, 0.f), Q);
+                }
+                if (w == 0) codes[t * kCodeK + j] = (uint8_t)q;
+                else codes[j * kCodeV + t] = (uint8_t)q;
             }
-            codes[t * CS + j] = (uint8_t)q;
         }
     }
     __syncthreads();
 
     uint8_t* rec = body_rec(L, p.pool, w, unit, tk.g) + (int64_t)half * (4096 * bits + 1152);
-    // code planes (kvarn_planes): K token-major (128 rows of 256 codes), V channel-major (256
-    // rows of 128 codes); byte i of a plane of width pw packs 8 / pw codes of one row
+    // code planes (kvarn_planes), 32-bit words at a time
     {
         int pw[2];
         const int np = kvarn_planes(bits, pw);
-        uint8_t* plane = rec;
+        uint32_t* plane = reinterpret_cast<uint32_t*>(rec);
         int sh = 0;
         for (int k = 0; k < np; ++k) {
-            const int wk = pw[k], per = 8 / wk, mask = (1 << wk) - 1;
-            const int row_bytes = (w == 0 ? 256 : 128) / per;
-            for (int i = threadIdx.x; i < 4096 * wk; i += kKvThreads) {
-                const int row = i / row_bytes, e0 = (i % row_bytes) * per;
-                uint32_t b = 0;
-#pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    if (m >= per) break;
-                    const uint32_t code = (w == 0) ? codes[row * CS + e0 + m] : codes[(e0 + m) * CS + row];
-                    b |= ((code >> sh) & mask) << (wk * m);
+            if (w == 0) {
+                switch (pw[k]) {
+                    case 1: kv_plane<1, 256, kCodeK>(plane, codes, sh); break;
+                    case 2: kv_plane<2, 256, kCodeK>(plane, codes, sh); break;
+                    case 4: kv_plane<4, 256, kCodeK>(plane, codes, sh); break;
+                    default: kv_plane<8, 256, kCodeK>(plane, codes, sh); break;
                 }
-                plane[i] = (uint8_t)b;
+            } else {
+                switch (pw[k]) {
+                    case 1: kv_plane<1, 128, kCodeV>(plane, codes, sh); break;
+                    case 2: kv_plane<2, 128, kCodeV>(plane, codes, sh); break;
+                    case 4: kv_plane<4, 128, kCodeV>(plane, codes, sh); break;
+                    default: kv_plane<8, 128, kCodeV>(plane, codes, sh); break;
+                }
             }
-            plane += 4096 * wk;
-            sh += wk;
+            plane += 1024 * pw[k];
+            sh += pw[k];
         }
     }
     uint16_t* sb = reinterpret_cast<uint16_t*>(rec + 4096 * bits);
@@ -1056,7 +1101,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
 template <int JK>
 int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
     constexpr int ROW = KvStage<JK>::ROW;
-    const size_t smem = 128 * 1028 + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
+    const size_t smem = kCodeBytes + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
     int e = (int)cudaFuncSetAttribute(seal_kvarn_kernel<JK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
     dim3 grid(groups, L.H, 2 * (L.D / 256));
