@@ -863,6 +863,7 @@ __device__ __forceinline__ void block_max_to(float v, float* wmax, float* out) {
 constexpr int kCodeK = 260;
 constexpr int kCodeV = 132;
 constexpr int kCodeBytes = 256 * kCodeV;     // >= 128 kCodeK, and >= the 16 KB of column partials
+constexpr int kTileBytes = 128 * 256 * 4;    // the fp32 copy of the unbalanced tile
 
 // One code plane of width WK (kvarn_planes) from the codes of a tile, rows of NCOLS codes (K
 // 256, V 128) STRIDE bytes apart: byte i of the plane packs 8 / WK codes of one row, code m at
@@ -898,7 +899,8 @@ __device__ __forceinline__ void kv_plane(uint32_t* plane, const uint8_t* codes, 
 
 // grid (groups, H, 2 * D/256), 512 threads. Dynamic shared memory: the column partials
 // [16][256] fp32, then (once the passes are done, over them) the codes; after them the staged
-// rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]).
+// rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]), then
+// (once decoded, over them) the fp32 copy of the unbalanced tile.
 template <int JK>
 __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
     constexpr int ROW = KvStage<JK>::ROW;
@@ -953,17 +955,35 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         cp_async_wait<0>();
     }
     // the thread's part of the tile from the staged rows (x[a][b] = row warp + 16 a, channel
-    // lane + 32 b), unit scales; the barrier first makes every thread's staged rows (cp.async,
-    // each thread waited only for its own copies) visible to all
+    // lane + 32 b), unit scales; the first barrier makes every thread's staged rows (cp.async,
+    // each thread waited only for its own copies) visible to all. Once every thread has decoded
+    // its values, a copy of them (x0: 16 float4 per thread, thread-major so a warp's accesses
+    // are contiguous) replaces the staged rows: the codes and a second balancing read it.
     float x[8][8];
-    auto load_tile = [&]() {
+    float4* x0 = reinterpret_cast<float4*>(st);
+    auto unit_scales = [&]() {
         for (int j = threadIdx.x; j < 256; j += kKvThreads) c[j] = 1.f;
         if (threadIdx.x < 128) r[threadIdx.x] = 1.f;
-        __syncthreads();
-#pragma unroll
-        for (int a = 0; a < 8; ++a) kv_row<JK>(st, sc, warp + 16 * a, nsc, half, lane, x[a], L.journal);
     };
-    load_tile();
+    auto reload = [&]() {
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+            const float4 v = x0[n * kKvThreads + threadIdx.x];
+            x[n >> 1][4 * (n & 1)] = v.x;
+            x[n >> 1][4 * (n & 1) + 1] = v.y;
+            x[n >> 1][4 * (n & 1) + 2] = v.z;
+            x[n >> 1][4 * (n & 1) + 3] = v.w;
+        }
+    };
+    unit_scales();
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 8; ++a) kv_row<JK>(st, sc, warp + 16 * a, nsc, half, lane, x[a], L.journal);
+    __syncthreads();
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+        x0[n * kKvThreads + threadIdx.x] = make_float4(x[n >> 1][4 * (n & 1)], x[n >> 1][4 * (n & 1) + 1],
+                                                       x[n >> 1][4 * (n & 1) + 2], x[n >> 1][4 * (n & 1) + 3]);
 
     int passes = 16;
     if (L.kvarn_best) {
@@ -991,7 +1011,9 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         }
         __syncthreads();
         passes = s_best + 1;
-        load_tile();
+        unit_scales();
+        __syncthreads();
+        reload();
     }
     for (int pass = 0; pass < passes; ++pass) {
         if ((pass & 1) == 0) kv_row_pass(x, r, warp, lane);
@@ -1034,24 +1056,24 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     }
     __syncthreads();
 
-    // codes from the unbalanced rows (decoded again from the stage: identical bits) and the
-    // stored scales, laid out as the record's rows: K token-major [128][kCodeK], V
-    // channel-major [256][kCodeV] (a warp's 32 channels of one token then fall in 32 banks)
+    // codes from the unbalanced values (x0) and the stored scales, laid out as the record's
+    // rows: K token-major [128][kCodeK], V channel-major [256][kCodeV] (a warp's 32 channels of
+    // one token then fall in 32 banks)
+    reload();
     {
         float ic[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) ic[b] = invC[lane + 32 * b];
+#pragma unroll
         for (int a = 0; a < 8; ++a) {
             const int t = warp + 16 * a;
-            float v[8];
-            kv_row<JK>(st, sc, t, nsc, half, lane, v, L.journal);
             const float is = invS[t], z = Zs[t];
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
                 const int j = lane + 32 * b;
                 float q = 0.f;
                 if (is != 0.f) {
-                    q = rintf(fmul(fsub(fmul(v[b], ic[b]), z), is));
+                    q = rintf(fmul(fsub(fmul(x[a][b], ic[b]), z), is));
                     q = fminf(fmaxf(q, 0.f), Q);
                 }
                 if (w == 0) codes[t * kCodeK + j] = (uint8_t)q;
@@ -1101,7 +1123,8 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
 template <int JK>
 int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
     constexpr int ROW = KvStage<JK>::ROW;
-    const size_t smem = kCodeBytes + 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
+    const size_t stage = 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
+    const size_t smem = kCodeBytes + (stage > kTileBytes ? stage : kTileBytes);
     int e = (int)cudaFuncSetAttribute(seal_kvarn_kernel<JK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
     dim3 grid(groups, L.H, 2 * (L.D / 256));
