@@ -613,6 +613,14 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
         const int64_t slots = (int64_t)std::max(1, decode_ctas_per_sm(L)) * c->sm_count;
         if (body_items + count(chunk) > slots && body_items + count(2 * chunk) <= slots) ring_chunk = 2 * chunk;
     }
+    // beside a tq6_0 ring, the 16-bit spans (exact tail, sink) take chunks half as long as the
+    // ring's: a 16-bit position costs about twice a ring position (measured on longctx: 73 and
+    // 30-42 ns per position and CTA), and a tail item of a whole ring chunk ran twice as long as
+    // the ring items, ending the launch late on the SMs that drew one
+    bool has_ring = false;
+    for (int i = 0; i < n_seq; ++i)
+        for (int r = 0; r < 4; ++r) has_ring |= p.seq[i].kind[r] == RK_RING && p.seq[i].hi[r] > p.seq[i].lo[r];
+    if (has_ring) chunk = std::max<int64_t>(kGroup, ring_chunk / 2 / kGroup * kGroup);
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {

@@ -16,10 +16,12 @@
 //      movmatrix gives the B fragments of step 3 (one 8-byte store per lane).
 //   3. values: warp w takes channels [wD/8, (w+1)D/8) (fp16 rows come in runs of 48 positions
 //      beside a ring, 32 at head_dim 512; warps past the run skip step 1). The rows are token-major, so the A
-//      fragments of V^T come from transposes: ldmatrix.trans of the fp16 rows, or of a small
-//      per-warp buffer of decoded tq6_0 rows for the ring (whose fragment rows then hold channels
-//      in the order 0,4,1,5,2,6,3,7 of each 8-channel group). An all-ones mma gives sum_t P'_t, which
-//      removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
+//      fragments of V^T come from transposes: ldmatrix.trans of the fp16 rows; for the ring,
+//      tq6_0 codes decoded in registers as 8 x 8 tiles (positions x channel pairs) and
+//      transposed by movmatrix (head_dim 256), or decoded into a small per-warp buffer that
+//      ldmatrix.trans reads back (head_dim 128); either way the fragment rows hold the channels
+//      in a fixed permutation that the partial's write undoes. An all-ones mma gives sum_t P'_t,
+//      which removes the code offset 96 (64 + the tq6_0 centre 32) once per run.
 // The partial (m, l, o) of a ring item is rotated back to the original domain; the merge
 // kernel (kernels_attn.cu) combines all partials of a (sequence, KV head) under one softmax.
 #pragma once
@@ -571,7 +573,32 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
             // word per lane: nibble pairs and high bits in a few operations) into its buffer, and
             // ldmatrix.trans reads the A fragments of V^T back (rows hold channels 0,4,1,5,2,6,3,7)
             uint32_t ar[MT][4];
-            if (ring) {
+            if (ring && Gm::CPW == 32) {
+                // D 256: no staging buffer. Thread (g, tq) decodes channels 8 tq .. 8 tq + 7 of the
+                // warp's 32 (register k: channels k and k + 4) of positions g and 8 + g of the k-step;
+                // register k over the 8 positions of an octet is an 8 x 8 tile (rows positions,
+                // column pairs tq) that movmatrix turns into 8 rows of V^T: row g' = channel
+                // 8 (g' >> 1) + k + 4 (g' & 1). m-tile mt takes tiles 2 mt (rows 0-7) and 2 mt + 1.
+                const int cw = warp * 32 + 8 * tq;
+                uint32_t tl[2][4];
+#pragma unroll
+                for (int o = 0; o < 2; ++o) {
+                    const uint8_t* rowp = vr + (16 * kk + 8 * o + g) * CLD + 96 * (cw >> 7);
+                    const uint32_t wq = *reinterpret_cast<const uint32_t*>(rowp + ((cw & 127) >> 1));
+                    const uint32_t u = hi2_spread(*reinterpret_cast<const uint16_t*>(rowp + 64 + ((cw & 127) >> 2)));
+                    tl[o][0] = movtrans(hi2_at<0>(nib64(wq, 0), u));
+                    tl[o][1] = movtrans(hi2_at<1>(nib64(wq, 1), u));
+                    tl[o][2] = movtrans(hi2_at<2>(nib64(wq, 2), u));
+                    tl[o][3] = movtrans(hi2_at<3>(nib64(wq, 3), u));
+                }
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    ar[mt][0] = tl[0][(2 * mt) & 3];
+                    ar[mt][1] = tl[0][(2 * mt + 1) & 3];
+                    ar[mt][2] = tl[1][(2 * mt) & 3];
+                    ar[mt][3] = tl[1][(2 * mt + 1) & 3];
+                }
+            } else if (ring) {
                 constexpr int WPP = Gm::WPP, VROWS = Gm::VROWS, VRS = Gm::VRS, NF = 16 / Gm::VROWS;
                 uint8_t* vb = vbuf + warp * Gm::VB_BYTES;
                 const int prow = lane / WPP, qd = lane % WPP;
@@ -657,18 +684,22 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
         }
     csync();
     float* ofin = reinterpret_cast<float*>(stages);                     // [NQ][D], stages drained
-    // ring fragment rows hold channels 0,4,1,5,2,6,3,7 of each 8-channel group
+    // channels of fragment rows g and g + 8: ring at D 256 (movmatrix tiles above) 8 (g >> 1) +
+    // 2 mt + 4 (g & 1) of the warp's and the next one; ring at D 128 (ldmatrix of the staging
+    // buffer) channels 0,4,1,5,2,6,3,7 of each 8-channel group; 16-bit rows in order
     const int cg = ring ? ((g >> 1) + 4 * (g & 1)) : g;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int qc = nt * 8 + 2 * tq;
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int c0 = warp * (D / 8) + 16 * mt + cg;
-            ofin[qc * D + c0] = O[mt][nt][0];
-            ofin[(qc + 1) * D + c0] = O[mt][nt][1];
-            ofin[qc * D + c0 + 8] = O[mt][nt][2];
-            ofin[(qc + 1) * D + c0 + 8] = O[mt][nt][3];
+            const bool mv = ring && Gm::CPW == 32;
+            const int cA = mv ? warp * 32 + 8 * (g >> 1) + 2 * mt + 4 * (g & 1) : warp * (D / 8) + 16 * mt + cg;
+            const int cB = mv ? cA + 1 : cA + 8;
+            ofin[qc * D + cA] = O[mt][nt][0];
+            ofin[(qc + 1) * D + cA] = O[mt][nt][1];
+            ofin[qc * D + cB] = O[mt][nt][2];
+            ofin[(qc + 1) * D + cB] = O[mt][nt][3];
         }
     }
     if (threadIdx.x < NQ) {
