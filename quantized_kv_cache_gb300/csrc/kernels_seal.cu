@@ -16,10 +16,11 @@
 // "Worked example" and "rotate first"; HAL #582 §1): one IEEE fp32 rounding per operation
 // through the _rn intrinsics (the unit is also built with -fmad=false), halving-tree sums,
 // round-half-even. The TBQ4 index, the number of boundaries beta_k with u > beta_k, is read
-// from a 2,048-bucket table indexed by the top 11 bits of u (sign, exponent, two mantissa
-// bits): a bucket spans a value ratio of at most 1.25 and the boundaries of the 16-level
-// Lloyd-Max table differ by a ratio of at least 1.28, so a bucket holds at most one
-// boundary and idx = base[bucket] + (u > thr[bucket]), the same fp32 comparison.
+// from a 2,048-bucket table indexed by the top 11 bits of an order-preserving integer key of u
+// (sign, exponent, two mantissa bits): a bucket spans a value ratio of at most 1.25 and the
+// boundaries of the 16-level Lloyd-Max table differ by a ratio of at least 1.28, so a bucket
+// holds at most one boundary and idx = base[bucket] + (u > thr[bucket]), the same fp32
+// comparison, taken on the keys as the carry of one 32-bit addition.
 #include <cuda_runtime.h>
 #include <algorithm>
 #include "append_row.cuh"
@@ -231,9 +232,18 @@ __device__ __forceinline__ float sq_tree(const float (&y)[128]) {
     }
 }
 
+// Order-preserving integer key of an fp32 value: its bits for +0 and above, its bits with the 31
+// magnitude bits inverted for negative values. Within one sign the key grows with the value.
+__device__ __forceinline__ uint32_t fkey(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return b ^ ((uint32_t)((int32_t)b >> 31) >> 1);
+}
+
 // TBQ4 block: n16 = fp16(sqrt(sum y^2)), u = y x (1 / fp32(n16)) (0 when n16 is 0), idx =
-// #{k : u > beta_k}; nibble e of P[m] is the index of channel 8m + e.
-__device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const float2* qt, uint32_t (&P)[16]) {
+// #{k : u > beta_k}; nibble e of P[m] is the index of channel 8m + e. The table entry of u's
+// bucket plus u's key has the index in its top four bits (build_qtab), which a funnel shift
+// moves into the packed word (channel 8m + 7 first, so that channel 8m ends in nibble 0).
+__device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const uint32_t* qt, uint32_t (&P)[16]) {
     const uint16_t n16 = f2h_bits(__fsqrt_rn(sq_tree<7, 0>(y)));
     const float n = h2f(n16);
     const float inv = (n == 0.f) ? 0.f : fdiv(1.0f, n);
@@ -241,11 +251,9 @@ __device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const flo
     for (int m = 0; m < 16; ++m) {
         uint32_t acc = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float u = fmul(y[8 * m + e], inv);
-            const float2 ent = qt[__float_as_uint(u) >> 21];
-            const uint32_t idx = (uint32_t)__float_as_int(ent.y) + (u > ent.x ? 1u : 0u);
-            acc |= idx << (4 * e);
+        for (int e = 7; e >= 0; --e) {
+            const uint32_t key = fkey(fmul(y[8 * m + e], inv));
+            acc = __funnelshift_l(qt[key >> 21] + key, acc, 4);
         }
         P[m] = acc;
     }
@@ -380,26 +388,33 @@ __device__ __forceinline__ void store_bytes(uint8_t* rec, int D, int b, int w, c
     }
 }
 
-// Decision table of a TBQ index (TBQ4: the 15 boundaries; turbo3: 7): bucket k = the floats
-// whose top 11 bits are k. base = boundaries below the bucket's smallest value, thr = the
-// boundary inside it (+inf if none); buckets of infinities and NaNs give 0 (a NaN exceeds no
-// boundary). Exact where no bucket holds two boundaries (consecutive boundaries differ by a
-// ratio above 1.25: TBQ4 >= 1.28, turbo3 >= 1.66).
-__device__ void build_qtab(float2* qt, const float* bnd, int nb) {
+// Decision table of a TBQ index (TBQ4: the 15 boundaries; turbo3: 7) over keys (fkey): bucket k
+// = the values whose key has top 11 bits k, a value range [vmin, vmax]. base = boundaries below
+// vmin; thr = the boundary inside the bucket, if any, as the low 21 bits t of the largest key
+// in the bucket whose value does not exceed it (the key of the boundary itself; for the zero
+// boundary in the bucket of -0, the bucket's largest key, which no value of the bucket exceeds);
+// without one t = 0x1FFFFF. Entry = (base << 28) + (2^28 - 1 - t) - (k << 21), so that for a key
+// x of the bucket the sum entry + x = (base << 28) + 2^28 - 1 - t + (x & 0x1FFFFF) carries into
+// bit 28 exactly when x & 0x1FFFFF > t, i.e. when u > thr: (entry + x) >> 28 = base + (u > thr)
+// (never above 15: a bucket with a boundary has base <= 14). Buckets of infinities and NaNs
+// give 0 (a NaN exceeds no boundary). Exact where no bucket holds two boundaries (consecutive
+// boundaries differ by a ratio above 1.25: TBQ4 >= 1.28, turbo3 >= 1.66).
+__device__ void build_qtab(uint32_t* qt, const float* bnd, int nb) {
     for (int k = threadIdx.x; k < kBuckets; k += blockDim.x) {
-        const uint32_t lo = (uint32_t)k << 21, hi = lo | 0x1FFFFFu;
-        float thr = __uint_as_float(0x7F800000u);
-        int base = 0;
-        if (((lo >> 23) & 0xFF) != 0xFF) {
-            const bool neg = lo >> 31;
-            const float vmin = __uint_as_float(neg ? hi : lo), vmax = __uint_as_float(neg ? lo : hi);
+        const uint32_t klo = (uint32_t)k << 21, khi = klo | 0x1FFFFFu;
+        const bool neg = k >= kBuckets / 2;
+        const uint32_t flip = neg ? 0x7FFFFFFFu : 0u;
+        const uint32_t blo = klo ^ flip, bhi = khi ^ flip;   // bits of the smallest and largest value
+        uint32_t t = 0x1FFFFFu, base = 0;
+        if (((blo >> 23) & 0xFF) != 0xFF) {
+            const float vmin = __uint_as_float(blo), vmax = __uint_as_float(bhi);
             for (int j = 0; j < nb; ++j) {
                 const float bj = bnd[j];
                 if (bj < vmin) ++base;
-                else if (bj <= vmax) thr = bj;
+                else if (bj <= vmax) t = (neg && bj == 0.f) ? 0x1FFFFFu : (fkey(bj) & 0x1FFFFFu);
             }
         }
-        qt[k] = make_float2(thr, __int_as_float(base));
+        qt[k] = (base << 28) + (0x0FFFFFFFu - t) - klo;
     }
 }
 
@@ -461,8 +476,8 @@ __global__ void __launch_bounds__(kRows, JK == J_TQ6 ? 3 : 2)
 seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
     extern __shared__ __align__(16) uint8_t sm[];
     __shared__ TileSlot slot[kSlots];
-    float2* qt = reinterpret_cast<float2*>(sm + kStages * stage_bytes);
-    float2* qt3 = qt + kBuckets;                    // turbo3's table, present when a body is turbo3
+    uint32_t* qt = reinterpret_cast<uint32_t*>(sm + kStages * stage_bytes);
+    uint32_t* qt3 = qt + kBuckets;                  // turbo3's table, present when a body is turbo3
     if constexpr (FAM == F_TBQ4) {                  // read after the first barrier below
         build_qtab(qt, c_tab.bnd, 15);
         if (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3) build_qtab(qt3, c_tab.bnd3, 7);
@@ -619,7 +634,7 @@ template <int JK, int FAM>
 int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
     const int stage = (JK == J_TQ6) ? kRows * kTq6Stride + 2 * L.D : kRows * kX16Stride;
     const bool t3 = (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3);
-    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? (t3 ? 2 : 1) * kBuckets * sizeof(float2) : 0);
+    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? (t3 ? 2 : 1) * kBuckets * sizeof(uint32_t) : 0);
     auto fn = seal_rows_kernel<JK, FAM>;
     int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
