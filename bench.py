@@ -387,13 +387,15 @@ def launches_per_layer(w):
 
 
 def seal_launches(w, states):
+    """Seal launches of the steps: where the decode kernel appends (every layer in lockstep), a
+    step's seals are one call over all layers, one launch; otherwise one launch per layer."""
     n = 0
     prev = None
     for st in states:
         if prev is not None:
             for (a, s0), (b, s1) in zip(prev, st):
                 if s1 != s0:
-                    n += w.n_layers
+                    n += 1 if launches_per_layer(w) == 2 else w.n_layers
                     break
         prev = st
     return n
@@ -481,16 +483,15 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
             _lib.kv_decode_step(cache.h, w.n_layers, seq_ids, inp.q[s].data_ptr(), inp.k[s].data_ptr(),
                                 inp.v[s].data_ptr(), out.data_ptr(), w.seal_trigger, w.keep, cache.ws.data_ptr(),
                                 cache.ws_bytes, None, stream)
-        t, groups = 0.0, 0
         for l in range(w.n_layers):
             _lib.kv_append(cache.h, l, seq_ids, 1, inp.k[target, l].data_ptr(), inp.v[target, l].data_ptr(), stream)
-            torch.cuda.synchronize()
-            ev0.record()
-            groups += _lib.kv_seal(cache.h, l, seq_ids, w.keep, stream)
-            ev1.record()
-            torch.cuda.synchronize()
-            t += ev0.elapsed_time(ev1) / 1e3
-        kind = "seal at the policy's trigger, one launch per layer"
+        torch.cuda.synchronize()
+        ev0.record()
+        groups = _lib.kv_seal(cache.h, -1, seq_ids, w.keep, stream)
+        ev1.record()
+        torch.cuda.synchronize()
+        t = ev0.elapsed_time(ev1) / 1e3
+        kind = "seal at the policy's trigger, all layers in one call (as the decode step issues it)"
     from quantized_kv_cache_gb300.configs import record_bytes
     D, H = w.head_dim, w.n_kv_heads
     read = 128 * H * 2 * ((D // 128) * 98 if w.journal == "tq6_0" else D * 2)

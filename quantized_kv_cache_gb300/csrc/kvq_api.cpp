@@ -733,39 +733,89 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
     const size_t qb = (size_t)n_seq * L.Hq * L.D * 2, kb = (size_t)n_seq * L.H * L.D * 2;
     int64_t total = 0;
     int32_t need[kMaxSeqPerCall];
-    for (int l = 0; l < n_layers; ++l) {
-        const char* kl = (const char*)k + l * kb;
-        const char* vl = (const char*)v + l * kb;
-        // the append goes into the decode kernel where it can (no separate launch); the seal,
-        // when due, reads only positions at least `keep` (>= T) behind the newest one, so it
-        // may run before that append
-        const bool fuse = fused_append_ok(c, l, seq_ids, n_seq);
-        if (fuse) {
+    // Where every layer appends inside its decode kernel, the step's seals go out first, in as
+    // few launches as the layers' states allow (kv_seal over all layers merges layers whose
+    // lengths agree: one launch in a lockstep decode, instead of one small launch per layer
+    // whose last wave leaves SMs idle). A seal reads only positions at least keep (>= T) behind
+    // the newest one, so it may precede the appends; the policy decides on the lengths after them.
+    bool all_fused = true;
+    for (int l = 0; l < n_layers && all_fused; ++l) all_fused = fused_append_ok(c, l, seq_ids, n_seq);
+    if (all_fused) {
+        for (int l = 0; l < n_layers; ++l)
             for (int i = 0; i < n_seq; ++i) {
                 const int s = seq_ids[i];
                 const int64_t N = NT(c, l, s), S = ST(c, l, s);
                 if (N + 1 > c->cfg.max_ctx) return KVQ_ENOSPC;
                 if (std::max<int64_t>(N + 1, kSink) - S > c->cfg.ring_capacity) return KVQ_ENOSPC;
             }
+        for (int l = 0; l < n_layers; ++l)
             for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) += 1;
-        } else {
+        auto rollback = [&](int from) {   // the appends of layers [from, n_layers) did not go out
+            for (int l = from; l < n_layers; ++l)
+                for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) -= 1;
+        };
+        auto due = [&](int l, int32_t* out) {
+            int nn = 0;
+            for (int i = 0; i < n_seq; ++i) {
+                const int s = seq_ids[i];
+                const int64_t N = NT(c, l, s), S = ST(c, l, s);
+                bool seal = false;
+                if (seal_trigger > 0) seal = std::max<int64_t>(N, kSink) - S >= seal_trigger;
+                else if (seal_trigger == 0) seal = N - keep - S >= kGroup;
+                if (seal) out[nn++] = s;
+            }
+            return nn;
+        };
+        // the same sequences due on every layer: one call over all layers (the library merges the
+        // layers whose lengths agree into one launch); otherwise one call per layer that is due
+        int32_t first[kMaxSeqPerCall];
+        const int n0 = due(0, first);
+        bool uniform = n_layers == c->cfg.n_layers;
+        for (int l = 1; l < n_layers && uniform; ++l) {
+            const int nl = due(l, need);
+            uniform = nl == n0 && std::equal(need, need + nl, first);
+        }
+        if (uniform && n0 > 0) {
+            int64_t g = 0;
+            st = kv_seal(c, -1, first, n0, keep, &g, stream);
+            if (st != KVQ_OK) { rollback(0); return st; }
+            total += g;
+        } else if (!uniform) {
+            for (int l = 0; l < n_layers; ++l) {
+                const int nn = due(l, need);
+                if (!nn) continue;
+                int64_t g = 0;
+                st = kv_seal(c, l, need, nn, keep, &g, stream);
+                if (st != KVQ_OK) { rollback(0); return st; }
+                total += g;
+            }
+        }
+    }
+    for (int l = 0; l < n_layers; ++l) {
+        const char* kl = (const char*)k + l * kb;
+        const char* vl = (const char*)v + l * kb;
+        // the append goes into the decode kernel where it can (no separate launch); the seal,
+        // when due, reads only positions at least `keep` (>= T) behind the newest one, so it
+        // may run before that append
+        const bool fuse = all_fused;
+        if (!fuse) {
             st = kv_append(c, l, seq_ids, n_seq, 1, kl, vl, stream);
             if (st != KVQ_OK) return st;
-        }
-        int nn = 0;
-        for (int i = 0; i < n_seq; ++i) {
-            const int s = seq_ids[i];
-            const int64_t N = NT(c, l, s), S = ST(c, l, s);
-            bool seal = false;
-            if (seal_trigger > 0) seal = std::max<int64_t>(N, kSink) - S >= seal_trigger;
-            else if (seal_trigger == 0) seal = N - keep - S >= kGroup;
-            if (seal) need[nn++] = s;
-        }
-        if (nn) {
-            int64_t g = 0;
-            st = kv_seal(c, l, need, nn, keep, &g, stream);
-            if (st != KVQ_OK) return st;
-            total += g;
+            int nn = 0;
+            for (int i = 0; i < n_seq; ++i) {
+                const int s = seq_ids[i];
+                const int64_t N = NT(c, l, s), S = ST(c, l, s);
+                bool seal = false;
+                if (seal_trigger > 0) seal = std::max<int64_t>(N, kSink) - S >= seal_trigger;
+                else if (seal_trigger == 0) seal = N - keep - S >= kGroup;
+                if (seal) need[nn++] = s;
+            }
+            if (nn) {
+                int64_t g = 0;
+                st = kv_seal(c, l, need, nn, keep, &g, stream);
+                if (st != KVQ_OK) return st;
+                total += g;
+            }
         }
         LaunchMarks marks;
         const bool side = events && ev_flags == cudaEventRecordExternal;
@@ -782,8 +832,9 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
         st = decode_attn(c, l, seq_ids, n_seq, (const char*)q + l * qb, (char*)out + l * qb, workspace, ws_bytes,
                          fuse ? kl : nullptr, fuse ? vl : nullptr, stream, marks);
         if (st != KVQ_OK) {
-            if (fuse)   // the launch that was to append the position did not go out
-                for (int i = 0; i < n_seq; ++i) NT(c, l, seq_ids[i]) -= 1;
+            if (fuse)   // the launches that were to append the position did not go out
+                for (int ll = l; ll < n_layers; ++ll)
+                    for (int i = 0; i < n_seq; ++i) NT(c, ll, seq_ids[i]) -= 1;
             return st;
         }
     }
