@@ -621,6 +621,23 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     for (int i = 0; i < n_seq; ++i)
         for (int r = 0; r < 4; ++r) has_ring |= p.seq[i].kind[r] == RK_RING && p.seq[i].hi[r] > p.seq[i].lo[r];
     if (has_ring) chunk = std::max<int64_t>(kGroup, ring_chunk / 2 / kGroup * kGroup);
+    // a launch that fits in one wave of resident CTAs gives the slots left over to more, shorter
+    // body items (down to kFillGroups groups each): the wave's end is set by its longest items
+    if (fused) {
+        constexpr int64_t kFillGroups = 4;
+        const int64_t slots = (int64_t)std::max(1, decode_ctas_per_sm(L)) * c->sm_count;
+        int64_t n_reg = 0;
+        for (int i = 0; i < n_seq; ++i) {
+            const SeqSpan& s = p.seq[i];
+            for (int r = 0; r < 4; ++r) {
+                const int64_t ck = (s.kind[r] == RK_RING) ? ring_chunk : chunk;
+                n_reg += (s.hi[r] - s.lo[r] + ck - 1) / ck;
+            }
+        }
+        n_reg *= L.H;
+        if (body_items + n_reg < slots)
+            body_items = std::max(body_items, std::min(slots - n_reg, body_groups * L.H / kFillGroups));
+    }
     for (;;) {
         int64_t items = 0;
         for (int i = 0; i < n_seq; ++i) {
