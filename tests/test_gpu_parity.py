@@ -200,6 +200,40 @@ def test_decode_step_call_across_sink_edge(base):
         p.gpu.close()
 
 
+@pytest.mark.parametrize("base", ["kvarn4_ring", "q8q4_bf16", "tbq4_ring"])
+def test_decode_step_layers_out_of_step(base):
+    # layers whose lengths differ: after the prefill, layer 0 and layer 1 get extra positions so
+    # that, with the policy 'seal whenever a full group is older than keep', layer 0 falls due in
+    # the first decode step and layer 1 in the second, each sequence on its own count. The step
+    # then seals per layer (not one call over all layers); every step's outputs, and in the end
+    # every stored byte and the dequantized values, are checked against the oracle.
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f0 = FAMILIES[base]
+    f = Family(f0.name + "_skew", f0.D, f0.H, f0.Hq, f0.k_body, f0.v_body, f0.journal, f0.tail_fmt, T=f0.T, R=f0.R,
+               contexts=f0.contexts, keep=f0.keep, steps=4, n_out=f0.n_out, factor=f0.factor, balance=f0.balance)
+    p = Pair(f)
+    try:
+        p.prefill()
+        for layer, due_step in ((0, 1), (1, 2)):
+            for s in p.seqs:
+                n, S = p.gpu.state(layer, s)
+                extra = 128 - due_step - (n - f.keep - S)     # the due step's append makes 128
+                assert 0 <= extra < 128
+                if extra:
+                    p.append(layer, [s], [n], extra)
+        states = [[p.gpu.state(layer, s) for s in p.seqs] for layer in range(f.L)]
+        assert states[0] != states[1]
+        _step_calls(p, f.steps, 1, f.keep)
+        for layer in (0, 1):
+            for s, (n, S) in zip(p.seqs, states[layer]):
+                assert p.gpu.state(layer, s)[1] == S + 128, (layer, s)
+        _check_bytes(p)
+        _check_dequant(p)
+    finally:
+        p.gpu.close()
+
+
 def test_decode_step_graph_and_direct_agree():
     # the same steps through one CUDA graph per step and through direct launches: outputs and
     # every stored byte agree exactly (a seal step changes the graph's topology mid-run)
