@@ -621,6 +621,21 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     for (int i = 0; i < n_seq; ++i)
         for (int r = 0; r < 4; ++r) has_ring |= p.seq[i].kind[r] == RK_RING && p.seq[i].hi[r] > p.seq[i].lo[r];
     if (has_ring) chunk = std::max<int64_t>(kGroup, ring_chunk / 2 / kGroup * kGroup);
+    // without a ring, where the region items are fewer than a wave and the body items fill one,
+    // the region items run in the slots the first body items to finish free (a body item's speed
+    // depends on its place among the CTAs of its SM: 36 to 52 us on fa14b for equal work); 16-bit
+    // spans then take 96 positions per item (two runs of the 16-bit reader at head_dim 128/256,
+    // three at 512) rather than 128, which those gaps absorb better (fa14b +1.5%, its q5_1 / q4_0
+    // variant +1.3%)
+    if (fused && !has_ring) {
+        constexpr int64_t kGapChunk = 96;
+        const int64_t slots = (int64_t)std::max(1, decode_ctas_per_sm(L)) * c->sm_count;
+        int64_t n_reg = 0;
+        for (int i = 0; i < n_seq; ++i)
+            for (int r = 0; r < 4; ++r) n_reg += (p.seq[i].hi[r] - p.seq[i].lo[r] + chunk - 1) / chunk;
+        n_reg *= L.H;
+        if (n_reg < slots && body_items >= slots) chunk = std::min<int64_t>(chunk, kGapChunk);
+    }
     // a launch that fits in one wave of resident CTAs gives the slots left over to more, shorter
     // body items (down to kFillGroups groups each): the wave's end is set by its longest items
     if (fused) {
