@@ -459,7 +459,11 @@ __device__ __forceinline__ uint32_t bit2_byte(uint32_t x) {
 // ---------------------------------------------------------------------------- kernel
 // One instance per journal kind and body family: TBQ4 layouts (K and V TBQ4: the rotation
 // is per layout) or Q8_0 / Q4_0 layouts, so that each instance holds one encoder's code.
-enum BodyFamily { F_TBQ4 = 0, F_Q = 1 };
+// The pure instances (F_TBQ4_ONLY: TBQ4 keys and values; F_Q84: Q8_0 / Q4_0 keys and values)
+// compile only their own encoders, which keeps the kernel's code, and its instruction-cache
+// misses, small for the layouts the workloads use.
+enum BodyFamily { F_TBQ4 = 0, F_Q = 1, F_TBQ4_ONLY = 2, F_Q84 = 3 };
+template <int FAM> constexpr bool kRotFam = FAM == F_TBQ4 || FAM == F_TBQ4_ONLY;
 
 // Decodes the tiles of iterations k0 .. k0 + kSlotBatch - 1 into the slot ring (threads 4j).
 __device__ __forceinline__ void fill_slots(const Layout& L, const SealParams& p, int n_tiles, TileSlot* slot, int k0) {
@@ -478,9 +482,9 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
     __shared__ TileSlot slot[kSlots];
     uint32_t* qt = reinterpret_cast<uint32_t*>(sm + kStages * stage_bytes);
     uint32_t* qt3 = qt + kBuckets;                  // turbo3's table, present when a body is turbo3
-    if constexpr (FAM == F_TBQ4) {                  // read after the first barrier below
+    if constexpr (kRotFam<FAM>) {                   // read after the first barrier below
         build_qtab(qt, c_tab.bnd, 15);
-        if (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3) build_qtab(qt3, c_tab.bnd3, 7);
+        if (FAM == F_TBQ4 && (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3)) build_qtab(qt3, c_tab.bnd3, 7);
     }
     const int t = threadIdx.x, D = L.D;
     // Iteration it encodes tile blockIdx.x + it * gridDim.x from stage it % kStages. After the
@@ -520,16 +524,16 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
 #pragma unroll
                 for (int i = 0; i < 128; ++i) y[i] = bf2f(f2bf_bits(y[i]));
             }
-            if constexpr (FAM == F_TBQ4) rotate_tbq128(y);
+            if constexpr (kRotFam<FAM>) rotate_tbq128(y);
             if (L.journal == KVQ_TQ6_0) tq6_roundtrip(y);
         } else {
             decode_x16<JK>(st, y);
-            if constexpr (FAM == F_TBQ4) rotate_tbq128(y);
+            if constexpr (kRotFam<FAM>) rotate_tbq128(y);
         }
         uint8_t* rec = tl.rec;
         const int fmt = L.fmt[tl.w];
-        if constexpr (FAM == F_TBQ4) {
-            if (fmt == KVQ_TQ5_0) {   // token-major: nibble plane, one-bit plane, scales
+        if constexpr (kRotFam<FAM>) {
+            if (FAM == F_TBQ4 && fmt == KVQ_TQ5_0) {   // token-major: nibble plane, one-bit plane, scales
                 uint32_t C[32], P[16], hb[4];
                 const uint16_t d16 = encode_tq5(y, C);
 #pragma unroll
@@ -545,7 +549,7 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
                 flag_nonfinite(L, p.pool, h2f(d16));
             } else {
                 uint32_t P[16];
-                const bool t3 = (fmt == KVQ_TURBO3);
+                const bool t3 = FAM == F_TBQ4 && fmt == KVQ_TURBO3;
                 const uint16_t n16 = encode_tbq4(y, t3 ? qt3 : qt, P);
                 if (t3) {   // token-major: 2-bit plane, one-bit plane, norms
                     uint32_t cw[8], bw[4];
@@ -573,18 +577,23 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 uint32_t c[8];
-                switch (fmt) {
-                    case KVQ_Q8_0: d16[j] = encode_q32<127>(y, 32 * j, c); break;
-                    case KVQ_Q4_0: d16[j] = encode_q32<7>(y, 32 * j, c); break;
-                    case KVQ_Q5_0: d16[j] = encode_q32<15>(y, 32 * j, c); break;
-                    case KVQ_Q6_0: d16[j] = encode_q32<31>(y, 32 * j, c); break;
-                    case KVQ_Q4_1: d16[j] = encode_qmin<15>(y, 32 * j, c, m16[j]); break;
-                    default: d16[j] = encode_qmin<31>(y, 32 * j, c, m16[j]); break;
+                if constexpr (FAM == F_Q84) {
+                    if (fmt == KVQ_Q8_0) d16[j] = encode_q32<127>(y, 32 * j, c);
+                    else d16[j] = encode_q32<7>(y, 32 * j, c);
+                } else {
+                    switch (fmt) {
+                        case KVQ_Q8_0: d16[j] = encode_q32<127>(y, 32 * j, c); break;
+                        case KVQ_Q4_0: d16[j] = encode_q32<7>(y, 32 * j, c); break;
+                        case KVQ_Q5_0: d16[j] = encode_q32<15>(y, 32 * j, c); break;
+                        case KVQ_Q6_0: d16[j] = encode_q32<31>(y, 32 * j, c); break;
+                        case KVQ_Q4_1: d16[j] = encode_qmin<15>(y, 32 * j, c, m16[j]); break;
+                        default: d16[j] = encode_qmin<31>(y, 32 * j, c, m16[j]); break;
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < 8; ++k) C[8 * j + k] = c[k];
             }
-            const int qbits = qblock_bits(fmt);
+            const int qbits = (FAM == F_Q84) ? 0 : qblock_bits(fmt);
             int64_t sc_off;
             if (fmt == KVQ_Q8_0) {
                 store_bytes(rec, D, tl.b, tl.w, C);
@@ -634,7 +643,7 @@ template <int JK, int FAM>
 int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t s) {
     const int stage = (JK == J_TQ6) ? kRows * kTq6Stride + 2 * L.D : kRows * kX16Stride;
     const bool t3 = (L.fmt[0] == KVQ_TURBO3 || L.fmt[1] == KVQ_TURBO3);
-    const size_t smem = (size_t)kStages * stage + (FAM == F_TBQ4 ? (t3 ? 2 : 1) * kBuckets * sizeof(uint32_t) : 0);
+    const size_t smem = (size_t)kStages * stage + (kRotFam<FAM> ? (t3 ? 2 : 1) * kBuckets * sizeof(uint32_t) : 0);
     auto fn = seal_rows_kernel<JK, FAM>;
     int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
@@ -1171,7 +1180,13 @@ int launch_seal_rows(const Layout& L, const SealParams& p, void* stream) {
     cudaStream_t s = (cudaStream_t)stream;
     const bool tbq = (rotation_of(L.fmt[0]) == ROT_TBQ128);
     if (tbq != (rotation_of(L.fmt[1]) == ROT_TBQ128)) return (int)cudaErrorInvalidValue;   // one rotation per layout
-    return tbq ? launch_family<F_TBQ4>(L, p, n_tiles, s) : launch_family<F_Q>(L, p, n_tiles, s);
+    if (tbq) {
+        if (L.fmt[0] == KVQ_TBQ4 && L.fmt[1] == KVQ_TBQ4) return launch_family<F_TBQ4_ONLY>(L, p, n_tiles, s);
+        return launch_family<F_TBQ4>(L, p, n_tiles, s);
+    }
+    auto q84 = [](int f) { return f == KVQ_Q8_0 || f == KVQ_Q4_0; };
+    if (q84(L.fmt[0]) && q84(L.fmt[1])) return launch_family<F_Q84>(L, p, n_tiles, s);
+    return launch_family<F_Q>(L, p, n_tiles, s);
 }
 
 int query_sm_count(int device) {
