@@ -925,14 +925,16 @@ __device__ __forceinline__ void kv_plane(uint32_t* plane, const uint8_t* codes, 
 // [16][256] fp32, then (once the passes are done, over them) the codes; after them the staged
 // rows of the half (tq6_0: [128][192] codes + [128][D/128] scales; 16-bit: [128][512]), then
 // (once decoded, over them) the fp32 copy of the unbalanced tile.
-template <int JK>
+// BITS: 0 = any code width and balancing read from the layout; 4 = 4-bit keys and values with
+// the 16-pass balancing (an instance with only that code: fewer instruction-cache misses).
+template <int JK, int BITS>
 __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
     constexpr int ROW = KvStage<JK>::ROW;
     const SealTaskPos tk = seal_task(p, blockIdx.x);
     const int nh = L.D / 256;
     const int h = blockIdx.y, w = blockIdx.z / nh, half = blockIdx.z % nh;
     const int fmt = L.fmt[w];
-    const int bits = kvarn_bits(fmt);
+    const int bits = BITS ? BITS : kvarn_bits(fmt);
     const float Q = (float)((1 << bits) - 1);
     const int64_t unit = L.unit(tk.layer, tk.slot, h);
     extern __shared__ __align__(16) uint8_t kv_sm[];
@@ -1010,7 +1012,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
                                                        x[n >> 1][4 * (n & 1) + 2], x[n >> 1][4 * (n & 1) + 3]);
 
     int passes = 16;
-    if (L.kvarn_best) {
+    if (BITS == 0 && L.kvarn_best) {
         // the KVarN reference configuration: 8 passes, keeping the state with the smallest
         // imbalance (largest |sigma - 1| over the lines the last pass left unbalanced). Pass p
         // measures the state of pass p - 1 on its own axis while it balances it; a measuring
@@ -1039,6 +1041,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         __syncthreads();
         reload();
     }
+#pragma unroll 1
     for (int pass = 0; pass < passes; ++pass) {
         if ((pass & 1) == 0) kv_row_pass(x, r, warp, lane);
         else kv_col_pass(x, c, part, mu_s, inv_s, warp, lane);
@@ -1144,16 +1147,22 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     }
 }
 
-template <int JK>
-int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
+template <int JK, int BITS>
+int launch_kvarn_b(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
     constexpr int ROW = KvStage<JK>::ROW;
     const size_t stage = 128 * ROW + (JK == J_TQ6 ? 2 * L.D : 0);
     const size_t smem = kCodeBytes + (stage > kTileBytes ? stage : kTileBytes);
-    int e = (int)cudaFuncSetAttribute(seal_kvarn_kernel<JK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto fn = seal_kvarn_kernel<JK, BITS>;
+    int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
     dim3 grid(groups, L.H, 2 * (L.D / 256));
-    seal_kvarn_kernel<JK><<<grid, kKvThreads, smem, s>>>(L, p);
+    fn<<<grid, kKvThreads, smem, s>>>(L, p);
     return (int)cudaGetLastError();
+}
+template <int JK>
+int launch_kvarn(const Layout& L, const SealParams& p, int groups, cudaStream_t s) {
+    if (L.fmt[0] == KVQ_KVARN4 && L.fmt[1] == KVQ_KVARN4 && !L.kvarn_best) return launch_kvarn_b<JK, 4>(L, p, groups, s);
+    return launch_kvarn_b<JK, 0>(L, p, groups, s);
 }
 
 }  // namespace
