@@ -927,7 +927,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
 // ------------------------------------------------------------------------------ the kernel
 // Decode attention over one call's work list: CTAs [0, n_body) take the body items (the long
 // ones, so they start first), the rest the region items (tq6_0 ring, 16-bit rows).
-template <int D, int NQ, int KF, int VF, int KB, int VB>
+template <int D, int NQ, int KF, int VF, int KB, int VB, int RK>
 __global__ void __launch_bounds__(kCT, (Geo<D, NQ, KF, VF, KB, VB>::MINB))
 decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ AttnParams p, int n_body, int nst) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -936,13 +936,13 @@ decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ Att
     // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory
     if (p.region_first) {
         if ((int)blockIdx.x < p.n_region_items)
-            region_item<D, NQ>(L, p, (int)blockIdx.x, smem, s_abort);
+            region_item<D, NQ, RK>(L, p, (int)blockIdx.x, smem, s_abort);
         else
             body_item<D, NQ, KF, VF, KB, VB>(L, p, (int)blockIdx.x, nst, smem, s_abort);
     } else if ((int)blockIdx.x < n_body) {
         body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
     } else {
-        region_item<D, NQ>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
+        region_item<D, NQ, RK>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
     }
 }
 
@@ -960,7 +960,12 @@ int nstages(const Layout& L) {
     return nst >= 2 ? nst : 0;
 }
 
-template <int D, int NQ, int KF, int VF, int KB, int VB>
+// The region kinds a layout can hold: bit 0 a tq6_0 ring, bit 1 bf16 rows (journal or tail).
+inline int region_kinds(const Layout& L) {
+    return (L.journal == KVQ_TQ6_0 ? 1 : 0) | ((L.journal == KVQ_BF16 || L.tail_fmt == KVQ_BF16) ? 2 : 0);
+}
+
+template <int D, int NQ, int KF, int VF, int KB, int VB, int RK>
 int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cudaStream_t st, bool pdl) {
     using Gm = Geo<D, NQ, KF, VF, KB, VB>;
     const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
@@ -970,7 +975,7 @@ int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cud
         const size_t sr = (size_t)RGeo<D, NQ>::smem(L.tail_fmt == KVQ_BF16 || L.journal == KVQ_BF16);
         smem = smem > sr ? smem : sr;
     }
-    auto kern = decode_attn_kernel<D, NQ, KF, VF, KB, VB>;
+    auto kern = decode_attn_kernel<D, NQ, KF, VF, KB, VB, RK>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
     const cudaError_t e = launch_k(kern, dim3(n_body + n_region), dim3(kCT), smem, st, pdl, L, p, n_body, nst);
@@ -982,20 +987,26 @@ int launch_t(const Layout& L, const AttnParams& p, int n_body, int n_region, cud
 template <typename F>
 int dispatch(const Layout& L, F&& f) {
     const int k = L.fmt[0], v = L.fmt[1];
-#define KVQ_BODY_CASE(D_, NQ_, KF_, VF_, KB_, VB_, KFMT, VFMT) \
-    if (L.D == D_ && L.NQ == NQ_ && k == KFMT && v == VFMT) return f.template run<D_, NQ_, KF_, VF_, KB_, VB_>();
-    KVQ_BODY_CASE(128, 8, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4)
-    KVQ_BODY_CASE(256, 8, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4)
-    KVQ_BODY_CASE(256, 16, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4)
-    KVQ_BODY_CASE(128, 8, KF_Q8, KF_Q4, 4, 4, KVQ_Q8_0, KVQ_Q4_0)
-    KVQ_BODY_CASE(128, 16, KF_Q8, KF_Q4, 4, 4, KVQ_Q8_0, KVQ_Q4_0)
-    KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4)
-    KVQ_BODY_CASE(256, 16, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4)
-    KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 3, 2, KVQ_KVARN3, KVQ_KVARN2)
-    KVQ_BODY_CASE(512, 8, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
-    KVQ_BODY_CASE(512, 16, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5)
-    KVQ_BODY_CASE(128, 8, KF_Q51, KF_Q4, 5, 4, KVQ_Q5_1, KVQ_Q4_0)
-    KVQ_BODY_CASE(256, 8, KF_TQ5, KF_TBQ4, 5, 4, KVQ_TQ5_0, KVQ_TBQ4)
+    const int rk = region_kinds(L);
+    // SPEC: the region kinds of the workloads' layout for that case, which gets an instance of
+    // its own (only those region readers: less code); other layouts take the generic instance
+#define KVQ_BODY_CASE(D_, NQ_, KF_, VF_, KB_, VB_, KFMT, VFMT, SPEC)                            \
+    if (L.D == D_ && L.NQ == NQ_ && k == KFMT && v == VFMT) {                                    \
+        if (SPEC != 3 && rk == SPEC) return f.template run<D_, NQ_, KF_, VF_, KB_, VB_, SPEC>(); \
+        return f.template run<D_, NQ_, KF_, VF_, KB_, VB_, 3>();                                 \
+    }
+    KVQ_BODY_CASE(128, 8, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4, 0)
+    KVQ_BODY_CASE(256, 8, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4, 1)
+    KVQ_BODY_CASE(256, 16, KF_TBQ4, KF_TBQ4, 4, 4, KVQ_TBQ4, KVQ_TBQ4, 3)
+    KVQ_BODY_CASE(128, 8, KF_Q8, KF_Q4, 4, 4, KVQ_Q8_0, KVQ_Q4_0, 2)
+    KVQ_BODY_CASE(128, 16, KF_Q8, KF_Q4, 4, 4, KVQ_Q8_0, KVQ_Q4_0, 3)
+    KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4, 1)
+    KVQ_BODY_CASE(256, 16, KF_KVARN, KF_KVARN, 4, 4, KVQ_KVARN4, KVQ_KVARN4, 3)
+    KVQ_BODY_CASE(256, 8, KF_KVARN, KF_KVARN, 3, 2, KVQ_KVARN3, KVQ_KVARN2, 1)
+    KVQ_BODY_CASE(512, 8, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5, 3)
+    KVQ_BODY_CASE(512, 16, KF_KVARN, KF_KVARN, 5, 5, KVQ_KVARN5, KVQ_KVARN5, 0)
+    KVQ_BODY_CASE(128, 8, KF_Q51, KF_Q4, 5, 4, KVQ_Q5_1, KVQ_Q4_0, 2)
+    KVQ_BODY_CASE(256, 8, KF_TQ5, KF_TBQ4, 5, 4, KVQ_TQ5_0, KVQ_TBQ4, 1)
 #undef KVQ_BODY_CASE
     return -1;
 }
@@ -1003,7 +1014,7 @@ int dispatch(const Layout& L, F&& f) {
 struct CtasFn {
     const Layout& L;
     bool regions;
-    template <int D, int NQ, int KF, int VF, int KB, int VB>
+    template <int D, int NQ, int KF, int VF, int KB, int VB, int RK>
     int run() {
         using Gm = Geo<D, NQ, KF, VF, KB, VB>;
         const int nst = nstages<D, NQ, KF, VF, KB, VB>(L);
@@ -1023,8 +1034,8 @@ struct LaunchFn {
     int n_body, n_region;
     cudaStream_t s;
     bool pdl;
-    template <int D, int NQ, int KF, int VF, int KB, int VB>
-    int run() { return launch_t<D, NQ, KF, VF, KB, VB>(L, p, n_body, n_region, s, pdl); }
+    template <int D, int NQ, int KF, int VF, int KB, int VB, int RK>
+    int run() { return launch_t<D, NQ, KF, VF, KB, VB, RK>(L, p, n_body, n_region, s, pdl); }
 };
 
 // The bounded wait's timeout path, exercised on purpose (a test launch): one CTA, thread 0

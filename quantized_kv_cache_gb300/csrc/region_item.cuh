@@ -107,8 +107,9 @@ __device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 
 // One region work item, run by a CTA of 8 warps on the dynamic shared memory `smem`; s_abort is
-// the CTA's abort flag (a __shared__ int).
-template <int D, int NQ>
+// the CTA's abort flag (a __shared__ int). RK: the region kinds the layout can hold (bit 0: a
+// tq6_0 ring, bit 1: bf16 rows); an instance compiles only their readers.
+template <int D, int NQ, int RK>
 __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p, const int item, uint8_t* smem,
                                             int& s_abort) {
     using Gm = RGeo<D, NQ>;
@@ -127,9 +128,9 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     const int ck = (kind == RK_RING) ? p.ring_chunk : p.chunk;
     const int t0 = sp.lo[r] + cidx * ck;
     const int t1 = min(t0 + ck, sp.hi[r]);
-    const bool ring = Gm::RING && (kind == RK_RING);
+    const bool ring = Gm::RING && (RK & 1) && (kind == RK_RING);
     // bf16 exact rows: bf16 mma, the query and P' each split into bf16 high and low parts
-    const bool bf = !ring && kind != RK_SINK && ((kind == RK_TAIL ? L.tail_fmt : L.journal) == KVQ_BF16);
+    const bool bf = (RK & 2) && !ring && kind != RK_SINK && ((kind == RK_TAIL ? L.tail_fmt : L.journal) == KVQ_BF16);
     const int RUN = ring ? 128 : Gm::RUNF;                // positions per run
     const int nrun = (t1 - t0 + RUN - 1) / RUN;
     const int64_t unit = L.unit(p.layer, sp.slot, h);
@@ -138,7 +139,8 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     const uint32_t stage_bytes = ring ? Gm::TQ_STAGE : Gm::F_STAGE;
     const uint32_t half_bytes = ring ? Gm::TQ_HALF : Gm::F_HALF;
     const int nst = min(4, Gm::AREA / (int)stage_bytes);
-    if (nst < 2 || (!Gm::RING && kind == RK_RING)) {   // a ring at head_dim 512 is not routed here: refuse
+    // a ring at head_dim 512 is not routed here, nor to an instance without the ring reader: refuse
+    if (nst < 2 || ((!Gm::RING || !(RK & 1)) && kind == RK_RING)) {
         grid_dep_wait();
         if (threadIdx.x == 0) atomicOr(status_word(L, p.pool), 4u);
         return;
@@ -146,7 +148,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     uint8_t* stages = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Gm::AREA);
     uint8_t* cur = smem + Gm::AREA + 128;
-    const bool has_bf = (L.tail_fmt == KVQ_BF16) || (L.journal == KVQ_BF16);
+    const bool has_bf = (RK & 2) && ((L.tail_fmt == KVQ_BF16) || (L.journal == KVQ_BF16));
     uint32_t* qb = reinterpret_cast<uint32_t*>(cur);      cur += (has_bf ? 2 : 1) * Gm::QB_BYTES;   // bf16: hi, lo
     uint32_t* pbuf = reinterpret_cast<uint32_t*>(cur);    cur += Gm::P_BYTES;
     float* red = reinterpret_cast<float*>(cur);           // [NQ][warp] maxima, then sums; m at 2 NQ 8
