@@ -199,8 +199,10 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     // free (the first barrier of group i - nst + 1 follows every read of group i - nst)
     const uint8_t* kb = body_rec(L, p.pool, 0, unit, g0);
     const uint8_t* vb = body_rec(L, p.pool, 1, unit, g0);
+    int isl = 0;                                          // stage of the next issue (thread 0): issued % nst
     auto issue = [&](int i) {
-        const int sl = i % nst;
+        const int sl = isl;
+        isl = (isl + 1 == nst) ? 0 : isl + 1;
         const uint32_t dst = su32(stages + (size_t)sl * stage_bytes);
         const uint32_t fb = su32(&full[sl]);
         mbar_expect_tx(fb, recK + recV);
@@ -385,9 +387,11 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
         for (int mt = 0; mt < MT; ++mt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
     }
 
-    for (int gi = 0; gi < ngroups; ++gi) {
-        const int sl = gi % nst;
-        mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
+    // the stage of group gi (gi % nst) and its barrier phase ((gi / nst) & 1), stepped per group
+    int sl = 0;
+    uint32_t phase = 0;
+    for (int gi = 0; gi < ngroups; ++gi, sl = (sl + 1 == nst) ? 0 : sl + 1, phase ^= (sl == 0)) {
+        mbar_wait(su32(&full[sl]), phase, status, &s_abort);
         const uint8_t* kr = stages + (size_t)sl * stage_bytes;
         const uint8_t* vr = kr + v_off;
         if constexpr (Gm::KIMG || Gm::VIMG) {

@@ -158,8 +158,10 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // thread 0 streams the runs: run i into stage i % nst, issued once stage i % nst is free
     // (the first barrier of run i - nst + 1 follows every read of run i - nst)
+    int isl = 0;                                          // stage of the next issue (thread 0): i % nst
     auto issue = [&](int i) {
-        const int sl = i % nst;
+        const int sl = isl;
+        isl = (isl + 1 == nst) ? 0 : isl + 1;
         const int pc = t0 + RUN * i, n = min(RUN, t1 - pc);
         uint8_t* st = stages + (size_t)sl * stage_bytes;
         const uint32_t fb = su32(&full[sl]);
@@ -363,9 +365,11 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
         for (int mt = 0; mt < MT; ++mt) O[mt][nt][0] = O[mt][nt][1] = O[mt][nt][2] = O[mt][nt][3] = 0.f;
     }
 
-    for (int gi = 0; gi < nrun; ++gi) {
-        const int sl = gi % nst;
-        mbar_wait(su32(&full[sl]), (gi / nst) & 1, status, &s_abort);
+    // the stage of run gi (gi % nst) and its barrier phase ((gi / nst) & 1), stepped per run
+    int sl = 0;
+    uint32_t phase = 0;
+    for (int gi = 0; gi < nrun; ++gi, sl = (sl + 1 == nst) ? 0 : sl + 1, phase ^= (sl == 0)) {
+        mbar_wait(su32(&full[sl]), phase, status, &s_abort);
         const int n = min(RUN, t1 - (t0 + RUN * gi));
         uint8_t* kr = stages + (size_t)sl * stage_bytes;
         uint8_t* vr = kr + half_bytes;
