@@ -31,6 +31,11 @@ namespace kvq {
 namespace {
 
 // ------------------------------------------------------------------------------ geometry
+// The rotation of a layout follows from its key format: HAD256 for KVarN, TBQ128 for TBQ4 and
+// tq5_0 keys, none for the block formats (an instance compiles only its own rotation).
+template <int KF>
+constexpr int kRotOf = (KF == KF_KVARN) ? (int)ROT_HAD256 : ((KF == KF_TBQ4 || KF == KF_TQ5) ? (int)ROT_TBQ128 : (int)ROT_NONE);
+
 template <int D, int NQ, int KF, int VF, int KB, int VB>
 struct Geo {
     static constexpr int NT = NQ / 8;
@@ -255,7 +260,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     mbar_wait(qbar, 0, status, &s_abort);
     {
         const uint16_t* q = reinterpret_cast<const uint16_t*>(qr);
-        const int rot = L.rot;
+        constexpr int rot = kRotOf<KF>;
         if (rot == ROT_HAD256) {
             if constexpr (D >= 256) {
                 for (int u = warp; u < NQ * (D / 256); u += kConsumers) {
@@ -925,7 +930,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
     }
     csync();
     write_partial<D, NQ>(ofin, red + (NVB + 1) * NQ * 8, red + (NVB + 1) * NQ * 8 + NQ,
-                         p.partials + (size_t)item * (2 * NQ + NQ * D), L.rot);
+                         p.partials + (size_t)item * (2 * NQ + NQ * D), kRotOf<KF>);
 }
 
 // ------------------------------------------------------------------------------ the kernel
@@ -940,13 +945,13 @@ decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ Att
     // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory
     if (p.region_first) {
         if ((int)blockIdx.x < p.n_region_items)
-            region_item<D, NQ, RK>(L, p, (int)blockIdx.x, smem, s_abort);
+            region_item<D, NQ, RK, kRotOf<KF>>(L, p, (int)blockIdx.x, smem, s_abort);
         else
             body_item<D, NQ, KF, VF, KB, VB>(L, p, (int)blockIdx.x, nst, smem, s_abort);
     } else if ((int)blockIdx.x < n_body) {
         body_item<D, NQ, KF, VF, KB, VB>(L, p, p.n_region_items + (int)blockIdx.x, nst, smem, s_abort);
     } else {
-        region_item<D, NQ, RK>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
+        region_item<D, NQ, RK, kRotOf<KF>>(L, p, (int)blockIdx.x - n_body, smem, s_abort);
     }
 }
 

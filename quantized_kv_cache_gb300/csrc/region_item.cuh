@@ -108,8 +108,9 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 
 // One region work item, run by a CTA of 8 warps on the dynamic shared memory `smem`; s_abort is
 // the CTA's abort flag (a __shared__ int). RK: the region kinds the layout can hold (bit 0: a
-// tq6_0 ring, bit 1: bf16 rows); an instance compiles only their readers.
-template <int D, int NQ, int RK>
+// tq6_0 ring, bit 1: bf16 rows); an instance compiles only their readers. ROT: the layout's
+// rotation (that of the ring's rows).
+template <int D, int NQ, int RK, int ROT>
 __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p, const int item, uint8_t* smem,
                                             int& s_abort) {
     using Gm = RGeo<D, NQ>;
@@ -245,7 +246,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     mbar_wait(qbar, 0, status, &s_abort);
     {
         const uint16_t* q = reinterpret_cast<const uint16_t*>(qr);
-        const int rot = ring ? L.rot : (int)ROT_NONE;
+        const int rot = ring ? ROT : (int)ROT_NONE;
         if (rot == ROT_HAD256) {
             if constexpr (D >= 256) {
                 for (int u = warp; u < NQ * (D / 256); u += kConsumers) {
@@ -715,7 +716,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
     }
     csync();
     write_partial<D, NQ>(ofin, red + 2 * NQ * 8, red + 2 * NQ * 8 + NQ, p.partials + (size_t)item * (2 * NQ + NQ * D),
-                         ring ? L.rot : (int)ROT_NONE);
+                         ring ? ROT : (int)ROT_NONE);
 }
 
 }  // namespace
