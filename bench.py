@@ -78,13 +78,13 @@ def peaks():
 # the line reports null until a new capture replaces it.
 DECODE_SOURCES = ("kernels_body.cu", "region_item.cuh", "stream_common.cuh", "device_common.cuh", "append_row.cuh")
 MEASURED_TRAFFIC = {
-    "hybrid27b_kvarn44": (42.89e6, "142a63383091"),
-    "fa14b_q8q4": (221.96e6, "142a63383091"),
-    "longctx_tbq4": (750.54e6, "142a63383091"),
-    "widehead_kvarn55": (193.64e6, "142a63383091"),
-    "hybrid27b_kvarn32_200k": (156.95e6, "142a63383091"),
-    "fa14b_q51q40": (180.41e6, "142a63383091"),
-    "hybrid27b_tq50tbq4_110k": (140.09e6, "142a63383091"),
+    "hybrid27b_kvarn44": (42.88e6, "f52ada9c5576"),
+    "fa14b_q8q4": (222.02e6, "f52ada9c5576"),
+    "longctx_tbq4": (750.89e6, "f52ada9c5576"),
+    "widehead_kvarn55": (193.69e6, "f52ada9c5576"),
+    "hybrid27b_kvarn32_200k": (156.95e6, "f52ada9c5576"),
+    "fa14b_q51q40": (180.48e6, "f52ada9c5576"),
+    "hybrid27b_tq50tbq4_110k": (140.15e6, "f52ada9c5576"),
 }
 
 
@@ -486,9 +486,11 @@ def measure_seal(w, cache, inp, seq_ids, out, restore, stream, K, ds=None):
         for l in range(w.n_layers):
             _lib.kv_append(cache.h, l, seq_ids, 1, inp.k[target, l].data_ptr(), inp.v[target, l].data_ptr(), stream)
         torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("policy_seal")
         ev0.record()
         groups = _lib.kv_seal(cache.h, -1, seq_ids, w.keep, stream)
         ev1.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize()
         t = ev0.elapsed_time(ev1) / 1e3
         kind = "seal at the policy's trigger, all layers in one call (as the decode step issues it)"
