@@ -79,13 +79,18 @@ __device__ __forceinline__ void flag_nonfinite(const Layout& L, const void* pool
 }
 
 // Programmatic dependent launch (sm_90 and later). A kernel launched with programmatic stream
-// serialization may be scheduled before the launch ahead of it in the stream has finished
-// (as that launch's CTAs exit: none of these kernels triggers earlier, since CTAs parked in
-// the wait early took SM time from the launch ahead: hybrid 32k decode steps 24% slower).
+// serialization may be scheduled before the launch ahead of it in the stream has finished:
+// as that launch's CTAs exit, or once every one of them has executed grid_dep_launch.
 // grid_dep_wait blocks until the launches it depends on have completed and their memory
 // operations are visible; it returns at once in a kernel launched without the attribute.
-// Every kernel launched this way executes grid_dep_wait before its first global memory access.
+// Every kernel launched this way executes grid_dep_wait before its first global memory access,
+// except the decode kernel's items when the launch ahead is the merge kernel (AttnParams::early).
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next launch in the stream start. Only the merge kernel calls it, after its own
+// grid_dep_wait: when the next launch starts, the launch ahead of the merge has completed.
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
 
 // Launches kernel k; with pdl, with programmatic stream serialization (see above).
 template <typename... P, typename... A>

@@ -620,6 +620,9 @@ constexpr int kMergeMaxItems = 1024;
 template <int D, int NQ>
 __global__ void __launch_bounds__(256) decode_merge_kernel(Layout L, AttnParams p) {
     grid_dep_wait();          // the partials of the launch ahead are complete and visible
+    // the next layer's decode kernel may start now: its items read nothing this kernel writes
+    // and write their partials only after waiting for it (AttnParams::early)
+    grid_dep_launch();
     const int bh = blockIdx.x;
     const int b = bh / L.H, h = bh % L.H;
     const SeqSpan& s = p.seq[b];

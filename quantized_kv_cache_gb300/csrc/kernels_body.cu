@@ -236,7 +236,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
             lut[i] = pack_f2(c_tab.cent[by & 15], c_tab.cent[by >> 4]);
         }
     }
-    grid_dep_wait();
+    if (!p.early) grid_dep_wait();
     if (threadIdx.x == 0) {
         mbar_expect_tx(qbar, (uint32_t)(G * D * 2));
         bulk_g2s(su32(qb), qsrc, (uint32_t)(G * D * 2), qbar);
@@ -929,6 +929,7 @@ __device__ __forceinline__ void body_item(const Layout& L, const AttnParams& p, 
         red[(NVB + 1) * NQ * 8 + NQ + threadIdx.x] = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
     }
     csync();
+    if (p.early) grid_dep_wait();   // the merge ahead has read the partials buffer
     write_partial<D, NQ>(ofin, red + (NVB + 1) * NQ * 8, red + (NVB + 1) * NQ * 8 + NQ,
                          p.partials + (size_t)item * (2 * NQ + NQ * D), kRotOf<KF>);
 }
@@ -942,7 +943,8 @@ decode_attn_kernel(const __grid_constant__ Layout L, const __grid_constant__ Att
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     // launched with programmatic serialization, the CTAs may be placed while the launch ahead
-    // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory
+    // drains: each item waits for it (grid_dep_wait) before it reads or writes global memory,
+    // or, after the previous layer's merge (p.early), before it writes its partial
     if (p.region_first) {
         if ((int)blockIdx.x < p.n_region_items)
             region_item<D, NQ, RK, kRotOf<KF>>(L, p, (int)blockIdx.x, smem, s_abort);

@@ -565,6 +565,7 @@ kvq_status decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_se
     p.n_seq = n_seq;
     const bool body_kernel = body_ctas_per_sm(L) > 0;
     const bool fused = body_kernel && region_kernel_ok(L);
+    p.early = (marks.early && marks.pdl && fused) ? 1 : 0;
     int64_t region_tok = 0, body_groups = 0;
     for (int i = 0; i < n_seq; ++i) {
         SeqSpan& s = p.seq[i];
@@ -740,6 +741,15 @@ bool pdl_enabled() {
     }();
     return on;
 }
+// The decode kernel of a step's later layers reads its inputs while the previous layer's merge
+// runs (AttnParams::early), unless the environment sets KVQ_EARLY=0.
+bool early_enabled() {
+    static const bool on = [] {
+        const char* e = std::getenv("KVQ_EARLY");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
 }  // namespace
 
 kvq_status kv_decode_attn(kvq_cache* c, int layer, const int32_t* seq_ids, int n_seq, const void* q, void* out,
@@ -857,6 +867,10 @@ kvq_status step_launches(kvq_cache* c, int n_layers, const int32_t* seq_ids, int
             marks.flags = ev_flags;
         }
         if (!events || side) marks.pdl = pdl_enabled();
+        // every layer after the first follows its predecessor's merge kernel in the stream (a
+        // layer's decode launch always holds at least the newest position). Not in a pass that
+        // times the decode kernels: their events would not bracket the work done early.
+        marks.early = all_fused && l > 0 && !events && early_enabled();
         if (side) {
             marks.side = c->mark_stream;
             marks.fork = c->mark_fork;

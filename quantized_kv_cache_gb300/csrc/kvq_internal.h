@@ -183,6 +183,11 @@ struct AttnParams {
     int32_t n_region_items;  // region items come first, body items after them
     int32_t ring_chunk;      // positions per region item of a tq6_0 ring span (others: chunk)
     int32_t region_first;    // the streaming kernel's first blocks take the region items (else the body items)
+    // 1: the launch ahead in the stream is the merge kernel of the previous layer of the same
+    // decode step, which lets this launch start once every launch before it has completed. The
+    // items then read the cache and the step's inputs at once (nothing the merge writes) and
+    // wait for the merge only before writing their partials (the buffer it is reading).
+    int32_t early;
     SeqSpan seq[kMaxSeqPerCall];
 };
 
@@ -243,6 +248,7 @@ struct LaunchMarks {
     void* after = nullptr;
     unsigned flags = 0;
     bool pdl = false;      // launch the decode and merge kernels with programmatic stream serialization
+    bool early = false;    // with pdl: the launch ahead is this step's previous merge (AttnParams::early)
     // with side (a stream joined to the capture) and fork (an event) set, each mark is recorded
     // on the side stream after a fork from the launching stream, so no event node sits between
     // two kernels and their programmatic launch stays in place

@@ -222,7 +222,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
         for (int i = 0; i < 5; ++i) mbar_init(su32(&full[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
-    grid_dep_wait();          // the launch ahead (programmatic serialization) has completed
+    if (!p.early) grid_dep_wait();   // the launch ahead (programmatic serialization) has completed
     if (threadIdx.x == 0) {
         mbar_expect_tx(qbar, (uint32_t)(G * D * 2));
         bulk_g2s(su32(qb), qsrc, (uint32_t)(G * D * 2), qbar);
@@ -715,6 +715,7 @@ __device__ __forceinline__ void region_item(const Layout& L, const AttnParams& p
         red[2 * NQ * 8 + NQ + threadIdx.x] = ((x.x + x.y) + (x.z + x.w)) + ((y.x + y.y) + (y.z + y.w));
     }
     csync();
+    if (p.early) grid_dep_wait();   // the merge ahead has read the partials buffer
     write_partial<D, NQ>(ofin, red + 2 * NQ * 8, red + 2 * NQ * 8 + NQ, p.partials + (size_t)item * (2 * NQ + NQ * D),
                          ring ? ROT : (int)ROT_NONE);
 }
