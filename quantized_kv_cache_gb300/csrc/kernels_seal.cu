@@ -156,6 +156,7 @@ __device__ __forceinline__ void decode_tq6(const uint8_t* st, int D, int b, floa
     }
     const float d = h2f(reinterpret_cast<const uint16_t*>(st + kRows * kTq6Stride)[t * (D / 128) + b]);
     const float a = fmul(-32800.0f, d);
+    const float2 d2 = make_float2(d, d), a2 = make_float2(a, a);
 #pragma unroll
     for (int w = 0; w < 16; ++w) {
         uint32_t x = (w & 1) ? (h[w >> 1] >> 16) : (h[w >> 1] & 0xFFFFu);
@@ -168,8 +169,9 @@ __device__ __forceinline__ void decode_tq6(const uint8_t* st, int D, int b, floa
         for (int k = 0; k < 4; ++k) {
             const float ce = __uint_as_float(__byte_perm(ev, 0x47000000u, 0x7404 + 16 * k));
             const float co = __uint_as_float(__byte_perm(od, 0x47000000u, 0x7404 + 16 * k));
-            y[8 * w + 2 * k] = __fmaf_rn(ce, d, a);
-            y[8 * w + 2 * k + 1] = __fmaf_rn(co, d, a);
+            const float2 v = ffma2(make_float2(ce, co), d2, a2);
+            y[8 * w + 2 * k] = v.x;
+            y[8 * w + 2 * k + 1] = v.y;
         }
     }
 }
@@ -222,7 +224,10 @@ __device__ __forceinline__ void rotate_tbq128(float (&y)[128]) {
 // ---------------------------------------------------------------------------- encoders
 // Node (K, I) of the halving tree of y_i^2 over 128 values: node(0, i) = y_i^2 and
 // node(K, i) = node(K-1, i) + node(K-1, i + 128 / 2^K); node(7, 0) is the sum. Evaluated
-// depth first so that few partial sums are live beside the 128 values.
+// depth first so that few partial sums are live beside the 128 values. Scalar operations: a
+// packed multiply whose result feeds a packed add may be contracted into a packed multiply-add
+// by the code generator even with explicit rounding modifiers (measured on GB300: one row in
+// eleven then differs), which the codec's one rounding per operation forbids.
 template <int K, int I>
 __device__ __forceinline__ float sq_tree(const float (&y)[128]) {
     if constexpr (K == 0) {
@@ -239,21 +244,34 @@ __device__ __forceinline__ uint32_t fkey(float x) {
     return b ^ ((uint32_t)((int32_t)b >> 31) >> 1);
 }
 
+// The bits b of a value as a 32-bit integer's absolute value: b for +0 and above, 2^32 - b for
+// negative values (2^31 for -0: abs.s32 keeps the most negative integer). For those it is
+// fkey(b) + 2^31 + 1 (mod 2^32), which the negative buckets' table entries absorb.
+__device__ __forceinline__ uint32_t iabs_bits(uint32_t b) {
+    uint32_t r;
+    asm("abs.s32 %0, %1;" : "=r"(r) : "r"(b));
+    return r;
+}
+
 // TBQ4 block: n16 = fp16(sqrt(sum y^2)), u = y x (1 / fp32(n16)) (0 when n16 is 0), idx =
-// #{k : u > beta_k}; nibble e of P[m] is the index of channel 8m + e. The table entry of u's
-// bucket plus u's key has the index in its top four bits (build_qtab), which a funnel shift
-// moves into the packed word (channel 8m + 7 first, so that channel 8m ends in nibble 0).
+// #{k : u > beta_k}; nibble e of P[m] is the index of channel 8m + e. The table entry of the
+// bucket of u's bits plus iabs_bits(u) has the index in its top four bits (build_qtab); a
+// funnel shift moves it into the packed word (channel 8m + 7 first, so that channel 8m ends
+// in nibble 0).
 __device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const uint32_t* qt, uint32_t (&P)[16]) {
     const uint16_t n16 = f2h_bits(__fsqrt_rn(sq_tree<7, 0>(y)));
     const float n = h2f(n16);
     const float inv = (n == 0.f) ? 0.f : fdiv(1.0f, n);
+    const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         uint32_t acc = 0;
 #pragma unroll
-        for (int e = 7; e >= 0; --e) {
-            const uint32_t key = fkey(fmul(y[8 * m + e], inv));
-            acc = __funnelshift_l(qt[key >> 21] + key, acc, 4);
+        for (int e = 6; e >= 0; e -= 2) {
+            const float2 u = fmul2(make_float2(y[8 * m + e], y[8 * m + e + 1]), inv2);
+            const uint32_t b1 = __float_as_uint(u.y), b0 = __float_as_uint(u.x);
+            acc = __funnelshift_l(qt[b1 >> 21] + iabs_bits(b1), acc, 4);
+            acc = __funnelshift_l(qt[b0 >> 21] + iabs_bits(b0), acc, 4);
         }
         P[m] = acc;
     }
@@ -399,6 +417,9 @@ __device__ __forceinline__ void store_bytes(uint8_t* rec, int D, int b, int w, c
 // (never above 15: a bucket with a boundary has base <= 14). Buckets of infinities and NaNs
 // give 0 (a NaN exceeds no boundary). Exact where no bucket holds two boundaries (consecutive
 // boundaries differ by a ratio above 1.25: TBQ4 >= 1.28, turbo3 >= 1.66).
+// The kernel indexes the table by u's own top 11 bits and adds iabs_bits(u) (encode_tbq4): the
+// entry of key bucket k of a negative value is stored at index k ^ 0x3FF (its bits' bucket)
+// and raised by 2^31 - 1, fkey(u) minus iabs_bits(u) (mod 2^32).
 __device__ void build_qtab(uint32_t* qt, const float* bnd, int nb) {
     for (int k = threadIdx.x; k < kBuckets; k += blockDim.x) {
         const uint32_t klo = (uint32_t)k << 21, khi = klo | 0x1FFFFFu;
@@ -414,7 +435,7 @@ __device__ void build_qtab(uint32_t* qt, const float* bnd, int nb) {
                 else if (bj <= vmax) t = (neg && bj == 0.f) ? 0x1FFFFFu : (fkey(bj) & 0x1FFFFFu);
             }
         }
-        qt[k] = (base << 28) + (0x0FFFFFFFu - t) - klo;
+        qt[neg ? (k ^ 0x3FF) : k] = (base << 28) + (0x0FFFFFFFu - t) - klo + (neg ? 0x7FFFFFFFu : 0u);
     }
 }
 

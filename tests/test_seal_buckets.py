@@ -1,12 +1,14 @@
-"""The seal kernel reads the TBQ4 index #{k : u > beta_k} from a 2,048-bucket table indexed by
-the top 11 bits of an order-preserving integer key of the fp32 value u (its bits, with the
-magnitude bits inverted for negative values), as the top four bits of entry + key: the entry
-holds base << 28 and a bias that makes the low 28 bits carry exactly when u exceeds the
-bucket's boundary. That is exact only if no bucket holds two boundaries. These CPU tests check
-the property on the oracle's boundary table and compare the bucket rule, built here the way
-the kernel builds it, with the plain count (the TBQ4 definition of the page "KV cache math",
-section "Worked example"), including the values that sit on a boundary or next to one, both
-zeros and NaNs.
+"""The seal kernel reads the TBQ4 index #{k : u > beta_k} from a 2,048-bucket table as the top
+four bits of entry + key. Over an order-preserving integer key of the fp32 value u (its bits,
+with the magnitude bits inverted for negative values) a bucket is the key's top 11 bits, and
+the entry holds base << 28 and a bias that makes the low 28 bits carry exactly when u exceeds
+the bucket's boundary. That is exact only if no bucket holds two boundaries. The kernel indexes
+the table by u's own top 11 bits and adds the absolute value of u's bits as a 32-bit integer
+(2^32 minus the bits for negative values: the order-preserving key plus 2^31 + 1), so it stores
+a negative bucket's entry at the index of its bits' bucket, raised by 2^31 - 1. These CPU tests check the property on the oracle's boundary
+table and compare the kernel's rule, built here the way the kernel builds it, with the plain
+count (the TBQ4 definition of the page "KV cache math", section "Worked example"), including
+the values that sit on a boundary or next to one, both zeros and NaNs.
 """
 
 import numpy as np
@@ -22,7 +24,7 @@ def fkey(u):
 
 
 def bucket_table(bnd):
-    """(entry, base, count) per bucket, the same rule the kernel builds in shared memory."""
+    """(entry, base, count) per key bucket (entry over the order-preserving key)."""
     entry = np.zeros(2048, dtype=np.uint64)
     base = np.zeros(2048, dtype=np.int64)
     count = np.zeros(2048, dtype=np.int64)
@@ -46,7 +48,27 @@ def bucket_table(bnd):
     return entry, base, count
 
 
+def kernel_table(entry):
+    """The table as the kernel stores it: indexed by the bits' bucket, negative entries + 2^31 - 1."""
+    qt = np.zeros(2048, dtype=np.uint64)
+    for k in range(2048):
+        if k >= 1024:
+            qt[k ^ 0x3FF] = (int(entry[k]) + (1 << 31) - 1) % (1 << 32)
+        else:
+            qt[k] = entry[k]
+    return qt
+
+
 def lookup(u, entry):
+    """The kernel's rule: table at u's bits' top 11 bits, plus |bits| as a 32-bit integer."""
+    qt = kernel_table(entry)
+    b = np.asarray(u, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    key = np.where(b >> np.uint64(31), (np.uint64(1 << 32) - b) % np.uint64(1 << 32), b)
+    return (((qt[(b >> np.uint64(21)).astype(np.int64)] + key) % np.uint64(1 << 32)) >> np.uint64(28)).astype(np.int64)
+
+
+def lookup_key(u, entry):
+    """The same index over the order-preserving key directly."""
     key = fkey(u)
     return (((entry[(key >> np.uint64(21)).astype(np.int64)] + key) % np.uint64(1 << 32)) >> np.uint64(28)).astype(np.int64)
 
@@ -78,6 +100,22 @@ def test_bucket_rule_equals_the_count(table):
                            np.array([0.0, -0.0, 1.0005, -1.0005, 1e-30, -1e-30], dtype=np.float32)])
     u = np.concatenate([u, edge.astype(np.float32)])
     assert np.array_equal(lookup(u, entry), plain_index(u, bnd))
+    assert np.array_equal(lookup_key(u, entry), plain_index(u, bnd))
+
+
+@pytest.mark.parametrize("table", ["tbq4", "turbo3"])
+def test_kernel_rule_equals_key_rule_at_every_bucket_edge(table):
+    """Both rules at the first and last two bit patterns of every bucket and next to every
+    boundary's pattern: equal sums mod 2^32 wherever the index is defined."""
+    _, bnd = (tables.tbq4_tables if table == "tbq4" else tables.tbq3_tables)()
+    entry, _, _ = bucket_table(bnd)
+    k = np.arange(2048, dtype=np.uint64) << np.uint64(21)
+    pats = np.concatenate([k, k + 1, k + 0x1FFFFE, k + 0x1FFFFF])
+    bb = np.asarray(bnd, dtype=np.float32).view(np.uint32).astype(np.int64)
+    near = np.concatenate([bb + d for d in (-1, 0, 1)] + [(bb ^ (1 << 31)) + d for d in (-1, 0, 1)])
+    pats = np.concatenate([pats, (near % (1 << 32)).astype(np.uint64)]).astype(np.uint32)
+    u = pats.view(np.float32)
+    assert np.array_equal(lookup(u, entry), lookup_key(u, entry))
 
 
 def test_nan_gives_index_zero():
