@@ -166,6 +166,7 @@ def test_bench_streaming_table_matches_the_dispatch_table():
              "KVQ_KVARN3": "kvarn3", "KVQ_KVARN4": "kvarn4", "KVQ_KVARN5": "kvarn5", "KVQ_Q5_1": "q5_1",
              "KVQ_TQ5_0": "tq5_0"}
     cases = set()
-    for m in re.finditer(r"KVQ_BODY_CASE\((\d+), (\d+), \w+, \w+, \d, \d, (\w+), (\w+)\)", src):
+    # (D, NQ, K reader, V reader, K bits, V bits, K format, V format, region kinds)
+    for m in re.finditer(r"KVQ_BODY_CASE\((\d+), (\d+), \w+, \w+, \d, \d, (\w+), (\w+), \d+\)", src):
         cases.add((int(m.group(1)), int(m.group(2)), names[m.group(3)], names[m.group(4)]))
-    assert cases == bench.STREAMING
+    assert cases and cases == bench.STREAMING
