@@ -22,10 +22,13 @@ __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b)
 __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
 __device__ __forceinline__ float fdiv(float a, float b) { return __fdiv_rn(a, b); }
 // Two of the same operations in one instruction (sm_100 and later): each half rounds to nearest
-// on its own, so the results are those of fmul / __fmaf_rn bit for bit (checked elementwise on
-// GB300). Only where the product feeds no addition: the code generator may contract a packed
-// multiply and a packed add into a packed multiply-add.
+// on its own, so the results are those of fmul / fadd / __fmaf_rn bit for bit (checked
+// elementwise on GB300). The code generator may contract a packed multiply whose result feeds
+// a packed add into a packed multiply-add, explicit rounding modifiers notwithstanding (one
+// row's sum of squares in eleven then differed): so no fmul2 result reaches an fadd2 or fsub2.
 __device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fsub2(float2 a, float2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 __device__ __forceinline__ float warp_max(float v) {

@@ -124,11 +124,14 @@ __device__ __forceinline__ void tq6_roundtrip(float (&y)[128]) {
     for (int i = 0; i < 128; ++i) a = fmaxf(a, fabsf(y[i]));
     const float d = h2f(f2h_bits(fdiv(a, 31.0f)));
     const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+    const float2 inv2 = make_float2(inv, inv), d2 = make_float2(d, d);
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-        float q = (d == 0.f) ? 0.f : rintf(fmul(y[i], inv));
-        q = fminf(fmaxf(q, -31.f), 31.f);
-        y[i] = fmul(q, d);
+    for (int i = 0; i < 128; i += 2) {
+        const float2 t = fmul2(make_float2(y[i], y[i + 1]), inv2);
+        float2 q = make_float2((d == 0.f) ? 0.f : rintf(t.x), (d == 0.f) ? 0.f : rintf(t.y));
+        q = make_float2(fminf(fmaxf(q.x, -31.f), 31.f), fminf(fmaxf(q.y, -31.f), 31.f));
+        const float2 r = fmul2(q, d2);
+        y[i] = r.x; y[i + 1] = r.y;
     }
 }
 
@@ -200,41 +203,58 @@ __device__ __forceinline__ void decode_x16(const uint8_t* st, float (&y)[128]) {
 
 // TBQ128 of one 128-channel block in registers: s2 . FWHT_128(s1 . x) x fp32(1/sqrt(128)),
 // butterflies in ascending stride order (the same operations as any other FWHT of the codec).
+// Strides 2 .. 64 go two butterflies (i, i + 1) per instruction pair; their inputs are sums
+// or the staged values, never products.
 __device__ __forceinline__ void rotate_tbq128(float (&y)[128]) {
 #pragma unroll
     for (int i = 0; i < 128; ++i)
         if (sign_neg(0, i)) y[i] = -y[i];
 #pragma unroll
-    for (int s = 1; s < 128; s <<= 1) {
+    for (int i = 0; i < 128; i += 2) {
+        const float a = y[i], c = y[i + 1];
+        y[i] = fadd(a, c);
+        y[i + 1] = fsub(a, c);
+    }
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
+    for (int s = 2; s < 128; s <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; i += 2) {
             if (i & s) continue;
-            const float a = y[i], c = y[i + s];
-            y[i] = fadd(a, c);
-            y[i + s] = fsub(a, c);
+            const float2 a = make_float2(y[i], y[i + 1]), c = make_float2(y[i + s], y[i + s + 1]);
+            const float2 u = fadd2(a, c), v = fsub2(a, c);
+            y[i] = u.x; y[i + 1] = u.y;
+            y[i + s] = v.x; y[i + s + 1] = v.y;
         }
     }
 #pragma unroll
-    for (int i = 0; i < 128; ++i) {
-        const float v = sign_neg(1, i) ? -y[i] : y[i];
-        y[i] = fmul(v, kTbqScale);
+    for (int i = 0; i < 128; i += 2) {
+        const float2 v = make_float2(sign_neg(1, i) ? -y[i] : y[i], sign_neg(1, i + 1) ? -y[i + 1] : y[i + 1]);
+        const float2 r = fmul2(v, make_float2(kTbqScale, kTbqScale));
+        y[i] = r.x; y[i + 1] = r.y;
     }
 }
 
 // ---------------------------------------------------------------------------- encoders
-// Node (K, I) of the halving tree of y_i^2 over 128 values: node(0, i) = y_i^2 and
-// node(K, i) = node(K-1, i) + node(K-1, i + 128 / 2^K); node(7, 0) is the sum. Evaluated
-// depth first so that few partial sums are live beside the 128 values. Scalar operations: a
-// packed multiply whose result feeds a packed add may be contracted into a packed multiply-add
-// by the code generator even with explicit rounding modifiers (measured on GB300: one row in
-// eleven then differs), which the codec's one rounding per operation forbids.
+// The halving tree of y_i^2 over 128 values: node(0, i) = y_i^2 and node(K, i) = node(K-1, i)
+// + node(K-1, i + 128 / 2^K); node(7, 0) is the sum. Nodes (K, I) and (K, I + 1) go as one
+// pair (I even, K <= 6: the partner offset 128 / 2^K is even, so the two nodes' terms pair up
+// level by level), evaluated depth first so that few partial sums are live beside the 128
+// values. The leaves are fma(y_i, y_i, z) with z a run-time +0 the code generator cannot fold:
+// exactly y_i^2 (a square is never -0), and a multiply-add result, which no later add can be
+// contracted with (a packed multiply feeding the packed adds could be).
 template <int K, int I>
-__device__ __forceinline__ float sq_tree(const float (&y)[128]) {
+__device__ __forceinline__ float2 sq_tree2(const float (&y)[128], float2 z) {
     if constexpr (K == 0) {
-        return fmul(y[I], y[I]);
+        const float2 v = make_float2(y[I], y[I + 1]);
+        return ffma2(v, v, z);
     } else {
-        return fadd(sq_tree<K - 1, I>(y), sq_tree<K - 1, I + (128 >> K)>(y));
+        return fadd2(sq_tree2<K - 1, I>(y, z), sq_tree2<K - 1, I + (128 >> K)>(y, z));
     }
+}
+// node (7, 0) = node (6, 0) + node (6, 1)
+__device__ __forceinline__ float sq_sum128(const float (&y)[128], float zero) {
+    const float2 p = sq_tree2<6, 0>(y, make_float2(zero, zero));
+    return fadd(p.x, p.y);
 }
 
 // Order-preserving integer key of an fp32 value: its bits for +0 and above, its bits with the 31
@@ -258,8 +278,9 @@ __device__ __forceinline__ uint32_t iabs_bits(uint32_t b) {
 // bucket of u's bits plus iabs_bits(u) has the index in its top four bits (build_qtab); a
 // funnel shift moves it into the packed word (channel 8m + 7 first, so that channel 8m ends
 // in nibble 0).
-__device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const uint32_t* qt, uint32_t (&P)[16]) {
-    const uint16_t n16 = f2h_bits(__fsqrt_rn(sq_tree<7, 0>(y)));
+__device__ __forceinline__ uint16_t encode_tbq4(const float (&y)[128], const uint32_t* qt, uint32_t (&P)[16],
+                                               float zero) {
+    const uint16_t n16 = f2h_bits(__fsqrt_rn(sq_sum128(y, zero)));
     const float n = h2f(n16);
     const float inv = (n == 0.f) ? 0.f : fdiv(1.0f, n);
     const float2 inv2 = make_float2(inv, inv);
@@ -293,13 +314,18 @@ __device__ __forceinline__ uint16_t encode_q32(const float (&y)[128], int j0, ui
     const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
     // 1.5 x 2^23 plus the zero level (Q8_0: 0, its codes are signed bytes; else QMAX + 1)
     constexpr float magic = 12582912.0f + (QMAX == 127 ? 0.f : (float)(QMAX + 1));
+    const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(magic, magic);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         uint32_t r[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float z = fminf(fmaxf(fmul(y[j0 + 4 * k + i], inv), -(float)QMAX), (float)QMAX);
-            r[i] = __float_as_uint(fadd(z, magic));
+        for (int i = 0; i < 4; i += 2) {   // the clamp stands between the packed multiply and add
+            const float2 t = fmul2(make_float2(y[j0 + 4 * k + i], y[j0 + 4 * k + i + 1]), inv2);
+            const float2 z = make_float2(fminf(fmaxf(t.x, -(float)QMAX), (float)QMAX),
+                                         fminf(fmaxf(t.y, -(float)QMAX), (float)QMAX));
+            const float2 v = fadd2(z, mg2);
+            r[i] = __float_as_uint(v.x);
+            r[i + 1] = __float_as_uint(v.y);
         }
         c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
     }
@@ -449,13 +475,16 @@ __device__ __forceinline__ uint16_t encode_tq5(const float (&y)[128], uint32_t (
     const uint16_t d16 = f2h_bits(fdiv(a, 15.0f));
     const float d = h2f(d16);
     const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+    const float2 inv2 = make_float2(inv, inv), mg2 = make_float2(12582928.0f, 12582928.0f);
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
         uint32_t r[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float z = fminf(fmaxf(fmul(y[4 * k + i], inv), -15.f), 15.f);
-            r[i] = __float_as_uint(fadd(z, 12582928.0f));
+        for (int i = 0; i < 4; i += 2) {   // the clamp stands between the packed multiply and add
+            const float2 t = fmul2(make_float2(y[4 * k + i], y[4 * k + i + 1]), inv2);
+            const float2 v = fadd2(make_float2(fminf(fmaxf(t.x, -15.f), 15.f), fminf(fmaxf(t.y, -15.f), 15.f)), mg2);
+            r[i] = __float_as_uint(v.x);
+            r[i + 1] = __float_as_uint(v.y);
         }
         c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
     }
@@ -498,7 +527,7 @@ __device__ __forceinline__ void fill_slots(const Layout& L, const SealParams& p,
 
 template <int JK, int FAM>
 __global__ void __launch_bounds__(kRows, JK == J_TQ6 ? 3 : 2)
-seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
+seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes, float zero) {
     extern __shared__ __align__(16) uint8_t sm[];
     __shared__ TileSlot slot[kSlots];
     uint32_t* qt = reinterpret_cast<uint32_t*>(sm + kStages * stage_bytes);
@@ -571,7 +600,7 @@ seal_rows_kernel(Layout L, SealParams p, int n_tiles, int stage_bytes) {
             } else {
                 uint32_t P[16];
                 const bool t3 = FAM == F_TBQ4 && fmt == KVQ_TURBO3;
-                const uint16_t n16 = encode_tbq4(y, t3 ? qt3 : qt, P);
+                const uint16_t n16 = encode_tbq4(y, t3 ? qt3 : qt, P, zero);
                 if (t3) {   // token-major: 2-bit plane, one-bit plane, norms
                     uint32_t cw[8], bw[4];
 #pragma unroll
@@ -674,7 +703,7 @@ int launch_rows(const Layout& L, const SealParams& p, int n_tiles, cudaStream_t 
     e = (int)cudaGetDevice(&dev);
     if (e) return e;
     const int grid = std::min(n_tiles, std::max(per_sm, 1) * query_sm_count(dev));
-    fn<<<grid, kRows, smem, s>>>(L, p, n_tiles, stage);
+    fn<<<grid, kRows, smem, s>>>(L, p, n_tiles, stage, 0.0f);   // zero: see sq_tree2
     return (int)cudaGetLastError();
 }
 
