@@ -757,7 +757,7 @@ __device__ __forceinline__ void tq6_roundtrip_warp(float (&v)[8], int k0) {
 // rotated here by HAD256.
 template <int JK>
 __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, int t, int nsc, int half, int lane,
-                                       float (&v)[8], int journal) {
+                                       float (&v)[8], int journal, float nz) {
     const uint8_t* row = st + t * KvStage<JK>::ROW;
     if constexpr (JK == J_IN) {
         // a prefill chunk's fp16 row: the stored value (bf16-rounded for a BF16 journal),
@@ -770,7 +770,7 @@ __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, in
         }
         warp_fwht<8>(v, lane);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
+        for (int k = 0; k < 8; ++k) v[k] = __fmaf_rn(v[k], kHad256Scale, nz);
         if (journal == KVQ_TQ6_0) {
             tq6_roundtrip_warp(v, 0);
             tq6_roundtrip_warp(v, 4);
@@ -782,7 +782,7 @@ __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, in
             const uint8_t* blk = row + 96 * b;
             const int lo = (blk[j >> 1] >> ((j & 1) * 4)) & 15;
             const int hi = (blk[64 + (j >> 2)] >> ((j & 3) * 2)) & 3;
-            v[k] = fmul((float)((lo | (hi << 4)) - 32), h2f(sc[t * nsc + 2 * half + b]));
+            v[k] = __fmaf_rn((float)((lo | (hi << 4)) - 32), h2f(sc[t * nsc + 2 * half + b]), nz);
         }
     } else {
         const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
@@ -790,7 +790,7 @@ __device__ __forceinline__ void kv_row(const uint8_t* st, const uint16_t* sc, in
         for (int k = 0; k < 8; ++k) v[k] = x16_to_f(r16[lane + 32 * k], JK == J_BF16 ? KVQ_BF16 : KVQ_F16);
         warp_fwht<8>(v, lane);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = fmul(v[k], kHad256Scale);
+        for (int k = 0; k < 8; ++k) v[k] = __fmaf_rn(v[k], kHad256Scale, nz);
     }
 }
 
@@ -827,26 +827,34 @@ __device__ __forceinline__ float kv_sigma(float var_sum, float inv_n) {
 // A row pass over the warp's 8 rows (n = 256: mean, population spread, row /= sigma, the row
 // scale r[t] *= sigma). Row positions j = l + 32 b: the thread's levels pair b with b + 4
 // (stride 128), b + 2 (64), b + 1 (32); warp_rows8 takes strides 16 .. 1. Returns |sigma - 1|
-// of row w + 16 (lane / 4); with APPLY false the pass only measures.
+// of row w + 16 (lane / 4); with APPLY false the pass only measures. Columns 2k and 2k + 1 go
+// as pairs, two operations per instruction. Every product that an add consumes is a packed
+// multiply-add with nz, a run-time -0 the code generator cannot fold: a + b x -0 rounds like
+// the product alone (signed zeros included), and a multiply-add result cannot be contracted
+// with the add that follows (a packed multiply feeding a packed add could be).
 template <bool APPLY = true>
-__device__ __forceinline__ float kv_row_pass(float (&x)[8][8], float* r, int warp, int lane) {
+__device__ __forceinline__ float kv_row_pass(float (&x)[8][8], float* r, int warp, int lane, float nz) {
     constexpr float INV_N = 1.0f / 256.0f;
+    const float2 nz2 = make_float2(nz, nz);
     float p[8];
+    // leaf(a, k): the leaves of columns 2k and 2k + 1 as a pair; (l0 + l4, l1 + l5) and
+    // (l2 + l6, l3 + l7), then their pair sum and its two halves
     auto partials = [&](auto leaf) {
 #pragma unroll
         for (int a = 0; a < 8; ++a) {
-            float s[4];
-#pragma unroll
-            for (int b = 0; b < 4; ++b) s[b] = fadd(leaf(a, b), leaf(a, b + 4));
-            p[a] = fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
+            const float2 t = fadd2(fadd2(leaf(a, 0), leaf(a, 2)), fadd2(leaf(a, 1), leaf(a, 3)));
+            p[a] = fadd(t.x, t.y);
         }
     };
-    partials([&](int a, int b) { return x[a][b]; });
-    const float mu_own = fmul(warp_rows8(p, lane, FAdd()), INV_N);
+    partials([&](int a, int k) { return make_float2(x[a][2 * k], x[a][2 * k + 1]); });
+    const float mu_own = __fmaf_rn(warp_rows8(p, lane, FAdd()), INV_N, nz);
     float mu[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) mu[a] = __shfl_sync(kFull, mu_own, 4 * a);
-    partials([&](int a, int b) { const float d = fsub(x[a][b], mu[a]); return fmul(d, d); });
+    partials([&](int a, int k) {
+        const float2 d = fsub2(make_float2(x[a][2 * k], x[a][2 * k + 1]), make_float2(mu[a], mu[a]));
+        return ffma2(d, d, nz2);
+    });
     const float sig = kv_sigma(warp_rows8(p, lane, FAdd()), INV_N);
     if constexpr (APPLY) {
         const float inv_own = fdiv(1.0f, sig);
@@ -854,7 +862,11 @@ __device__ __forceinline__ float kv_row_pass(float (&x)[8][8], float* r, int war
         for (int a = 0; a < 8; ++a) {
             const float inv = __shfl_sync(kFull, inv_own, 4 * a);
 #pragma unroll
-            for (int b = 0; b < 8; ++b) x[a][b] = fmul(x[a][b], inv);
+            for (int k = 0; k < 4; ++k) {
+                const float2 v = ffma2(make_float2(x[a][2 * k], x[a][2 * k + 1]), make_float2(inv, inv), nz2);
+                x[a][2 * k] = v.x;
+                x[a][2 * k + 1] = v.y;
+            }
         }
         if ((lane & 3) == 0) {
             const int t = warp + 16 * (lane >> 2);
@@ -872,16 +884,21 @@ __device__ __forceinline__ float kv_row_pass(float (&x)[8][8], float* r, int war
 // partials, the last the inverses; a column pass's reads of part, mu_s and inv_s all come
 // before the next column pass writes them again (past one or more of these barriers).
 __device__ __forceinline__ float kv_col_pass(float (&x)[8][8], float* c, float* part, float* mu_s, float* inv_s,
-                                             int warp, int lane) {
+                                             int warp, int lane, float nz) {
     constexpr float INV_N = 1.0f / 128.0f;
     const int tid = threadIdx.x;
+    const float2 nz2 = make_float2(nz, nz);
+    // leaf(a, k): the leaves of columns 2k and 2k + 1 of row a as a pair, the two columns'
+    // trees side by side
     auto partials = [&](auto leaf) {
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            float s[4];
+        for (int k = 0; k < 4; ++k) {
+            float2 s[4];
 #pragma unroll
-            for (int a = 0; a < 4; ++a) s[a] = fadd(leaf(a, b), leaf(a + 4, b));
-            part[warp * 256 + lane + 32 * b] = fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
+            for (int a = 0; a < 4; ++a) s[a] = fadd2(leaf(a, k), leaf(a + 4, k));
+            const float2 t = fadd2(fadd2(s[0], s[2]), fadd2(s[1], s[3]));
+            part[warp * 256 + lane + 32 * (2 * k)] = t.x;
+            part[warp * 256 + lane + 32 * (2 * k + 1)] = t.y;
         }
     };
     auto column_total = [&]() {
@@ -892,14 +909,17 @@ __device__ __forceinline__ float kv_col_pass(float (&x)[8][8], float* c, float* 
         for (int w = 0; w < 4; ++w) s[w] = fadd(s[w], s[w + 4]);
         return fadd(fadd(s[0], s[2]), fadd(s[1], s[3]));
     };
-    partials([&](int a, int b) { return x[a][b]; });
+    partials([&](int a, int k) { return make_float2(x[a][2 * k], x[a][2 * k + 1]); });
     __syncthreads();
     if (tid < 256) mu_s[tid] = fmul(column_total(), INV_N);
     __syncthreads();
     float mu[8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) mu[b] = mu_s[lane + 32 * b];
-    partials([&](int a, int b) { const float d = fsub(x[a][b], mu[b]); return fmul(d, d); });
+    partials([&](int a, int k) {
+        const float2 d = fsub2(make_float2(x[a][2 * k], x[a][2 * k + 1]), make_float2(mu[2 * k], mu[2 * k + 1]));
+        return ffma2(d, d, nz2);
+    });
     __syncthreads();
     float dev = 0.f;
     if (tid < 256) {
@@ -910,10 +930,14 @@ __device__ __forceinline__ float kv_col_pass(float (&x)[8][8], float* c, float* 
     }
     __syncthreads();
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-        const float inv = inv_s[lane + 32 * b];
+    for (int k = 0; k < 4; ++k) {
+        const float2 inv = make_float2(inv_s[lane + 64 * k], inv_s[lane + 64 * k + 32]);
 #pragma unroll
-        for (int a = 0; a < 8; ++a) x[a][b] = fmul(x[a][b], inv);
+        for (int a = 0; a < 8; ++a) {
+            const float2 v = ffma2(make_float2(x[a][2 * k], x[a][2 * k + 1]), inv, nz2);
+            x[a][2 * k] = v.x;
+            x[a][2 * k + 1] = v.y;
+        }
     }
     return dev;
 }
@@ -978,7 +1002,7 @@ __device__ __forceinline__ void kv_plane(uint32_t* plane, const uint8_t* codes, 
 // BITS: 0 = any code width and balancing read from the layout; 4 = 4-bit keys and values with
 // the 16-pass balancing (an instance with only that code: fewer instruction-cache misses).
 template <int JK, int BITS>
-__global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p) {
+__global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealParams p, float nz) {
     constexpr int ROW = KvStage<JK>::ROW;
     const SealTaskPos tk = seal_task(p, blockIdx.x);
     const int nh = L.D / 256;
@@ -1054,7 +1078,7 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     unit_scales();
     __syncthreads();
 #pragma unroll
-    for (int a = 0; a < 8; ++a) kv_row<JK>(st, sc, warp + 16 * a, nsc, half, lane, x[a], L.journal);
+    for (int a = 0; a < 8; ++a) kv_row<JK>(st, sc, warp + 16 * a, nsc, half, lane, x[a], L.journal, nz);
     __syncthreads();
 #pragma unroll
     for (int n = 0; n < 16; ++n)
@@ -1071,14 +1095,14 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
         __shared__ float s_wmax[kKvWarps], s_eps[8];
         __shared__ int s_best;
         for (int pass = 0; pass < 8; ++pass) {
-            const float dev = (pass & 1) == 0 ? kv_row_pass(x, r, warp, lane)
-                                              : kv_col_pass(x, c, part, mu_s, inv_s, warp, lane);
+            const float dev = (pass & 1) == 0 ? kv_row_pass(x, r, warp, lane, nz)
+                                              : kv_col_pass(x, c, part, mu_s, inv_s, warp, lane, nz);
             if (pass > 0) {
                 block_max_to(dev, s_wmax, &s_eps[pass - 1]);
                 __syncthreads();
             }
         }
-        block_max_to(kv_row_pass<false>(x, r, warp, lane), s_wmax, &s_eps[7]);
+        block_max_to(kv_row_pass<false>(x, r, warp, lane, nz), s_wmax, &s_eps[7]);
         if (threadIdx.x == 0) {
             int b = 0;
             for (int i = 1; i < 8; ++i)
@@ -1093,8 +1117,8 @@ __global__ void __launch_bounds__(kKvThreads) seal_kvarn_kernel(Layout L, SealPa
     }
 #pragma unroll 1
     for (int pass = 0; pass < passes; ++pass) {
-        if ((pass & 1) == 0) kv_row_pass(x, r, warp, lane);
-        else kv_col_pass(x, c, part, mu_s, inv_s, warp, lane);
+        if ((pass & 1) == 0) kv_row_pass(x, r, warp, lane, nz);
+        else kv_col_pass(x, c, part, mu_s, inv_s, warp, lane, nz);
     }
 
     // row rounding parameters: each row's extremes over the balanced values; lanes 4k .. 4k + 3
@@ -1206,7 +1230,7 @@ int launch_kvarn_b(const Layout& L, const SealParams& p, int groups, cudaStream_
     int e = (int)cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e) return e;
     dim3 grid(groups, L.H, 2 * (L.D / 256));
-    fn<<<grid, kKvThreads, smem, s>>>(L, p);
+    fn<<<grid, kKvThreads, smem, s>>>(L, p, -0.0f);   // nz: see kv_row_pass
     return (int)cudaGetLastError();
 }
 template <int JK>
