@@ -78,13 +78,13 @@ def peaks():
 # the line reports null until a new capture replaces it.
 DECODE_SOURCES = ("kernels_body.cu", "region_item.cuh", "stream_common.cuh", "device_common.cuh", "append_row.cuh")
 MEASURED_TRAFFIC = {
-    "hybrid27b_kvarn44": (42.88e6, "f52ada9c5576"),
-    "fa14b_q8q4": (222.02e6, "f52ada9c5576"),
-    "longctx_tbq4": (750.89e6, "f52ada9c5576"),
-    "widehead_kvarn55": (193.69e6, "f52ada9c5576"),
-    "hybrid27b_kvarn32_200k": (156.95e6, "f52ada9c5576"),
-    "fa14b_q51q40": (180.48e6, "f52ada9c5576"),
-    "hybrid27b_tq50tbq4_110k": (140.15e6, "f52ada9c5576"),
+    "hybrid27b_kvarn44": (42.88e6, "e4787c2cf91b"),
+    "fa14b_q8q4": (222.05e6, "e4787c2cf91b"),
+    "longctx_tbq4": (750.91e6, "e4787c2cf91b"),
+    "widehead_kvarn55": (193.74e6, "e4787c2cf91b"),
+    "hybrid27b_kvarn32_200k": (156.86e6, "e4787c2cf91b"),
+    "fa14b_q51q40": (180.38e6, "e4787c2cf91b"),
+    "hybrid27b_tq50tbq4_110k": (140.15e6, "e4787c2cf91b"),
 }
 
 
