@@ -347,13 +347,16 @@ __device__ __forceinline__ uint16_t encode_qmin(const float (&y)[128], int j0, u
     const uint16_t d16 = f2h_bits(fdiv(fsub(hi, lo), (float)Q));
     const float d = h2f(d16), m = h2f(m16);
     const float inv = (d == 0.f) ? 0.f : fdiv(1.0f, d);
+    const float2 m2 = make_float2(m, m), inv2 = make_float2(inv, inv), mg2 = make_float2(12582912.0f, 12582912.0f);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         uint32_t r[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float z = fminf(fmaxf(fmul(fsub(y[j0 + 4 * k + i], m), inv), 0.f), (float)Q);
-            r[i] = __float_as_uint(fadd(z, 12582912.0f));
+        for (int i = 0; i < 4; i += 2) {   // the clamp stands between the packed multiply and add
+            const float2 t = fmul2(fsub2(make_float2(y[j0 + 4 * k + i], y[j0 + 4 * k + i + 1]), m2), inv2);
+            const float2 v = fadd2(make_float2(fminf(fmaxf(t.x, 0.f), (float)Q), fminf(fmaxf(t.y, 0.f), (float)Q)), mg2);
+            r[i] = __float_as_uint(v.x);
+            r[i + 1] = __float_as_uint(v.y);
         }
         c[k] = __byte_perm(__byte_perm(r[0], r[1], 0x0040), __byte_perm(r[2], r[3], 0x0040), 0x5410);
     }
